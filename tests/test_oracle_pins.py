@@ -1,0 +1,450 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+None of these tests re-types an oracle formula: each compares the oracle with
+a hand-derived value, a closed form, an invariant, a special case that reduces
+to a textbook routine, or a brute-force evaluation written as plain loops.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------
+
+def test_bf16_bits_known_values():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x4300, 0x3C23], dtype=np.uint16)
+    want = [1.0, -2.0, 0.0, -0.0, 128.0, 0.00994873046875]
+    assert O.bf16_bits_to_f64(bits).tolist() == want
+
+
+def test_f32_to_bf16_round_half_even():
+    # 1 + 2^-8 lies half-way between 1 and 1 + 2^-7: ties to the even code 0x3F80.
+    # 1 + 3*2^-8 lies half-way between 1 + 2^-7 (odd code) and 1 + 2^-6: goes up.
+    # 1 + 2^-8 + 2^-20 is above the half-way point: rounds up.
+    v = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, -(1 + 2 ** -8)], dtype=np.float32)
+    assert O.f32_to_bf16_bits(v).tolist() == [0x3F80, 0x3F82, 0x3F81, 0xBF80]
+
+
+# ----------------------------------------------------------------------------
+# PackedInt4Linear storage
+# ----------------------------------------------------------------------------
+
+def test_unpack_golden_words(golden_dir):
+    with open(os.path.join(golden_dir, "int4_words.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        assert int(c["int32"]) & 0xFFFFFFFF == int(c["word_hex"], 16)
+        got = O.unpack_int4(np.array([[c["int32"]]], dtype=np.int32))[0].tolist()
+        assert got == c["values"], c["word_hex"]
+
+
+def test_unpack_every_value_in_every_position():
+    # one non-zero nibble per word: all 16 codes x 8 positions
+    for j in range(8):
+        for code in range(16):
+            word = np.array([[code << (4 * j)]], dtype=np.uint32).view(np.int32)
+            got = O.unpack_int4(word)[0]
+            want = np.zeros(8, dtype=np.int64)
+            want[j] = code - 16 if code >= 8 else code
+            assert got.tolist() == want.tolist()
+
+
+def test_pack_unpack_round_trip():
+    w = RNG.integers(0, 2 ** 32, size=(512, 2048), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    assert np.array_equal(O.pack_int4(O.unpack_int4(w)), w)
+    q = RNG.integers(-8, 8, size=(33, 64))
+    assert np.array_equal(O.unpack_int4(O.pack_int4(q)), q)
+    # columns of a multi-word row land at 8i+j
+    q = np.arange(16) % 16 - 8  # -8..7
+    words = O.pack_int4(q[None, :])
+    assert O.unpack_int4(words)[0].tolist() == q.tolist()
+
+
+def test_pack_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        O.pack_int4(np.array([[8] * 8]))
+    with pytest.raises(ValueError):
+        O.pack_int4(np.array([[0] * 7]))
+
+
+def test_dequantize_group_scales():
+    # row 0: all q = 1, group scales 0.5 / 2.0 -> 32 copies of each
+    q = np.ones((2, 64), dtype=np.int64)
+    q[1] = -8
+    packed = O.pack_int4(q)
+    scale = np.array([[0x3F00, 0x4000], [0x3F80, 0x3C23]], dtype=np.uint16)  # 0.5, 2.0 ; 1.0, 0.00994873046875
+    W = O.dequantize(packed, scale)
+    assert W[0, :32].tolist() == [0.5] * 32 and W[0, 32:].tolist() == [2.0] * 32
+    assert W[1, :32].tolist() == [-8.0] * 32
+    assert W[1, 32:].tolist() == [-8 * 0.00994873046875] * 32
+    with pytest.raises(ValueError):
+        O.dequantize(packed, scale[:, :1])
+
+
+# ----------------------------------------------------------------------------
+# router
+# ----------------------------------------------------------------------------
+
+def test_sigmoid_closed_forms():
+    assert O.sigmoid(0.0) == 0.5
+    assert abs(O.sigmoid(math.log(3.0)) - 0.75) < 1e-15
+    z = RNG.normal(size=100) * 5
+    assert np.allclose(O.sigmoid(-z), 1 - O.sigmoid(z), atol=1e-15)
+
+
+def _brute_route(x, W, b, k, renorm):
+    T, E = x.shape[0], W.shape[0]
+    idx, wts = [], []
+    for t in range(T):
+        s = []
+        for e in range(E):
+            z = sum(float(x[t, h]) * float(W[e, h]) for h in range(x.shape[1]))
+            s.append(1.0 / (1.0 + math.exp(-z)))
+        ranked = sorted(range(E), key=lambda e: (-(s[e] + float(b[e])), e))[:k]
+        w = [s[e] for e in ranked]
+        if renorm:
+            tot = sum(w) + 1e-20
+            w = [v / tot for v in w]
+        idx.append(ranked)
+        wts.append(w)
+    return np.array(idx), np.array(wts)
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_matches_brute_force(renorm):
+    x = RNG.normal(size=(6, 24))
+    W = RNG.normal(size=(10, 24)) * 0.3
+    b = RNG.normal(size=10) * 0.05
+    rt = O.route(x, W, b, 3, renorm)
+    idx, w = _brute_route(x, W, b, 3, renorm)
+    assert np.array_equal(rt.idx, idx)
+    assert np.allclose(rt.weight, w, rtol=1e-13, atol=0)
+
+
+def test_route_ranks_by_biased_score_weights_by_unbiased():
+    # x = 0: every logit is 0 and every affinity 0.5, so the bias alone ranks.
+    E, k = 6, 2
+    b = np.array([0.0, 0.3, -0.1, 0.2, 0.0, 0.05])
+    rt = O.route(np.zeros((1, 4)), np.ones((E, 4)), b, k, renorm=False)
+    assert rt.idx[0].tolist() == [1, 3]
+    assert rt.weight[0].tolist() == [0.5, 0.5]          # unbiased affinities
+    rt = O.route(np.zeros((1, 4)), np.ones((E, 4)), b, k, renorm=True)
+    assert rt.weight[0].tolist() == [0.5 / (1.0 + 1e-20)] * 2
+
+
+def test_route_ties_go_to_lower_expert():
+    b = np.zeros(5)
+    rt = O.route(np.zeros((1, 3)), np.zeros((5, 3)), b, 3)
+    assert rt.idx[0].tolist() == [0, 1, 2]
+
+
+def test_route_k_equals_E_and_k_one():
+    x = RNG.normal(size=(5, 16))
+    W = RNG.normal(size=(7, 16))
+    b = RNG.normal(size=7) * 0.01
+    rt = O.route(x, W, b, 7)
+    assert all(sorted(r) == list(range(7)) for r in rt.idx.tolist())
+    assert np.allclose(rt.weight.sum(1), 1.0, atol=1e-15)
+    rt1 = O.route(x, W, b, 1)
+    assert np.all(rt1.weight == 1.0)    # s / (s + 1e-20) == 1 in float64
+    assert np.all(np.isinf(O.topk_gap(rt.r, 7)))
+
+
+def test_renorm_sums_to_one_and_gap():
+    x = RNG.normal(size=(50, 32))
+    W = RNG.normal(size=(20, 32)) * 0.2
+    rt = O.route(x, W, np.zeros(20), 4)
+    assert np.allclose(rt.weight.sum(1), 1.0, rtol=0, atol=4e-16)
+    gap = O.topk_gap(rt.r, 4)
+    for t in range(50):
+        srt = sorted(rt.r[t], reverse=True)
+        assert gap[t] == srt[3] - srt[4]
+
+
+# ----------------------------------------------------------------------------
+# dispatch
+# ----------------------------------------------------------------------------
+
+def _random_topk(T, E, k):
+    return np.stack([RNG.permutation(E)[:k] for _ in range(T)])
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 2), (37, 9, 3), (200, 16, 8), (64, 64, 1)])
+def test_dispatch_invariants_and_brute_force(T, E, k):
+    idx = _random_topk(T, E, k)
+    d = O.dispatch(idx, E)
+    assert d.counts.sum() == T * k and d.offsets[-1] == T * k and d.offsets[0] == 0
+    assert np.array_equal(np.diff(d.offsets), d.counts)
+    assert np.array_equal(np.bincount(d.row_token, minlength=T), np.full(T, k))
+    # brute force: sort (expert, token) pairs
+    pairs = sorted((int(idx[t, j]), t, j) for t in range(T) for j in range(k))
+    assert [p[1] for p in pairs] == d.row_token.tolist()
+    assert [p[2] for p in pairs] == d.row_slot.tolist()
+    # inverse permutation: gather then scatter is the identity
+    for t in range(T):
+        for j in range(k):
+            r = d.inv_row[t * k + j]
+            assert d.row_token[r] == t and d.row_slot[r] == j
+            assert d.offsets[idx[t, j]] <= r < d.offsets[idx[t, j] + 1]
+    assert sorted(d.inv_row.tolist()) == list(range(T * k))
+
+
+def test_dispatch_idle_experts():
+    idx = np.array([[2, 0], [0, 2], [2, 0]])
+    d = O.dispatch(idx, 5)
+    assert d.counts.tolist() == [3, 0, 3, 0, 0]
+    assert d.offsets.tolist() == [0, 3, 3, 6, 6, 6]
+    assert d.row_token.tolist() == [0, 1, 2, 0, 1, 2]
+    assert d.row_slot.tolist() == [1, 0, 1, 0, 1, 0]
+
+
+# ----------------------------------------------------------------------------
+# act_bits = 8
+# ----------------------------------------------------------------------------
+
+def test_quantizer_golden(golden_dir):
+    with open(os.path.join(golden_dir, "quantizer_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q, s = O.quantize_rows_int8(np.array([c["v"]], dtype=np.float32))
+        assert q[0].tolist() == c["q"]
+        assert float(s[0]) == c["scale"]
+
+
+def test_quantizer_identity_on_int8_rows():
+    x = RNG.integers(-127, 128, size=(20, 96)).astype(np.float32)
+    x[:, 5] = 127.0
+    q, s = O.quantize_rows_int8(x)
+    assert np.all(s == 1.0) and np.array_equal(q, x.astype(np.int8))
+
+
+def test_quantizer_bounds_and_rounding():
+    v = (RNG.normal(size=(40, 300)) * RNG.uniform(0.01, 100, size=(40, 1))).astype(np.float32)
+    q, s = O.quantize_rows_int8(v)
+    assert q.dtype == np.int8 and np.abs(q.astype(int)).max() <= 127
+    # amax maps to +-127 and every code is within half a step of v / scale
+    for r in range(40):
+        sc = Fraction(float(s[r]))
+        assert sc == Fraction(float(np.float32(np.abs(v[r]).max()) / np.float32(127)))
+        for c in range(0, 300, 7):
+            assert abs(Fraction(float(v[r, c])) / sc - int(q[r, c])) <= Fraction(1, 2) + Fraction(1, 10 ** 5)
+    # rows are independent
+    q2, s2 = O.quantize_rows_int8(v[::-1])
+    assert np.array_equal(q2, q[::-1]) and np.array_equal(s2, s[::-1])
+
+
+def _brute_partials(qx, qw):
+    R, K = qx.shape
+    N = qw.shape[0]
+    P = np.zeros((R, N, K // 32), dtype=np.int64)
+    for r in range(R):
+        for n in range(N):
+            for c in range(K):
+                P[r, n, c // 32] += int(qx[r, c]) * int(qw[n, c])
+    return P
+
+
+def test_group_partials_brute_force_and_extremes():
+    qx = RNG.integers(-127, 128, size=(3, 96)).astype(np.int8)
+    qw = RNG.integers(-8, 8, size=(5, 96))
+    P = O.int4_group_partials(qx, O.pack_int4(qw))
+    assert np.array_equal(P, _brute_partials(qx, qw))
+    # worst-case magnitude 32*8*127 per group
+    qx = np.full((1, 64), 127, dtype=np.int8)
+    qw = np.full((2, 64), -8)
+    assert O.int4_group_partials(qx, O.pack_int4(qw)).tolist() == [[[-32512, -32512]] * 2]
+
+
+def test_group_partials_int32_bound_rejected():
+    K = 2 ** 31 // (8 * 127) // 32 * 32 + 32   # first multiple of 32 with K*8*127 >= 2^31
+    assert K * 8 * 127 >= 2 ** 31 and (K - 32) * 8 * 127 < 2 ** 31
+    with pytest.raises(ValueError):
+        O.int4_group_partials(np.zeros((1, K), np.int8), np.zeros((1, K // 8), np.int32))
+
+
+# ----------------------------------------------------------------------------
+# PackedInt4Linear and the expert
+# ----------------------------------------------------------------------------
+
+ONE = 0x3F80  # bf16 1.0
+
+
+def test_int4_linear_unit_scales_is_integer_matmul():
+    qw = RNG.integers(-8, 8, size=(7, 64))
+    u = RNG.integers(-127, 128, size=(4, 64)).astype(np.float64)
+    u[:, 0] = 127
+    scale = np.full((7, 2), ONE, dtype=np.uint16)
+    want = [[sum(int(u[r, c]) * int(qw[n, c]) for c in range(64)) for n in range(7)] for r in range(4)]
+    y16 = O.int4_linear(u, O.pack_int4(qw), scale, 16)
+    y8 = O.int4_linear(u, O.pack_int4(qw), scale, 8)
+    assert y16.tolist() == want
+    assert y8.tolist() == want          # sc = 1, q = u: the integer accumulator itself
+
+
+def test_int4_linear_exact_mode_close_to_w4a16():
+    qw = RNG.integers(-8, 8, size=(16, 256))
+    scale = O.f32_to_bf16_bits(RNG.uniform(0.002, 0.01, size=(16, 8)).astype(np.float32))
+    u = O.round_bf16(RNG.normal(size=(5, 256)))
+    y16 = O.int4_linear(u, O.pack_int4(qw), scale, 16)
+    y8 = O.int4_linear(u, O.pack_int4(qw), scale, 8)
+    # int8 activations carry a relative error below one half step (1/254 of max|u|)
+    bound = (np.abs(u).max(1, keepdims=True) / 254) * np.abs(O.dequantize(O.pack_int4(qw), scale)).sum(1)[None, :]
+    assert np.all(np.abs(y8 - y16) <= bound * 1.0001)
+
+
+def _brute_expert(u, ex, act_bits=16):
+    """Plain loops of down(SiLU(gate u) * up u) with explicit unpack and scales."""
+    def lin(vec, packed, scale):
+        N, K8 = packed.shape
+        out = []
+        for n in range(N):
+            acc = 0.0
+            for i in range(K8):
+                word = int(packed[n, i]) & 0xFFFFFFFF
+                for j in range(8):
+                    code = (word >> (4 * j)) & 0xF
+                    qv = code - 16 if code >= 8 else code
+                    c = 8 * i + j
+                    acc += vec[c] * qv * float(O.bf16_bits_to_f64(scale[n, c // 32]))
+            out.append(acc)
+        return out
+    g = lin(u, ex["gate_packed"], ex["gate_scale"])
+    up = lin(u, ex["up_packed"], ex["up_scale"])
+    h = [gv / (1.0 + math.exp(-gv)) * uv for gv, uv in zip(g, up)]
+    return lin(h, ex["down_packed"], ex["down_scale"])
+
+
+def _random_expert(D, I):
+    def sc(n, k):
+        return O.f32_to_bf16_bits(RNG.uniform(0.02, 0.2, size=(n, k // 32)).astype(np.float32))
+    return {
+        "gate_packed": O.pack_int4(RNG.integers(-8, 8, size=(I, D))), "gate_scale": sc(I, D),
+        "up_packed": O.pack_int4(RNG.integers(-8, 8, size=(I, D))), "up_scale": sc(I, D),
+        "down_packed": O.pack_int4(RNG.integers(-8, 8, size=(D, I))), "down_scale": sc(D, I),
+    }
+
+
+def test_expert_matches_brute_force_loops():
+    ex = _random_expert(64, 32)
+    u = O.round_bf16(RNG.normal(size=(2, 64)))
+    y = O.expert_ffn(u, ex, 16)
+    for r in range(2):
+        assert np.allclose(y[r], _brute_expert(u[r], ex), rtol=1e-12, atol=1e-12)
+
+
+def test_expert_closed_form_swiglu():
+    # u = 1, every gate/up weight 1 * 2^-5 over 32 inputs -> G = U = 1;
+    # down weights 1 * 2^-5 over 32 hidden -> y = SiLU(1) * 1 = 1 / (1 + e^-1).
+    D = I = 32
+    ones = O.pack_int4(np.ones((32, 32), dtype=np.int64))
+    s = np.full((32, 1), 0x3D00, dtype=np.uint16)   # 2^-5
+    ex = {"gate_packed": ones, "gate_scale": s, "up_packed": ones, "up_scale": s,
+          "down_packed": ones, "down_scale": s}
+    y = O.expert_ffn(np.ones((1, D)), ex, 16)
+    assert np.allclose(y, 1.0 / (1.0 + math.exp(-1.0)), rtol=1e-15)
+    # negative gate: SiLU(-1) * 1 = -1 / (1 + e)
+    ex["gate_packed"] = O.pack_int4(-np.ones((32, 32), dtype=np.int64))
+    y = O.expert_ffn(np.ones((1, D)), ex, 16)
+    assert np.allclose(y, -1.0 / (1.0 + math.e), rtol=1e-15)
+
+
+def test_rmsnorm_closed_form():
+    c, eps = -3.0, 1e-6
+    g = O.f32_to_bf16_bits(np.array([1.0, 0.5, 2.0, -1.0], np.float32))
+    y = O.rmsnorm(np.full((1, 4), c), g, eps)
+    base = c / math.sqrt(c * c + eps)
+    assert np.allclose(y[0], [base, 0.5 * base, 2 * base, -base], rtol=1e-15)
+    v = np.array([[3.0, -4.0]])   # mean square 12.5
+    y = O.rmsnorm(v, np.full(2, ONE, np.uint16), 0.0)
+    assert np.allclose(y, v / math.sqrt(12.5), rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# the layer
+# ----------------------------------------------------------------------------
+
+def _small_params(E=5, D=64, I=32, k=2, act_bits=16, latent=None, renorm=True):
+    experts = [_random_expert(D, I) for _ in range(E)]
+    H = latent[0].shape[1] if latent else D
+    p = O.LayerParams(k=k, renorm=renorm, act_bits=act_bits,
+                      w_router=RNG.normal(size=(E, H)) * 0.2, bias=RNG.normal(size=E) * 0.01,
+                      expert=lambda e: experts[e], E=E)
+    if latent:
+        p.lat_down, p.lat_norm, p.lat_up = latent
+    return p
+
+
+@pytest.mark.parametrize("act_bits", [16, 8])
+def test_sorted_dispatch_equals_per_token_definition(act_bits):
+    p = _small_params(E=6, k=3, act_bits=act_bits)
+    x = O.round_bf16(RNG.normal(size=(17, 64)))
+    a = O.moe_forward(x, p)
+    b = O.moe_forward_sorted(x, p)
+    assert np.allclose(a, b.out, rtol=1e-12, atol=1e-12 * np.abs(a).max())
+    # evaluating a subset of tokens gives the same rows
+    sub = O.moe_forward(x, p, tokens=[3, 11, 0])
+    assert np.allclose(sub, a[[3, 11, 0]], rtol=1e-12, atol=1e-14)
+
+
+def test_single_expert_layer_is_the_textbook_mlp():
+    p = _small_params(E=1, k=1)
+    x = O.round_bf16(RNG.normal(size=(3, 64)))
+    y = O.moe_forward(x, p)
+    for t in range(3):
+        assert np.allclose(y[t], _brute_expert(x[t], p.expert(0)), rtol=1e-12, atol=1e-12)
+
+
+def test_layer_brute_force_two_tokens():
+    p = _small_params(E=4, k=2, D=32, I=32)
+    x = O.round_bf16(RNG.normal(size=(2, 32)))
+    y = O.moe_forward(x, p)
+    idx, w = _brute_route(x, p.w_router, p.bias, 2, True)
+    for t in range(2):
+        want = np.zeros(32)
+        for j in range(2):
+            want += w[t, j] * np.array(_brute_expert(x[t], p.expert(int(idx[t, j]))))
+        assert np.allclose(y[t], want, rtol=1e-12, atol=1e-12)
+
+
+def test_renorm_off_scales_by_raw_affinities():
+    p = _small_params(E=4, k=2, renorm=False)
+    x = O.round_bf16(RNG.normal(size=(3, 64)))
+    y = O.moe_forward(x, p)
+    rt = O.route(x, p.w_router, p.bias, 2, False)
+    for t in range(3):
+        want = sum(rt.s[t, e] * O.expert_ffn(x[t:t + 1], p.expert(int(e)))[0] for e in rt.idx[t])
+        assert np.allclose(y[t], want, rtol=1e-12)
+
+
+def test_latent_identity_projections_reduce_to_rmsnorm_of_moe():
+    D = 64
+    eye = np.where(np.eye(D) > 0, ONE, 0).astype(np.uint16)
+    gain = O.f32_to_bf16_bits(RNG.uniform(0.5, 1.5, size=D).astype(np.float32))
+    p = _small_params(latent=(eye, gain, eye))
+    x = O.round_bf16(RNG.normal(size=(4, D)))
+    y = O.moe_forward(x, p)
+    p_plain = O.LayerParams(k=p.k, renorm=p.renorm, act_bits=16, w_router=p.w_router, bias=p.bias,
+                            expert=p.expert, E=p.E)
+    want = O.rmsnorm(O.moe_forward(x, p_plain), gain, p.eps)
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_latent_projection_orientation():
+    # [out, in] layout: lat_down [L, H] maps H -> L; lat_up [H, L] maps L -> H.
+    H, L = 8, 32
+    down = np.zeros((L, H), np.uint16)
+    down[np.arange(L), np.arange(L) % H] = ONE      # latent c copies x[c mod H]
+    p = _small_params(D=L, latent=(down, None, np.zeros((H, L), np.uint16)))
+    x = O.round_bf16(RNG.normal(size=(2, H)))
+    u = O.expert_input(x, p)
+    assert np.array_equal(u, x[:, np.arange(L) % H])
