@@ -1,0 +1,408 @@
+"""Benchmark of the routed int4 MoE layer (tokens/s per layer and roofline).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl reference]
+
+One step = one full layer forward (router, dispatch, experts, combine) over one
+batch of seeded synthetic tokens of the named workload, through
+``moe_layer_forward``.  Default workload: one decode step of the K2.5-shaped
+layer (T=32, H=7168, 384 experts, top-8, I=2048, int4 g32).  The expert
+weights read per step (~4.5 GB) are far larger than L2, so no L2 flush is
+needed between steps.
+
+For N > 1 (torchrun) every rank runs an independent replica of the layer on its
+own GPU (no data-path collective); value = total tokens / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the oracle is the reference of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (int4 experts, top-8) & % of HBM / tensor-core roofline"
+EXPERT_BYTES_PER_ROW_COL = 0.5 + 2.0 / 32  # int4 weight + bf16 scale per 32 columns
+
+
+def _env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def expert_bytes(w: wl.Workload) -> int:
+    """Packed int4 + bf16 scale bytes of one expert (gate, up, down)."""
+    D, I = w.D, w.I
+    return int(3 * D * I * EXPERT_BYTES_PER_ROW_COL)
+
+
+def launches_per_step(w: wl.Workload) -> int:
+    """Kernels of ours per layer forward (mirrors the C orchestration)."""
+    n = 2          # router logits + top-k
+    n += 3         # dispatch count, scan, place
+    n += 3         # expert schedule, gate/up stream, down stream
+    if w.act_bits == 8:
+        n += 1     # re-quantise h
+    n += 1         # combine (fused with RMSNorm on the latent path)
+    if w.L:
+        n += 2     # latent down and up projections
+    return n
+
+
+def _source_hash() -> str:
+    h = hashlib.sha1()
+    with open(os.path.join(ROOT, "int4_routed_expert_fp32_gb300", "csrc", "ffn_stream.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def _profiled_traffic(config: str):
+    """DRAM bytes per expert-FFN call from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = _source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == config and parts[1] == src:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [s.strip() for s in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _setup(w: wl.Workload, device):
+    import int4_routed_expert_fp32_gb300 as moe
+    x = wl.gen_x(w)
+    W, b = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    weights = {"router_w": W.to(device), "router_bias": b.to(device), **wl.gen_experts(w, device)}
+    if lat is not None:
+        weights.update({k: v.to(device) for k, v in lat.items()})
+    layer = moe.MoeLayer(w.T, w.H, w.E, w.k, w.I, weights, L=w.L, act_bits=w.act_bits,
+                         renorm=w.renorm, eps=w.eps)
+    return moe, x, layer, weights
+
+
+def _ffn_pass(moe, w, layer, weights, x_dev, steps):
+    """Average duration of the expert-FFN call (schedule + gate/up + down stream
+    kernels) inside a layer step, timed with CUDA events on its stream; the step
+    is the same work as moe_layer_forward, issued stage by stage."""
+    lib = moe.lib
+    dev = x_dev.device
+    T, k, E, D, I = w.T, w.k, w.E, w.D, w.I
+    R = T * k
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    rt, rs, inv = (torch.empty(R, dtype=torch.int32, device=dev) for _ in range(3))
+    xs = torch.empty(R, D, dtype=torch.bfloat16 if w.act_bits == 16 else torch.int8, device=dev)
+    xsc = torch.empty(R, dtype=torch.float32, device=dev) if w.act_bits == 8 else None
+    y = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    u = x_dev
+    if w.L:
+        u = moe.linear_bf16(x_dev, weights["lat_down"])
+    ws_n = max(lib.moe_route_workspace_size(T, w.H, E), lib.moe_dispatch_workspace_size(T, E, k),
+               lib.moe_expert_ffn_workspace_size(E, D, I, R, w.act_bits))
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+
+    def step(i=None):
+        assert lib.moe_route(p(x_dev), p(weights["router_w"]), p(weights["router_bias"]), T, w.H, E,
+                             k, int(w.renorm), p(idx), p(tw), p(ws), ws.numel(), s) == 0
+        assert lib.moe_dispatch(p(idx), p(u), T, D, E, k, w.act_bits, p(counts), p(offsets), p(rt),
+                                p(rs), p(inv), p(xs), p(xsc), p(ws), ws.numel(), s) == 0
+        if i is not None:
+            ev[i][0].record()
+        assert lib.moe_expert_ffn(p(xs), p(xsc), p(offsets), E, D, I, R, p(weights["gate_packed"]),
+                                  p(weights["gate_scale"]), p(weights["up_packed"]),
+                                  p(weights["up_scale"]), p(weights["down_packed"]),
+                                  p(weights["down_scale"]), w.act_bits, p(y), p(ws), ws.numel(),
+                                  s) == 0
+        if i is not None:
+            ev[i][1].record()
+        assert lib.moe_combine(p(y), p(inv), p(tw), T, D, k, p(out), s) == 0
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(i)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return statistics.mean(ms), counts.cpu().numpy()
+
+
+def _cpu_baseline(w: wl.Workload, budget_s: float = 20.0):
+    """The fp64 oracle on the host cores: per-token layer evaluation on a
+    bounded sample of tokens of the same workload."""
+    import oracle
+    from oracle import inputs as oi
+    x = wl.gen_x(w)
+    W, b = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    params = oi.layer_params(w, router=(W, b), latent=lat)
+    xf = oi.x_f64(x)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(w.T)
+    done = 0
+    t0 = time.perf_counter()
+    while done < w.T:
+        # a fresh expert cache per token: each token pays for its own experts
+        params.expert = oi.LazyExperts(w, keep=w.k)
+        oracle.moe_forward(xf, params, tokens=[int(order[done])])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {w.T} tokens of the {w.name} workload, fp64 per-token "
+                      f"definition, expert weights generated per token ({dt:.1f} s)"}
+
+
+def run_reference(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.config]
+    steps = []
+    for i in range(args.warmup + args.steps):
+        r = _cpu_baseline(w, budget_s=max(2.0, 60.0 / max(1, args.warmup + args.steps)))
+        if i >= args.warmup:
+            steps.append(r)
+    value = statistics.mean(s["value"] for s in steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * w.T / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+                   "L": w.L, "act_bits": w.act_bits},
+        "cpu_baseline": {**steps[-1], "value": value},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode", choices=list(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = _env_rank()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    w = wl.WORKLOADS[args.config]
+    from int4_routed_expert_fp32_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if dist:
+        dist.barrier()
+    moe, x, layer, weights = _setup(w, device)
+    x_dev = x.to(device)
+    out = torch.empty_like(x_dev)
+
+    for _ in range(args.warmup):
+        layer.forward(x_dev, out)
+    torch.cuda.synchronize()
+    rc = moe.check_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(rc)}")
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        layer.forward(x_dev, out)
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    rc = moe.check_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {moe.status_string(rc)}")
+    value = world * w.T / (ms / 1000.0)
+
+    # dominant kernel: the expert FFN stream kernels
+    ffn_ms, counts = _ffn_pass(moe, w, layer, weights, x_dev, min(args.steps, 100))
+    active = int((counts > 0).sum())
+    R = w.T * w.k
+    act_bytes = R * w.D * (1 if w.act_bits == 8 else 2) + 2 * R * w.I * 2 + R * w.D * 2
+    alg_bytes = active * expert_bytes(w) + act_bytes
+    flops = 2.0 * R * 3 * w.D * w.I
+    peaks = _peaks()
+    hbm_bound = w.name in ("decode", "latent")
+    if hbm_bound:
+        achieved = alg_bytes / (ffn_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = flops / (ffn_ms / 1000.0) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    roof.update({"traffic": _profiled_traffic(w.name), "kernel": "expert FFN (ffn_stream_kernel "
+                 "gate/up + down, schedule)", "kernel_ms": ffn_ms,
+                 "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
+                 "active_experts": active, "peak_source": peaks["source"]})
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    xh = x.pin_memory()
+    oh = torch.empty_like(x).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, oh)
+    torch.cuda.synchronize()
+    e_steps = min(args.steps, 100)
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(e_steps):
+        layer.forward_host(xh, oh)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / e_steps
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * w.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
+           "host_wall_ms_per_step": wall * 1000.0}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8" if w.act_bits == 8 else "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+                       "L": w.L, "act_bits": w.act_bits, "weights": "int4 g32 bf16 scales",
+                       "l2": "no flush: >4 GB of expert weights per step exceed L2"
+                             if hbm_bound or w.name == "prefill" else "working set vs L2 not checked",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step(w) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

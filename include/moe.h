@@ -1,0 +1,241 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed int4 mixture-of-experts layer.
+ *
+ * The layer is the inference forward of a routed MoE block whose experts hold
+ * PackedInt4Linear weights:
+ *   - router: sigmoid affinities of fp32 logits plus an fp32 correction bias,
+ *     top-k on the biased score, weights from the unbiased affinities divided
+ *     by their sum + 1e-20 (Kimi K2.5 donor-reference page, equations
+ *     "MoEGate.forward: logits", "Independent sigmoid scores for the router",
+ *     "Bias the choice of experts while retaining original affinities",
+ *     "Normalize the selected routing affinities");
+ *   - dispatch: counts per expert, stable sort by expert, gather of token rows
+ *     (Kimi K3 latent up-projection page, KimiSparseMoeBlock.moe_infer listing;
+ *     donor-reference equations "DeepSeek MoE.moe_infer: tokens per expert" and
+ *     "... sorted tokens"), done on the device with no host synchronisation;
+ *   - experts: down(SiLU(gate(x)) * up(x)) with int4 weights (Kimi
+ *     exact-generator adaptation page, sections "The proposed substitution",
+ *     "The preserved forward form" and "Sources & provenance"; donor-reference
+ *     equation "SwiGLU-style gated feed-forward projection");
+ *   - combine: un-permute and fp32 sum of the k expert outputs times their
+ *     routing weights (donor-reference equation "Sum the selected expert
+ *     outputs with their routing weights"; moe_infer listing);
+ *   - optional latent wrap: bf16 down-projection, RMSNorm, bf16
+ *     up-projection (KimiSparseMoeBlock.forward listing, "Latent
+ *     up-projection" section; donor-reference RMSNorm equations).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless the
+ *     name says _host.  The library never allocates device memory in these
+ *     calls; scratch space is the caller-provided workspace `ws` of
+ *     `ws_bytes` bytes (256-byte aligned), sized by the matching
+ *     *_workspace_size function.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Every tensor is
+ *     dense, row-major, with the shape given in brackets.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; they never synchronise the host, so a
+ *     sequence of calls may be captured in a CUDA graph after one warm-up
+ *     call per device (the warm-up resolves per-device symbols).
+ *   - Packed int4 weights: int32 [E, N, K/8]; column 8*i + j of row n is
+ *     nibble j (bits 4j..4j+3) of word i, a two's-complement value in
+ *     [-8, 7].  Scales: bf16 [E, N, K/32], one per output row and 32-column
+ *     group; W[n, c] = q[n, c] * scale[n, c / 32].
+ *   - act_bits = 16: bf16 activations, weights dequantised exactly, fp32
+ *     accumulation.  act_bits = 8 ("exact" mode): every int4 linear quantises
+ *     its input per row to int8 (scale = max|v| / 127, q = clamp(rint(v /
+ *     scale), -127, 127), IEEE fp32), integer products are summed exactly per
+ *     32-column weight group, y = scale_x * sum_g scale_w[n, g] * P[g] in fp32.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code.  Argument errors are
+ *     detected on the host before any launch.  Device-side problems (a
+ *     bounded wait that ran out, offsets that exceed the stated capacity) are
+ *     recorded in a per-device status word read by moe_check_error().
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID (-1)     /* null pointer, negative size, misaligned pointer */
+#define MOE_ERR_UNSUPPORTED (-2) /* shape outside the supported set (see below) */
+#define MOE_ERR_WORKSPACE (-3)   /* ws_bytes smaller than the *_workspace_size */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed */
+#define MOE_ERR_TIMEOUT (-5)     /* a device wait ran out (moe_check_error) */
+
+/* Supported shapes: widths D, H, I multiples of 64; 1 <= k <= min(E, 32);
+ * 1 <= E <= 2048; act_bits 16 or 8; T >= 0 (T = 0 is a no-op). */
+
+typedef struct moe_config {
+  int32_t T;        /* tokens */
+  int32_t H;        /* width of x and of the output */
+  int32_t E;        /* routed experts */
+  int32_t k;        /* experts per token */
+  int32_t I;        /* expert intermediate width */
+  int32_t L;        /* latent width; 0 = no latent projections (experts see H) */
+  int32_t act_bits; /* 16 or 8 */
+  int32_t renorm;   /* 1: divide the top-k affinities by their sum + 1e-20 */
+  float eps;        /* RMSNorm epsilon (latent path) */
+} moe_config;
+
+/* Weights of one layer.  D = L if L > 0 else H. */
+typedef struct moe_weights {
+  const float* router_w;       /* fp32 [E, H] */
+  const float* router_bias;    /* fp32 [E] correction bias (ranking only) */
+  const int32_t* gate_packed;  /* [E, I, D/8] */
+  const uint16_t* gate_scale;  /* bf16 [E, I, D/32] */
+  const int32_t* up_packed;    /* [E, I, D/8] */
+  const uint16_t* up_scale;    /* bf16 [E, I, D/32] */
+  const int32_t* down_packed;  /* [E, D, I/8] */
+  const uint16_t* down_scale;  /* bf16 [E, D, I/32] */
+  const uint16_t* lat_down;    /* bf16 [L, H]  (latent only) */
+  const uint16_t* lat_norm;    /* bf16 [L] RMSNorm gain, NULL = no norm (latent only) */
+  const uint16_t* lat_up;      /* bf16 [H, L]  (latent only) */
+} moe_weights;
+
+/* ---------------------------------------------------------------- router -- */
+
+/* Workspace bytes of moe_route for T tokens, width H, E experts. */
+size_t moe_route_workspace_size(int T, int H, int E);
+
+/* Router (donor-reference equations "MoEGate.forward: logits" through
+ * "Normalize the selected routing affinities").
+ *   x         bf16 [T, H]
+ *   w_router  fp32 [E, H];  bias fp32 [E]
+ *   topk_idx  int32 [T, k] out: experts by descending s + b (equal scores:
+ *             lower expert id first)
+ *   topk_w    fp32 [T, k] out: s_j / (sum_j s_j + 1e-20) if renorm, else s_j
+ * Logits are fp32 dot products of the bf16 x (exact in fp32) with w_router. */
+int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
+              int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
+              size_t ws_bytes, void* stream);
+
+/* -------------------------------------------------------------- dispatch -- */
+
+size_t moe_dispatch_workspace_size(int T, int E, int k);
+
+/* Count, stable sort and permute (moe_infer listing: one-hot counts, argsort,
+ * gather), with no host synchronisation.
+ *   topk_idx  int32 [T, k] (values in [0, E); each token lists an expert once)
+ *   x         bf16 [T, D] rows the experts see
+ *   counts    int32 [E] out: rows per expert (sum = T*k)
+ *   offsets   int32 [E+1] out: exclusive prefix of counts
+ *   row_token int32 [T*k] out: token of expert-sorted row r; rows of one
+ *             expert are in ascending token order
+ *   row_slot  int32 [T*k] out: top-k slot of row r
+ *   inv_row   int32 [T*k] out: row of (token t, slot j) at index t*k + j
+ *   x_sorted  out: bf16 [T*k, D] (act_bits 16) or int8 [T*k, D] (act_bits 8)
+ *   x_scale   fp32 [T*k] out, act_bits 8 only (may be NULL for 16) */
+int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                 int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                 int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ expert FFN -- */
+
+size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_bits);
+
+/* Gated expert MLP over expert-sorted rows (exact-generator adaptation page,
+ * "The preserved forward form"): for rows r of expert e (offsets[e] <= r <
+ * offsets[e+1]): y[r] = down_e( SiLU(gate_e(x[r])) * up_e(x[r]) ).
+ *   x_sorted  bf16 or int8 [rows_max, D] (as written by moe_dispatch)
+ *   x_scale   fp32 [rows_max] (act_bits 8 only)
+ *   offsets   int32 [E+1], offsets[E] <= rows_max (checked on the device;
+ *             a violation records MOE_ERR_INVALID and computes nothing)
+ *   weights   gate/up [E, I, D/8] + bf16 [E, I, D/32]; down [E, D, I/8] +
+ *             bf16 [E, D, I/32]
+ *   y_sorted  bf16 [rows_max, D] out (rows >= offsets[E] untouched)
+ * The intermediate h = SiLU(G) * U is computed in fp32 and stored as bf16; in
+ * act_bits 8 mode it is re-quantised per row before the down projection. */
+int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets, int E,
+                   int D, int I, int rows_max, const int32_t* gate_packed,
+                   const uint16_t* gate_scale, const int32_t* up_packed, const uint16_t* up_scale,
+                   const int32_t* down_packed, const uint16_t* down_scale, int act_bits,
+                   uint16_t* y_sorted, void* ws, size_t ws_bytes, void* stream);
+
+size_t moe_int4_linear_workspace_size(int E, int rows_max);
+
+/* One grouped PackedInt4Linear (exact-generator adaptation page, "Sources &
+ * provenance"): out[r] = x[r] W_e^T for the rows r of expert e, fp32 out.
+ *   x         bf16 or int8 [rows_max, K]; x_scale fp32 [rows_max] (act_bits 8)
+ *   w_packed  int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
+ *   out       fp32 [rows_max, N]
+ * With unit weight scales and an int8 input of scale 1 the output equals the
+ * integer accumulator sum_c q_x * q_w exactly (|sum| < 2^24). */
+int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E, int K,
+                    int N, int rows_max, const int32_t* w_packed, const uint16_t* w_scale,
+                    int act_bits, float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Per-row symmetric int8 quantisation (the act_bits 8 input step):
+ * v bf16 [R, C] -> q int8 [R, C], scale fp32 [R].  R rows, C % 64 == 0. */
+int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale, void* stream);
+
+/* --------------------------------------------------------------- combine -- */
+
+/* Un-permute and weighted sum (moe_infer listing; donor-reference "Sum the
+ * selected expert outputs with their routing weights"):
+ *   out[t] = bf16( sum_j fp32(y_sorted[inv_row[t*k + j]]) * topk_w[t*k + j] ),
+ * j ascending.  y_sorted bf16 [T*k, D], inv_row int32 [T*k], topk_w fp32
+ * [T*k], out bf16 [T, D]. */
+int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, const float* topk_w, int T,
+                int D, int k, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------- latent -- */
+
+/* y = x W^T with bf16 operands, fp32 accumulation, bf16 out ([out, in]
+ * weight layout, "Latent up-projection" section).  x [M, K], w [N, K],
+ * y [M, N]; K % 32 == 0. */
+int moe_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
+                    void* stream);
+
+/* y = bf16( x / sqrt(mean(x^2) + eps) * gain ) per row, fp32 arithmetic
+ * (donor-reference RMSNorm equations).  x, y bf16 [M, N]; gain bf16 [N]. */
+int moe_rmsnorm(const uint16_t* x, const uint16_t* gain, int M, int N, float eps, uint16_t* y,
+                void* stream);
+
+/* ----------------------------------------------------------------- layer -- */
+
+/* Workspace bytes of moe_layer_forward / moe_layer_forward_host. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* The whole layer (KimiSparseMoeBlock.forward listing without the shared
+ * expert): route on x, optional latent down-projection, dispatch, experts,
+ * combine (+ RMSNorm and up-projection when cfg->L > 0).
+ *   x bf16 [T, H] in, out bf16 [T, H] out.  All intermediates live in ws. */
+int moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
+                      uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Same, with x and out in HOST memory (pinned memory gives asynchronous
+ * copies): copies x to the device, runs the layer and copies out back, all
+ * on `stream`.  The caller synchronises the stream before reading out_host. */
+int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w, const uint16_t* x_host,
+                           uint16_t* out_host, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ status etc -- */
+
+/* Synchronises `stream`, returns and clears the current device's status word
+ * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_INVALID), or MOE_ERR_CUDA if the stream
+ * reports a CUDA error.  Test and harness use only: it blocks the host. */
+int moe_check_error(void* stream);
+
+/* Launches a kernel that waits on a barrier nothing completes, with a limit
+ * of `limit_ns` nanoseconds (1e3 .. 5e9).  When the limit runs out the kernel
+ * records MOE_ERR_TIMEOUT and returns; moe_check_error() then reports it.
+ * Exercises the bounded-wait path of the pipelined kernels. */
+int moe_wait_selftest(int64_t limit_ns, void* stream);
+
+/* Human-readable name of a status code. */
+const char* moe_status_string(int status);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,180 @@
+// Un-permute + weighted top-k combine (Kimi K3 latent up-projection page,
+// KimiSparseMoeBlock.moe_infer listing: scatter back, cast to the routing
+// weights' fp32, multiply, sum over the k slots, cast back; Kimi K2.5
+// donor-reference equation "Sum the selected expert outputs with their routing
+// weights"), optionally fused with the latent RMSNorm (donor-reference
+// equations "RMSNorm mean square ...", "Normalize by the root mean square",
+// "Apply learned per-feature RMSNorm gains").
+#include <math.h>
+
+#include "combine.cuh"
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kCbThreads = 128;
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = static_cast<uint32_t>(f32_to_bf16_bits(f[2 * i])) |
+           (static_cast<uint32_t>(f32_to_bf16_bits(f[2 * i + 1])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float tot = 0.f;
+  if (threadIdx.x < 32) {
+    tot = lane < (blockDim.x >> 5) ? red[lane] : 0.f;
+    tot = warp_sum(tot);
+    if (lane == 0) red[0] = tot;
+  }
+  __syncthreads();
+  tot = red[0];
+  __syncthreads();
+  return tot;
+}
+
+// One CTA per token.  NORM: keep the bf16-rounded combined row, then RMSNorm.
+template <bool NORM>
+__global__ void __launch_bounds__(kCbThreads) combine_kernel(
+    const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_row,
+    const float* __restrict__ w, int T, int D, int k, const uint16_t* __restrict__ gain, float eps,
+    uint16_t* __restrict__ out) {
+  extern __shared__ float rowbuf[];  // NORM: D floats
+  __shared__ int32_t rows[kMaxTopK];
+  __shared__ float wts[kMaxTopK];
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int nv = D / 8;
+  const uint4* yv = reinterpret_cast<const uint4*>(y);
+  uint4* ov = reinterpret_cast<uint4*>(out + (size_t)t * D);
+  float ss = 0.f;
+  for (int v = threadIdx.x; v < nv; v += kCbThreads) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      float f[8];
+      unpack8(yv[(size_t)r * nv + v], f);
+      const float wj = wts[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(f[i], wj, acc[i]);
+    }
+    if (!NORM) {
+      ov[v] = pack8(acc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float rb = bf16_bits_to_f32(f32_to_bf16_bits(acc[i]));  // the module's bf16 output
+        rowbuf[8 * v + i] = rb;
+        ss = fmaf(rb, rb, ss);
+      }
+    }
+  }
+  if (NORM) {
+    const float tot = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(D) + eps);
+    for (int v = threadIdx.x; v < nv; v += kCbThreads) {
+      float f[8];
+      const uint4 gv = reinterpret_cast<const uint4*>(gain)[v];
+      float gf[8];
+      unpack8(gv, gf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = rowbuf[8 * v + i] * inv * gf[i];
+      ov[v] = pack8(f);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kCbThreads) rmsnorm_kernel(const uint16_t* __restrict__ x,
+                                                             const uint16_t* __restrict__ gain,
+                                                             int D, float eps,
+                                                             uint16_t* __restrict__ out) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int nv = D / 8;
+  const uint4* xv = reinterpret_cast<const uint4*>(x + (size_t)r * D);
+  float ss = 0.f;
+  for (int v = threadIdx.x; v < nv; v += kCbThreads) {
+    float f[8];
+    unpack8(xv[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  const float tot = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(tot / static_cast<float>(D) + eps);
+  uint4* ov = reinterpret_cast<uint4*>(out + (size_t)r * D);
+  for (int v = threadIdx.x; v < nv; v += kCbThreads) {
+    float f[8], gf[8];
+    unpack8(xv[v], f);
+    unpack8(reinterpret_cast<const uint4*>(gain)[v], gf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = f[i] * inv * gf[i];
+    ov[v] = pack8(f);
+  }
+}
+
+int launch_combine(const uint16_t* y, const int32_t* inv_row, const float* w, int T, int D, int k,
+                   const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  if (gain) {
+    const size_t smem = (size_t)D * sizeof(float);
+    if (smem > 48 * 1024)
+      MOE_TRY_CUDA(cudaFuncSetAttribute(combine_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    combine_kernel<true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out);
+  } else {
+    combine_kernel<false><<<T, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
+  }
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, const float* topk_w,
+                           int T, int D, int k, uint16_t* out, void* stream) {
+  if (T < 0 || D <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (D % 64 != 0 || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_sorted || !inv_row || !topk_w || !out) return MOE_ERR_INVALID;
+  if (!aligned(y_sorted, 16) || !aligned(out, 16)) return MOE_ERR_INVALID;
+  return launch_combine(y_sorted, inv_row, topk_w, T, D, k, nullptr, 0.f, out,
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_rmsnorm(const uint16_t* x, const uint16_t* gain, int M, int N, float eps,
+                           uint16_t* y, void* stream) {
+  if (M < 0 || N <= 0 || !(eps >= 0.f)) return MOE_ERR_INVALID;
+  if (N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (M == 0) return MOE_OK;
+  if (!x || !gain || !y || !aligned(x, 16) || !aligned(gain, 16) || !aligned(y, 16))
+    return MOE_ERR_INVALID;
+  rmsnorm_kernel<<<M, kCbThreads, 0, static_cast<cudaStream_t>(stream)>>>(x, gain, N, eps, y);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}

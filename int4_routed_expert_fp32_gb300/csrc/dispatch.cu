@@ -1,0 +1,304 @@
+// Dispatch: per-expert counts, exclusive scan, stable expert-major order and
+// the gather of token rows, all on the device (Kimi K3 latent up-projection
+// page, KimiSparseMoeBlock.moe_infer listing: one-hot counts, argsort, gather;
+// Kimi K2.5 donor-reference equations "DeepSeek MoE.moe_infer: tokens per
+// expert" and "... sorted tokens").  The argsort is read as stable: the rows
+// of one expert ascend by token id.  In act_bits 8 mode each token row is
+// quantised to int8 on the way (per-row symmetric, IEEE fp32 steps).
+#include <math.h>
+
+#include "common.cuh"
+#include "dispatch.cuh"
+
+namespace moe {
+
+constexpr int kChunkTokens = 32;  // tokens per counting chunk (one warp)
+constexpr int kCountWarps = 4;
+
+// Per chunk of 32 tokens: the chunk's expert histogram hist[c, :] and, for
+// every (t, j), the number of earlier tokens of the chunk that chose the same
+// expert (its rank inside the chunk).
+__global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int k, int32_t* __restrict__ hist,
+    int32_t* __restrict__ local_rank, int* status) {
+  extern __shared__ int32_t smc[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kCountWarps + warp;
+  if (c * kChunkTokens >= T) return;
+  int32_t* cnt = smc + warp * (E + kChunkTokens * kMaxTopK);
+  int32_t* ids = cnt + E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  const int t = c * kChunkTokens + lane;
+  const bool valid = t < T;
+  for (int j = 0; j < k; ++j) {
+    int e = valid ? idx[(size_t)t * k + j] : -1;
+    if (valid && (e < 0 || e >= E)) {
+      record_status(status, MOE_ERR_INVALID);
+      e = -1;
+    }
+    ids[lane * k + j] = e;
+  }
+  __syncwarp();
+  if (valid) {
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[lane * k + j];
+      if (e < 0) continue;
+      for (int jj = 0; jj < j; ++jj)
+        if (ids[lane * k + jj] == e) record_status(status, MOE_ERR_INVALID);  // listed twice
+      int rank = 0;
+      for (int l = 0; l < lane; ++l)
+        for (int jj = 0; jj < k; ++jj) rank += (ids[l * k + jj] == e);
+      local_rank[(size_t)t * k + j] = rank;
+      atomicAdd(&cnt[e], 1);
+    }
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = cnt[e];
+}
+
+// Exclusive scan of n <= 2048 ints held in shared memory, by 1024 threads.
+__device__ void block_exclusive_scan_2048(int32_t* v, int n, int32_t* total) {
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 2 * tid;
+  const int a = i0 < n ? v[i0] : 0;
+  const int b = i0 + 1 < n ? v[i0 + 1] : 0;
+  int incl = a + b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int excl = incl - (a + b) + warp_tot[warp];
+  if (i0 < n) v[i0] = excl;
+  if (i0 + 1 < n) v[i0 + 1] = excl + a;
+  __syncthreads();
+}
+
+// Column-wise exclusive scan of hist over chunks (per expert), then the
+// exclusive scan of the expert totals.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ hist, int C,
+                                                             int E, int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[kMaxExperts];
+  __shared__ int32_t total;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    int c = 0;
+    for (; c + 4 <= C; c += 4) {
+      const int v0 = hist[(size_t)(c + 0) * E + e];
+      const int v1 = hist[(size_t)(c + 1) * E + e];
+      const int v2 = hist[(size_t)(c + 2) * E + e];
+      const int v3 = hist[(size_t)(c + 3) * E + e];
+      hist[(size_t)(c + 0) * E + e] = run;
+      hist[(size_t)(c + 1) * E + e] = run + v0;
+      hist[(size_t)(c + 2) * E + e] = run + v0 + v1;
+      hist[(size_t)(c + 3) * E + e] = run + v0 + v1 + v2;
+      run += v0 + v1 + v2 + v3;
+    }
+    for (; c < C; ++c) {
+      const int v = hist[(size_t)c * E + e];
+      hist[(size_t)c * E + e] = run;
+      run += v;
+    }
+    tot[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan_2048(tot, E, &total);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = tot[e];
+  if (threadIdx.x == 0) offsets[E] = total;
+}
+
+// Quantise the 8 values of one 16-byte bf16 vector with a row scale: IEEE
+// division, round half to even, clamp to [-127, 127]; packs 8 int8 in a uint2.
+__device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
+    const float f = bf16_bits_to_f32(bits);
+    float q = sc > 0.f ? rintf(__fdiv_rn(f, sc)) : 0.f;
+    q = fminf(fmaxf(q, -127.f), 127.f);
+    const uint32_t b = static_cast<uint32_t>(static_cast<int>(q)) & 0xffu;
+    out[i >> 2] |= b << (8 * (i & 3));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ float amax8(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[i] & 0xffffu)));
+    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[i] >> 16)));
+  }
+  return m;
+}
+
+// Row scale of one warp's row: max|v| / 127 in IEEE fp32.
+__device__ __forceinline__ float warp_row_scale(const uint4* row, int nv, int lane) {
+  float m = 0.f;
+  for (int v = lane; v < nv; v += 32) m = fmaxf(m, amax8(row[v]));
+  m = warp_max(m);
+  return __fdiv_rn(m, 127.0f);
+}
+
+// One warp per token: place its k (token, slot) pairs, then copy (or quantise
+// once and copy) the token row into each of its k expert-sorted rows.
+template <bool Q8>
+__global__ void __launch_bounds__(256) dispatch_place_kernel(
+    const int32_t* __restrict__ idx, const uint16_t* __restrict__ x, int T, int D, int E, int k,
+    const int32_t* __restrict__ hist, const int32_t* __restrict__ local_rank,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+    int32_t* __restrict__ row_slot, int32_t* __restrict__ inv_row, void* __restrict__ x_sorted,
+    float* __restrict__ x_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    const int e = idx[(size_t)t * k + lane];
+    if (e >= 0 && e < E) {
+      row = offsets[e] + hist[(size_t)(t / kChunkTokens) * E + e] + local_rank[(size_t)t * k + lane];
+      row_token[row] = t;
+      row_slot[row] = lane;
+    }
+    inv_row[(size_t)t * k + lane] = row;
+  }
+  const int nv = D / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * D);
+  if (!Q8) {
+    uint4* dst = static_cast<uint4*>(x_sorted);
+    for (int v = lane; v < nv; v += 32) {
+      const uint4 val = src[v];
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, row, j);
+        if (r >= 0) dst[(size_t)r * nv + v] = val;
+      }
+    }
+  } else {
+    const float sc = warp_row_scale(src, nv, lane);
+    uint2* dst = static_cast<uint2*>(x_sorted);
+    for (int v = lane; v < nv; v += 32) {
+      const uint2 q = quant8(src[v], sc);
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, row, j);
+        if (r >= 0) dst[(size_t)r * nv + v] = q;
+      }
+    }
+    if (lane < k && row >= 0) x_scale[row] = sc;
+  }
+}
+
+// Per-row int8 quantisation of R rows of C bf16 values (one warp per row).
+// Rows at or beyond *row_count (when given) are skipped.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ v, int R,
+                                                            int C, const int32_t* row_count,
+                                                            int8_t* __restrict__ q,
+                                                            float* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= R) return;
+  if (row_count && r >= *row_count) return;
+  const int nv = C / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(v + (size_t)r * C);
+  const float sc = warp_row_scale(src, nv, lane);
+  uint2* dst = reinterpret_cast<uint2*>(q + (size_t)r * C);
+  for (int i = lane; i < nv; i += 32) dst[i] = quant8(src[i], sc);
+  if (lane == 0) scale[r] = sc;
+}
+
+int launch_quantize_rows(const uint16_t* v, int R, int C, const int32_t* row_count, int8_t* q,
+                         float* scale, cudaStream_t s) {
+  if (R == 0) return MOE_OK;
+  quantize_rows_kernel<<<(R + 7) / 8, 256, 0, s>>>(v, R, C, row_count, q, scale);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+static size_t dispatch_chunks(int T) { return (size_t)(T + kChunkTokens - 1) / kChunkTokens; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_dispatch_workspace_size(int T, int E, int k) {
+  if (T <= 0 || E <= 0 || k <= 0) return 256;
+  return align_up(dispatch_chunks(T) * E * sizeof(int32_t), 256) +
+         align_up((size_t)T * k * sizeof(int32_t), 256);
+}
+
+extern "C" int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                            int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                            int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                            void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    MOE_TRY_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
+    MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
+    return MOE_OK;
+  }
+  if (!topk_idx || !x || !row_token || !row_slot || !inv_row || !x_sorted || !ws)
+    return MOE_ERR_INVALID;
+  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(x_sorted, 16)) return MOE_ERR_INVALID;
+  if (ws_bytes < moe_dispatch_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+
+  const int C = static_cast<int>(dispatch_chunks(T));
+  int32_t* hist = static_cast<int32_t*>(ws);
+  int32_t* local_rank = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
+                                                   align_up((size_t)C * E * sizeof(int32_t), 256));
+  const size_t smem = (size_t)kCountWarps * (E + kChunkTokens * kMaxTopK) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    MOE_TRY_CUDA(cudaFuncSetAttribute(dispatch_count_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  }
+  dispatch_count_kernel<<<(C + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
+      topk_idx, T, E, k, hist, local_rank, status);
+  MOE_LAUNCH_CHECK();
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, counts, offsets);
+  MOE_LAUNCH_CHECK();
+  if (act_bits == 16) {
+    dispatch_place_kernel<false><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
+                                                              local_rank, offsets, row_token,
+                                                              row_slot, inv_row, x_sorted, x_scale);
+  } else {
+    dispatch_place_kernel<true><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
+                                                             local_rank, offsets, row_token,
+                                                             row_slot, inv_row, x_sorted, x_scale);
+  }
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+extern "C" int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale,
+                                 void* stream) {
+  if (R < 0 || C <= 0) return MOE_ERR_INVALID;
+  if (C % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (R == 0) return MOE_OK;
+  if (!v || !q || !scale || !aligned(v, 16) || !aligned(q, 8)) return MOE_ERR_INVALID;
+  return launch_quantize_rows(v, R, C, nullptr, q, scale, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,155 @@
+// The whole routed int4 MoE layer on one stream (Kimi K3 latent up-projection
+// page, KimiSparseMoeBlock.forward listing, without the shared expert): the
+// router sees the full-width x; the latent down-projection (if any) feeds the
+// dispatch; experts; combine (+ RMSNorm and up-projection on the latent path).
+#include "combine.cuh"
+#include "common.cuh"
+
+namespace moe {
+
+struct LayerWs {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* row_slot;
+  int32_t* inv_row;
+  uint16_t* x_lat;     // [T, L] (latent)
+  void* x_sorted;      // [T*k, D] bf16 or int8
+  float* x_scale;      // [T*k] (act_bits 8)
+  uint16_t* y_sorted;  // [T*k, D]
+  uint16_t* comb;      // [T, L] (latent)
+  uint16_t* x_dev;     // [T, H] staging of the host-buffer variant
+  uint16_t* out_dev;   // [T, H]
+  void* scratch;       // shared by router, dispatch and experts (used one after another)
+  size_t scratch_bytes;
+  size_t total;
+};
+
+static size_t scratch_need(const moe_config& c) {
+  const int D = c.L > 0 ? c.L : c.H;
+  const int R = c.T * c.k;
+  size_t a = moe_route_workspace_size(c.T, c.H, c.E);
+  size_t b = moe_dispatch_workspace_size(c.T, c.E, c.k);
+  size_t f = moe_expert_ffn_workspace_size(c.E, D, c.I, R, c.act_bits);
+  size_t m = a > b ? a : b;
+  return m > f ? m : f;
+}
+
+// Carve the workspace; with base == nullptr only the total size is computed.
+static LayerWs carve(const moe_config& c, void* base) {
+  const size_t T = c.T, k = c.k, E = c.E, H = c.H;
+  const size_t L = c.L > 0 ? c.L : 0;
+  const size_t D = L ? L : H;
+  const size_t R = T * k;
+  LayerWs w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? static_cast<char*>(base) + off : nullptr;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return p;
+  };
+  w.topk_idx = static_cast<int32_t*>(take(R * 4));
+  w.topk_w = static_cast<float*>(take(R * 4));
+  w.counts = static_cast<int32_t*>(take(E * 4));
+  w.offsets = static_cast<int32_t*>(take((E + 1) * 4));
+  w.row_token = static_cast<int32_t*>(take(R * 4));
+  w.row_slot = static_cast<int32_t*>(take(R * 4));
+  w.inv_row = static_cast<int32_t*>(take(R * 4));
+  w.x_lat = L ? static_cast<uint16_t*>(take(T * L * 2)) : nullptr;
+  w.x_sorted = take(R * D * (c.act_bits == 8 ? 1 : 2));
+  w.x_scale = c.act_bits == 8 ? static_cast<float*>(take(R * 4)) : nullptr;
+  w.y_sorted = static_cast<uint16_t*>(take(R * D * 2));
+  w.comb = L ? static_cast<uint16_t*>(take(T * L * 2)) : nullptr;
+  w.x_dev = static_cast<uint16_t*>(take(T * H * 2));
+  w.out_dev = static_cast<uint16_t*>(take(T * H * 2));
+  w.scratch_bytes = scratch_need(c);
+  w.scratch = take(w.scratch_bytes);
+  w.total = off;
+  return w;
+}
+
+static int validate(const moe_config* c, const moe_weights* w) {
+  if (!c || !w) return MOE_ERR_INVALID;
+  if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->k <= 0 || c->I <= 0 || c->L < 0)
+    return MOE_ERR_INVALID;
+  if (c->H % 64 || c->I % 64 || (c->L > 0 && c->L % 64)) return MOE_ERR_UNSUPPORTED;
+  if (c->E > kMaxExperts || c->k > c->E || c->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (c->act_bits != 16 && c->act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!(c->eps >= 0.f)) return MOE_ERR_INVALID;
+  if (!w->router_w || !w->router_bias || !w->gate_packed || !w->gate_scale || !w->up_packed ||
+      !w->up_scale || !w->down_packed || !w->down_scale)
+    return MOE_ERR_INVALID;
+  if (c->L > 0 && (!w->lat_down || !w->lat_up)) return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x, uint16_t* out,
+                   const LayerWs& ws, cudaStream_t s) {
+  const int D = c.L > 0 ? c.L : c.H;
+  const int R = c.T * c.k;
+  int rc = moe_route(x, w.router_w, w.router_bias, c.T, c.H, c.E, c.k, c.renorm, ws.topk_idx,
+                     ws.topk_w, ws.scratch, ws.scratch_bytes, s);
+  if (rc) return rc;
+  const uint16_t* u = x;
+  if (c.L > 0) {
+    rc = launch_linear_bf16(x, w.lat_down, c.T, c.L, c.H, ws.x_lat, s);
+    if (rc) return rc;
+    u = ws.x_lat;
+  }
+  rc = moe_dispatch(ws.topk_idx, u, c.T, D, c.E, c.k, c.act_bits, ws.counts, ws.offsets,
+                    ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale, ws.scratch,
+                    ws.scratch_bytes, s);
+  if (rc) return rc;
+  rc = moe_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, w.gate_packed,
+                      w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,
+                      c.act_bits, ws.y_sorted, ws.scratch, ws.scratch_bytes, s);
+  if (rc) return rc;
+  if (c.L > 0) {
+    rc = launch_combine(ws.y_sorted, ws.inv_row, ws.topk_w, c.T, c.L, c.k, w.lat_norm, c.eps,
+                        ws.comb, s);
+    if (rc) return rc;
+    return launch_linear_bf16(ws.comb, w.lat_up, c.T, c.H, c.L, out, s);
+  }
+  return launch_combine(ws.y_sorted, ws.inv_row, ws.topk_w, c.T, c.H, c.k, nullptr, 0.f, out, s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_workspace_size(const moe_config* cfg) {
+  if (!cfg || cfg->T < 0 || cfg->k <= 0 || cfg->E <= 0 || cfg->H <= 0 || cfg->I <= 0) return 0;
+  return carve(*cfg, nullptr).total;
+}
+
+extern "C" int moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
+                                 uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = validate(cfg, w);
+  if (rc) return rc;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !out || !ws) return MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID;
+  const LayerWs lw = carve(*cfg, ws);
+  if (ws_bytes < lw.total) return MOE_ERR_WORKSPACE;
+  return forward(*cfg, *w, x, out, lw, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
+                                      const uint16_t* x_host, uint16_t* out_host, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  int rc = validate(cfg, w);
+  if (rc) return rc;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x_host || !out_host || !ws || !aligned(ws, 256)) return MOE_ERR_INVALID;
+  const LayerWs lw = carve(*cfg, ws);
+  if (ws_bytes < lw.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)cfg->T * cfg->H * sizeof(uint16_t);
+  MOE_TRY_CUDA(cudaMemcpyAsync(lw.x_dev, x_host, bytes, cudaMemcpyHostToDevice, s));
+  rc = forward(*cfg, *w, lw.x_dev, lw.out_dev, lw, s);
+  if (rc) return rc;
+  MOE_TRY_CUDA(cudaMemcpyAsync(out_host, lw.out_dev, bytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}

@@ -1,0 +1,190 @@
+// Router: fp32 logits of the bf16 tokens against the fp32 router weight,
+// sigmoid affinities, correction bias for ranking, warp-level top-k and
+// renormalisation (Kimi K2.5 donor-reference page, equations
+// "MoEGate.forward: logits", "Independent sigmoid scores for the router",
+// "Bias the choice of experts while retaining original affinities",
+// "MoEGate.forward: topk weight" and "Normalize the selected routing
+// affinities").  One expert group: group-limited masking is the identity.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRtTokens = 64;   // tokens per logits tile
+constexpr int kRtExperts = 64;  // experts per logits tile
+constexpr int kRtK = 32;        // K step staged in shared memory
+constexpr int kRtTargetCtas = 304;
+
+struct RouterSplit {
+  int splits;  // K slices
+  int kslice;  // elements per slice (multiple of kRtK)
+};
+
+// K is split so that small token counts still spread the weight read over
+// about two CTAs per SM; the partial sums are reduced in a fixed order.
+static RouterSplit router_split(int T, int H, int E) {
+  const int tiles = ((T + kRtTokens - 1) / kRtTokens) * ((E + kRtExperts - 1) / kRtExperts);
+  int s = (kRtTargetCtas + tiles - 1) / tiles;
+  const int max_s = H / kRtK;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  int kslice = ((H + s - 1) / s + kRtK - 1) / kRtK * kRtK;
+  RouterSplit r;
+  r.kslice = kslice;
+  r.splits = (H + kslice - 1) / kslice;
+  return r;
+}
+
+// part[z, t, e] = sum over the z-th K slice of x[t, k] * W[e, k] (fp32 FMA).
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ W, int T,
+                                                            int H, int E, int kslice,
+                                                            float* __restrict__ part) {
+  __shared__ float xs[kRtK][kRtTokens + 1];
+  __shared__ float wsm[kRtK][kRtExperts + 1];
+  const int t0 = blockIdx.x * kRtTokens;
+  const int e0 = blockIdx.y * kRtExperts;
+  const int kb = blockIdx.z * kslice;
+  const int ke = min(H, kb + kslice);
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  for (int k0 = kb; k0 < ke; k0 += kRtK) {
+    for (int i = tid; i < kRtTokens * kRtK; i += 256) {
+      const int r = i / kRtK, c = i % kRtK;
+      const int t = t0 + r, kk = k0 + c;
+      xs[c][r] = (t < T && kk < ke) ? bf16_bits_to_f32(x[(size_t)t * H + kk]) : 0.f;
+    }
+    for (int i = tid; i < kRtExperts * kRtK; i += 256) {
+      const int r = i / kRtK, c = i % kRtK;
+      const int e = e0 + r, kk = k0 + c;
+      wsm[c][r] = (e < E && kk < ke) ? W[(size_t)e * H + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < kRtK; ++c) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = xs[c][ty * 4 + i];
+        b[i] = wsm[c][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// One warp per token: reduce the K slices in order, sigmoid, bias, k rounds of
+// warp arg-max (equal scores: lower expert id), renormalise.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int S,
+                                                          const float* __restrict__ bias, int T,
+                                                          int E, int k, int renorm,
+                                                          int32_t* __restrict__ topk_idx,
+                                                          float* __restrict__ topk_w) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  float* r = sm + warp * (2 * E + kMaxTopK);
+  float* s = r + E;
+  float* sel = s + E;
+  for (int e = lane; e < E; e += 32) {
+    float z = 0.f;
+    for (int p = 0; p < S; ++p) z += part[((size_t)p * T + t) * E + e];
+    const float sg = 1.0f / (1.0f + expf(-z));
+    float rv = sg + bias[e];
+    if (rv != rv) rv = -INFINITY;  // a NaN score never wins
+    s[e] = sg;
+    r[e] = rv;
+  }
+  __syncwarp();
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = E;
+    for (int e = lane; e < E; e += 32) {
+      const float v = r[e];
+      if (v != v) continue;  // already selected
+      if (v > best || (v == best && e < bi)) {
+        best = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      topk_idx[(size_t)t * k + j] = bi;
+      sel[j] = s[bi];
+      r[bi] = __int_as_float(0x7fc00000);  // mark selected
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += sel[j];
+    const float den = sum + 1e-20f;
+    for (int j = 0; j < k; ++j) topk_w[(size_t)t * k + j] = renorm ? __fdiv_rn(sel[j], den) : sel[j];
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
+  if (T <= 0 || H <= 0 || E <= 0) return 256;
+  const RouterSplit sp = router_split(T, H, E);
+  return align_up((size_t)sp.splits * T * E * sizeof(float), 256);
+}
+
+extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
+                         int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (H % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID;
+  if (ws_bytes < moe_route_workspace_size(T, H, E)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const RouterSplit sp = router_split(T, H, E);
+  float* part = static_cast<float*>(ws);
+  dim3 grid((T + kRtTokens - 1) / kRtTokens, (E + kRtExperts - 1) / kRtExperts, sp.splits);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, T, H, E, sp.kslice, part);
+  MOE_LAUNCH_CHECK();
+  const int warps = 8;
+  const size_t smem = (size_t)warps * (2 * E + kMaxTopK) * sizeof(float);
+  if (smem > 48 * 1024) {
+    MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
+  }
+  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, s>>>(part, sp.splits, bias, T, E,
+                                                                        k, renorm, topk_idx, topk_w);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}

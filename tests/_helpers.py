@@ -1,0 +1,84 @@
+"""Shared test utilities: conditioned inputs, device weights, tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import workloads as wl
+from oracle import inputs as oi
+
+# Float tolerance of the layer output against the fp64 oracle (relative L2 and
+# max-abs as a fraction of the oracle's RMS).
+REL_L2 = 5e-3
+MAX_ABS_FRAC = 3e-2
+GAP_MIN = 1e-3
+
+
+def conditioned_attempts(w: wl.Workload, max_rounds: int = 100) -> dict:
+    """Re-draw counters that give every token a top-k gap >= GAP_MIN (oracle router).
+
+    Named workloads use the stored calibration; other shapes are conditioned here."""
+    if w.name in wl.calibration() and w.T == wl.WORKLOADS[w.name].T and w.H == wl.WORKLOADS[w.name].H \
+            and w.E == wl.WORKLOADS[w.name].E and w.k == wl.WORKLOADS[w.name].k:
+        return wl.resample_counts(w)
+    W, b = wl.gen_router(w)
+    attempts: dict = {}
+    x = wl.gen_x(w, attempts=attempts)
+    for _ in range(max_rounds):
+        rt = O.route(oi.x_f64(x), W.numpy(), b.numpy(), w.k, w.renorm)
+        bad = np.nonzero(O.topk_gap(rt.r, w.k) < GAP_MIN)[0]
+        if len(bad) == 0:
+            return attempts
+        for t in bad:
+            attempts[int(t)] = attempts.get(int(t), 0) + 1
+        x[bad] = wl.gen_x(w, tokens=bad, attempts=attempts)
+    raise RuntimeError("could not condition the router gap")
+
+
+def device_weights(w: wl.Workload, device, router=None, latent=None):
+    if router is None:
+        router = wl.gen_router(w)
+    if latent is None and w.L:
+        latent = wl.gen_latent(w)
+    W, b = router
+    out = {"router_w": W.to(device), "router_bias": b.to(device), **wl.gen_experts(w, device)}
+    if latent is not None:
+        out.update({k: v.to(device) for k, v in latent.items()})
+    return out
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_close(got, ref, rel=REL_L2, max_abs_frac=MAX_ABS_FRAC, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    e = rel_l2(got, ref)
+    rms = np.sqrt(np.mean(ref * ref))
+    mx = float(np.abs(got - ref).max()) if got.size else 0.0
+    assert e <= rel, f"{what}: relative L2 {e:.3e} > {rel:.1e}"
+    assert mx <= max_abs_frac * rms, f"{what}: max abs {mx:.3e} > {max_abs_frac:.0e} * rms {rms:.3e}"
+    return e
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return oi.bf16_bits(t)
+
+
+def random_topk(T: int, E: int, k: int, rng: np.random.Generator, hot=None) -> np.ndarray:
+    """Random valid top-k lists (distinct experts per token); ``hot`` experts
+    are preferred with the given probability weights when set."""
+    out = np.empty((T, k), dtype=np.int32)
+    p = None
+    if hot is not None:
+        p = np.asarray(hot, dtype=np.float64)
+        p = p / p.sum()
+    for t in range(T):
+        out[t] = rng.choice(E, size=k, replace=False, p=p)
+    return out

@@ -1,0 +1,94 @@
+"""The C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+symbol that include/moe.h declares, and rejects bad arguments on the host
+before any CUDA call (no compute is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from int4_routed_expert_fp32_gb300.build import build
+    build()
+    from int4_routed_expert_fp32_gb300 import capi as c
+    return c
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+                     "moe_layer_forward", "moe_workspace_size", "moe_check_error"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(capi):
+    for name in declared_functions():
+        assert hasattr(capi.lib, name), name
+        assert name in capi.SIGNATURES, f"{name} has no ctypes signature"
+    assert set(capi.SIGNATURES) == set(declared_functions())
+
+
+def test_struct_layouts_match_header(capi):
+    assert ctypes.sizeof(capi.MoeConfig) == 9 * 4
+    assert ctypes.sizeof(capi.MoeWeights) == 11 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def test_status_strings(capi):
+    assert capi.status_string(0) == "MOE_OK"
+    assert capi.status_string(-5) == "MOE_ERR_TIMEOUT"
+    assert capi.lib.moe_version().decode().startswith("int4-routed-moe")
+
+
+def test_workspace_sizes_are_host_only(capi):
+    cfg = capi.MoeConfig(32, 7168, 384, 8, 2048, 0, 16, 1, 1e-6)
+    n = capi.lib.moe_workspace_size(ctypes.byref(cfg))
+    # at least the sorted activations and expert outputs (256 rows x 7168 bf16 each)
+    assert n >= 2 * 256 * 7168 * 2
+    cfg8 = capi.MoeConfig(32, 7168, 384, 8, 2048, 0, 8, 1, 1e-6)
+    assert capi.lib.moe_workspace_size(ctypes.byref(cfg8)) > 0
+    assert capi.lib.moe_route_workspace_size(32, 7168, 384) >= 32 * 384 * 4
+    assert capi.lib.moe_expert_ffn_workspace_size(384, 7168, 2048, 256, 16) >= 256 * 2048 * 2
+
+
+def test_argument_errors_return_before_any_launch(capi):
+    L = capi.lib
+    n = None
+    # null pointers
+    assert L.moe_route(n, n, n, 4, 64, 8, 2, 1, n, n, n, 0, n) == capi.MOE_ERR_INVALID
+    # unsupported shapes
+    assert L.moe_route(n, n, n, 4, 100, 8, 2, 1, n, n, n, 0, n) == capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_route(n, n, n, 4, 64, 8, 9, 1, n, n, n, 0, n) == capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_dispatch(n, n, 4, 64, 8, 2, 12, n, n, n, n, n, n, n, n, 0, n) == capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_expert_ffn(n, n, n, 8, 96, 128, 8, n, n, n, n, n, n, 16, n, n, 0, n) == \
+        capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_expert_ffn(n, n, n, 8, 128, 128, 8, n, n, n, n, n, n, 16, n, n, 0, n) == \
+        capi.MOE_ERR_INVALID
+    assert L.moe_combine(n, n, n, 4, 64, 2, n, n) == capi.MOE_ERR_INVALID
+    assert L.moe_linear_bf16(n, n, 4, 64, 48, n, n) == capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_rmsnorm(n, n, 4, 64, -1.0, n, n) == capi.MOE_ERR_INVALID
+    assert L.moe_wait_selftest(10, n) == capi.MOE_ERR_INVALID
+    assert L.moe_layer_forward(n, n, n, n, n, 0, n) == capi.MOE_ERR_INVALID
+    cfg = capi.MoeConfig(4, 64, 8, 2, 64, 0, 16, 1, 1e-6)
+    w = capi.MoeWeights()
+    assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), n, n, n, 0, n) == capi.MOE_ERR_INVALID
+    bad = capi.MoeConfig(4, 64, 8, 2, 64, 0, 4, 1, 1e-6)
+    assert L.moe_layer_forward(ctypes.byref(bad), ctypes.byref(w), n, n, n, 0, n) == \
+        capi.MOE_ERR_UNSUPPORTED
+
+
+def test_workspace_too_small_is_reported(capi):
+    # non-null but fake pointers: the size check comes before any use
+    fake = ctypes.c_void_p(0x10000)
+    rc = capi.lib.moe_route(fake, fake, fake, 4, 64, 8, 2, 1, fake, fake, fake, 16, None)
+    assert rc == capi.MOE_ERR_WORKSPACE

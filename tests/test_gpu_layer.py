@@ -1,0 +1,115 @@
+"""Whole-layer GPU parity against the fp64 oracle, at small sizes (every token)
+and at every full workload size in the launch configuration the benchmark
+times (sampled tokens, evaluated one by one by the oracle).
+
+Tolerance (layer output, bf16): relative L2 <= 5e-3 and max abs <= 3e-2 x RMS
+of the oracle output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as wl
+from oracle import inputs as oi
+from tests._helpers import assert_close, conditioned_attempts, device_weights
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from int4_routed_expert_fp32_gb300.build import build
+    build()
+    import int4_routed_expert_fp32_gb300 as m
+    torch.cuda.set_device(DEV)
+    assert m.check_error() == 0
+    yield m
+    assert m.check_error() == 0
+
+
+def _layer(moe, w, weights):
+    return moe.MoeLayer(w.T, w.H, w.E, w.k, w.I, weights, L=w.L, act_bits=w.act_bits,
+                        renorm=w.renorm, eps=w.eps)
+
+
+SMALL = {
+    "tiny": wl.WORKLOADS["tiny"],
+    "tiny_exact": wl.workload("tiny", act_bits=8),
+    "ragged": wl.workload("tiny", name="ragged", T=77, H=512, E=40, k=6, I=192, seed=3),
+    "ragged_exact": wl.workload("tiny", name="ragged", T=77, H=512, E=40, k=6, I=192, seed=3,
+                                act_bits=8),
+    "small_latent": wl.workload("tiny", name="small_latent", T=50, H=512, L=256, E=16, k=4,
+                                I=128, seed=9, norm_gain_std=0.1),
+    "small_adversarial": wl.workload("tiny", name="small_adv", T=60, H=512, E=16, k=4, I=192,
+                                     seed=10, act_bits=8, routing="adversarial"),
+    "one_token": wl.workload("tiny", name="one", T=1, H=256, E=8, k=2, I=128, seed=12),
+    "multi_chunk": wl.workload("tiny", name="multi", T=200, H=256, E=4, k=2, I=128, seed=13),
+    "no_renorm": wl.workload("tiny", name="nr", T=40, H=256, E=24, k=3, I=64, renorm=False, seed=6),
+}
+
+
+@pytest.mark.parametrize("case", list(SMALL))
+def test_layer_small_all_tokens(moe, case):
+    w = SMALL[case]
+    x = wl.gen_x(w, attempts=conditioned_attempts(w))
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    layer = _layer(moe, w, device_weights(w, DEV, router, lat))
+    out = layer.forward(x.to(DEV))
+    assert moe.check_error() == 0
+    ref = O.moe_forward(oi.x_f64(x), oi.layer_params(w, router=router, latent=lat))
+    assert_close(out.float().cpu().numpy(), ref, what=case)
+
+
+# ----------------------------------------------------------- full sizes
+
+FULL_SAMPLE = {"decode": 8, "prefill": 4, "latent": 4, "exact": 4}
+
+
+def _sample_tokens(w, n, counts_hot=True):
+    rng = np.random.default_rng(2024)
+    toks = set(rng.choice(w.T, size=n - 1, replace=False).tolist())
+    toks.add(w.T - 1)   # the ragged end of the last chunk
+    return sorted(toks)
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "latent", "exact"])
+def test_layer_full_size_sampled(moe, name):
+    w = wl.WORKLOADS[name]
+    x = wl.gen_x(w)
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    layer = _layer(moe, w, device_weights(w, DEV, router, lat))
+    out = layer.forward(x.to(DEV))
+    assert moe.check_error() == 0
+    out = out.float().cpu().numpy()
+    assert np.all(np.isfinite(out))
+    toks = _sample_tokens(w, FULL_SAMPLE[name])
+    ref = O.moe_forward(oi.x_f64(x), oi.layer_params(w, router=router, latent=lat), tokens=toks)
+    assert_close(out[toks], ref, what=name)
+
+
+def test_layer_deterministic_and_host_variant(moe):
+    w = wl.WORKLOADS["decode"]
+    x = wl.gen_x(w)
+    layer = _layer(moe, w, device_weights(w, DEV))
+    a = layer.forward(x.to(DEV))
+    b = layer.forward(x.to(DEV))
+    assert torch.equal(a, b)
+    xh = x.pin_memory()
+    oh = torch.empty_like(x).pin_memory()
+    layer.forward_host(xh, oh)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(oh, a.cpu())
+    assert moe.check_error() == 0
+
+
+def test_layer_zero_tokens(moe):
+    w = wl.workload("tiny", T=0)
+    weights = device_weights(wl.WORKLOADS["tiny"], DEV)
+    layer = _layer(moe, w, weights)
+    out = layer.forward(torch.empty(0, w.H, dtype=torch.bfloat16, device=DEV))
+    assert out.shape == (0, w.H)
+    assert moe.check_error() == 0

@@ -1,0 +1,347 @@
+"""GPU parity of each C-ABI stage against the fp64 oracle.
+
+Integer and index results are compared bit for bit (routing sets, counts,
+offsets, permutation, int8 codes and scales, integer accumulators); float
+results within tolerances derived from their arithmetic (stated per test).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as wl
+from oracle import inputs as oi
+from tests._helpers import assert_close, bf16_bits, conditioned_attempts, random_topk, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from int4_routed_expert_fp32_gb300.build import build
+    build()
+    import int4_routed_expert_fp32_gb300 as m
+    torch.cuda.set_device(DEV)
+    assert m.check_error() == 0
+    yield m
+    assert m.check_error() == 0
+
+
+def _bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def test_generator_cpu_and_cuda_agree(moe):
+    w = wl.WORKLOADS["decode"]
+    cpu = wl.gen_expert(w, 17, "cpu")
+    gpu = wl.gen_expert(w, 17, DEV)
+    for name in cpu:
+        assert torch.equal(cpu[name], gpu[name].cpu()), name
+
+
+# --------------------------------------------------------------------- router
+
+ROUTE_CASES = {
+    "tiny": wl.WORKLOADS["tiny"],
+    "decode": wl.WORKLOADS["decode"],
+    "exact": wl.WORKLOADS["exact"],
+    "ragged": wl.workload("tiny", name="ragged", T=77, H=512, E=40, k=6, seed=3),
+    "k1": wl.workload("tiny", name="k1", T=33, H=128, E=5, k=1, seed=4),
+    "k_eq_E": wl.workload("tiny", name="kE", T=9, H=64, E=4, k=4, seed=5),
+    "no_renorm": wl.workload("tiny", name="nr", T=40, H=256, E=24, k=3, renorm=False, seed=6),
+}
+
+
+@pytest.mark.parametrize("case", list(ROUTE_CASES))
+def test_route_parity(moe, case):
+    w = ROUTE_CASES[case]
+    x = wl.gen_x(w, attempts=conditioned_attempts(w))
+    W, b = wl.gen_router(w)
+    idx, wt = moe.route(x.to(DEV), W.to(DEV), b.to(DEV), w.k, w.renorm)
+    assert moe.check_error() == 0
+    gi, gw = idx.cpu().numpy(), wt.cpu().numpy()
+    rt = O.route(oi.x_f64(x), W.numpy(), b.numpy(), w.k, w.renorm)
+    # the selected expert sets are bit-exact
+    assert np.array_equal(np.sort(gi, 1), np.sort(rt.idx, 1))
+    # each slot's weight is the oracle weight of the same expert (fp32 vs fp64)
+    for t in range(w.T):
+        ref = dict(zip(rt.idx[t].tolist(), rt.weight[t].tolist()))
+        for j in range(w.k):
+            assert abs(gw[t, j] - ref[int(gi[t, j])]) <= 2e-6 * max(1.0, abs(ref[int(gi[t, j])]))
+        # slots in descending ranking score (up to fp32 rounding of the scores)
+        r = rt.r[t, gi[t]]
+        assert np.all(np.diff(r) <= 1e-6)
+
+
+def test_route_prefill_full(moe):
+    w = wl.WORKLOADS["prefill"]
+    x = wl.gen_x(w)
+    W, b = wl.gen_router(w)
+    idx, _ = moe.route(x.to(DEV), W.to(DEV), b.to(DEV), w.k, w.renorm)
+    gi = idx.cpu().numpy()
+    rt = O.route(oi.x_f64(x), W.numpy(), b.numpy(), w.k, w.renorm)
+    assert np.array_equal(np.sort(gi, 1), np.sort(rt.idx, 1))
+    counts = np.bincount(gi.ravel(), minlength=w.E)
+    assert counts.tolist() == wl.calibration()["prefill"]["counts"]
+
+
+# ------------------------------------------------------------------- dispatch
+
+def _dispatch_case(name):
+    rng = np.random.default_rng(11)
+    if name == "random":
+        T, E, k, D = 77, 40, 6, 192
+        idx = random_topk(T, E, k, rng)
+    elif name == "adversarial":
+        T, E, k, D = 100, 32, 4, 128
+        idx = np.tile(np.array([[7, 30, 2, 11]], np.int32), (T, 1))
+    elif name == "one_token":
+        T, E, k, D = 1, 16, 3, 64
+        idx = np.array([[15, 0, 4]], np.int32)
+    elif name == "zipf_prefill":
+        T, E, k, D = 8192, 384, 8, 256
+        p = np.arange(1, E + 1, dtype=np.float64) ** -1.1
+        p[-16:] = 0
+        idx = random_topk(T, E, k, rng, hot=p)
+    else:
+        raise KeyError(name)
+    x = _bf16(rng.normal(size=(T, D)))
+    return idx, x, E
+
+
+@pytest.mark.parametrize("name", ["random", "adversarial", "one_token", "zipf_prefill"])
+@pytest.mark.parametrize("act_bits", [16, 8])
+def test_dispatch_parity(moe, name, act_bits):
+    idx, x, E = _dispatch_case(name)
+    T, k = idx.shape
+    out = moe.dispatch(torch.from_numpy(idx).to(DEV), x.to(DEV), E, act_bits)
+    assert moe.check_error() == 0
+    d = O.dispatch(idx, E)
+    got = {n: t.cpu().numpy() for n, t in out.items() if t is not None}
+    assert got["counts"].tolist() == d.counts.tolist()
+    assert got["offsets"].tolist() == d.offsets.tolist()
+    assert got["row_token"].tolist() == d.row_token.tolist()
+    assert got["row_slot"].tolist() == d.row_slot.tolist()
+    assert got["inv_row"].tolist() == d.inv_row.tolist()
+    if act_bits == 16:
+        assert np.array_equal(bf16_bits(out["x_sorted"]), bf16_bits(x)[d.row_token])
+    else:
+        q, sc = O.quantize_rows_int8(x.float().numpy())
+        assert np.array_equal(got["x_sorted"], q[d.row_token])
+        assert np.array_equal(got["x_scale"].view(np.uint32), sc[d.row_token].view(np.uint32))
+
+
+def test_quantize_rows_bit_exact(moe, golden_dir):
+    import json
+    import os
+    rng = np.random.default_rng(5)
+    v = rng.normal(size=(37, 448)) * rng.uniform(1e-3, 50, size=(37, 1))
+    v[3] = 0.0                                     # zero row
+    v[4, :] = np.round(v[4, :] * 0) + 1.0          # constant row
+    vb = _bf16(v)
+    q, s = moe.quantize_rows(vb.to(DEV))
+    qo, so = O.quantize_rows_int8(vb.float().numpy())
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    # the golden cases, padded to 64 columns with zeros
+    with open(os.path.join(golden_dir, "quantizer_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    rows = np.zeros((len(cases), 64), np.float32)
+    for i, c in enumerate(cases):
+        rows[i, :len(c["v"])] = c["v"]
+    q, s = moe.quantize_rows(_bf16(rows).to(DEV))
+    for i, c in enumerate(cases):
+        assert q[i, :len(c["q"])].cpu().tolist() == c["q"]
+        assert float(s[i]) == c["scale"]
+
+
+# ------------------------------------------------------------ int4 linear
+
+def _segments(counts):
+    off = np.zeros(len(counts) + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    return off
+
+
+def _random_int4(rng, E, N, K, lo=0.002, hi=0.01):
+    packed = rng.integers(0, 2 ** 32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    scale = O.f32_to_bf16_bits(rng.uniform(lo, hi, size=(E, N, K // 32)).astype(np.float32))
+    return packed, scale
+
+
+def _t(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(DEV)
+
+
+@pytest.mark.parametrize("K,N,counts", [
+    (320, 300, [0, 1, 33, 70, 8]),        # ragged K tail, ragged N tile, multi-chunk experts
+    (2048, 512, [5, 0, 0, 64, 2]),
+    (128, 64, [3, 3]),                    # K below one stage, N below one tile
+])
+def test_int4_linear_w4a16(moe, K, N, counts):
+    rng = np.random.default_rng(K + N)
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed, scale = _random_int4(rng, E, N, K)
+    x = _bf16(rng.normal(size=(R, K)))
+    got = moe.int4_linear(x.to(DEV), None, _t(off), _t(packed), _t(scale, torch.bfloat16), 16)
+    assert moe.check_error() == 0
+    got = got.cpu().numpy()
+    xf = oi.x_f64(x)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        ref = O.int4_linear(xf[a:b], packed[e], scale[e], 16)
+        # fp32 accumulation of exact products over K terms
+        assert rel_l2(got[a:b], ref) <= 1e-5
+
+
+@pytest.mark.parametrize("K,N,counts", [(320, 300, [0, 1, 33, 70, 8]), (7168, 256, [2, 40])])
+def test_int4_linear_exact_integer_accumulators(moe, K, N, counts):
+    """Unit scales and an int8 input of scale 1: the output is the integer sum
+    itself and must match the int64 oracle bit for bit (|sum| <= K*8*127 < 2^24)."""
+    rng = np.random.default_rng(7)
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed = rng.integers(0, 2 ** 32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    packed[:, :, :4] = np.int32(-2004318072)   # 0x88888888: every nibble -8 (extreme)
+    scale = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    q = rng.integers(-127, 128, size=(R, K)).astype(np.int8)
+    q[:, 0] = 127
+    q[:, 1:32] = -127                           # extreme products in the first group
+    xs = np.ones(R, np.float32)
+    got = moe.int4_linear(_t(q), _t(xs), _t(off), _t(packed), _t(scale, torch.bfloat16), 8)
+    assert moe.check_error() == 0
+    got = got.cpu().numpy()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        P = O.int4_group_partials(q[a:b], packed[e]).sum(axis=2)
+        assert np.array_equal(got[a:b].astype(np.int64), P)
+        assert np.all(got[a:b] == P)   # exactly integral in fp32
+
+
+def test_int4_linear_exact_mode_scaled(moe):
+    rng = np.random.default_rng(8)
+    K, N, counts = 512, 384, [9, 0, 41]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed, scale = _random_int4(rng, E, N, K)
+    x = _bf16(rng.normal(size=(R, K)) * 3)
+    q, sx = O.quantize_rows_int8(x.float().numpy())
+    got = moe.int4_linear(_t(q), _t(sx), _t(off), _t(packed), _t(scale, torch.bfloat16), 8)
+    got = got.cpu().numpy()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        ref = O.int4_linear(oi.x_f64(x)[a:b], packed[e], scale[e], 8)
+        # exact integer partials; fp32 scaling and group sum only
+        assert rel_l2(got[a:b], ref) <= 1e-6
+
+
+# ------------------------------------------------------------- expert FFN
+
+@pytest.mark.parametrize("act_bits", [16, 8])
+@pytest.mark.parametrize("D,I,counts", [
+    (320, 192, [0, 3, 40, 1, 0, 9]),
+    (256, 128, [16, 16]),
+    (1024, 512, [1, 2, 65, 0]),
+])
+def test_expert_ffn_parity(moe, act_bits, D, I, counts):
+    rng = np.random.default_rng(D + I + act_bits)
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    x = _bf16(rng.normal(size=(R, D)))
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    if act_bits == 16:
+        xin, xs = x.to(DEV), None
+    else:
+        q, s = O.quantize_rows_int8(x.float().numpy())
+        xin, xs = _t(q), _t(s)
+    y = moe.expert_ffn(xin, xs, _t(off), ex, act_bits)
+    assert moe.check_error() == 0
+    y = y.float().cpu().numpy()
+    xf = oi.x_f64(x)
+    refs, gots = [], []
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        exn = {"gate_packed": gp[e], "gate_scale": gs[e], "up_packed": up[e], "up_scale": us[e],
+               "down_packed": dp[e], "down_scale": ds[e]}
+        refs.append(O.expert_ffn(xf[a:b], exn, act_bits))
+        gots.append(y[a:b])
+    assert_close(np.concatenate(gots), np.concatenate(refs), what=f"ffn act{act_bits}")
+
+
+def test_ffn_rejects_offsets_beyond_capacity(moe):
+    rng = np.random.default_rng(1)
+    E, D, I = 2, 128, 128
+    gp, gs = _random_int4(rng, E, I, D)
+    dp, ds = _random_int4(rng, E, D, I)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16), "up_packed": _t(gp),
+          "up_scale": _t(gs, torch.bfloat16), "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    x = torch.zeros(8, D, dtype=torch.bfloat16, device=DEV)
+    bad = _t(np.array([0, 5, 3], np.int32))      # decreasing
+    moe.expert_ffn(x, None, bad, ex, 16)
+    assert moe.check_error() == moe.capi.MOE_ERR_INVALID
+    assert moe.check_error() == 0
+
+
+# ---------------------------------------------------------------- combine
+
+def test_combine_parity(moe):
+    rng = np.random.default_rng(3)
+    T, k, D = 70, 6, 448
+    R = T * k
+    y = _bf16(rng.normal(size=(R, D)))
+    inv = rng.permutation(R).astype(np.int32)
+    w = rng.uniform(0, 1, size=(T, k)).astype(np.float32)
+    out = moe.combine(y.to(DEV), _t(inv), _t(w))
+    got = out.float().cpu().numpy()
+    yf = oi.x_f64(y)
+    ref = (yf[inv].reshape(T, k, D) * w.astype(np.float64)[:, :, None]).sum(1)
+    # fp32 accumulation, one bf16 rounding of the result (2^-9 relative)
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-5)
+
+
+def test_linear_bf16_and_rmsnorm(moe):
+    rng = np.random.default_rng(4)
+    M, N, K = 100, 136, 96
+    x = _bf16(rng.normal(size=(M, K)))
+    W = _bf16(rng.normal(size=(N, K)) * 0.1)
+    y = moe.linear_bf16(x.to(DEV), W.to(DEV)).float().cpu().numpy()
+    ref = oi.x_f64(x) @ oi.x_f64(W).T
+    assert np.all(np.abs(y - ref) <= 2 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max())
+    g = _bf16(rng.uniform(0.5, 1.5, size=192))
+    v = _bf16(rng.normal(size=(33, 192)) * 4)
+    out = moe.rmsnorm(v.to(DEV), g.to(DEV), 1e-6).float().cpu().numpy()
+    ref = O.rmsnorm(oi.x_f64(v), bf16_bits(g), 1e-6)
+    assert np.all(np.abs(out - ref) <= 2 ** -8 * np.abs(ref) + 1e-6)
+
+
+# ---------------------------------------------------------- bounded waits
+
+def test_bounded_wait_reports_timeout_and_context_survives(moe):
+    moe.wait_selftest(20_000_000)   # 20 ms on a barrier that nothing completes
+    assert moe.check_error() == moe.capi.MOE_ERR_TIMEOUT
+    assert moe.check_error() == 0   # cleared
+    q, s = moe.quantize_rows(torch.ones(2, 64, dtype=torch.bfloat16, device=DEV))
+    assert float(s[0]) == float(np.float32(1.0) / np.float32(127.0))
+    assert moe.check_error() == 0

@@ -31,6 +31,7 @@ import os
 from dataclasses import dataclass, field, replace
 from typing import Dict, Optional
 
+import numpy as np
 import torch
 
 MASK32 = 0xFFFFFFFF
@@ -79,11 +80,31 @@ def stream_key(seed: int, tag: int, a: int = 0, b: int = 0) -> int:
     return k
 
 
+def _mix32_np(x: np.ndarray) -> np.ndarray:
+    """mix32 on uint32 numpy arrays (multiplication wraps modulo 2**32)."""
+    x = x ^ (x >> np.uint32(16))
+    x = x * np.uint32(0x7FEB352D)
+    x = x ^ (x >> np.uint32(15))
+    x = x * np.uint32(0x846CA68B)
+    x = x ^ (x >> np.uint32(16))
+    return x
+
+
 def words(key, start: int, count: int, device="cpu") -> torch.Tensor:
     """``count`` hashed 32-bit words of stream ``key`` from counter ``start``.
 
     ``key`` is an int (result [count]) or an int64 tensor of keys [R] (result
-    [R, count], row r being stream key[r]).  Values are int64 in [0, 2**32)."""
+    [R, count], row r being stream key[r]).  Values are int64 in [0, 2**32).
+    The CPU path evaluates the same hash with numpy uint32 arithmetic."""
+    if str(device) == "cpu" and start + count <= 2 ** 32:
+        i = np.arange(start, start + count, dtype=np.uint64).astype(np.uint32)
+        if isinstance(key, torch.Tensor):
+            i = i[None, :] ^ key.numpy().astype(np.uint32)[:, None]
+        else:
+            i = i ^ np.uint32(key)
+        with np.errstate(over="ignore"):
+            w = _mix32_np(_mix32_np(i) ^ np.uint32(0x5BD1E995))
+        return torch.from_numpy(w.astype(np.int64))
     i = torch.arange(start, start + count, dtype=torch.int64, device=device)
     if isinstance(key, torch.Tensor):
         i = i[None, :] ^ key.to(device=device, dtype=torch.int64)[:, None]
@@ -133,6 +154,8 @@ def uniform_bf16(key: int, count: int, lo: float, hi: float, start: int = 0,
 
 def as_int32(w: torch.Tensor) -> torch.Tensor:
     """Reinterpret words in [0, 2**32) as two's-complement int32."""
+    if w.device.type == "cpu":
+        return torch.from_numpy(w.numpy().astype(np.uint32).view(np.int32))
     return (w - ((w >> 31) << 32)).to(torch.int32)
 
 
@@ -321,6 +344,6 @@ def gen_latent(w: Workload):
     return {"lat_down": down, "lat_norm": g.to(torch.float32).to(torch.bfloat16), "lat_up": up}
 
 
-def workload(name: str, **overrides) -> Workload:
-    """A named workload, optionally with fields replaced (for test shapes)."""
-    return replace(WORKLOADS[name], **overrides)
+def workload(base: str, **overrides) -> Workload:
+    """Workload ``base`` with fields replaced (test shapes; ``name`` may be replaced too)."""
+    return replace(WORKLOADS[base], **overrides)
