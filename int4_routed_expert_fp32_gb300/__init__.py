@@ -1,9 +1,23 @@
 """Routed int4 mixture-of-experts layer for GB300 (sm_103a).
 
 The compute runs in ``libmoe.so`` (C ABI in ``include/moe.h``); this package is
-the Python binding.  Importing it fails when the library has not been built.
+the Python binding.  The library is loaded on first use of any binding name
+and that use raises ImportError when the library has not been built (there is
+no fallback).  ``int4_routed_expert_fp32_gb300.build`` compiles it.
 """
-from .capi import (MoeConfig, MoeError, MoeLayer, MoeWeights, check_error, combine, dispatch,  # noqa: F401
-                   expert_ffn, int4_linear, lib, linear_bf16, quantize_rows, rmsnorm, route,
-                   status_string, wait_selftest)
-from .build import LIB_PATH  # noqa: F401
+import importlib
+
+_BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "combine",
+            "dispatch", "expert_ffn", "int4_linear", "lib", "linear_bf16", "quantize_rows",
+            "rmsnorm", "route", "status_string", "wait_selftest", "capi")
+
+
+def __getattr__(name):
+    if name in _BINDING:
+        capi = importlib.import_module(".capi", __name__)
+        return capi if name == "capi" else getattr(capi, name)
+    raise AttributeError(name)
+
+
+def __dir__():
+    return sorted(list(globals()) + list(_BINDING))
