@@ -275,6 +275,11 @@ def main(argv=None):
     ap.add_argument("--config", default="decode", choices=list(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling case: replace the workload's expert count (routing uncalibrated)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling case: replace the workload's token count")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
@@ -290,6 +295,9 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=device)
 
     w = wl.WORKLOADS[args.config]
+    if args.experts or args.tokens:
+        w = wl.workload(args.config, name=f"{args.config}_small", E=args.experts or w.E,
+                        T=args.tokens or w.T)
     from int4_routed_expert_fp32_gb300.build import build
     if rank == 0 or world == 1:
         build()
@@ -355,12 +363,26 @@ def main(argv=None):
                  "active_experts": active, "peak_source": peaks["source"]})
 
     # end to end through the C ABI with host buffers (pinned), copies inside
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_pass(layer, x, w, world, dist, device, min(args.steps, 100))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(w)
+    _report(args, rank, world, w, value, ms, roof, cpu, e2e, clocks, hbm_bound)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e_pass(layer, x, w, world, dist, device, e_steps):
     xh = x.pin_memory()
     oh = torch.empty_like(x).pin_memory()
     for _ in range(3):
         layer.forward_host(xh, oh)
     torch.cuda.synchronize()
-    e_steps = min(args.steps, 100)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record()
     for _ in range(e_steps):
@@ -373,14 +395,12 @@ def main(argv=None):
         t = torch.tensor([e2e_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e = {"value": world * w.T / (e2e_ms / 1000.0), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
-           "host_wall_ms_per_step": wall * 1000.0}
+    return {"value": world * w.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
+            "host_wall_ms_per_step": wall * 1000.0}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = _cpu_baseline(w)
 
+def _report(args, rank, world, w, value, ms, roof, cpu, e2e, clocks, hbm_bound):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -399,9 +419,6 @@ def main(argv=None):
             "clocks": clocks,
         }
         print(json.dumps(line))
-    if dist:
-        dist.destroy_process_group()
-    return 0
 
 
 if __name__ == "__main__":

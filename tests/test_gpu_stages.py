@@ -118,7 +118,7 @@ def test_dispatch_parity(moe, name, act_bits):
     out = moe.dispatch(torch.from_numpy(idx).to(DEV), x.to(DEV), E, act_bits)
     assert moe.check_error() == 0
     d = O.dispatch(idx, E)
-    got = {n: t.cpu().numpy() for n, t in out.items() if t is not None}
+    got = {n: t.cpu().numpy() for n, t in out.items() if t is not None and t.dtype != torch.bfloat16}
     assert got["counts"].tolist() == d.counts.tolist()
     assert got["offsets"].tolist() == d.offsets.tolist()
     assert got["row_token"].tolist() == d.row_token.tolist()
