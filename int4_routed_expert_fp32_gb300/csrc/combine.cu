@@ -49,11 +49,23 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return tot;
 }
 
-// One CTA per token.  NORM: keep the bf16-rounded combined row, then RMSNorm.
-template <bool NORM>
+__device__ __forceinline__ void load8(const uint16_t* y, size_t row, int nv, int v, float (&f)[8]) {
+  unpack8(reinterpret_cast<const uint4*>(y)[row * nv + v], f);
+}
+
+__device__ __forceinline__ void load8(const float* y, size_t row, int nv, int v, float (&f)[8]) {
+  const float4* p = reinterpret_cast<const float4*>(y) + (row * nv + v) * 2;
+  const float4 a = p[0], b = p[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// One CTA per token.  YT: bf16 bits or fp32 expert outputs.  NORM: RMSNorm of
+// the fp32 combined row (no intermediate rounding), times the gain.
+template <typename YT, bool NORM>
 __global__ void __launch_bounds__(kCbThreads) combine_kernel(
-    const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_row,
-    const float* __restrict__ w, int T, int D, int k, const uint16_t* __restrict__ gain, float eps,
+    const YT* __restrict__ y, const int32_t* __restrict__ inv_row, const float* __restrict__ w,
+    int T, int D, int k, const uint16_t* __restrict__ gain, float eps,
     uint16_t* __restrict__ out) {
   extern __shared__ float rowbuf[];  // NORM: D floats
   __shared__ int32_t rows[kMaxTopK];
@@ -66,7 +78,6 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(
   }
   __syncthreads();
   const int nv = D / 8;
-  const uint4* yv = reinterpret_cast<const uint4*>(y);
   uint4* ov = reinterpret_cast<uint4*>(out + (size_t)t * D);
   float ss = 0.f;
   for (int v = threadIdx.x; v < nv; v += kCbThreads) {
@@ -77,7 +88,7 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(
       const int r = rows[j];
       if (r < 0) continue;
       float f[8];
-      unpack8(yv[(size_t)r * nv + v], f);
+      load8(y, static_cast<size_t>(r), nv, v, f);
       const float wj = wts[j];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(f[i], wj, acc[i]);
@@ -87,9 +98,8 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float rb = bf16_bits_to_f32(f32_to_bf16_bits(acc[i]));  // the module's bf16 output
-        rowbuf[8 * v + i] = rb;
-        ss = fmaf(rb, rb, ss);
+        rowbuf[8 * v + i] = acc[i];
+        ss = fmaf(acc[i], acc[i], ss);
       }
     }
   }
@@ -136,20 +146,28 @@ __global__ void __launch_bounds__(kCbThreads) rmsnorm_kernel(const uint16_t* __r
   }
 }
 
-int launch_combine(const uint16_t* y, const int32_t* inv_row, const float* w, int T, int D, int k,
-                   const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s) {
-  if (T == 0) return MOE_OK;
+template <typename YT>
+static int launch_combine_t(const YT* y, const int32_t* inv_row, const float* w, int T, int D,
+                            int k, const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s) {
   if (gain) {
     const size_t smem = (size_t)D * sizeof(float);
     if (smem > 48 * 1024)
-      MOE_TRY_CUDA(cudaFuncSetAttribute(combine_kernel<true>,
+      MOE_TRY_CUDA(cudaFuncSetAttribute(combine_kernel<YT, true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    combine_kernel<true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out);
+    combine_kernel<YT, true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out);
   } else {
-    combine_kernel<false><<<T, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
+    combine_kernel<YT, false><<<T, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+int launch_combine(const void* y, bool y_f32, const int32_t* inv_row, const float* w, int T, int D,
+                   int k, const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  if (y_f32)
+    return launch_combine_t(static_cast<const float*>(y), inv_row, w, T, D, k, gain, eps, out, s);
+  return launch_combine_t(static_cast<const uint16_t*>(y), inv_row, w, T, D, k, gain, eps, out, s);
 }
 
 }  // namespace moe
@@ -163,7 +181,7 @@ extern "C" int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, con
   if (T == 0) return MOE_OK;
   if (!y_sorted || !inv_row || !topk_w || !out) return MOE_ERR_INVALID;
   if (!aligned(y_sorted, 16) || !aligned(out, 16)) return MOE_ERR_INVALID;
-  return launch_combine(y_sorted, inv_row, topk_w, T, D, k, nullptr, 0.f, out,
+  return launch_combine(y_sorted, false, inv_row, topk_w, T, D, k, nullptr, 0.f, out,
                         static_cast<cudaStream_t>(stream));
 }
 

@@ -10,10 +10,13 @@
 //     matching bf16 group scales with 4-byte cp.async, and the rows of the
 //     current token chunk (<= 32 expert-sorted rows) with 1-D bulk copies,
 //     into a 4-stage shared-memory ring guarded by mbarriers;
-//   * eight consumer warps each own 32 weight rows.  A packed word is turned
-//     into eight exact bf16 integers in registers (nibble | 0x4300 magic,
-//     minus 136), fed as the A operand of m16n8k16 tensor-core MMAs against
-//     up to 4 blocks of 8 token rows; the 32-column group's fp32 partial is
+//   * eight consumer warps each own 32 weight rows.  One ldmatrix gives a
+//     lane its packed words; each word becomes four bf16x2 registers holding
+//     136 + q exactly (nibble | 0x4300 magic), the A operand of m16n8k16
+//     tensor-core MMAs against up to 2 blocks of 8 token rows.  The constant
+//     136 is removed through the accumulator: each chain starts from the MMA
+//     of a constant -136 tile with the same activations, i.e. -136 * (sum of
+//     the group's activations).  The 32-column group's fp32 partial is then
 //     multiplied by its bf16 scale and accumulated in fp32, so the
 //     dequantised weight q * scale is never rounded;
 //   * the gate/up variant holds gate and up rows of the same outputs in one
@@ -23,6 +26,7 @@
 // applied in the epilogue.
 #include <math.h>
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
 
@@ -30,18 +34,18 @@ namespace moe {
 
 constexpr int kFsKc = 256;                 // K columns per stage
 constexpr int kFsGroups = kFsKc / kGroup;  // 8 scale groups per stage
-constexpr int kFsMc = 32;                  // token rows per chunk
+constexpr int kFsMc = 16;                  // token rows per chunk
 constexpr int kFsTb = kFsMc / 8;           // token blocks of 8 (MMA N)
 constexpr int kFsCWarps = 8;               // consumer warps
 constexpr int kFsThreads = (kFsCWarps + 1) * 32;
 constexpr int kFsRows = 256;               // weight rows per stage tile
-constexpr int kFsStages = 4;
+constexpr int kFsStages = 5;
 constexpr int kFsWBytes = kFsRows * 128;   // 32 KiB of packed int4 per stage
 constexpr int kFsSBytes = kFsRows * 16;    // 8 bf16 scales per row per stage
 constexpr int kFsXStride16 = kFsKc * 2 + 64;  // bf16 row stride in shared memory
 constexpr int kFsXStride8 = kFsKc + 32;       // int8 row stride in shared memory
 constexpr int kFsXBytes = kFsMc * kFsXStride16;
-constexpr int kFsStageBytes = kFsWBytes + kFsSBytes + kFsXBytes;  // 55296 = 54 KiB
+constexpr int kFsStageBytes = kFsWBytes + kFsSBytes + kFsXBytes;  // 46080 = 45 KiB
 constexpr int kFsSmemBytes = kFsStages * kFsStageBytes + 1024 + 128;
 static_assert(kFsStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 
@@ -73,19 +77,23 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "f"(c[2]), "f"(c[3]));
 }
 
-// Eight two's-complement nibbles -> four bf16x2 exact integers:
-// out[i] = (nibble i, nibble i+4) for i = 0..3 (low half = nibble i).
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&out)[4]) {
-  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    // (nibble ^ 8) lands in the low mantissa bits of 128.0 (0x4300).
-    const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
-    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&v);
-    h = __hsub2(h, bias);
-    out[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
+__device__ __forceinline__ void ldsm_x4(const void* addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(addr)));
 }
+
+// Eight two's-complement nibbles n -> four bf16x2 holding 128 + (n ^ 8), i.e.
+// 136 + value, exactly: out[i] = (nibble i, nibble i+4), low half = nibble i.
+// The constant 136 is removed through the MMA accumulator (see kNeg136).
+__device__ __forceinline__ void dequant_magic(uint32_t w, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+}
+
+// bf16x2 (-136, -136): A operand of the MMA that forms -136 * (sum of the
+// group's activations), the start value of every weight MMA chain.
+constexpr uint32_t kNeg136 = 0xC308C308u;
 
 __device__ __forceinline__ uint32_t i8pair_bf16x2(uint32_t lo_byte_word, int lo_shift,
                                                   uint32_t hi_byte_word, int hi_shift) {
@@ -113,6 +121,130 @@ __device__ __forceinline__ void load_b_frag(const uint8_t* xrow, int G, int t, u
     b[2] = i8pair_bf16x2(v.x, 16, v.y, 16);  // (x2, x6)
     b[3] = i8pair_bf16x2(v.x, 24, v.y, 24);  // (x3, x7)
   }
+}
+
+// Per-thread constants of a consumer warp.
+struct Lane {
+  int g, t;            // MMA group id (row / token) and thread in group
+  int li;              // row of this lane's 8x8 ldmatrix tile (swizzle phase)
+  uint32_t lrow_off;   // byte offset of that row in a stage's weight tile
+  int rlo[2];          // tile row of each m16 block's upper half (scales)
+};
+
+// One K stage: up to 8 groups of 32 columns for this warp's two m16 blocks
+// and NTB blocks of 8 tokens.  FULL: all 8 groups present (no tail checks).
+template <bool Q8, int NTB, bool FULL>
+__device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S, const uint8_t* X,
+                                              int ng, const Lane& L, float (&acc)[2][NTB][4]) {
+  constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
+  uint4 sc[2][2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    sc[b][0] = *reinterpret_cast<const uint4*>(S + L.rlo[b] * 16);
+    sc[b][1] = *reinterpret_cast<const uint4*>(S + (L.rlo[b] + 8) * 16);
+  }
+  const uint32_t neg[4] = {kNeg136, kNeg136, kNeg136, kNeg136};
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int G = 0; G < kFsGroups; ++G) {
+    if (!FULL && G >= ng) break;
+    uint32_t bfr[NTB][4];
+    float corr[NTB][4];
+#pragma unroll
+    for (int tb = 0; tb < NTB; ++tb) {
+      load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr[tb]);
+      mma_bf16_16816(corr[tb], neg, bfr[tb][0], bfr[tb][1], zero);
+      mma_bf16_16816(corr[tb], neg, bfr[tb][2], bfr[tb][3], corr[tb]);
+    }
+    uint32_t wr[4];  // words of (block 0 row g, row g+8, block 1 row g, row g+8)
+    ldsm_x4(W + L.lrow_off + ((G ^ L.li) << 4), wr);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      uint32_t P[4], Q[4];
+      dequant_magic(wr[2 * b], P);
+      dequant_magic(wr[2 * b + 1], Q);
+      const uint32_t a0[4] = {P[0], Q[0], P[1], Q[1]};
+      const uint32_t a1[4] = {P[2], Q[2], P[3], Q[3]};
+      const uint32_t slo_w = (&sc[b][0].x)[G >> 1];
+      const uint32_t shi_w = (&sc[b][1].x)[G >> 1];
+      const float s_lo = __uint_as_float((G & 1) ? (slo_w & 0xffff0000u) : (slo_w << 16));
+      const float s_hi = __uint_as_float((G & 1) ? (shi_w & 0xffff0000u) : (shi_w << 16));
+#pragma unroll
+      for (int tb = 0; tb < NTB; ++tb) {
+        float c[4];
+        mma_bf16_16816(c, a0, bfr[tb][0], bfr[tb][1], corr[tb]);
+        mma_bf16_16816(c, a1, bfr[tb][2], bfr[tb][3], c);
+        acc[b][tb][0] = fmaf(s_lo, c[0], acc[b][tb][0]);
+        acc[b][tb][1] = fmaf(s_lo, c[1], acc[b][tb][1]);
+        acc[b][tb][2] = fmaf(s_hi, c[2], acc[b][tb][2]);
+        acc[b][tb][3] = fmaf(s_hi, c[3], acc[b][tb][3]);
+      }
+    }
+  }
+}
+
+// All K stages of one unit (expert chunk x row tile) for NTB token blocks,
+// then the epilogue.  Returns false when a wait gave up.
+template <int MODE, bool Q8, int NTB>
+__device__ __forceinline__ bool consume_unit(uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             uint32_t& it, int ksteps, int row0, int rows, int n0,
+                                             int cw, int lane, const Lane& L, const FsParams& p) {
+  const int K = p.K, N = p.N;
+  float acc[2][NTB][4];
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int tb = 0; tb < NTB; ++tb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[b][tb][c] = 0.f;
+
+  for (int ks = 0; ks < ksteps; ++ks, ++it) {
+    const int s = it % kFsStages;
+    const uint32_t ph = (it / kFsStages) & 1u;
+    if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return false;
+    const uint8_t* W = smem + s * kFsStageBytes;
+    const uint8_t* S = W + kFsWBytes;
+    const uint8_t* X = S + kFsSBytes;
+    const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
+    if (ng == kFsGroups)
+      stage_compute<Q8, NTB, true>(W, S, X, ng, L, acc);
+    else
+      stage_compute<Q8, NTB, false>(W, S, X, ng, L, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  const int g = L.g, t = L.t;
+#pragma unroll
+  for (int tb = 0; tb < NTB; ++tb) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tok = tb * 8 + 2 * t + (c & 1);
+      if (tok >= rows) continue;
+      const int row = row0 + tok;
+      const float xs = Q8 ? p.x_scale[row] : 1.0f;
+      if (MODE == kGateUp) {
+        const int n = n0 + 16 * cw + g + ((c & 2) ? 8 : 0);
+        if (n >= N) continue;
+        const float G = acc[0][tb][c] * xs;
+        const float U = acc[1][tb][c] * xs;
+        const float h = G / (1.0f + expf(-G)) * U;
+        static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(h);
+      } else {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int n = n0 + 32 * cw + 16 * b + g + ((c & 2) ? 8 : 0);
+          if (n >= N) continue;
+          const float y = acc[b][tb][c] * xs;
+          if (MODE == kDown)
+            static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(y);
+          else
+            static_cast<float*>(p.out)[(size_t)row * N + n] = y;
+        }
+      }
+    }
+  }
+  return true;
 }
 
 template <int MODE, bool Q8>
@@ -219,16 +351,23 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int g = lane >> 2, t = lane & 3;
-  const int cw = warp;
-  // shared-memory rows of this warp's two m16 blocks (low half of the block)
-  int rlo[2];
-  if (MODE == kGateUp) {
-    rlo[0] = 16 * cw + g;                 // gate rows
-    rlo[1] = kFsRows / 2 + 16 * cw + g;   // up rows
-  } else {
-    rlo[0] = 32 * cw + g;
-    rlo[1] = 32 * cw + 16 + g;
+  Lane L;
+  L.g = lane >> 2;
+  L.t = lane & 3;
+  L.li = lane & 7;
+  {
+    // ldmatrix: lanes 8m..8m+7 address rows of matrix m = (block m/2, half m%2)
+    const int m = lane >> 3;
+    const int b = m >> 1, h = m & 1;
+    const int base = (MODE == kGateUp) ? b * (kFsRows / 2) + 16 * warp : 32 * warp + 16 * b;
+    L.lrow_off = static_cast<uint32_t>((base + 8 * h + L.li) * 128);
+    if (MODE == kGateUp) {
+      L.rlo[0] = 16 * warp + L.g;                 // gate rows
+      L.rlo[1] = kFsRows / 2 + 16 * warp + L.g;   // up rows
+    } else {
+      L.rlo[0] = 32 * warp + L.g;
+      L.rlo[1] = 32 * warp + 16 + L.g;
+    }
   }
   uint32_t it = 0;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -236,107 +375,13 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
     const int n0 = jt * tile_n;
     const int ntb = (rows + 7) >> 3;
-    float acc[2][kFsTb][4];
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-      for (int tb = 0; tb < kFsTb; ++tb)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[b][tb][c] = 0.f;
-
-    bool ok = true;
-    for (int ks = 0; ks < ksteps; ++ks, ++it) {
-      const int s = it % kFsStages;
-      const uint32_t ph = (it / kFsStages) & 1u;
-      if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* W = smem + s * kFsStageBytes;
-      const uint8_t* S = W + kFsWBytes;
-      const uint8_t* X = S + kFsSBytes;
-      const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
-      // this stage's scales for the four rows this thread touches
-      uint4 sc[2][2];
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        sc[b][0] = *reinterpret_cast<const uint4*>(S + rlo[b] * 16);
-        sc[b][1] = *reinterpret_cast<const uint4*>(S + (rlo[b] + 8) * 16);
-      }
-#pragma unroll
-      for (int G = 0; G < kFsGroups; ++G) {
-        if (G >= ng) break;
-        uint32_t bfr[kFsTb][4];
-#pragma unroll
-        for (int tb = 0; tb < kFsTb; ++tb)
-          if (tb < ntb) load_b_frag<Q8>(X + (tb * 8 + g) * xstride, G, t, bfr[tb]);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int rl = rlo[b], rh = rlo[b] + 8;
-          const uint32_t wlo =
-              *reinterpret_cast<const uint32_t*>(W + rl * 128 + ((G ^ g) << 4) + 4 * t);
-          const uint32_t whi =
-              *reinterpret_cast<const uint32_t*>(W + rh * 128 + ((G ^ g) << 4) + 4 * t);
-          uint32_t P[4], Q[4];
-          dequant_word(wlo, P);
-          dequant_word(whi, Q);
-          const uint32_t a0[4] = {P[0], Q[0], P[1], Q[1]};
-          const uint32_t a1[4] = {P[2], Q[2], P[3], Q[3]};
-          const uint32_t slo_w = (&sc[b][0].x)[G >> 1];
-          const uint32_t shi_w = (&sc[b][1].x)[G >> 1];
-          const float s_lo = bf16_bits_to_f32((G & 1) ? (slo_w >> 16) : (slo_w & 0xffffu));
-          const float s_hi = bf16_bits_to_f32((G & 1) ? (shi_w >> 16) : (shi_w & 0xffffu));
-#pragma unroll
-          for (int tb = 0; tb < kFsTb; ++tb) {
-            if (tb < ntb) {
-              const float z[4] = {0.f, 0.f, 0.f, 0.f};
-              float c[4];
-              mma_bf16_16816(c, a0, bfr[tb][0], bfr[tb][1], z);
-              mma_bf16_16816(c, a1, bfr[tb][2], bfr[tb][3], c);
-              acc[b][tb][0] = fmaf(s_lo, c[0], acc[b][tb][0]);
-              acc[b][tb][1] = fmaf(s_lo, c[1], acc[b][tb][1]);
-              acc[b][tb][2] = fmaf(s_hi, c[2], acc[b][tb][2]);
-              acc[b][tb][3] = fmaf(s_hi, c[3], acc[b][tb][3]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
+    bool ok;
+    static_assert(kFsTb == 2, "token-block dispatch below covers 1 or 2 blocks");
+    if (ntb == 1)
+      ok = consume_unit<MODE, Q8, 1>(smem, full, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+    else
+      ok = consume_unit<MODE, Q8, 2>(smem, full, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
     if (!ok) return;
-
-    // ------------------------------------------------------------ epilogue
-#pragma unroll
-    for (int tb = 0; tb < kFsTb; ++tb) {
-      if (tb >= ntb) continue;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int tok = tb * 8 + 2 * t + (c & 1);
-        if (tok >= rows) continue;
-        const int row = row0 + tok;
-        const float xs = Q8 ? p.x_scale[row] : 1.0f;
-        if (MODE == kGateUp) {
-          const int n = n0 + 16 * cw + g + ((c & 2) ? 8 : 0);
-          if (n >= N) continue;
-          const float G = acc[0][tb][c] * xs;
-          const float U = acc[1][tb][c] * xs;
-          const float h = G / (1.0f + expf(-G)) * U;
-          static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(h);
-        } else {
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const int n = n0 + 32 * cw + 16 * b + g + ((c & 2) ? 8 : 0);
-            if (n >= N) continue;
-            const float y = acc[b][tb][c] * xs;
-            if (MODE == kDown)
-              static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(y);
-            else
-              static_cast<float*>(p.out)[(size_t)row * N + n] = y;
-          }
-        }
-      }
-    }
   }
 }
 
@@ -496,30 +541,14 @@ extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_ma
   return b;
 }
 
-extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
-                              int E, int D, int I, int rows_max, const int32_t* gate_packed,
-                              const uint16_t* gate_scale, const int32_t* up_packed,
-                              const uint16_t* up_scale, const int32_t* down_packed,
-                              const uint16_t* down_scale, int act_bits, uint16_t* y_sorted,
-                              void* ws, size_t ws_bytes, void* stream) {
-  if (E <= 0 || rows_max < 0) return MOE_ERR_INVALID;
-  if (check_width(D) || check_width(I) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
-  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
-  if (rows_max == 0) return MOE_OK;
-  if (!x_sorted || !offsets || !gate_packed || !gate_scale || !up_packed || !up_scale ||
-      !down_packed || !down_scale || !y_sorted || !ws)
-    return MOE_ERR_INVALID;
-  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
-  if (!aligned(x_sorted, 16) || !aligned(gate_packed, 16) || !aligned(up_packed, 16) ||
-      !aligned(down_packed, 16) || !aligned(gate_scale, 4) || !aligned(up_scale, 4) ||
-      !aligned(down_scale, 4))
-    return MOE_ERR_INVALID;
-  if (ws_bytes < moe_expert_ffn_workspace_size(E, D, I, rows_max, act_bits))
-    return MOE_ERR_WORKSPACE;
+int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
+                           int E, int D, int I, int rows_max, const int32_t* gate_packed,
+                           const uint16_t* gate_scale, const int32_t* up_packed,
+                           const uint16_t* up_scale, const int32_t* down_packed,
+                           const uint16_t* down_scale, int act_bits, void* y, bool y_f32, void* ws,
+                           cudaStream_t s) {
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
   Schedule sch = carve_schedule(ws, E, rows_max);
   char* b = static_cast<char*>(ws) + sch.bytes;
   uint16_t* h = reinterpret_cast<uint16_t*>(b);
@@ -566,7 +595,7 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
   pd.N = D;
   pd.scale0 = down_scale;
   pd.scale1 = nullptr;
-  pd.out = y_sorted;
+  pd.out = y;
   if (q8) {
     rc = launch_quantize_rows(h, rows_max, I, offsets + E, hq, hs, s);
     if (rc) return rc;
@@ -575,7 +604,32 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
   } else {
     pd.x = h;
   }
-  return run_stream(kDown, q8, md, md, pd, s);
+  return run_stream(y_f32 ? kLinear : kDown, q8, md, md, pd, s);
+}
+
+extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
+                              int E, int D, int I, int rows_max, const int32_t* gate_packed,
+                              const uint16_t* gate_scale, const int32_t* up_packed,
+                              const uint16_t* up_scale, const int32_t* down_packed,
+                              const uint16_t* down_scale, int act_bits, uint16_t* y_sorted,
+                              void* ws, size_t ws_bytes, void* stream) {
+  if (E <= 0 || rows_max < 0) return MOE_ERR_INVALID;
+  if (check_width(D) || check_width(I) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (rows_max == 0) return MOE_OK;
+  if (!x_sorted || !offsets || !gate_packed || !gate_scale || !up_packed || !up_scale ||
+      !down_packed || !down_scale || !y_sorted || !ws)
+    return MOE_ERR_INVALID;
+  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+  if (!aligned(x_sorted, 16) || !aligned(gate_packed, 16) || !aligned(up_packed, 16) ||
+      !aligned(down_packed, 16) || !aligned(gate_scale, 4) || !aligned(up_scale, 4) ||
+      !aligned(down_scale, 4))
+    return MOE_ERR_INVALID;
+  if (ws_bytes < moe_expert_ffn_workspace_size(E, D, I, rows_max, act_bits))
+    return MOE_ERR_WORKSPACE;
+  return launch_expert_ffn(x_sorted, x_scale, offsets, E, D, I, rows_max, gate_packed, gate_scale,
+                           up_packed, up_scale, down_packed, down_scale, act_bits, y_sorted, false,
+                           ws, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t moe_int4_linear_workspace_size(int E, int rows_max) {

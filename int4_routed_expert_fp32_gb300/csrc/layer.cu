@@ -18,7 +18,8 @@ struct LayerWs {
   uint16_t* x_lat;     // [T, L] (latent)
   void* x_sorted;      // [T*k, D] bf16 or int8
   float* x_scale;      // [T*k] (act_bits 8)
-  uint16_t* y_sorted;  // [T*k, D]
+  void* y_sorted;      // [T*k, D] bf16, or fp32 on the latent path
+  bool y_f32;
   uint16_t* comb;      // [T, L] (latent)
   uint16_t* x_dev;     // [T, H] staging of the host-buffer variant
   uint16_t* out_dev;   // [T, H]
@@ -60,7 +61,8 @@ static LayerWs carve(const moe_config& c, void* base) {
   w.x_lat = L ? static_cast<uint16_t*>(take(T * L * 2)) : nullptr;
   w.x_sorted = take(R * D * (c.act_bits == 8 ? 1 : 2));
   w.x_scale = c.act_bits == 8 ? static_cast<float*>(take(R * 4)) : nullptr;
-  w.y_sorted = static_cast<uint16_t*>(take(R * D * 2));
+  w.y_f32 = L > 0;  // keeps the expert outputs unrounded before the latent RMSNorm
+  w.y_sorted = take(R * D * (w.y_f32 ? 4 : 2));
   w.comb = L ? static_cast<uint16_t*>(take(T * L * 2)) : nullptr;
   w.x_dev = static_cast<uint16_t*>(take(T * H * 2));
   w.out_dev = static_cast<uint16_t*>(take(T * H * 2));
@@ -82,6 +84,12 @@ static int validate(const moe_config* c, const moe_weights* w) {
       !w->up_scale || !w->down_packed || !w->down_scale)
     return MOE_ERR_INVALID;
   if (c->L > 0 && (!w->lat_down || !w->lat_up)) return MOE_ERR_INVALID;
+  if (!aligned(w->gate_packed, 16) || !aligned(w->up_packed, 16) || !aligned(w->down_packed, 16) ||
+      !aligned(w->gate_scale, 4) || !aligned(w->up_scale, 4) || !aligned(w->down_scale, 4))
+    return MOE_ERR_INVALID;
+  if (c->L > 0 && (!aligned(w->lat_down, 16) || !aligned(w->lat_up, 16) ||
+                   (w->lat_norm && !aligned(w->lat_norm, 16))))
+    return MOE_ERR_INVALID;
   return MOE_OK;
 }
 
@@ -102,17 +110,18 @@ static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x,
                     ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale, ws.scratch,
                     ws.scratch_bytes, s);
   if (rc) return rc;
-  rc = moe_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, w.gate_packed,
-                      w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,
-                      c.act_bits, ws.y_sorted, ws.scratch, ws.scratch_bytes, s);
+  rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, w.gate_packed,
+                         w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,
+                         c.act_bits, ws.y_sorted, ws.y_f32, ws.scratch, s);
   if (rc) return rc;
   if (c.L > 0) {
-    rc = launch_combine(ws.y_sorted, ws.inv_row, ws.topk_w, c.T, c.L, c.k, w.lat_norm, c.eps,
-                        ws.comb, s);
+    rc = launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.L, c.k, w.lat_norm,
+                        c.eps, ws.comb, s);
     if (rc) return rc;
     return launch_linear_bf16(ws.comb, w.lat_up, c.T, c.H, c.L, out, s);
   }
-  return launch_combine(ws.y_sorted, ws.inv_row, ws.topk_w, c.T, c.H, c.k, nullptr, 0.f, out, s);
+  return launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.H, c.k, nullptr, 0.f,
+                        out, s);
 }
 
 }  // namespace moe
