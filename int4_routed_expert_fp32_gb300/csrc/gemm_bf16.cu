@@ -1,10 +1,17 @@
 // bf16 x bf16 -> fp32 -> bf16 GEMM for the latent projections, y = x W^T with
 // the [out, in] weight layout (Kimi K3 latent up-projection page, "Latent
 // up-projection"; KimiSparseMoeBlock listing: routed_expert_down_proj and
-// routed_expert_up_proj, no bias).  128x128x32 CTA tiles, 8 warps of 64x32,
-// 3-stage cp.async pipeline, ldmatrix + m16n8k16 MMAs.
+// routed_expert_up_proj, no bias).
+//
+// gemm_tc_kernel: 128 x 256 output tile per CTA on the 5th-generation tensor
+// cores: a TMA warp streams 128x64 (A) and 256x64 (B) bf16 tiles with the
+// 128-byte swizzle into a 4-stage ring, one thread issues tcgen05.mma
+// (M=128, N=256, K=16) into a 256-column TMEM accumulator, and four epilogue
+// warps read it back with tcgen05.ld and store bf16.
+// gemm_bf16_kernel (mma.sync, 128x128x32) is the check kernel of the former.
 #include "combine.cuh"
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 
@@ -123,8 +130,148 @@ __global__ void __launch_bounds__(256) gemm_bf16_kernel(const uint16_t* __restri
   }
 }
 
-int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
-                       cudaStream_t s) {
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4;
+constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KiB
+constexpr int kTcBBytes = kTcBN * kTcBK * 2;  // 32 KiB
+constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024 + 256;
+constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: epilogue
+constexpr uint32_t kTcCols = 256;
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+                   uint16_t* __restrict__ C, int M, int N, int K, int* status, long long wait_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* accf = empty + kTcStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTcCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int m0 = blockIdx.y * kTcBM, n0 = blockIdx.x * kTcBN;
+  const int ktiles = (K + kTcBK - 1) / kTcBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensor_map(&ma);
+      prefetch_tensor_map(&mb);
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const int s = kt % kTcStages;
+        const uint32_t ph = (kt / kTcStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, wait_ns, status)) break;
+        uint8_t* st = smem + s * kTcStageBytes;
+        mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+        tma_g2s_2d(st, &ma, &full[s], kt * kTcBK, m0);
+        tma_g2s_2d(st + kTcABytes, &mb, &full[s], kt * kTcBK, n0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
+      bool ok = true;
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const int s = kt % kTcStages;
+        const uint32_t ph = (kt / kTcStages) & 1u;
+        if (!mbar_wait(&full[s], ph, wait_ns, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* st = smem + s * kTcStageBytes;
+        const uint64_t da = smem_desc_sw128(st);
+        const uint64_t db = smem_desc_sw128(st + kTcABytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          umma_f16(tbase, da + 2 * kk, db + 2 * kk, idesc, (kt | kk) != 0);
+        umma_commit(&empty[s]);
+      }
+      if (ok) umma_commit(accf);
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+    const int q = warp & 3;
+    const int row = m0 + 32 * q + lane;
+    if (mbar_wait(accf, 0, wait_ns, status)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = 0; c0 < kTcBN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * q) << 16) + c0, r);
+        tmem_ld_wait();
+        const int col = n0 + c0;
+        if (row < M && col < N) {
+          uint16_t* dst = C + (size_t)row * N + col;
+          if (col + 32 <= N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w[i] = static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(r[8 * v + 2 * i]))) |
+                       (static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(r[8 * v + 2 * i + 1])))
+                        << 16);
+              d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = f32_to_bf16_bits(__uint_as_float(r[i]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTcCols);
+  }
+}
+
+static bool bf16_map(CUtensorMap* m, const uint16_t* base, int rows, int K, int box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+  const uint32_t box[2] = {static_cast<uint32_t>(kTcBK), static_cast<uint32_t>(box_rows)};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
+                     cudaStream_t s) {
+  if (M == 0) return MOE_OK;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  CUtensorMap ma, mb;
+  if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map(&mb, w, N, K, kTcBN)) return MOE_ERR_CUDA;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kTcSmem));
+  dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
+  gemm_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, status, kDefaultWaitNs);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+int launch_linear_mma(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
+                      cudaStream_t s) {
   if (M == 0) return MOE_OK;
   MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kGbSmem));
@@ -132,6 +279,11 @@ int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K
   gemm_bf16_kernel<<<grid, 256, kGbSmem, s>>>(x, w, y, M, N, K);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
+                       cudaStream_t s) {
+  return launch_linear_tc(x, w, M, N, K, y, s);
 }
 
 }  // namespace moe
