@@ -135,6 +135,30 @@ int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E
                  int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* Same as moe_dispatch, for callers that cannot provide device memory.
+ *
+ * No page has a counterpart of this call: it exists for host programs that
+ * cannot allocate device memory for a workspace -- for instance a plugin
+ * whose host owns every device allocation and hands it only its input and
+ * output buffers, or a runtime that forbids allocation once it is serving.
+ * The call allocates nothing.  Its scratch (the per-chunk expert histograms
+ * and in-chunk ranks) is one fixed 2 MiB array in the library's device data,
+ * held on every GPU that loads the library until the process exits.
+ *   Limit: ceil(T/32)*E rounded up to 64, plus T*k, must not exceed 524288
+ *   (for example T = 16384 with E = 384, k = 8); larger requests return
+ *   MOE_ERR_WORKSPACE before any launch.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls whose executions overlap on the GPU
+ *   (different streams, or several host threads) race and give wrong
+ *   results.  Nothing in the array needs to start at zero.
+ * Arguments, layouts, results and the other error codes are those of
+ * moe_dispatch. */
+int moe_dispatch_noalloc(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                         int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                         int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                         void* stream);
+
 /* ------------------------------------------------------------ expert FFN -- */
 
 size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_bits);

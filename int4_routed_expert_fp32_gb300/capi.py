@@ -51,6 +51,9 @@ SIGNATURES = {
     "moe_dispatch": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_size_t, c_void_p]),
+    "moe_dispatch_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p]),
     "moe_expert_ffn_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "moe_expert_ffn": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
@@ -155,6 +158,32 @@ def dispatch(topk_idx: torch.Tensor, x: torch.Tensor, E: int, act_bits: int = 16
         _p(topk_idx), _p(x), T, D, E, k, act_bits, _p(out["counts"]), _p(out["offsets"]),
         _p(out["row_token"]), _p(out["row_slot"]), _p(out["inv_row"]), _p(out["x_sorted"]),
         _p(out["x_scale"]), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def dispatch_noalloc(topk_idx: torch.Tensor, x: torch.Tensor, E: int,
+                     act_bits: int = 16) -> Dict[str, torch.Tensor]:
+    """moe_dispatch without a workspace: the library's fixed device scratch is
+    used instead (for callers that cannot allocate device memory; calls must
+    not overlap on the GPU)."""
+    _dev(topk_idx, torch.int32); _dev(x, torch.bfloat16)
+    T, k = topk_idx.shape
+    D = x.shape[1]
+    dev = x.device
+    R = T * k
+    out = {
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "row_token": torch.empty(R, dtype=torch.int32, device=dev),
+        "row_slot": torch.empty(R, dtype=torch.int32, device=dev),
+        "inv_row": torch.empty(R, dtype=torch.int32, device=dev),
+        "x_sorted": torch.empty(R, D, dtype=torch.bfloat16 if act_bits == 16 else torch.int8, device=dev),
+        "x_scale": torch.empty(R, dtype=torch.float32, device=dev) if act_bits == 8 else None,
+    }
+    _check("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
+        _p(topk_idx), _p(x), T, D, E, k, act_bits, _p(out["counts"]), _p(out["offsets"]),
+        _p(out["row_token"]), _p(out["row_slot"]), _p(out["inv_row"]), _p(out["x_sorted"]),
+        _p(out["x_scale"]), _stream()))
     return out
 
 

@@ -7,6 +7,8 @@
 // quantised to int8 on the way (per-row symmetric, IEEE fp32 steps).
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "dispatch.cuh"
 
@@ -235,6 +237,30 @@ int launch_quantize_rows(const uint16_t* v, int R, int C, const int32_t* row_cou
 
 static size_t dispatch_chunks(int T) { return (size_t)(T + kChunkTokens - 1) / kChunkTokens; }
 
+// Scratch of moe_dispatch_noalloc: the per-chunk expert histograms followed by
+// the in-chunk ranks.  Every GPU that loads the library holds these 2 MiB
+// until the process exits.  Host code must not use the symbol as a device
+// address; noalloc_scratch() resolves the address per device.
+constexpr size_t kNoAllocScratchInts = 512 * 1024;
+static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchInts];
+
+static std::mutex g_noalloc_mu;
+static int32_t* g_noalloc_ptr[64] = {};
+
+// Device address of g_dispatch_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static int32_t* noalloc_scratch() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return nullptr;
+    g_noalloc_ptr[d] = static_cast<int32_t*>(p);
+  }
+  return g_noalloc_ptr[d];
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -301,4 +327,56 @@ extern "C" int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, flo
   if (R == 0) return MOE_OK;
   if (!v || !q || !scale || !aligned(v, 16) || !aligned(q, 8)) return MOE_ERR_INVALID;
   return launch_quantize_rows(v, R, C, nullptr, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_dispatch_noalloc(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E,
+                                    int k, int act_bits, int32_t* counts, int32_t* offsets,
+                                    int32_t* row_token, int32_t* row_slot, int32_t* inv_row,
+                                    void* x_sorted, float* x_scale, void* stream) {
+  if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID;
+  if (T > 0) {
+    if (!topk_idx || !x || !row_token || !row_slot || !inv_row || !x_sorted) return MOE_ERR_INVALID;
+    if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(x_sorted, 16)) return MOE_ERR_INVALID;
+  }
+  const size_t C = dispatch_chunks(T);
+  const size_t hist_ints = align_up(C * E * sizeof(int32_t), 256) / sizeof(int32_t);
+  if (hist_ints + (size_t)T * k > kNoAllocScratchInts) return MOE_ERR_WORKSPACE;
+  int32_t* scratch = noalloc_scratch();
+  if (!scratch) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    MOE_TRY_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
+    MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
+    return MOE_OK;
+  }
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  int32_t* hist = scratch;
+  int32_t* local_rank = scratch + hist_ints;
+  const int Ci = static_cast<int>(C);
+  const size_t smem = (size_t)kCountWarps * (E + kChunkTokens * kMaxTopK) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    MOE_TRY_CUDA(cudaFuncSetAttribute(dispatch_count_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  }
+  dispatch_count_kernel<<<(Ci + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
+      topk_idx, T, E, k, hist, local_rank, status);
+  MOE_LAUNCH_CHECK();
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, Ci, E, counts, offsets);
+  MOE_LAUNCH_CHECK();
+  if (act_bits == 16) {
+    dispatch_place_kernel<false><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
+                                                              local_rank, offsets, row_token,
+                                                              row_slot, inv_row, x_sorted, x_scale);
+  } else {
+    dispatch_place_kernel<true><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
+                                                             local_rank, offsets, row_token,
+                                                             row_slot, inv_row, x_sorted, x_scale);
+  }
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }
