@@ -13,13 +13,19 @@ int launch_combine(const void* y, bool y_f32, const int32_t* inv_row, const floa
                    int k, const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s);
 
 // Gated expert MLP over expert-sorted rows (validated arguments); y is bf16
-// [rows_max, D] or, with y_f32, fp32.
+// [rows_max, D] or, with y_f32, fp32.  No expert has more than
+// max_rows_per_expert rows (the token count when called from the layer).
 int launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets, int E,
-                      int D, int I, int rows_max, const int32_t* gate_packed,
+                      int D, int I, int rows_max, int max_rows_per_expert,
+                      const int32_t* gate_packed,
                       const uint16_t* gate_scale, const int32_t* up_packed,
                       const uint16_t* up_scale, const int32_t* down_packed,
                       const uint16_t* down_scale, int act_bits, void* y, bool y_f32, void* ws,
                       cudaStream_t s);
+
+// y[M, N] = x[M, K] w[N, K]^T, bf16 operands, fp32 output (tcgen05).
+int launch_linear_tc_f32(const uint16_t* x, const uint16_t* w, int M, int N, int K, float* y,
+                         cudaStream_t s);
 
 // y[M, N] = x[M, K] w[N, K]^T in bf16 with fp32 accumulation.
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,

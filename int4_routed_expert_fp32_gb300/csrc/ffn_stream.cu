@@ -6,21 +6,24 @@
 //
 // Design (one persistent CTA per SM):
 //   * a producer warp streams, per K step of 256 columns, a 256-row tile of
-//     packed int4 weights with one 3-D TMA copy (128-byte swizzle), the
-//     matching bf16 group scales with 4-byte cp.async, and the rows of the
-//     current token chunk (<= 32 expert-sorted rows) with 1-D bulk copies,
-//     into a 4-stage shared-memory ring guarded by mbarriers;
-//   * eight consumer warps each own 32 weight rows.  One ldmatrix gives a
-//     lane its packed words; each word becomes four bf16x2 registers holding
-//     136 + q exactly (nibble | 0x4300 magic), the A operand of m16n8k16
-//     tensor-core MMAs against up to 2 blocks of 8 token rows.  The constant
-//     136 is removed through the accumulator: each chain starts from the MMA
-//     of a constant -136 tile with the same activations, i.e. -136 * (sum of
-//     the group's activations).  The 32-column group's fp32 partial is then
-//     multiplied by its bf16 scale and accumulated in fp32, so the
-//     dequantised weight q * scale is never rounded;
-//   * the gate/up variant holds gate and up rows of the same outputs in one
-//     warp and writes h = SiLU(G) * U (bf16); the down variant writes y.
+//     packed int4 weights and the matching bf16 group scales with 3-D TMA
+//     copies (128-byte swizzle for the weights), and the rows of the current
+//     token chunk (<= 16 expert-sorted rows) with 1-D bulk copies, into a
+//     4-stage shared-memory ring guarded by mbarriers.  When K is not a
+//     multiple of 256 the scale rows are not 16-byte aligned and the scales
+//     go through 4-byte cp.async instead;
+//   * sixteen consumer warps each own one 16-row block.  One ldmatrix gives a
+//     lane its packed words of two groups; each word becomes four bf16x2
+//     registers holding 136 + q exactly (nibble | 0x4300 magic), the A
+//     operand of m16n8k16 tensor-core MMAs against up to 2 blocks of 8 token
+//     rows.  The constant 136 is removed through the accumulator: each chain
+//     starts from the MMA of a constant -136 tile with the same activations,
+//     i.e. -136 * (sum of the group's activations).  The 32-column group's
+//     fp32 partial is then multiplied by its bf16 scale and accumulated in
+//     fp32, so the dequantised weight q * scale is never rounded;
+//   * in the gate/up variant warps 0-7 hold gate rows and warps 8-15 the up
+//     rows of the same outputs; the up partials go through shared memory and
+//     the gate warps write h = SiLU(G) * U (bf16).  The down variant writes y.
 // act_bits 8: the int8 activations become exact bf16 integers, the group
 // partials are exact integers (|P| <= 32*8*127 < 2^24) and the row scale is
 // applied in the epilogue.
@@ -29,6 +32,7 @@
 #include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
+#include "ffn_tc.cuh"
 
 namespace moe {
 
@@ -36,18 +40,24 @@ constexpr int kFsKc = 256;                 // K columns per stage
 constexpr int kFsGroups = kFsKc / kGroup;  // 8 scale groups per stage
 constexpr int kFsMc = 16;                  // token rows per chunk
 constexpr int kFsTb = kFsMc / 8;           // token blocks of 8 (MMA N)
-constexpr int kFsCWarps = 8;               // consumer warps
+#ifndef FS_CWARPS
+#define FS_CWARPS 16
+#endif
+constexpr int kFsCWarps = FS_CWARPS;       // consumer warps, one 16-row block each
 constexpr int kFsThreads = (kFsCWarps + 1) * 32;
-constexpr int kFsRows = 256;               // weight rows per stage tile
-constexpr int kFsStages = 5;
+constexpr int kFsRows = 16 * kFsCWarps;    // weight rows per stage tile
+constexpr int kFsStages = (FS_CWARPS <= 12) ? 5 : 4;
 constexpr int kFsWBytes = kFsRows * 128;   // 32 KiB of packed int4 per stage
 constexpr int kFsSBytes = kFsRows * 16;    // 8 bf16 scales per row per stage
 constexpr int kFsXStride16 = kFsKc * 2 + 64;  // bf16 row stride in shared memory
 constexpr int kFsXStride8 = kFsKc + 32;       // int8 row stride in shared memory
 constexpr int kFsXBytes = kFsMc * kFsXStride16;
-constexpr int kFsStageBytes = kFsWBytes + kFsSBytes + kFsXBytes;  // 46080 = 45 KiB
-constexpr int kFsSmemBytes = kFsStages * kFsStageBytes + 1024 + 128;
+constexpr int kFsStageBytes =
+    (kFsWBytes + kFsSBytes + kFsXBytes + 1023) / 1024 * 1024;  // keeps 1024-byte alignment
+constexpr int kFsXchBytes = (kFsRows / 2) * kFsMc * 4;          // up partials of one unit
+constexpr int kFsSmemBytes = kFsStages * kFsStageBytes + 2 * kFsXchBytes + 1024 + 256;
 static_assert(kFsStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(kFsTb == 2, "token-block dispatch covers 1 or 2 blocks");
 
 enum FsMode { kGateUp = 0, kDown = 1, kLinear = 2 };
 
@@ -65,6 +75,12 @@ struct FsParams {
   long long wait_ns;
   int K;
   int N;
+  int tma_scales;         // 1: scales by TMA (K % 256 == 0), 0: 4-byte cp.async
+};
+
+struct FsMaps {
+  CUtensorMap w0, w1;     // packed weights (gate/up, or the single matrix twice)
+  CUtensorMap s0, s1;     // scales (used when tma_scales)
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -127,141 +143,169 @@ __device__ __forceinline__ void load_b_frag(const uint8_t* xrow, int G, int t, u
 struct Lane {
   int g, t;            // MMA group id (row / token) and thread in group
   int li;              // row of this lane's 8x8 ldmatrix tile (swizzle phase)
+  int gsel;            // which of the two groups this lane's ldmatrix tile holds
   uint32_t lrow_off;   // byte offset of that row in a stage's weight tile
-  int rlo[2];          // tile row of each m16 block's upper half (scales)
+  int rlo;             // tile row of the block's upper half (scales)
 };
 
-// One K stage: up to 8 groups of 32 columns for this warp's two m16 blocks
-// and NTB blocks of 8 tokens.  FULL: all 8 groups present (no tail checks).
+// One K stage: up to 8 groups of 32 columns for this warp's 16-row block and
+// NTB blocks of 8 tokens.  FULL: all 8 groups present (no tail checks).
 template <bool Q8, int NTB, bool FULL>
 __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S, const uint8_t* X,
-                                              int ng, const Lane& L, float (&acc)[2][NTB][4]) {
+                                              int ng, const Lane& L, float (&acc)[NTB][4]) {
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
-  uint4 sc[2][2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    sc[b][0] = *reinterpret_cast<const uint4*>(S + L.rlo[b] * 16);
-    sc[b][1] = *reinterpret_cast<const uint4*>(S + (L.rlo[b] + 8) * 16);
-  }
   const uint32_t neg[4] = {kNeg136, kNeg136, kNeg136, kNeg136};
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t* s_lo_row = reinterpret_cast<const uint32_t*>(S + L.rlo * 16);
+  const uint32_t* s_hi_row = reinterpret_cast<const uint32_t*>(S + (L.rlo + 8) * 16);
+  // two token blocks keep more values live: unroll less there
+#pragma unroll(NTB == 1 ? 4 : 1)
+  for (int G2 = 0; G2 < kFsGroups; G2 += 2) {
+    if (!FULL && G2 >= ng) break;
+    uint32_t wr[4];  // (row g, row g+8) words of groups G2 and G2+1
+    ldsm_x4(W + L.lrow_off + (((G2 + L.gsel) ^ L.li) << 4), wr);
+    const uint32_t slo_w = s_lo_row[G2 >> 1];  // bf16 scales of groups G2 (low) and G2+1
+    const uint32_t shi_w = s_hi_row[G2 >> 1];
 #pragma unroll
-  for (int G = 0; G < kFsGroups; ++G) {
-    if (!FULL && G >= ng) break;
-    uint32_t bfr[NTB][4];
-    float corr[NTB][4];
+    for (int gg = 0; gg < 2; ++gg) {
+      const int G = G2 + gg;
+      uint32_t bfr[NTB][4];
+      float corr[NTB][4];
 #pragma unroll
-    for (int tb = 0; tb < NTB; ++tb) {
-      load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr[tb]);
-      mma_bf16_16816(corr[tb], neg, bfr[tb][0], bfr[tb][1], zero);
-      mma_bf16_16816(corr[tb], neg, bfr[tb][2], bfr[tb][3], corr[tb]);
-    }
-    uint32_t wr[4];  // words of (block 0 row g, row g+8, block 1 row g, row g+8)
-    ldsm_x4(W + L.lrow_off + ((G ^ L.li) << 4), wr);
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
+      for (int tb = 0; tb < NTB; ++tb) {
+        load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr[tb]);
+        mma_bf16_16816(corr[tb], neg, bfr[tb][0], bfr[tb][1], zero);
+        mma_bf16_16816(corr[tb], neg, bfr[tb][2], bfr[tb][3], corr[tb]);
+      }
       uint32_t P[4], Q[4];
-      dequant_magic(wr[2 * b], P);
-      dequant_magic(wr[2 * b + 1], Q);
+      dequant_magic(wr[2 * gg], P);
+      dequant_magic(wr[2 * gg + 1], Q);
       const uint32_t a0[4] = {P[0], Q[0], P[1], Q[1]};
       const uint32_t a1[4] = {P[2], Q[2], P[3], Q[3]};
-      const uint32_t slo_w = (&sc[b][0].x)[G >> 1];
-      const uint32_t shi_w = (&sc[b][1].x)[G >> 1];
-      const float s_lo = __uint_as_float((G & 1) ? (slo_w & 0xffff0000u) : (slo_w << 16));
-      const float s_hi = __uint_as_float((G & 1) ? (shi_w & 0xffff0000u) : (shi_w << 16));
+      const float s_lo = __uint_as_float(gg ? (slo_w & 0xffff0000u) : (slo_w << 16));
+      const float s_hi = __uint_as_float(gg ? (shi_w & 0xffff0000u) : (shi_w << 16));
 #pragma unroll
       for (int tb = 0; tb < NTB; ++tb) {
         float c[4];
         mma_bf16_16816(c, a0, bfr[tb][0], bfr[tb][1], corr[tb]);
         mma_bf16_16816(c, a1, bfr[tb][2], bfr[tb][3], c);
-        acc[b][tb][0] = fmaf(s_lo, c[0], acc[b][tb][0]);
-        acc[b][tb][1] = fmaf(s_lo, c[1], acc[b][tb][1]);
-        acc[b][tb][2] = fmaf(s_hi, c[2], acc[b][tb][2]);
-        acc[b][tb][3] = fmaf(s_hi, c[3], acc[b][tb][3]);
+        acc[tb][0] = fmaf(s_lo, c[0], acc[tb][0]);
+        acc[tb][1] = fmaf(s_lo, c[1], acc[tb][1]);
+        acc[tb][2] = fmaf(s_hi, c[2], acc[tb][2]);
+        acc[tb][3] = fmaf(s_hi, c[3], acc[tb][3]);
       }
     }
   }
+}
+
+__device__ __forceinline__ void consumer_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFsCWarps * 32) : "memory");
 }
 
 // All K stages of one unit (expert chunk x row tile) for NTB token blocks,
 // then the epilogue.  Returns false when a wait gave up.
 template <int MODE, bool Q8, int NTB>
-__device__ __forceinline__ bool consume_unit(uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                             uint32_t& it, int ksteps, int row0, int rows, int n0,
-                                             int cw, int lane, const Lane& L, const FsParams& p) {
+__device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t* full,
+                                             uint64_t* empty, uint32_t& it, int ksteps, int row0,
+                                             int rows, int n0, int cw, int lane, const Lane& L,
+                                             const FsParams& p) {
   const int K = p.K, N = p.N;
-  float acc[2][NTB][4];
+  float acc[NTB][4];
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
+  for (int tb = 0; tb < NTB; ++tb)
 #pragma unroll
-    for (int tb = 0; tb < NTB; ++tb)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[b][tb][c] = 0.f;
+    for (int c = 0; c < 4; ++c) acc[tb][c] = 0.f;
 
+  bool ok = true;
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return false;
-    const uint8_t* W = smem + s * kFsStageBytes;
-    const uint8_t* S = W + kFsWBytes;
-    const uint8_t* X = S + kFsSBytes;
-    const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
-    if (ng == kFsGroups)
-      stage_compute<Q8, NTB, true>(W, S, X, ng, L, acc);
-    else
-      stage_compute<Q8, NTB, false>(W, S, X, ng, L, acc);
+    if (ok && !mbar_wait(&full[s], ph, p.wait_ns, p.status)) ok = false;
+    if (ok) {
+      const uint8_t* W = smem + s * kFsStageBytes;
+      const uint8_t* S = W + kFsWBytes;
+      const uint8_t* X = S + kFsSBytes;
+      const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
+      if (ng == kFsGroups)
+        stage_compute<Q8, NTB, true>(W, S, X, ng, L, acc);
+      else
+        stage_compute<Q8, NTB, false>(W, S, X, ng, L, acc);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
 
   const int g = L.g, t = L.t;
+  if (MODE == kGateUp) {
+    // up warps (8..15) hand their partials to the gate warps (0..7)
+    const int half = kFsCWarps / 2;
+    if (cw >= half) {
+#pragma unroll
+      for (int tb = 0; tb < NTB; ++tb) {
+        const int r = (cw - half) * 16 + g;
+        const int col = tb * 8 + 2 * t;
+        *reinterpret_cast<float2*>(xch + r * kFsMc + col) = make_float2(acc[tb][0], acc[tb][1]);
+        *reinterpret_cast<float2*>(xch + (r + 8) * kFsMc + col) = make_float2(acc[tb][2], acc[tb][3]);
+      }
+    }
+    consumer_bar_sync();
+    if (cw >= half) return ok;
+    {
+#pragma unroll
+    for (int tb = 0; tb < NTB; ++tb) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int tok = tb * 8 + 2 * t + (c & 1);
+        const int rr = cw * 16 + g + ((c & 2) ? 8 : 0);
+        const int n = n0 + rr;
+        if (!ok || tok >= rows || n >= N) continue;
+        const int row = row0 + tok;
+        const float xs = Q8 ? p.x_scale[row] : 1.0f;
+        const float G = acc[tb][c] * xs;
+        const float U = xch[rr * kFsMc + tok] * xs;
+        const float h = G / (1.0f + expf(-G)) * U;
+        static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(h);
+      }
+    }
+    }
+  } else {
 #pragma unroll
   for (int tb = 0; tb < NTB; ++tb) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int tok = tb * 8 + 2 * t + (c & 1);
-      if (tok >= rows) continue;
+      const int n = n0 + cw * 16 + g + ((c & 2) ? 8 : 0);
+      if (!ok || tok >= rows || n >= N) continue;
       const int row = row0 + tok;
       const float xs = Q8 ? p.x_scale[row] : 1.0f;
-      if (MODE == kGateUp) {
-        const int n = n0 + 16 * cw + g + ((c & 2) ? 8 : 0);
-        if (n >= N) continue;
-        const float G = acc[0][tb][c] * xs;
-        const float U = acc[1][tb][c] * xs;
-        const float h = G / (1.0f + expf(-G)) * U;
-        static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(h);
-      } else {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int n = n0 + 32 * cw + 16 * b + g + ((c & 2) ? 8 : 0);
-          if (n >= N) continue;
-          const float y = acc[b][tb][c] * xs;
-          if (MODE == kDown)
-            static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(y);
-          else
-            static_cast<float*>(p.out)[(size_t)row * N + n] = y;
-        }
-      }
+      const float y = acc[tb][c] * xs;
+      if (MODE == kDown)
+        static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(y);
+      else
+        static_cast<float*>(p.out)[(size_t)row * N + n] = y;
     }
   }
-  return true;
+  }
+  return ok;
 }
 
 template <int MODE, bool Q8>
 __global__ void __launch_bounds__(kFsThreads, 1)
-    ffn_stream_kernel(const __grid_constant__ CUtensorMap wmap0,
-                      const __grid_constant__ CUtensorMap wmap1, const FsParams p) {
+    ffn_stream_kernel(const __grid_constant__ FsMaps maps, const FsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFsStages * kFsStageBytes);
+  float* xch = reinterpret_cast<float*>(smem + kFsStages * kFsStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFsStages * kFsStageBytes + 2 * kFsXchBytes);
   uint64_t* empty = full + kFsStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tma_s = p.tma_scales != 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFsStages; ++s) {
-      mbar_init(&full[s], 1 + 32);     // producer arrive.expect_tx + 32 cp.async arrivals
-      mbar_init(&empty[s], kFsCWarps); // one arrival per consumer warp
+      // producer arrive.expect_tx (+ 32 cp.async arrivals when scales use cp.async)
+      mbar_init(&full[s], tma_s ? 1 : 1 + 32);
+      mbar_init(&empty[s], kFsCWarps);  // one arrival per consumer warp
     }
     fence_mbarrier_init();
   }
@@ -279,8 +323,12 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   if (warp == kFsCWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensor_map(&wmap0);
-      if (MODE == kGateUp) prefetch_tensor_map(&wmap1);
+      prefetch_tensor_map(&maps.w0);
+      if (MODE == kGateUp) prefetch_tensor_map(&maps.w1);
+      if (tma_s) {
+        prefetch_tensor_map(&maps.s0);
+        if (MODE == kGateUp) prefetch_tensor_map(&maps.s1);
+      }
     }
     uint32_t it = 0;
     bool ok = true;
@@ -296,16 +344,23 @@ __global__ void __launch_bounds__(kFsThreads, 1)
           break;
         }
         uint8_t* st = smem + s * kFsStageBytes;
+        uint8_t* sdst = st + kFsWBytes;
         const int k0 = ks * kFsKc;
         const int ng = min(kFsGroups, (K - k0) / kGroup);
         const uint32_t xrow_bytes = static_cast<uint32_t>(ng * kGroup * elem);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], kFsWBytes + static_cast<uint32_t>(rows) * xrow_bytes);
+          mbar_arrive_expect_tx(&full[s], kFsWBytes + (tma_s ? kFsSBytes : 0) +
+                                              static_cast<uint32_t>(rows) * xrow_bytes);
           if (MODE == kGateUp) {
-            tma_g2s_3d(st, &wmap0, &full[s], k0 / 8, n0, e);
-            tma_g2s_3d(st + kFsWBytes / 2, &wmap1, &full[s], k0 / 8, n0, e);
+            tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
+            tma_g2s_3d(st + kFsWBytes / 2, &maps.w1, &full[s], k0 / 8, n0, e);
+            if (tma_s) {
+              tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
+              tma_g2s_3d(sdst + kFsSBytes / 2, &maps.s1, &full[s], k0 / kGroup, n0, e);
+            }
           } else {
-            tma_g2s_3d(st, &wmap0, &full[s], k0 / 8, n0, e);
+            tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
+            if (tma_s) tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
           }
         }
         __syncwarp();
@@ -314,27 +369,29 @@ __global__ void __launch_bounds__(kFsThreads, 1)
                                ((size_t)(row0 + lane) * K + k0) * elem;
           bulk_g2s(st + kFsWBytes + kFsSBytes + lane * xstride, src, xrow_bytes, &full[s]);
         }
-        // scales: row r of the tile, group pair pr (4 bytes)
-        uint8_t* sdst = st + kFsWBytes;
-        const int g0 = k0 / kGroup;
+        if (!tma_s) {
+          // scales: row r of the tile, group pair pr (4 bytes)
+          const int g0 = k0 / kGroup;
 #pragma unroll 4
-        for (int i = 0; i < kFsRows * 4 / 32; ++i) {
-          const int c = lane + 32 * i;
-          const int r = c >> 2, pr = c & 3;
-          if (2 * pr >= ng) continue;
-          int n;
-          const uint16_t* sbase;
-          if (MODE == kGateUp) {
-            n = n0 + (r & (kFsRows / 2 - 1));
-            sbase = (r < kFsRows / 2) ? p.scale0 : p.scale1;
-          } else {
-            n = n0 + r;
-            sbase = p.scale0;
+          for (int i = 0; i < kFsRows * 4 / 32; ++i) {
+            const int c = lane + 32 * i;
+            const int r = c >> 2, pr = c & 3;
+            if (2 * pr >= ng) continue;
+            int n;
+            const uint16_t* sbase;
+            if (MODE == kGateUp) {
+              const bool up = r >= kFsRows / 2;
+              n = n0 + (up ? r - kFsRows / 2 : r);
+              sbase = up ? p.scale1 : p.scale0;
+            } else {
+              n = n0 + r;
+              sbase = p.scale0;
+            }
+            if (n >= N) continue;
+            cp_async_4(sdst + r * 16 + pr * 4, sbase + ((size_t)e * N + n) * G_all + g0 + 2 * pr);
           }
-          if (n >= N) continue;
-          cp_async_4(sdst + r * 16 + pr * 4, sbase + ((size_t)e * N + n) * G_all + g0 + 2 * pr);
+          cp_async_arrive_noinc(&full[s]);
         }
-        cp_async_arrive_noinc(&full[s]);
       }
     }
     if (!ok) {
@@ -356,40 +413,38 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   L.t = lane & 3;
   L.li = lane & 7;
   {
-    // ldmatrix: lanes 8m..8m+7 address rows of matrix m = (block m/2, half m%2)
+    // ldmatrix x4: lanes 8m..8m+7 address matrix m = (half m&1, group m>>1)
     const int m = lane >> 3;
-    const int b = m >> 1, h = m & 1;
-    const int base = (MODE == kGateUp) ? b * (kFsRows / 2) + 16 * warp : 32 * warp + 16 * b;
-    L.lrow_off = static_cast<uint32_t>((base + 8 * h + L.li) * 128);
-    if (MODE == kGateUp) {
-      L.rlo[0] = 16 * warp + L.g;                 // gate rows
-      L.rlo[1] = kFsRows / 2 + 16 * warp + L.g;   // up rows
-    } else {
-      L.rlo[0] = 32 * warp + L.g;
-      L.rlo[1] = 32 * warp + 16 + L.g;
-    }
+    const int rb = 16 * warp;  // first tile row of this warp's block
+    L.gsel = m >> 1;
+    L.lrow_off = static_cast<uint32_t>((rb + 8 * (m & 1) + L.li) * 128);
+    L.rlo = rb + L.g;
   }
   uint32_t it = 0;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  int parity = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, parity ^= 1) {
     const int q = u / n_tiles, jt = u - q * n_tiles;
     const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
     const int n0 = jt * tile_n;
-    const int ntb = (rows + 7) >> 3;
+    float* x = xch + parity * (kFsXchBytes / 4);
     bool ok;
-    static_assert(kFsTb == 2, "token-block dispatch below covers 1 or 2 blocks");
-    if (ntb == 1)
-      ok = consume_unit<MODE, Q8, 1>(smem, full, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+    if (rows <= 8)
+      ok = consume_unit<MODE, Q8, 1>(smem, x, full, empty, it, ksteps, row0, rows, n0, warp, lane,
+                                     L, p);
     else
-      ok = consume_unit<MODE, Q8, 2>(smem, full, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+      ok = consume_unit<MODE, Q8, 2>(smem, x, full, empty, it, ksteps, row0, rows, n0, warp, lane,
+                                     L, p);
     if (!ok) return;
   }
 }
 
-// Chunk list of the expert-sorted rows: every expert's rows cut into chunks of
-// at most kFsMc rows.  One CTA of 1024 threads.  Offsets that are not
-// non-decreasing or exceed rows_max record MOE_ERR_INVALID and give no chunk.
+// Chunk list of the expert-sorted rows: the rows of every expert whose row
+// count lies in [lo, hi] cut into chunks of at most mc rows.  One CTA of 1024
+// threads.  Offsets that are not non-decreasing or exceed rows_max record
+// MOE_ERR_INVALID and give no chunk.
 __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __restrict__ offsets,
-                                                            int E, int rows_max, int max_chunks,
+                                                            int E, int rows_max, int mc, int lo,
+                                                            int hi, int max_chunks,
                                                             int32_t* __restrict__ chunk_e,
                                                             int32_t* __restrict__ chunk_row0,
                                                             int32_t* __restrict__ chunk_rows,
@@ -404,7 +459,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
     const int a = offsets[e], b = offsets[e + 1];
     const int cnt = b - a;
     if (a < 0 || cnt < 0 || b > rows_max) bad = 1;
-    nch[e] = cnt > 0 ? (cnt + kFsMc - 1) / kFsMc : 0;
+    nch[e] = (cnt > 0 && cnt >= lo && cnt <= hi) ? (cnt + mc - 1) / mc : 0;
   }
   __syncthreads();
   if (bad) {
@@ -454,42 +509,60 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int a = offsets[e], cnt = offsets[e + 1] - a;
+    if (cnt <= 0 || cnt < lo || cnt > hi) continue;
     const int base = nch[e];
-    for (int i = 0; i * kFsMc < cnt; ++i) {
+    for (int i = 0; i * mc < cnt; ++i) {
       chunk_e[base + i] = e;
-      chunk_row0[base + i] = a + i * kFsMc;
-      chunk_rows[base + i] = min(kFsMc, cnt - i * kFsMc);
+      chunk_row0[base + i] = a + i * mc;
+      chunk_rows[base + i] = min(mc, cnt - i * mc);
     }
   }
   if (threadIdx.x == 0) *n_chunks = total;
 }
 
-static int max_chunks_for(int E, int rows_max) { return (rows_max + kFsMc - 1) / kFsMc + E; }
+// Experts with at least this many rows go to the tensor-core path
+// (act_bits 16); the others to the stream kernel.
+constexpr int kTcMinRows = 48;
+
+static int max_chunks_for(int E, int rows_max, int mc) { return (rows_max + mc - 1) / mc + E; }
 
 struct Schedule {
   int32_t* chunk_e;
   int32_t* chunk_row0;
   int32_t* chunk_rows;
   int32_t* n_chunks;
-  size_t bytes;
+  int max_chunks;
 };
 
-static Schedule carve_schedule(void* ws, int E, int rows_max) {
-  const size_t mc = static_cast<size_t>(max_chunks_for(E, rows_max));
+static size_t schedule_bytes_one(int E, int rows_max, int mc) {
+  const size_t n = static_cast<size_t>(max_chunks_for(E, rows_max, mc));
+  return 3 * align_up(n * sizeof(int32_t), 256) + 256;
+}
+
+static Schedule carve_one(char*& b, int E, int rows_max, int mc) {
   Schedule s;
-  char* b = static_cast<char*>(ws);
-  const size_t arr = align_up(mc * sizeof(int32_t), 256);
+  s.max_chunks = max_chunks_for(E, rows_max, mc);
+  const size_t arr = align_up(static_cast<size_t>(s.max_chunks) * sizeof(int32_t), 256);
   s.chunk_e = reinterpret_cast<int32_t*>(b);
   s.chunk_row0 = reinterpret_cast<int32_t*>(b + arr);
   s.chunk_rows = reinterpret_cast<int32_t*>(b + 2 * arr);
   s.n_chunks = reinterpret_cast<int32_t*>(b + 3 * arr);
-  s.bytes = 3 * arr + 256;
+  b += 3 * arr + 256;
   return s;
 }
 
+// Stream-kernel list plus tensor-core list.
 static size_t schedule_bytes(int E, int rows_max) {
-  const size_t mc = static_cast<size_t>(max_chunks_for(E, rows_max));
-  return 3 * align_up(mc * sizeof(int32_t), 256) + 256;
+  return schedule_bytes_one(E, rows_max, kFsMc) + schedule_bytes_one(E, rows_max, kTcChunkRows);
+}
+
+static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
+                           const Schedule& sc, int* status, cudaStream_t s) {
+  ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, mc, lo, hi, sc.max_chunks,
+                                         sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks,
+                                         status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }
 
 // Tensor map of a packed weight [E, N, K/8] int32 with a box of `rows` rows x
@@ -504,24 +577,51 @@ static bool weight_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Tensor map of bf16 scales [E, N, K/32] with a box of `rows` rows x 8 groups
+// (16 bytes, no swizzle).  Valid when K % 256 == 0 (16-byte row strides).
+static bool scale_map(CUtensorMap* m, const uint16_t* sc, int E, int N, int K, int rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K / kGroup), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(E)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K / kGroup) * 2,
+                               static_cast<uint64_t>(N) * (K / kGroup) * 2};
+  const uint32_t box[3] = {static_cast<uint32_t>(kFsGroups), static_cast<uint32_t>(rows), 1};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, sc, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+static bool tma_scales_ok(int K) { return K % kFsKc == 0; }
+
+// Maps of one stream launch: w0/s0 the first (or only) matrix, w1/s1 the second.
+static bool make_maps(FsMaps* m, const int32_t* w0, const uint16_t* s0, const int32_t* w1,
+                      const uint16_t* s1, int E, int N, int K, int rows) {
+  if (!weight_map(&m->w0, w0, E, N, K, rows) || !weight_map(&m->w1, w1, E, N, K, rows))
+    return false;
+  if (tma_scales_ok(K)) {
+    if (!scale_map(&m->s0, s0, E, N, K, rows) || !scale_map(&m->s1, s1, E, N, K, rows))
+      return false;
+  } else {
+    m->s0 = m->w0;  // unused
+    m->s1 = m->w1;
+  }
+  return true;
+}
+
 template <int MODE, bool Q8>
-static int launch_stream(const CUtensorMap& m0, const CUtensorMap& m1, const FsParams& p,
-                         cudaStream_t s) {
+static int launch_stream(const FsMaps& maps, const FsParams& p, cudaStream_t s) {
   auto kern = ffn_stream_kernel<MODE, Q8>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kFsSmemBytes));
-  kern<<<num_sms(), kFsThreads, kFsSmemBytes, s>>>(m0, m1, p);
+  kern<<<num_sms(), kFsThreads, kFsSmemBytes, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
-static int run_stream(int mode, bool q8, const CUtensorMap& m0, const CUtensorMap& m1,
-                      const FsParams& p, cudaStream_t s) {
-  if (mode == kGateUp) return q8 ? launch_stream<kGateUp, true>(m0, m1, p, s)
-                                 : launch_stream<kGateUp, false>(m0, m1, p, s);
-  if (mode == kDown) return q8 ? launch_stream<kDown, true>(m0, m1, p, s)
-                               : launch_stream<kDown, false>(m0, m1, p, s);
-  return q8 ? launch_stream<kLinear, true>(m0, m1, p, s) : launch_stream<kLinear, false>(m0, m1, p, s);
+static int run_stream(int mode, bool q8, const FsMaps& maps, const FsParams& p, cudaStream_t s) {
+  if (mode == kGateUp) return q8 ? launch_stream<kGateUp, true>(maps, p, s)
+                                 : launch_stream<kGateUp, false>(maps, p, s);
+  if (mode == kDown) return q8 ? launch_stream<kDown, true>(maps, p, s)
+                               : launch_stream<kDown, false>(maps, p, s);
+  return q8 ? launch_stream<kLinear, true>(maps, p, s) : launch_stream<kLinear, false>(maps, p, s);
 }
 
 static int check_width(int v) { return (v > 0 && v % 64 == 0) ? MOE_OK : MOE_ERR_UNSUPPORTED; }
@@ -537,39 +637,53 @@ extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_ma
   if (act_bits == 8) {
     b += align_up((size_t)rows_max * I, 256);                // h as int8
     b += align_up((size_t)rows_max * sizeof(float), 256);    // its row scales
+  } else {
+    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);  // fp16 x (tensor-core path)
+    b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);  // fp16 h (tensor-core path)
   }
   return b;
 }
 
 int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
-                           int E, int D, int I, int rows_max, const int32_t* gate_packed,
-                           const uint16_t* gate_scale, const int32_t* up_packed,
-                           const uint16_t* up_scale, const int32_t* down_packed,
-                           const uint16_t* down_scale, int act_bits, void* y, bool y_f32, void* ws,
-                           cudaStream_t s) {
+                           int E, int D, int I, int rows_max, int max_rows_per_expert,
+                           const int32_t* gate_packed, const uint16_t* gate_scale,
+                           const int32_t* up_packed, const uint16_t* up_scale,
+                           const int32_t* down_packed, const uint16_t* down_scale, int act_bits,
+                           void* y, bool y_f32, void* ws, cudaStream_t s) {
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
-  Schedule sch = carve_schedule(ws, E, rows_max);
-  char* b = static_cast<char*>(ws) + sch.bytes;
+  char* b = static_cast<char*>(ws);
+  Schedule small = carve_one(b, E, rows_max, kFsMc);
+  Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
   uint16_t* h = reinterpret_cast<uint16_t*>(b);
   b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   int8_t* hq = nullptr;
   float* hs = nullptr;
+  uint16_t* x16 = nullptr;
+  uint16_t* h16 = nullptr;
   if (act_bits == 8) {
     hq = reinterpret_cast<int8_t*>(b);
     b += align_up((size_t)rows_max * I, 256);
     hs = reinterpret_cast<float*>(b);
+  } else {
+    x16 = reinterpret_cast<uint16_t*>(b);
+    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
+    h16 = reinterpret_cast<uint16_t*>(b);
+  }
+  // experts with many rows go to the tensor-core kernels (bf16 activations)
+  const bool use_tc = act_bits == 16 && tc_path_supported(D) && tc_path_supported(I) &&
+                      max_rows_per_expert >= kTcMinRows;
+  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max,
+                           small, status, s);
+  if (rc) return rc;
+  if (use_tc) {
+    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s);
+    if (rc) return rc;
   }
 
-  ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, max_chunks_for(E, rows_max),
-                                         sch.chunk_e, sch.chunk_row0, sch.chunk_rows, sch.n_chunks,
-                                         status);
-  MOE_LAUNCH_CHECK();
-
-  CUtensorMap mg, mu, md;
-  if (!weight_map(&mg, gate_packed, E, I, D, kFsRows / 2) ||
-      !weight_map(&mu, up_packed, E, I, D, kFsRows / 2) ||
-      !weight_map(&md, down_packed, E, D, I, kFsRows))
+  FsMaps mgu, md;
+  if (!make_maps(&mgu, gate_packed, gate_scale, up_packed, up_scale, E, I, D, kFsRows / 2) ||
+      !make_maps(&md, down_packed, down_scale, down_packed, down_scale, E, D, I, kFsRows))
     return MOE_ERR_CUDA;
 
   const bool q8 = act_bits == 8;
@@ -579,20 +693,29 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   p.scale0 = gate_scale;
   p.scale1 = up_scale;
   p.out = h;
-  p.chunk_e = sch.chunk_e;
-  p.chunk_row0 = sch.chunk_row0;
-  p.chunk_rows = sch.chunk_rows;
-  p.n_chunks = sch.n_chunks;
+  p.chunk_e = small.chunk_e;
+  p.chunk_row0 = small.chunk_row0;
+  p.chunk_rows = small.chunk_rows;
+  p.n_chunks = small.n_chunks;
   p.status = status;
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  int rc = run_stream(kGateUp, q8, mg, mu, p, s);
+  p.tma_scales = tma_scales_ok(D) ? 1 : 0;
+  rc = run_stream(kGateUp, q8, mgu, p, s);
   if (rc) return rc;
+  if (use_tc) {
+    rc = launch_to_f16_rows(static_cast<const uint16_t*>(x_sorted), rows_max, D, offsets + E, x16, s);
+    if (rc) return rc;
+    rc = launch_tc_gateup(x16, rows_max, E, D, I, gate_packed, gate_scale, up_packed, up_scale, h16,
+                          big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+    if (rc) return rc;
+  }
 
   FsParams pd = p;
   pd.K = I;
   pd.N = D;
+  pd.tma_scales = tma_scales_ok(I) ? 1 : 0;
   pd.scale0 = down_scale;
   pd.scale1 = nullptr;
   pd.out = y;
@@ -604,7 +727,14 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   } else {
     pd.x = h;
   }
-  return run_stream(y_f32 ? kLinear : kDown, q8, md, md, pd, s);
+  rc = run_stream(y_f32 ? kLinear : kDown, q8, md, pd, s);
+  if (rc) return rc;
+  if (use_tc) {
+    rc = launch_tc_down(h16, rows_max, E, D, I, down_packed, down_scale, y, y_f32, big.chunk_e,
+                        big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+    if (rc) return rc;
+  }
+  return MOE_OK;
 }
 
 extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
@@ -627,14 +757,14 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
     return MOE_ERR_INVALID;
   if (ws_bytes < moe_expert_ffn_workspace_size(E, D, I, rows_max, act_bits))
     return MOE_ERR_WORKSPACE;
-  return launch_expert_ffn(x_sorted, x_scale, offsets, E, D, I, rows_max, gate_packed, gate_scale,
-                           up_packed, up_scale, down_packed, down_scale, act_bits, y_sorted, false,
-                           ws, static_cast<cudaStream_t>(stream));
+  return launch_expert_ffn(x_sorted, x_scale, offsets, E, D, I, rows_max, rows_max, gate_packed,
+                           gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
+                           y_sorted, false, ws, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t moe_int4_linear_workspace_size(int E, int rows_max) {
   if (E <= 0 || rows_max < 0) return 256;
-  return schedule_bytes(E, rows_max);
+  return schedule_bytes_one(E, rows_max, kFsMc);
 }
 
 extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E,
@@ -652,13 +782,12 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Schedule sch = carve_schedule(ws, E, rows_max);
-  ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, max_chunks_for(E, rows_max),
-                                         sch.chunk_e, sch.chunk_row0, sch.chunk_rows, sch.n_chunks,
-                                         status);
-  MOE_LAUNCH_CHECK();
-  CUtensorMap m;
-  if (!weight_map(&m, w_packed, E, N, K, kFsRows)) return MOE_ERR_CUDA;
+  char* b = static_cast<char*>(ws);
+  Schedule sch = carve_one(b, E, rows_max, kFsMc);
+  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, sch, status, s);
+  if (rc) return rc;
+  FsMaps m;
+  if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
   FsParams p{};
   p.x = x;
   p.x_scale = x_scale;
@@ -672,5 +801,6 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   p.wait_ns = kDefaultWaitNs;
   p.K = K;
   p.N = N;
-  return run_stream(kLinear, act_bits == 8, m, m, p, s);
+  p.tma_scales = tma_scales_ok(K) ? 1 : 0;
+  return run_stream(kLinear, act_bits == 8, m, p, s);
 }

@@ -1,0 +1,492 @@
+// Grouped W4A16 expert GEMMs on the 5th-generation tensor cores, for experts
+// with many rows (prefill-shaped loads).  Same computation as the stream
+// kernel (Kimi exact-generator adaptation page, "The preserved forward form";
+// Kimi K2.5 donor-reference "SwiGLU-style gated feed-forward projection"),
+// with the weights dequantised once per 128-row token tile:
+//   * warp 0 (one thread): TMA of the 128 x 64 bf16 activation tile (128-byte
+//     swizzle) and of the 256-row x 64-column packed int4 weight tile into a
+//     4-stage ring;
+//   * warps 2-9: dequantisation, one weight row per thread, to fp16
+//     q * scale written in the K-major 128-byte-swizzle layout the MMA reads,
+//     then fence.proxy.async.  With a bf16 scale (8 significant bits) and
+//     |q| <= 8, q * scale has at most 11 significant bits: it is exact in fp16
+//     for scales in [2^-17, 8188].  The activations arrive in fp16 (a copy
+//     made once per call; bf16 values are exact in fp16 for
+//     2^-17 <= |x| <= 65504), and the gate/up tiles write h in fp16 for the
+//     down tiles.  So, as in the stream kernel, the weights are never
+//     rounded; a value beyond the fp16 range makes its output row non-finite
+//     and records MOE_ERR_UNSUPPORTED;
+//   * warp 1 (one thread): tcgen05.mma kind::f16 (fp16 inputs), M=128, N=256,
+//     K=16, into one of two 256-column TMEM accumulators (the epilogue of a
+//     tile overlaps the main loop of the next);
+//   * warps 10-13: tcgen05.ld of the accumulator; gate/up tiles hold gate in
+//     columns 0-127 and up in 128-255 and store h = SiLU(G) * U (fp16); down
+//     tiles store y (bf16, or fp32).
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "ffn_tc.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+
+constexpr int kTxBM = 128;                     // token rows per tile (MMA M)
+constexpr int kTxBN = 256;                     // weight rows per tile (MMA N)
+constexpr int kTxBK = 64;                      // K per stage (one swizzle atom of bf16)
+constexpr int kTxStages = 4;
+constexpr int kTxABytes = kTxBM * kTxBK * 2;   // 16 KiB activations
+constexpr int kTxBBytes = kTxBN * kTxBK * 2;   // 32 KiB dequantised weights
+constexpr int kTxQBytes = kTxBN * kTxBK / 2;   // 8 KiB packed int4
+constexpr int kTxStageBytes = kTxABytes + kTxBBytes + kTxQBytes;
+constexpr int kTxDqWarps = 8;
+constexpr int kTxEpWarps = 4;
+constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
+constexpr uint32_t kTxCols = 2 * kTxBN;        // two accumulators
+constexpr int kTxSmem = kTxStages * kTxStageBytes + 1024 + 256;
+static_assert(kTxStageBytes % 1024 == 0, "stage alignment");
+static_assert(kTxDqWarps * 32 == kTxBN, "one dequantisation thread per weight row");
+
+enum TxMode { kTxGateUp = 0, kTxDown = 1, kTxLinear = 2 };
+
+// Two nibbles n (bits 0-3 and 16-19 of v, two's complement) -> fp16x2 q * s,
+// exactly: (n ^ 8) lands in the low mantissa bits of 1024.0 (0x6400); minus
+// 1032 gives q; times the fp16 scale pair s2.
+__device__ __forceinline__ uint32_t nib_lo_f16(uint32_t v, uint32_t s2) {
+  const uint32_t m = (v & 0x000F000Fu) ^ 0x64086408u;
+  __half2 h = *reinterpret_cast<const __half2*>(&m);
+  h = __hsub2(h, __floats2half2_rn(1032.0f, 1032.0f));
+  h = __hmul2(h, *reinterpret_cast<const __half2*>(&s2));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Same for nibbles at bits 4-7 and 20-23: 1024 + 16 (n ^ 8), scaled by 1/16
+// and shifted by -72 (exact) to q, then times s2.
+__device__ __forceinline__ uint32_t nib_hi_f16(uint32_t v, uint32_t s2) {
+  const uint32_t m = (v & 0x00F000F0u) ^ 0x64806480u;
+  __half2 h = *reinterpret_cast<const __half2*>(&m);
+  h = __hfma2(h, __floats2half2_rn(0.0625f, 0.0625f), __floats2half2_rn(-72.0f, -72.0f));
+  h = __hmul2(h, *reinterpret_cast<const __half2*>(&s2));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// bf16x2 -> fp16x2 (exact for values in the fp16 range; beyond it: inf).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// bf16 scale bits -> fp16 bits, replicated in both halves.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t bf16_bits) {
+  const __half h = __float2half_rn(__uint_as_float(bf16_bits << 16));
+  const uint32_t u = __half_as_ushort(h);
+  return u | (u << 16);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTxThreads, 1)
+    ffn_tc_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTxStages * kTxStageBytes);
+  uint64_t* bready = full + kTxStages;
+  uint64_t* sfree = bready + kTxStages;
+  uint64_t* accfull = sfree + kTxStages;
+  uint64_t* accempty = accfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&bready[s], kTxDqWarps);
+      mbar_init(&sfree[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kTxEpWarps);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTxCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int K = p.K, N = p.N;
+  const int tile_n = (MODE == kTxGateUp) ? kTxBN / 2 : kTxBN;
+  const int n_tiles = (N + tile_n - 1) / tile_n;
+  const int units = (*p.n_chunks) * n_tiles;
+  const int ksteps = K / kTxBK;
+  const int G_all = K / kGroup;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensor_map(&maps.a);
+      prefetch_tensor_map(&maps.q0);
+      if (MODE == kTxGateUp) prefetch_tensor_map(&maps.q1);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int q = u / n_tiles, jt = u - q * n_tiles;
+        const int e = p.chunk_e[q], row0 = p.chunk_row0[q];
+        const int n0 = jt * tile_n;
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const int s = it % kTxStages;
+          const uint32_t ph = (it / kTxStages) & 1u;
+          if (!mbar_wait(&sfree[s], ph ^ 1u, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kTxStageBytes;
+          uint8_t* qd = st + kTxABytes + kTxBBytes;
+          mbar_arrive_expect_tx(&full[s], kTxABytes + kTxQBytes);
+          tma_g2s_2d(st, &maps.a, &full[s], ks * kTxBK, row0);
+          if (MODE == kTxGateUp) {
+            tma_g2s_3d(qd, &maps.q0, &full[s], ks * (kTxBK / 8), n0, e);
+            tma_g2s_3d(qd + kTxQBytes / 2, &maps.q1, &full[s], ks * (kTxBK / 8), n0, e);
+          } else {
+            tma_g2s_3d(qd, &maps.q0, &full[s], ks * (kTxBK / 8), n0, e);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(kTxBM, kTxBN);
+      uint32_t it = 0, uc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+        const uint32_t b = uc & 1u, uph = (uc >> 1) & 1u;
+        if (!mbar_wait(&accempty[b], uph ^ 1u, p.wait_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t dt = tbase + b * kTxBN;
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const int s = it % kTxStages;
+          const uint32_t ph = (it / kTxStages) & 1u;
+          if (!mbar_wait(&bready[s], ph, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* st = smem + s * kTxStageBytes;
+          const uint64_t da = smem_desc_sw128(st);
+          const uint64_t db = smem_desc_sw128(st + kTxABytes);
+#pragma unroll
+          for (int kk = 0; kk < kTxBK / 16; ++kk)
+            umma_f16(dt, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+          umma_commit(&sfree[s]);
+        }
+        if (ok) umma_commit(&accfull[b]);
+      }
+    }
+  } else if (warp < 2 + kTxDqWarps) {
+    // ----------------------------------------------------- dequantisation
+    const int r = threadIdx.x - 64;  // weight row of this thread within the tile
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int q = u / n_tiles, jt = u - q * n_tiles;
+      const int e = p.chunk_e[q];
+      const int n0 = jt * tile_n;
+      int n;
+      const uint16_t* sb;
+      if (MODE == kTxGateUp) {
+        n = n0 + (r & (kTxBN / 2 - 1));
+        sb = r < kTxBN / 2 ? p.scale0 : p.scale1;
+      } else {
+        n = n0 + r;
+        sb = p.scale0;
+      }
+      const bool valid = n < N;
+      const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all;
+      // scales: 16 bytes (8 groups = 4 stages) per load, fetched 4 stages ahead
+      // when the rows are 16-byte aligned (K % 256 == 0), else 4 bytes per stage
+      const bool vec = (G_all & 7) == 0;
+      uint4 scur = make_uint4(0u, 0u, 0u, 0u), snxt = scur;
+      if (valid) {
+        if (vec) {
+          scur = *reinterpret_cast<const uint4*>(srow);
+          if (ksteps > 4) snxt = *reinterpret_cast<const uint4*>(srow + 8);
+        } else {
+          scur.x = *reinterpret_cast<const uint32_t*>(srow);
+        }
+      }
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        uint32_t sw;  // bf16 scales of groups 2ks (low) and 2ks+1 (high)
+        if (vec) {
+          const int j = ks & 3;
+          sw = (j & 2) ? ((j & 1) ? scur.w : scur.z) : ((j & 1) ? scur.y : scur.x);
+          if (j == 3) {
+            scur = snxt;
+            if (valid && ks + 5 < ksteps) snxt = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 5));
+          }
+        } else {
+          sw = scur.x;
+          if (valid && ks + 1 < ksteps) scur.x = *reinterpret_cast<const uint32_t*>(srow + 2 * (ks + 1));
+        }
+        const int s = it % kTxStages;
+        const uint32_t ph = (it / kTxStages) & 1u;
+        if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * kTxStageBytes;
+        // int4 rows of 32 bytes, stored with the 32-byte swizzle: 16-byte half
+        // h of row r sits at half h ^ ((r >> 2) & 1)
+        const uint8_t* qrow = st + kTxABytes + kTxBBytes + r * 32;
+        const int qx = (r >> 2) & 1;
+        uint8_t* brow = st + kTxABytes + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + (qx << 4));
+        const uint4 w1 = *reinterpret_cast<const uint4*>(qrow + ((qx ^ 1) << 4));
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 2ks
+        const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 2ks+1
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w = wv[c];
+          const uint32_t sc = c < 4 ? s_lo : s_hi;
+          // pairs (n0,n4), (n1,n5) from w; (n2,n6), (n3,n7) from w >> 8
+          const uint32_t p04 = nib_lo_f16(w, sc), p15 = nib_hi_f16(w, sc);
+          const uint32_t w8 = w >> 8;
+          const uint32_t p26 = nib_lo_f16(w8, sc), p37 = nib_hi_f16(w8, sc);
+          // natural column order: (n0,n1), (n2,n3), (n4,n5), (n6,n7)
+          uint4 o;
+          o.x = __byte_perm(p04, p15, 0x5410);
+          o.y = __byte_perm(p26, p37, 0x5410);
+          o.z = __byte_perm(p04, p15, 0x7632);
+          o.w = __byte_perm(p26, p37, 0x7632);
+          *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bready[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3;  // TMEM lane quarter of this warp
+    const int mrow = 32 * qd + lane;
+    uint32_t uc = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+      const uint32_t b = uc & 1u, uph = (uc >> 1) & 1u;
+      const int q = u / n_tiles, jt = u - q * n_tiles;
+      const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
+      const int n0 = jt * tile_n;
+      if (!mbar_wait(&accfull[b], uph, p.wait_ns, p.status)) break;
+      tc_fence_after();
+      const uint32_t ta = tbase + b * kTxBN + (static_cast<uint32_t>(32 * qd) << 16);
+      const bool vrow = mrow < rows;
+      const size_t orow = static_cast<size_t>(row0 + mrow) * N;
+      if (MODE == kTxGateUp) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTxBN / 2; c0 += 32) {
+          uint32_t g[32], v[32];
+          tmem_ld32(ta + c0, g);
+          tmem_ld32(ta + kTxBN / 2 + c0, v);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (vrow && col < N) {
+            bool fin = true;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              fin &= fabsf(__uint_as_float(g[i])) <= 3.0e38f && fabsf(__uint_as_float(v[i])) <= 3.0e38f;
+            if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
+            uint32_t hw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float h0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(v[2 * i]);
+              const float h1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(v[2 * i + 1]);
+              const __half2 hh = __floats2half2_rn(h0, h1);
+              hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            if (col + 32 <= N) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col + i < N) dst[i] = static_cast<uint16_t>((hw[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTxBN; c0 += 32) {
+          uint32_t y[32];
+          tmem_ld32(ta + c0, y);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (vrow && col < N) {
+            bool fin = true;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) fin &= fabsf(__uint_as_float(y[i])) <= 3.0e38f;
+            if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
+            if (MODE == kTxDown) {
+              uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
+              if (col + 32 <= N) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t w4[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    w4[j] = static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(y[8 * i + 2 * j]))) |
+                            (static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(y[8 * i + 2 * j + 1])))
+                             << 16);
+                  d4[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col + i < N) dst[i] = f32_to_bf16_bits(__uint_as_float(y[i]));
+              }
+            } else {
+              float* dst = static_cast<float*>(p.out) + orow + col;
+              if (col + 32 <= N) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  d4[i] = make_float4(__uint_as_float(y[4 * i]), __uint_as_float(y[4 * i + 1]),
+                                      __uint_as_float(y[4 * i + 2]), __uint_as_float(y[4 * i + 3]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col + i < N) dst[i] = __uint_as_float(y[i]);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTxCols);
+  }
+}
+
+static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+  const uint32_t box[2] = {static_cast<uint32_t>(kTxBK), static_cast<uint32_t>(kTxBM)};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// bf16 -> fp16 copy of the rows below *row_count (one warp per row).
+__global__ void __launch_bounds__(256) to_f16_rows_kernel(const uint16_t* __restrict__ src, int R,
+                                                          int C, const int32_t* row_count,
+                                                          uint16_t* __restrict__ dst) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= R || r >= *row_count) return;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)r * C);
+  uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)r * C);
+  for (int v = lane; v < C / 8; v += 32) {
+    uint4 x = s4[v];
+    x.x = bf16x2_to_f16x2(x.x);
+    x.y = bf16x2_to_f16x2(x.y);
+    x.z = bf16x2_to_f16x2(x.z);
+    x.w = bf16x2_to_f16x2(x.w);
+    d4[v] = x;
+  }
+}
+
+int launch_to_f16_rows(const uint16_t* src, int R, int C, const int32_t* row_count, uint16_t* dst,
+                       cudaStream_t s) {
+  if (R == 0) return MOE_OK;
+  to_f16_rows_kernel<<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, int rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(E)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K / 8) * 4,
+                               static_cast<uint64_t>(N) * (K / 8) * 4};
+  const uint32_t box[3] = {static_cast<uint32_t>(kTxBK / 8), static_cast<uint32_t>(rows), 1};
+  // 32-byte rows with the 32-byte swizzle: conflict-free 16-byte reads per row
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, w, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+template <int MODE>
+static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
+  auto kern = ffn_tc_kernel<MODE>;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTxSmem));
+  kern<<<num_sms(), kTxThreads, kTxSmem, s>>>(maps, p);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+bool tc_path_supported(int K) { return K % kTxBK == 0; }
+
+int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
+                     const int32_t* gate_packed, const uint16_t* gate_scale,
+                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h16,
+                     const int32_t* chunk_e,
+                     const int32_t* chunk_row0, const int32_t* chunk_rows, const int32_t* n_chunks,
+                     int* status, cudaStream_t s) {
+  TxMaps maps;
+  if (!act_map(&maps.a, x16, rows_max, D) ||
+      !packed_map(&maps.q0, gate_packed, E, I, D, kTxBN / 2) ||
+      !packed_map(&maps.q1, up_packed, E, I, D, kTxBN / 2))
+    return MOE_ERR_CUDA;
+  TxParams p{};
+  p.scale0 = gate_scale;
+  p.scale1 = up_scale;
+  p.out = h16;
+  p.chunk_e = chunk_e;
+  p.chunk_row0 = chunk_row0;
+  p.chunk_rows = chunk_rows;
+  p.n_chunks = n_chunks;
+  p.status = status;
+  p.wait_ns = kDefaultWaitNs;
+  p.K = D;
+  p.N = I;
+  return launch_tc<kTxGateUp>(maps, p, s);
+}
+
+int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
+                   const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
+                   const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
+                   const int32_t* n_chunks, int* status, cudaStream_t s) {
+  TxMaps maps;
+  if (!act_map(&maps.a, h16, rows_max, I) || !packed_map(&maps.q0, down_packed, E, D, I, kTxBN))
+    return MOE_ERR_CUDA;
+  maps.q1 = maps.q0;
+  TxParams p{};
+  p.scale0 = down_scale;
+  p.scale1 = down_scale;
+  p.out = y;
+  p.chunk_e = chunk_e;
+  p.chunk_row0 = chunk_row0;
+  p.chunk_rows = chunk_rows;
+  p.n_chunks = n_chunks;
+  p.status = status;
+  p.wait_ns = kDefaultWaitNs;
+  p.K = I;
+  p.N = D;
+  return y_f32 ? launch_tc<kTxLinear>(maps, p, s) : launch_tc<kTxDown>(maps, p, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,56 @@
+// tcgen05 grouped W4A16 expert GEMMs (ffn_tc.cu), used for the experts with
+// many rows.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct TxParams {
+  const uint16_t* scale0;  // bf16 [E, N, K/32] (gate, or the single matrix)
+  const uint16_t* scale1;  // bf16 [E, N, K/32] (up)
+  void* out;               // bf16 h / bf16 y / fp32 y  [rows_max, N]
+  const int32_t* chunk_e;
+  const int32_t* chunk_row0;
+  const int32_t* chunk_rows;
+  const int32_t* n_chunks;
+  int* status;
+  long long wait_ns;
+  int K;
+  int N;
+};
+
+struct TxMaps {
+  CUtensorMap a;   // activations bf16 [rows_max, K], 128 x 64 box, 128-byte swizzle
+  CUtensorMap q0;  // packed weights [E, N, K/8], box 8 words x rows
+  CUtensorMap q1;
+};
+
+// Rows per token tile of the tensor-core path (chunks of that many rows).
+constexpr int kTcChunkRows = 128;
+
+// K of the tensor-core path must be a multiple of 64.
+bool tc_path_supported(int K);
+
+// fp16 copy of bf16 rows [R, C] below *row_count.
+int launch_to_f16_rows(const uint16_t* src, int R, int C, const int32_t* row_count, uint16_t* dst,
+                       cudaStream_t s);
+
+// h16[rows] = fp16(SiLU(x W_gate^T) * (x W_up^T)) for the listed 128-row
+// chunks; x16 is the fp16 copy of the activations.
+int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
+                     const int32_t* gate_packed, const uint16_t* gate_scale,
+                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h16,
+                     const int32_t* chunk_e, const int32_t* chunk_row0,
+                     const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                     cudaStream_t s);
+
+// y[rows] = h16 W_down^T (bf16, or fp32 with y_f32) for the listed chunks.
+int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
+                   const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
+                   const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
+                   const int32_t* n_chunks, int* status, cudaStream_t s);
+
+}  // namespace moe

@@ -138,9 +138,10 @@ constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024 + 256;
 constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: epilogue
 constexpr uint32_t kTcCols = 256;
 
+template <bool F32OUT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                   uint16_t* __restrict__ C, int M, int N, int K, int* status, long long wait_ns) {
+                   void* __restrict__ Cout, int M, int N, int K, int* status, long long wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -218,8 +219,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld32(tbase + (static_cast<uint32_t>(32 * q) << 16) + c0, r);
         tmem_ld_wait();
         const int col = n0 + c0;
-        if (row < M && col < N) {
-          uint16_t* dst = C + (size_t)row * N + col;
+        if (F32OUT && row < M && col < N) {
+          float* dst = static_cast<float*>(Cout) + (size_t)row * N + col;
+          if (col + 32 <= N && (N & 3) == 0) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < N) dst[i] = __uint_as_float(r[i]);
+          }
+        } else if (row < M && col < N) {
+          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * N + col;
           if (col + 32 <= N) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -233,7 +247,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
-            for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = f32_to_bf16_bits(__uint_as_float(r[i]));
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < N) dst[i] = f32_to_bf16_bits(__uint_as_float(r[i]));
           }
         }
       }
@@ -255,19 +271,31 @@ static bool bf16_map(CUtensorMap* m, const uint16_t* base, int rows, int K, int 
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
-                     cudaStream_t s) {
+template <bool F32OUT>
+static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, int K, void* y,
+                          cudaStream_t s) {
   if (M == 0) return MOE_OK;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   CUtensorMap ma, mb;
   if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map(&mb, w, N, K, kTcBN)) return MOE_ERR_CUDA;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kTcSmem));
+  MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<F32OUT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem));
   dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
-  gemm_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, status, kDefaultWaitNs);
+  gemm_tc_kernel<F32OUT><<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, status,
+                                                           kDefaultWaitNs);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
+                     cudaStream_t s) {
+  return launch_tc_gemm<false>(x, w, M, N, K, y, s);
+}
+
+int launch_linear_tc_f32(const uint16_t* x, const uint16_t* w, int M, int N, int K, float* y,
+                         cudaStream_t s) {
+  return launch_tc_gemm<true>(x, w, M, N, K, y, s);
 }
 
 int launch_linear_mma(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,

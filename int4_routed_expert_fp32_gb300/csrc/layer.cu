@@ -110,7 +110,7 @@ static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x,
                     ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale, ws.scratch,
                     ws.scratch_bytes, s);
   if (rc) return rc;
-  rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, w.gate_packed,
+  rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, c.T, w.gate_packed,
                          w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,
                          c.act_bits, ws.y_sorted, ws.y_f32, ws.scratch, s);
   if (rc) return rc;

@@ -5,8 +5,14 @@
 // "Bias the choice of experts while retaining original affinities",
 // "MoEGate.forward: topk weight" and "Normalize the selected routing
 // affinities").  One expert group: group-limited masking is the identity.
+// Few tokens: split-K fp32 SIMT logits (the weight read dominates).  Many
+// tokens: the fp32 weight is split exactly into three bf16 terms and the
+// logits come from tcgen05 GEMMs with fp32 accumulation.
 #include <math.h>
 
+#include <algorithm>
+
+#include "combine.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -94,9 +100,31 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   }
 }
 
-// One warp per token: reduce the K slices in order, sigmoid, bias, k rounds of
-// warp arg-max (equal scores: lower expert id), renormalise.
+// Tokens from which the router uses the tensor cores.
+constexpr int kRtTcMinTokens = 512;
+
+// W fp32 [E, H] -> three bf16 terms [3E, H] with W = W1 + W2 + W3 to the last
+// bit of the fp32 significand (each term is the rounded remainder of the
+// previous ones); x (bf16) times each term is exact in fp32.
+__global__ void router_split_kernel(const float* __restrict__ W, size_t n, uint16_t* __restrict__ Ws) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float w = W[i];
+    const uint16_t b1 = f32_to_bf16_bits(w);
+    const float r1 = w - bf16_bits_to_f32(b1);
+    const uint16_t b2 = f32_to_bf16_bits(r1);
+    const float r2 = r1 - bf16_bits_to_f32(b2);
+    Ws[i] = b1;
+    Ws[n + i] = b2;
+    Ws[2 * n + i] = f32_to_bf16_bits(r2);
+  }
+}
+
+// One warp per token: reduce the partial logits in order (partial p of
+// (t, e) at part[p * sp + t * st + e]), sigmoid, bias, k rounds of warp
+// arg-max (equal scores: lower expert id), renormalise.
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int S,
+                                                          size_t sp, size_t st,
                                                           const float* __restrict__ bias, int T,
                                                           int E, int k, int renorm,
                                                           int32_t* __restrict__ topk_idx,
@@ -110,7 +138,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   float* sel = s + E;
   for (int e = lane; e < E; e += 32) {
     float z = 0.f;
-    for (int p = 0; p < S; ++p) z += part[((size_t)p * T + t) * E + e];
+    for (int p = 0; p < S; ++p) z += part[p * sp + t * st + e];
     const float sg = 1.0f / (1.0f + expf(-z));
     float rv = sg + bias[e];
     if (rv != rv) rv = -INFINITY;  // a NaN score never wins
@@ -159,6 +187,9 @@ using namespace moe;
 
 extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
   if (T <= 0 || H <= 0 || E <= 0) return 256;
+  if (T >= kRtTcMinTokens)  // split weights [3E, H] bf16 + logits [T, 3E] fp32
+    return align_up((size_t)3 * E * H * sizeof(uint16_t), 256) +
+           align_up((size_t)T * 3 * E * sizeof(float), 256);
   const RouterSplit sp = router_split(T, H, E);
   return align_up((size_t)sp.splits * T * E * sizeof(float), 256);
 }
@@ -172,19 +203,41 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
   if (!x || !w_router || !bias || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID;
   if (ws_bytes < moe_route_workspace_size(T, H, E)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const RouterSplit sp = router_split(T, H, E);
-  float* part = static_cast<float*>(ws);
-  dim3 grid((T + kRtTokens - 1) / kRtTokens, (E + kRtExperts - 1) / kRtExperts, sp.splits);
-  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, T, H, E, sp.kslice, part);
-  MOE_LAUNCH_CHECK();
+  float* part;
+  int S;
+  size_t sp_stride, st_stride;
+  if (T >= kRtTcMinTokens) {
+    // tensor cores: logits of the three weight terms, [T, 3E] fp32
+    uint16_t* Ws = static_cast<uint16_t*>(ws);
+    part = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                    align_up((size_t)3 * E * H * sizeof(uint16_t), 256));
+    if (!aligned(x, 16)) return MOE_ERR_INVALID;
+    const size_t n = (size_t)E * H;
+    router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(w_router, n, Ws);
+    MOE_LAUNCH_CHECK();
+    const int rc = launch_linear_tc_f32(x, Ws, T, 3 * E, H, part, s);
+    if (rc) return rc;
+    S = 3;
+    sp_stride = E;
+    st_stride = (size_t)3 * E;
+  } else {
+    const RouterSplit spl = router_split(T, H, E);
+    part = static_cast<float*>(ws);
+    dim3 grid((T + kRtTokens - 1) / kRtTokens, (E + kRtExperts - 1) / kRtExperts, spl.splits);
+    router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, T, H, E, spl.kslice, part);
+    MOE_LAUNCH_CHECK();
+    S = spl.splits;
+    sp_stride = (size_t)T * E;
+    st_stride = E;
+  }
   const int warps = 8;
   const size_t smem = (size_t)warps * (2 * E + kMaxTopK) * sizeof(float);
   if (smem > 48 * 1024) {
     MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
   }
-  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, s>>>(part, sp.splits, bias, T, E,
-                                                                        k, renorm, topk_idx, topk_w);
+  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, s>>>(
+      part, S, sp_stride, st_stride, bias, T, E, k, renorm, topk_idx, topk_w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -69,6 +69,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor of kind::f16 with fp16 A and B (fp32 accumulator).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8  (A, B format 0: f16)
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Shared-memory matrix descriptor of a K-major tile stored with the 128-byte
 // swizzle: rows of 64 bf16 (128 bytes), 8-row atoms of 1024 bytes.
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void* tile) {

@@ -255,7 +255,8 @@ def test_int4_linear_exact_mode_scaled(moe):
 @pytest.mark.parametrize("D,I,counts", [
     (320, 192, [0, 3, 40, 1, 0, 9]),
     (256, 128, [16, 16]),
-    (1024, 512, [1, 2, 65, 0]),
+    (1024, 512, [1, 2, 65, 0]),          # one expert on the tensor-core path (>= 48 rows)
+    (320, 192, [130, 5, 64, 0, 47, 48]), # ragged 128-row tails, ragged N tiles, threshold edges
 ])
 def test_expert_ffn_parity(moe, act_bits, D, I, counts):
     rng = np.random.default_rng(D + I + act_bits)
