@@ -181,15 +181,18 @@ int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* of
                    const int32_t* down_packed, const uint16_t* down_scale, int act_bits,
                    uint16_t* y_sorted, void* ws, size_t ws_bytes, void* stream);
 
-size_t moe_int4_linear_workspace_size(int E, int rows_max);
+/* Workspace bytes of moe_int4_linear (host only). */
+size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);
 
 /* One grouped PackedInt4Linear (exact-generator adaptation page, "Sources &
  * provenance"): out[r] = x[r] W_e^T for the rows r of expert e, fp32 out.
  *   x         bf16 or int8 [rows_max, K]; x_scale fp32 [rows_max] (act_bits 8)
  *   w_packed  int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
- *   out       fp32 [rows_max, N]
- * With unit weight scales and an int8 input of scale 1 the output equals the
- * integer accumulator sum_c q_x * q_w exactly (|sum| < 2^24). */
+ *   out       fp32 [rows_max, N], 16-byte aligned
+ * Experts with up to 16 rows run on the stream kernel, larger ones (when
+ * rows_max >= 48 and K % 64 == 0) on the tensor-core kernel.  With unit
+ * weight scales and an int8 input of scale 1 the output equals the integer
+ * accumulator sum_c q_x * q_w exactly on both (|sum| <= K*8*127 < 2^24). */
 int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E, int K,
                     int N, int rows_max, const int32_t* w_packed, const uint16_t* w_scale,
                     int act_bits, float* out, void* ws, size_t ws_bytes, void* stream);
@@ -257,6 +260,12 @@ const char* moe_status_string(int status);
 
 /* Library version string. */
 const char* moe_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads), counted on the host as each launch is issued; a launch that
+ * fails to start is counted too.  For measurement: the difference of two reads
+ * around a region is the number of kernels of the library issued in it. */
+uint64_t moe_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -58,7 +58,7 @@ SIGNATURES = {
     "moe_expert_ffn": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
-    "moe_int4_linear_workspace_size": (c_size_t, [c_int, c_int]),
+    "moe_int4_linear_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_int4_linear": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                 c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
@@ -74,6 +74,7 @@ SIGNATURES = {
     "moe_wait_selftest": (c_int, [c_int64, c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [c_int]),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_launch_count": (ctypes.c_uint64, []),
 }
 
 
@@ -94,6 +95,11 @@ lib = _load()
 
 def status_string(code: int) -> str:
     return lib.moe_status_string(code).decode()
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(lib.moe_launch_count())
 
 
 def _check(name: str, rc: int) -> None:
@@ -210,7 +216,7 @@ def int4_linear(x: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch
     rows, K = x.shape
     E, N = w_packed.shape[0], w_packed.shape[1]
     out = torch.empty(rows, N, dtype=torch.float32, device=x.device)
-    ws = _ws(lib.moe_int4_linear_workspace_size(E, rows), x.device)
+    ws = _ws(lib.moe_int4_linear_workspace_size(E, K, rows), x.device)
     _check("moe_int4_linear", lib.moe_int4_linear(
         _p(x), _p(x_scale), _p(offsets), E, K, N, rows, _p(w_packed), _p(w_scale), act_bits,
         _p(out), _p(ws), ws.numel(), _stream()))

@@ -60,8 +60,10 @@ __device__ __forceinline__ void load8(const float* y, size_t row, int nv, int v,
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// One CTA per token.  YT: bf16 bits or fp32 expert outputs.  NORM: RMSNorm of
-// the fp32 combined row (no intermediate rounding), times the gain.
+// CTA (t, y) combines the 16-byte column vectors y, y + gridDim.y, ... of
+// token t (gridDim.y > 1 spreads few tokens over the SMs).  YT: bf16 bits or
+// fp32 expert outputs.  NORM (gridDim.y == 1): RMSNorm of the fp32 combined
+// row (no intermediate rounding), times the gain.
 template <typename YT, bool NORM>
 __global__ void __launch_bounds__(kCbThreads) combine_kernel(
     const YT* __restrict__ y, const int32_t* __restrict__ inv_row, const float* __restrict__ w,
@@ -80,10 +82,11 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(
   const int nv = D / 8;
   uint4* ov = reinterpret_cast<uint4*>(out + (size_t)t * D);
   float ss = 0.f;
-  for (int v = threadIdx.x; v < nv; v += kCbThreads) {
+  for (int v = blockIdx.y * kCbThreads + threadIdx.x; v < nv; v += kCbThreads * gridDim.y) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int r = rows[j];
       if (r < 0) continue;
@@ -156,7 +159,12 @@ static int launch_combine_t(const YT* y, const int32_t* inv_row, const float* w,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     combine_kernel<YT, true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out);
   } else {
-    combine_kernel<YT, false><<<T, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
+    // few tokens: split each row over CTAs so that about 4 CTAs per SM run
+    const int nv = D / 8;
+    const int max_split = (nv + kCbThreads - 1) / kCbThreads;
+    const int want = (4 * num_sms() + T - 1) / T;
+    const dim3 grid(T, want < 1 ? 1 : (want > max_split ? max_split : want));
+    combine_kernel<YT, false><<<grid, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;

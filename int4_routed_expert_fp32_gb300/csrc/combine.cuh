@@ -23,9 +23,12 @@ int launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t*
                       const uint16_t* down_scale, int act_bits, void* y, bool y_f32, void* ws,
                       cudaStream_t s);
 
-// y[M, N] = x[M, K] w[N, K]^T, bf16 operands, fp32 output (tcgen05).
-int launch_linear_tc_f32(const uint16_t* x, const uint16_t* w, int M, int N, int K, float* y,
-                         cudaStream_t s);
+// Split-K partials of x[M, K] w[N, K]^T (bf16 operands, tcgen05, fp32
+// accumulation over each slice of kc columns, kc a multiple of 64):
+// y[m, z * N + n] = sum over k in [z * kc, (z + 1) * kc) of x[m, k] w[n, k],
+// z = 0 .. ceil(K / kc) - 1.
+int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
+                                float* y, cudaStream_t s);
 
 // y[M, N] = x[M, K] w[N, K]^T in bf16 with fp32 accumulation.
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,

@@ -1,5 +1,6 @@
 // Status word, device queries, tensor-map encoding, and the status /
 // self-test entry points of the C ABI.
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -17,6 +18,7 @@ int* g_status_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+std::atomic<uint64_t> g_launches{0};
 
 int current_device() {
   int d = 0;
@@ -50,6 +52,8 @@ int num_sms() {
 }
 
 void note_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
@@ -139,5 +143,7 @@ const char* moe_status_string(int status) {
 }
 
 const char* moe_version(void) { return "int4-routed-moe sm_103a 0.1"; }
+
+uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -24,6 +24,8 @@ int* status_word();
 int num_sms();
 // Record the last CUDA error for moe_check_error diagnostics.
 void note_cuda_error(cudaError_t e);
+// Count one kernel launch of this library (read by moe_launch_count).
+void count_launch();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -42,7 +44,12 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
     }                                         \
   } while (0)
 
-#define MOE_LAUNCH_CHECK() MOE_TRY_CUDA(cudaGetLastError())
+// Follows every kernel launch of the library: counts it and checks it.
+#define MOE_LAUNCH_CHECK()                    \
+  do {                                        \
+    ::moe::count_launch();                    \
+    MOE_TRY_CUDA(cudaGetLastError());         \
+  } while (0)
 
 // ---------------------------------------------------------------- device side
 

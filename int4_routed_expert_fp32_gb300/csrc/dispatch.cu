@@ -17,45 +17,50 @@ namespace moe {
 constexpr int kChunkTokens = 32;  // tokens per counting chunk (one warp)
 constexpr int kCountWarps = 4;
 
-// Per chunk of 32 tokens: the chunk's expert histogram hist[c, :] and, for
-// every (t, j), the number of earlier tokens of the chunk that chose the same
-// expert (its rank inside the chunk).
+// Per chunk of 32 tokens (one warp, lane = token): the chunk's expert
+// histogram hist[c, :] and, for every (t, j), the number of earlier tokens of
+// the chunk that chose the same expert (its rank inside the chunk).  A token
+// lists an expert at most once, so each expert keeps a 32-bit mask of the
+// chunk's tokens that chose it: count = popc(mask), rank = popc(mask & lower
+// lanes).
 __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k, int32_t* __restrict__ hist,
     int32_t* __restrict__ local_rank, int* status) {
-  extern __shared__ int32_t smc[];
+  extern __shared__ uint32_t smc[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kCountWarps + warp;
   if (c * kChunkTokens >= T) return;
-  int32_t* cnt = smc + warp * (E + kChunkTokens * kMaxTopK);
-  int32_t* ids = cnt + E;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  uint32_t* mask = smc + warp * (E + kChunkTokens * kMaxTopK);
+  int32_t* ids = reinterpret_cast<int32_t*>(mask + E) + lane * k;
+  for (int e = lane; e < E; e += 32) mask[e] = 0u;
+  __syncwarp();
   const int t = c * kChunkTokens + lane;
   const bool valid = t < T;
-  for (int j = 0; j < k; ++j) {
-    int e = valid ? idx[(size_t)t * k + j] : -1;
-    if (valid && (e < 0 || e >= E)) {
-      record_status(status, MOE_ERR_INVALID);
-      e = -1;
+  if (valid) {
+    for (int j = 0; j < k; ++j) {
+      int e = idx[(size_t)t * k + j];
+      if (e < 0 || e >= E) {
+        record_status(status, MOE_ERR_INVALID);
+        e = -1;
+      }
+      // an expert listed twice is an error; both slots then share one row,
+      // which keeps every row below the total count
+      for (int jj = 0; jj < j; ++jj)
+        if (e >= 0 && ids[jj] == e) record_status(status, MOE_ERR_INVALID);
+      ids[j] = e;
+      if (e >= 0) atomicOr(&mask[e], 1u << lane);
     }
-    ids[lane * k + j] = e;
   }
   __syncwarp();
   if (valid) {
+    const uint32_t lower = (1u << lane) - 1u;
     for (int j = 0; j < k; ++j) {
-      const int e = ids[lane * k + j];
-      if (e < 0) continue;
-      for (int jj = 0; jj < j; ++jj)
-        if (ids[lane * k + jj] == e) record_status(status, MOE_ERR_INVALID);  // listed twice
-      int rank = 0;
-      for (int l = 0; l < lane; ++l)
-        for (int jj = 0; jj < k; ++jj) rank += (ids[l * k + jj] == e);
-      local_rank[(size_t)t * k + j] = rank;
-      atomicAdd(&cnt[e], 1);
+      const int e = ids[j];
+      if (e >= 0) local_rank[(size_t)t * k + j] = __popc(mask[e] & lower);
     }
   }
   __syncwarp();
-  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = cnt[e];
+  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = __popc(mask[e]);
 }
 
 // Exclusive scan of n <= 2048 ints held in shared memory, by 1024 threads.

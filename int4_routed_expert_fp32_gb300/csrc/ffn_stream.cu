@@ -520,9 +520,14 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
   if (threadIdx.x == 0) *n_chunks = total;
 }
 
-// Experts with at least this many rows go to the tensor-core path
-// (act_bits 16); the others to the stream kernel.
-constexpr int kTcMinRows = 48;
+// Experts with more than one stream chunk of rows (>= 17) go to the
+// tensor-core path (act_bits 16): from the second chunk on the stream kernel
+// would stream the expert's weights again, while one 128-row tensor-core tile
+// dequantises them once.  The tensor-core kernels are launched only when an
+// expert can hold at least kTcMinBatchRows rows (prefill-shaped batches), so
+// that decode-shaped batches pay for no extra launches or fp16 copy.
+constexpr int kTcMinRows = kFsMc + 1;
+constexpr int kTcMinBatchRows = 48;
 
 static int max_chunks_for(int E, int rows_max, int mc) { return (rows_max + mc - 1) / mc + E; }
 
@@ -589,14 +594,17 @@ static bool scale_map(CUtensorMap* m, const uint16_t* sc, int E, int N, int K, i
                            CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-static bool tma_scales_ok(int K) { return K % kFsKc == 0; }
+// Scales by TMA: rows of a multiple of 8 groups starting on 16-byte boundaries.
+static bool tma_scales_ok(int K, const uint16_t* s0, const uint16_t* s1) {
+  return K % kFsKc == 0 && aligned(s0, 16) && aligned(s1, 16);
+}
 
 // Maps of one stream launch: w0/s0 the first (or only) matrix, w1/s1 the second.
 static bool make_maps(FsMaps* m, const int32_t* w0, const uint16_t* s0, const int32_t* w1,
                       const uint16_t* s1, int E, int N, int K, int rows) {
   if (!weight_map(&m->w0, w0, E, N, K, rows) || !weight_map(&m->w1, w1, E, N, K, rows))
     return false;
-  if (tma_scales_ok(K)) {
+  if (tma_scales_ok(K, s0, s1)) {
     if (!scale_map(&m->s0, s0, E, N, K, rows) || !scale_map(&m->s1, s1, E, N, K, rows))
       return false;
   } else {
@@ -637,10 +645,10 @@ extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_ma
   if (act_bits == 8) {
     b += align_up((size_t)rows_max * I, 256);                // h as int8
     b += align_up((size_t)rows_max * sizeof(float), 256);    // its row scales
-  } else {
-    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);  // fp16 x (tensor-core path)
-    b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);  // fp16 h (tensor-core path)
   }
+  // tensor-core path: fp16 copies of the activations and of h (or of its int8 form)
+  b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
+  b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   return b;
 }
 
@@ -652,6 +660,7 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
                            void* y, bool y_f32, void* ws, cudaStream_t s) {
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
+  const bool q8 = act_bits == 8;
   char* b = static_cast<char*>(ws);
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
@@ -659,20 +668,19 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   int8_t* hq = nullptr;
   float* hs = nullptr;
-  uint16_t* x16 = nullptr;
-  uint16_t* h16 = nullptr;
-  if (act_bits == 8) {
+  if (q8) {
     hq = reinterpret_cast<int8_t*>(b);
     b += align_up((size_t)rows_max * I, 256);
     hs = reinterpret_cast<float*>(b);
-  } else {
-    x16 = reinterpret_cast<uint16_t*>(b);
-    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
-    h16 = reinterpret_cast<uint16_t*>(b);
+    b += align_up((size_t)rows_max * sizeof(float), 256);
   }
-  // experts with many rows go to the tensor-core kernels (bf16 activations)
-  const bool use_tc = act_bits == 16 && tc_path_supported(D) && tc_path_supported(I) &&
-                      max_rows_per_expert >= kTcMinRows;
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
+  b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
+  uint16_t* h16 = reinterpret_cast<uint16_t*>(b);
+
+  // experts with more than one chunk of rows go to the tensor-core kernels
+  const bool use_tc = tc_path_supported(D) && tc_path_supported(I) &&
+                      max_rows_per_expert >= kTcMinBatchRows;
   int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max,
                            small, status, s);
   if (rc) return rc;
@@ -686,7 +694,6 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
       !make_maps(&md, down_packed, down_scale, down_packed, down_scale, E, D, I, kFsRows))
     return MOE_ERR_CUDA;
 
-  const bool q8 = act_bits == 8;
   FsParams p{};
   p.x = x_sorted;
   p.x_scale = x_scale;
@@ -701,21 +708,24 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  p.tma_scales = tma_scales_ok(D) ? 1 : 0;
+  p.tma_scales = tma_scales_ok(D, gate_scale, up_scale) ? 1 : 0;
   rc = run_stream(kGateUp, q8, mgu, p, s);
   if (rc) return rc;
   if (use_tc) {
-    rc = launch_to_f16_rows(static_cast<const uint16_t*>(x_sorted), rows_max, D, offsets + E, x16, s);
+    // act_bits 16: h of these rows in fp16 (h16); act_bits 8: in bf16 (h),
+    // re-quantised below with the stream kernel's rows
+    rc = launch_to_f16_rows(x_sorted, q8, rows_max, D, offsets + E, x16, s);
     if (rc) return rc;
-    rc = launch_tc_gateup(x16, rows_max, E, D, I, gate_packed, gate_scale, up_packed, up_scale, h16,
-                          big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+    rc = launch_tc_gateup(x16, q8 ? x_scale : nullptr, rows_max, E, D, I, gate_packed, gate_scale,
+                          up_packed, up_scale, q8 ? h : h16, big.chunk_e, big.chunk_row0,
+                          big.chunk_rows, big.n_chunks, status, s);
     if (rc) return rc;
   }
 
   FsParams pd = p;
   pd.K = I;
   pd.N = D;
-  pd.tma_scales = tma_scales_ok(I) ? 1 : 0;
+  pd.tma_scales = tma_scales_ok(I, down_scale, down_scale) ? 1 : 0;
   pd.scale0 = down_scale;
   pd.scale1 = nullptr;
   pd.out = y;
@@ -730,8 +740,13 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   rc = run_stream(y_f32 ? kLinear : kDown, q8, md, pd, s);
   if (rc) return rc;
   if (use_tc) {
-    rc = launch_tc_down(h16, rows_max, E, D, I, down_packed, down_scale, y, y_f32, big.chunk_e,
-                        big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+    if (q8) {
+      rc = launch_to_f16_rows(hq, true, rows_max, I, offsets + E, h16, s);
+      if (rc) return rc;
+    }
+    rc = launch_tc_down(h16, q8 ? hs : nullptr, rows_max, E, D, I, down_packed, down_scale, y,
+                        y_f32, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status,
+                        s);
     if (rc) return rc;
   }
   return MOE_OK;
@@ -762,9 +777,10 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
                            y_sorted, false, ws, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" size_t moe_int4_linear_workspace_size(int E, int rows_max) {
-  if (E <= 0 || rows_max < 0) return 256;
-  return schedule_bytes_one(E, rows_max, kFsMc);
+extern "C" size_t moe_int4_linear_workspace_size(int E, int K, int rows_max) {
+  if (E <= 0 || K <= 0 || rows_max < 0) return 256;
+  return schedule_bytes(E, rows_max) +
+         align_up((size_t)rows_max * K * sizeof(uint16_t), 256);  // fp16 copy (tensor cores)
 }
 
 extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E,
@@ -777,14 +793,20 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   if (rows_max == 0) return MOE_OK;
   if (!x || !offsets || !w_packed || !w_scale || !out || !ws) return MOE_ERR_INVALID;
   if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
-  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4)) return MOE_ERR_INVALID;
-  if (ws_bytes < moe_int4_linear_workspace_size(E, rows_max)) return MOE_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID;
+  if (ws_bytes < moe_int4_linear_workspace_size(E, K, rows_max)) return MOE_ERR_WORKSPACE;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool q8 = act_bits == 8;
   char* b = static_cast<char*>(ws);
-  Schedule sch = carve_one(b, E, rows_max, kFsMc);
-  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, sch, status, s);
+  Schedule small = carve_one(b, E, rows_max, kFsMc);
+  Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
+  const bool use_tc = tc_path_supported(K) && rows_max >= kTcMinBatchRows;
+  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max,
+                           small, status, s);
   if (rc) return rc;
   FsMaps m;
   if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
@@ -793,14 +815,21 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   p.x_scale = x_scale;
   p.scale0 = w_scale;
   p.out = out;
-  p.chunk_e = sch.chunk_e;
-  p.chunk_row0 = sch.chunk_row0;
-  p.chunk_rows = sch.chunk_rows;
-  p.n_chunks = sch.n_chunks;
+  p.chunk_e = small.chunk_e;
+  p.chunk_row0 = small.chunk_row0;
+  p.chunk_rows = small.chunk_rows;
+  p.n_chunks = small.n_chunks;
   p.status = status;
   p.wait_ns = kDefaultWaitNs;
   p.K = K;
   p.N = N;
-  p.tma_scales = tma_scales_ok(K) ? 1 : 0;
-  return run_stream(kLinear, act_bits == 8, m, p, s);
+  p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
+  rc = run_stream(kLinear, q8, m, p, s);
+  if (rc || !use_tc) return rc;
+  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s);
+  if (rc) return rc;
+  rc = launch_to_f16_rows(x, q8, rows_max, K, offsets + E, x16, s);
+  if (rc) return rc;
+  return launch_tc_down(x16, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale, out,
+                        true, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
 }

@@ -22,6 +22,11 @@
 //   * warps 10-13: tcgen05.ld of the accumulator; gate/up tiles hold gate in
 //     columns 0-127 and up in 128-255 and store h = SiLU(G) * U (fp16); down
 //     tiles store y (bf16, or fp32).
+// act_bits 8 (Q8): the A operand is the fp16 copy of the int8 rows (exact);
+// every product q * scale * x_q is exact in fp32 and the accumulation is in
+// fp32 (with unit scales the integer sum itself, exact while |sum| < 2^24).
+// The epilogue applies the row scales; gate/up tiles store h in bf16 for the
+// per-row re-quantisation of the down input.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -84,7 +89,7 @@ __device__ __forceinline__ uint32_t scale_f16x2(uint32_t bf16_bits) {
   return u | (u << 16);
 }
 
-template <int MODE>
+template <int MODE, bool Q8>
 __global__ void __launch_bounds__(kTxThreads, 1)
     ffn_tc_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -209,8 +214,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const bool valid = n < N;
       const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all;
       // scales: 16 bytes (8 groups = 4 stages) per load, fetched 4 stages ahead
-      // when the rows are 16-byte aligned (K % 256 == 0), else 4 bytes per stage
-      const bool vec = (G_all & 7) == 0;
+      // when the rows are 16-byte aligned (checked on the host), else 4 bytes
+      // per stage
+      const bool vec = p.vec_scales != 0;
       uint4 scur = make_uint4(0u, 0u, 0u, 0u), snxt = scur;
       if (valid) {
         if (vec) {
@@ -286,6 +292,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const uint32_t ta = tbase + b * kTxBN + (static_cast<uint32_t>(32 * qd) << 16);
       const bool vrow = mrow < rows;
       const size_t orow = static_cast<size_t>(row0 + mrow) * N;
+      const float xs = (Q8 && vrow) ? p.x_scale[row0 + mrow] : 1.0f;
       if (MODE == kTxGateUp) {
 #pragma unroll 1
         for (int c0 = 0; c0 < kTxBN / 2; c0 += 32) {
@@ -304,13 +311,25 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             uint32_t hw[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              const float h0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(v[2 * i]);
-              const float h1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(v[2 * i + 1]);
-              const __half2 hh = __floats2half2_rn(h0, h1);
-              hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
+              float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              float u0 = __uint_as_float(v[2 * i]), u1 = __uint_as_float(v[2 * i + 1]);
+              if (Q8) {
+                g0 *= xs;
+                g1 *= xs;
+                u0 *= xs;
+                u1 *= xs;
+              }
+              const float h0 = g0 / (1.0f + expf(-g0)) * u0;
+              const float h1 = g1 / (1.0f + expf(-g1)) * u1;
+              if (Q8) {  // bf16 h, as the stream kernel writes it
+                hw[i] = static_cast<uint32_t>(f32_to_bf16_bits(h0)) |
+                        (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
+              } else {
+                const __half2 hh = __floats2half2_rn(h0, h1);
+                hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
+              }
             }
-            if (col + 32 <= N) {
+            if (col + 32 <= N && (N & 7) == 0) {
               uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
@@ -334,9 +353,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) fin &= fabsf(__uint_as_float(y[i])) <= 3.0e38f;
             if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
+            if (Q8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * xs);
+            }
             if (MODE == kTxDown) {
               uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
-              if (col + 32 <= N) {
+              if (col + 32 <= N && (N & 7) == 0) {
                 uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -355,7 +378,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
               }
             } else {
               float* dst = static_cast<float*>(p.out) + orow + col;
-              if (col + 32 <= N) {
+              if (col + 32 <= N && (N & 3) == 0) {
                 float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -391,29 +414,51 @@ static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K) {
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// bf16 -> fp16 copy of the rows below *row_count (one warp per row).
-__global__ void __launch_bounds__(256) to_f16_rows_kernel(const uint16_t* __restrict__ src, int R,
+// int8 pair (bytes at bit offsets a, b of w) -> fp16x2, exactly.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t w, int a, int b) {
+  const float lo = static_cast<float>(static_cast<int8_t>((w >> a) & 0xffu));
+  const float hi = static_cast<float>(static_cast<int8_t>((w >> b) & 0xffu));
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 copy of the bf16 (I8 = false) or int8 (I8 = true) rows below
+// *row_count (one warp per row, 8 values per lane step).
+template <bool I8>
+__global__ void __launch_bounds__(256) to_f16_rows_kernel(const void* __restrict__ src, int R,
                                                           int C, const int32_t* row_count,
                                                           uint16_t* __restrict__ dst) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= R || r >= *row_count) return;
-  const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)r * C);
   uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)r * C);
-  for (int v = lane; v < C / 8; v += 32) {
-    uint4 x = s4[v];
-    x.x = bf16x2_to_f16x2(x.x);
-    x.y = bf16x2_to_f16x2(x.y);
-    x.z = bf16x2_to_f16x2(x.z);
-    x.w = bf16x2_to_f16x2(x.w);
-    d4[v] = x;
+  if (!I8) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + (size_t)r * C);
+    for (int v = lane; v < C / 8; v += 32) {
+      uint4 x = s4[v];
+      x.x = bf16x2_to_f16x2(x.x);
+      x.y = bf16x2_to_f16x2(x.y);
+      x.z = bf16x2_to_f16x2(x.z);
+      x.w = bf16x2_to_f16x2(x.w);
+      d4[v] = x;
+    }
+  } else {
+    const uint2* s2 = reinterpret_cast<const uint2*>(static_cast<const int8_t*>(src) + (size_t)r * C);
+    for (int v = lane; v < C / 8; v += 32) {
+      const uint2 q = s2[v];
+      d4[v] = make_uint4(i8x2_to_f16x2(q.x, 0, 8), i8x2_to_f16x2(q.x, 16, 24),
+                         i8x2_to_f16x2(q.y, 0, 8), i8x2_to_f16x2(q.y, 16, 24));
+    }
   }
 }
 
-int launch_to_f16_rows(const uint16_t* src, int R, int C, const int32_t* row_count, uint16_t* dst,
-                       cudaStream_t s) {
+int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
+                       uint16_t* dst, cudaStream_t s) {
   if (R == 0) return MOE_OK;
-  to_f16_rows_kernel<<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst);
+  if (src_i8)
+    to_f16_rows_kernel<true><<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst);
+  else
+    to_f16_rows_kernel<false><<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -429,9 +474,9 @@ static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
                            CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-template <int MODE>
+template <int MODE, bool Q8>
 static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
-  auto kern = ffn_tc_kernel<MODE>;
+  auto kern = ffn_tc_kernel<MODE, Q8>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTxSmem));
   kern<<<num_sms(), kTxThreads, kTxSmem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
@@ -440,9 +485,13 @@ static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
 
 bool tc_path_supported(int K) { return K % kTxBK == 0; }
 
-int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
+bool scale_rows_16b(const uint16_t* scale, int K) {
+  return (K / kGroup) % 8 == 0 && aligned(scale, 16);
+}
+
+int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
-                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h16,
+                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e,
                      const int32_t* chunk_row0, const int32_t* chunk_rows, const int32_t* n_chunks,
                      int* status, cudaStream_t s) {
@@ -454,7 +503,8 @@ int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
   TxParams p{};
   p.scale0 = gate_scale;
   p.scale1 = up_scale;
-  p.out = h16;
+  p.x_scale = x_scale;
+  p.out = h;
   p.chunk_e = chunk_e;
   p.chunk_row0 = chunk_row0;
   p.chunk_rows = chunk_rows;
@@ -463,10 +513,11 @@ int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  return launch_tc<kTxGateUp>(maps, p, s);
+  p.vec_scales = scale_rows_16b(gate_scale, D) && scale_rows_16b(up_scale, D);
+  return x_scale ? launch_tc<kTxGateUp, true>(maps, p, s) : launch_tc<kTxGateUp, false>(maps, p, s);
 }
 
-int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
+int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s) {
@@ -477,6 +528,7 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
   TxParams p{};
   p.scale0 = down_scale;
   p.scale1 = down_scale;
+  p.x_scale = h_scale;
   p.out = y;
   p.chunk_e = chunk_e;
   p.chunk_row0 = chunk_row0;
@@ -486,7 +538,10 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
   p.wait_ns = kDefaultWaitNs;
   p.K = I;
   p.N = D;
-  return y_f32 ? launch_tc<kTxLinear>(maps, p, s) : launch_tc<kTxDown>(maps, p, s);
+  p.vec_scales = scale_rows_16b(down_scale, I);
+  if (h_scale)
+    return y_f32 ? launch_tc<kTxLinear, true>(maps, p, s) : launch_tc<kTxDown, true>(maps, p, s);
+  return y_f32 ? launch_tc<kTxLinear, false>(maps, p, s) : launch_tc<kTxDown, false>(maps, p, s);
 }
 
 }  // namespace moe

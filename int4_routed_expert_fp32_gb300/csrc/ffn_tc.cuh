@@ -11,7 +11,8 @@ namespace moe {
 struct TxParams {
   const uint16_t* scale0;  // bf16 [E, N, K/32] (gate, or the single matrix)
   const uint16_t* scale1;  // bf16 [E, N, K/32] (up)
-  void* out;               // bf16 h / bf16 y / fp32 y  [rows_max, N]
+  const float* x_scale;    // act_bits 8: row scales of the int8 rows, else null
+  void* out;               // fp16 h (bf16 h in act_bits 8) / bf16 y / fp32 y  [rows_max, N]
   const int32_t* chunk_e;
   const int32_t* chunk_row0;
   const int32_t* chunk_rows;
@@ -20,6 +21,7 @@ struct TxParams {
   long long wait_ns;
   int K;
   int N;
+  int vec_scales;  // scale rows 16-byte aligned: 8 groups per load
 };
 
 struct TxMaps {
@@ -34,21 +36,27 @@ constexpr int kTcChunkRows = 128;
 // K of the tensor-core path must be a multiple of 64.
 bool tc_path_supported(int K);
 
-// fp16 copy of bf16 rows [R, C] below *row_count.
-int launch_to_f16_rows(const uint16_t* src, int R, int C, const int32_t* row_count, uint16_t* dst,
-                       cudaStream_t s);
+// Scale rows of [E, N, K/32] bf16 at `scale` start on 16-byte boundaries.
+bool scale_rows_16b(const uint16_t* scale, int K);
 
-// h16[rows] = fp16(SiLU(x W_gate^T) * (x W_up^T)) for the listed 128-row
-// chunks; x16 is the fp16 copy of the activations.
-int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
+// fp16 copy of bf16 (src_i8 false) or int8 (src_i8 true) rows [R, C] below
+// *row_count.
+int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
+                       uint16_t* dst, cudaStream_t s);
+
+// h[rows] = SiLU(x W_gate^T) * (x W_up^T) for the listed 128-row chunks; x16
+// is the fp16 copy of the activations.  x_scale null: bf16 activations, h in
+// fp16.  x_scale set: int8 activations with these row scales, h in bf16.
+int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
-                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h16,
+                     const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e, const int32_t* chunk_row0,
                      const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
                      cudaStream_t s);
 
-// y[rows] = h16 W_down^T (bf16, or fp32 with y_f32) for the listed chunks.
-int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
+// y[rows] = h16 W_down^T (times h_scale[row] when given: int8 rows) for the
+// listed chunks; bf16 y, or fp32 with y_f32.
+int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s);

@@ -138,10 +138,14 @@ constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024 + 256;
 constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: epilogue
 constexpr uint32_t kTcCols = 256;
 
+// CTA (x, y, z) computes the 128 x 256 tile (y, x) over the K slice
+// [z * kc, min(K, (z + 1) * kc)) and stores it at columns z * N + n of rows of
+// ldc elements (split-K partials side by side; z = 0, ldc = N: plain C).
 template <bool F32OUT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                   void* __restrict__ Cout, int M, int N, int K, int* status, long long wait_ns) {
+                   void* __restrict__ Cout, int M, int N, int K, int kc, int ldc, int* status,
+                   long long wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -169,7 +173,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const int m0 = blockIdx.y * kTcBM, n0 = blockIdx.x * kTcBN;
-  const int ktiles = (K + kTcBK - 1) / kTcBK;
+  const int kbase = blockIdx.z * kc;
+  const int ktiles = (min(K - kbase, kc) + kTcBK - 1) / kTcBK;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -181,8 +186,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(&empty[s], ph ^ 1u, wait_ns, status)) break;
         uint8_t* st = smem + s * kTcStageBytes;
         mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-        tma_g2s_2d(st, &ma, &full[s], kt * kTcBK, m0);
-        tma_g2s_2d(st + kTcABytes, &mb, &full[s], kt * kTcBK, n0);
+        tma_g2s_2d(st, &ma, &full[s], kbase + kt * kTcBK, m0);
+        tma_g2s_2d(st + kTcABytes, &mb, &full[s], kbase + kt * kTcBK, n0);
       }
     }
   } else if (warp == 1) {
@@ -220,8 +225,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld_wait();
         const int col = n0 + c0;
         if (F32OUT && row < M && col < N) {
-          float* dst = static_cast<float*>(Cout) + (size_t)row * N + col;
-          if (col + 32 <= N && (N & 3) == 0) {
+          float* dst = static_cast<float*>(Cout) + (size_t)row * ldc + (size_t)blockIdx.z * N + col;
+          if (col + 32 <= N && (N & 3) == 0 && (ldc & 3) == 0) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -233,8 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (col + i < N) dst[i] = __uint_as_float(r[i]);
           }
         } else if (row < M && col < N) {
-          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * N + col;
-          if (col + 32 <= N) {
+          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * ldc + (size_t)blockIdx.z * N + col;
+          if (col + 32 <= N && (N & 7) == 0 && (ldc & 7) == 0) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -272,17 +277,18 @@ static bool bf16_map(CUtensorMap* m, const uint16_t* base, int rows, int K, int 
 }
 
 template <bool F32OUT>
-static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, int K, void* y,
-                          cudaStream_t s) {
+static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
+                          int ldc, void* y, cudaStream_t s) {
   if (M == 0) return MOE_OK;
+  if (kc <= 0 || kc % kTcBK != 0) return MOE_ERR_INVALID;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   CUtensorMap ma, mb;
   if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map(&mb, w, N, K, kTcBN)) return MOE_ERR_CUDA;
   MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<F32OUT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem));
-  dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
-  gemm_tc_kernel<F32OUT><<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, status,
+  dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM, (K + kc - 1) / kc);
+  gemm_tc_kernel<F32OUT><<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, kc, ldc, status,
                                                            kDefaultWaitNs);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -290,12 +296,13 @@ static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, in
 
 int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                      cudaStream_t s) {
-  return launch_tc_gemm<false>(x, w, M, N, K, y, s);
+  return launch_tc_gemm<false>(x, w, M, N, K, (K + kTcBK - 1) / kTcBK * kTcBK, N, y, s);
 }
 
-int launch_linear_tc_f32(const uint16_t* x, const uint16_t* w, int M, int N, int K, float* y,
-                         cudaStream_t s) {
-  return launch_tc_gemm<true>(x, w, M, N, K, y, s);
+int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
+                                float* y, cudaStream_t s) {
+  const int splits = (K + kc - 1) / kc;
+  return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, y, s);
 }
 
 int launch_linear_mma(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,

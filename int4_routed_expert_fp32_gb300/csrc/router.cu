@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 
 // Tokens from which the router uses the tensor cores.
 constexpr int kRtTcMinTokens = 512;
+// K columns per tensor-core accumulation; the slices' fp32 partials are added
+// in order afterwards (a short accumulation chain per partial, as in the
+// split-K SIMT path).
+constexpr int kRtTcKSlice = 1024;
+
+static int router_tc_splits(int H) { return (H + kRtTcKSlice - 1) / kRtTcKSlice; }
 
 // W fp32 [E, H] -> three bf16 terms [3E, H] with W = W1 + W2 + W3 to the last
 // bit of the fp32 significand (each term is the rounded remainder of the
@@ -120,32 +126,42 @@ __global__ void router_split_kernel(const float* __restrict__ W, size_t n, uint1
   }
 }
 
-// One warp per token: reduce the partial logits in order (partial p of
-// (t, e) at part[p * sp + t * st + e]), sigmoid, bias, k rounds of warp
-// arg-max (equal scores: lower expert id), renormalise.
-__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int S,
-                                                          size_t sp, size_t st,
-                                                          const float* __restrict__ bias, int T,
-                                                          int E, int k, int renorm,
-                                                          int32_t* __restrict__ topk_idx,
-                                                          float* __restrict__ topk_w) {
+// One CTA per token.  Its threads reduce the partial logits of the token in
+// order (partial p of (t, e) at part[p * sp + t * st + e]), then take the
+// sigmoid and add the bias; warp 0 runs k rounds of warp arg-max (equal
+// scores: lower expert id) and renormalises.
+constexpr int kTopkThreads = 128;
+
+__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
+    const float* __restrict__ part, int S, size_t sp, size_t st, const float* __restrict__ bias,
+    int T, int E, int k, int renorm, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   extern __shared__ float sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
-  float* r = sm + warp * (2 * E + kMaxTopK);
-  float* s = r + E;
-  float* sel = s + E;
-  for (int e = lane; e < E; e += 32) {
+  __shared__ float sel[kMaxTopK];
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  float* r = sm;
+  float* s = sm + E;
+  const float* pt = part + (size_t)t * st;
+  for (int e = threadIdx.x; e < E; e += kTopkThreads) {
+    const float* pe = pt + e;
     float z = 0.f;
-    for (int p = 0; p < S; ++p) z += part[p * sp + t * st + e];
+    int p = 0;
+    for (; p + 8 <= S; p += 8) {  // loads issued together, summed in order
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = pe[(size_t)(p + i) * sp];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) z += v[i];
+    }
+    for (; p < S; ++p) z += pe[(size_t)p * sp];
     const float sg = 1.0f / (1.0f + expf(-z));
     float rv = sg + bias[e];
     if (rv != rv) rv = -INFINITY;  // a NaN score never wins
     s[e] = sg;
     r[e] = rv;
   }
-  __syncwarp();
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
   for (int j = 0; j < k; ++j) {
     float best = -INFINITY;
     int bi = E;
@@ -187,9 +203,9 @@ using namespace moe;
 
 extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
   if (T <= 0 || H <= 0 || E <= 0) return 256;
-  if (T >= kRtTcMinTokens)  // split weights [3E, H] bf16 + logits [T, 3E] fp32
+  if (T >= kRtTcMinTokens)  // split weights [3E, H] bf16 + partials [T, splits * 3E] fp32
     return align_up((size_t)3 * E * H * sizeof(uint16_t), 256) +
-           align_up((size_t)T * 3 * E * sizeof(float), 256);
+           align_up((size_t)T * router_tc_splits(H) * 3 * E * sizeof(float), 256);
   const RouterSplit sp = router_split(T, H, E);
   return align_up((size_t)sp.splits * T * E * sizeof(float), 256);
 }
@@ -207,7 +223,8 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
   int S;
   size_t sp_stride, st_stride;
   if (T >= kRtTcMinTokens) {
-    // tensor cores: logits of the three weight terms, [T, 3E] fp32
+    // tensor cores: partial logits of the three weight terms per K slice,
+    // [T, splits, 3, E] fp32, summed in that order
     uint16_t* Ws = static_cast<uint16_t*>(ws);
     part = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                     align_up((size_t)3 * E * H * sizeof(uint16_t), 256));
@@ -215,11 +232,12 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
     const size_t n = (size_t)E * H;
     router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(w_router, n, Ws);
     MOE_LAUNCH_CHECK();
-    const int rc = launch_linear_tc_f32(x, Ws, T, 3 * E, H, part, s);
+    const int splits = router_tc_splits(H);
+    const int rc = launch_linear_tc_f32_splitk(x, Ws, T, 3 * E, H, kRtTcKSlice, part, s);
     if (rc) return rc;
-    S = 3;
+    S = 3 * splits;
     sp_stride = E;
-    st_stride = (size_t)3 * E;
+    st_stride = (size_t)S * E;
   } else {
     const RouterSplit spl = router_split(T, H, E);
     part = static_cast<float*>(ws);
@@ -230,14 +248,9 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
     sp_stride = (size_t)T * E;
     st_stride = E;
   }
-  const int warps = 8;
-  const size_t smem = (size_t)warps * (2 * E + kMaxTopK) * sizeof(float);
-  if (smem > 48 * 1024) {
-    MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
-  }
-  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, s>>>(
-      part, S, sp_stride, st_stride, bias, T, E, k, renorm, topk_idx, topk_w);
+  const size_t smem = (size_t)2 * E * sizeof(float);  // at most 16 KiB (E <= 2048)
+  router_topk_kernel<<<T, kTopkThreads, smem, s>>>(part, S, sp_stride, st_stride, bias, T, E, k,
+                                                   renorm, topk_idx, topk_w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -64,6 +64,7 @@ def test_workspace_sizes_are_host_only(capi):
 def test_argument_errors_return_before_any_launch(capi):
     L = capi.lib
     n = None
+    launches = capi.launch_count()
     # null pointers
     assert L.moe_route(n, n, n, 4, 64, 8, 2, 1, n, n, n, 0, n) == capi.MOE_ERR_INVALID
     # unsupported shapes
@@ -85,6 +86,7 @@ def test_argument_errors_return_before_any_launch(capi):
     bad = capi.MoeConfig(4, 64, 8, 2, 64, 0, 4, 1, 1e-6)
     assert L.moe_layer_forward(ctypes.byref(bad), ctypes.byref(w), n, n, n, 0, n) == \
         capi.MOE_ERR_UNSUPPORTED
+    assert capi.launch_count() == launches
 
 
 def test_workspace_too_small_is_reported(capi):

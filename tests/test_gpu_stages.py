@@ -50,6 +50,9 @@ ROUTE_CASES = {
     "k1": wl.workload("tiny", name="k1", T=33, H=128, E=5, k=1, seed=4),
     "k_eq_E": wl.workload("tiny", name="kE", T=9, H=64, E=4, k=4, seed=5),
     "no_renorm": wl.workload("tiny", name="nr", T=40, H=256, E=24, k=3, renorm=False, seed=6),
+    # from 512 tokens the logits come from the tensor cores: ragged in both
+    # the 128-token and the 256-logit tiles
+    "tc_ragged": wl.workload("tiny", name="tc_ragged", T=601, H=512, E=100, k=6, seed=7),
 }
 
 
@@ -72,6 +75,20 @@ def test_route_parity(moe, case):
         # slots in descending ranking score (up to fp32 rounding of the scores)
         r = rt.r[t, gi[t]]
         assert np.all(np.diff(r) <= 1e-6)
+
+
+@pytest.mark.parametrize("T,kernels", [(40, 2), (512, 3)])
+def test_route_launch_count(moe, T, kernels):
+    # the library counts its launches: SIMT logits + top-k below 512 tokens,
+    # weight split + tensor-core logits + top-k from 512
+    w = wl.workload("tiny", name="lc", T=T, H=256, E=24, k=3, seed=8)
+    x = wl.gen_x(w)
+    W, b = wl.gen_router(w)
+    xd, Wd, bd = x.to(DEV), W.to(DEV), b.to(DEV)
+    n0 = moe.launch_count()
+    moe.route(xd, Wd, bd, w.k, w.renorm)
+    assert moe.launch_count() - n0 == kernels
+    assert moe.check_error() == 0
 
 
 def test_route_prefill_full(moe):
@@ -202,7 +219,11 @@ def test_int4_linear_w4a16(moe, K, N, counts):
         assert rel_l2(got[a:b], ref) <= 1e-5
 
 
-@pytest.mark.parametrize("K,N,counts", [(320, 300, [0, 1, 33, 70, 8]), (7168, 256, [2, 40])])
+@pytest.mark.parametrize("K,N,counts", [
+    (320, 300, [0, 1, 33, 70, 8]),   # 33 and 70 rows on the tensor cores
+    (7168, 256, [2, 40]),            # all on the stream kernel (fewer than 48 rows)
+    (7168, 256, [2, 40, 17]),        # 40 and 17 rows on the tensor cores, full hidden width
+])
 def test_int4_linear_exact_integer_accumulators(moe, K, N, counts):
     """Unit scales and an int8 input of scale 1: the output is the integer sum
     itself and must match the int64 oracle bit for bit (|sum| <= K*8*127 < 2^24)."""
@@ -255,8 +276,9 @@ def test_int4_linear_exact_mode_scaled(moe):
 @pytest.mark.parametrize("D,I,counts", [
     (320, 192, [0, 3, 40, 1, 0, 9]),
     (256, 128, [16, 16]),
-    (1024, 512, [1, 2, 65, 0]),          # one expert on the tensor-core path (>= 48 rows)
-    (320, 192, [130, 5, 64, 0, 47, 48]), # ragged 128-row tails, ragged N tiles, threshold edges
+    (1024, 512, [1, 2, 65, 0]),          # one expert on the tensor-core path (>= 17 rows)
+    (320, 192, [130, 5, 64, 0, 16, 17]), # ragged 128-row tails, ragged N tiles, threshold edges
+    (256, 128, [16, 16, 16, 0, 3]),      # tensor-core kernels launched with no tile to do
 ])
 def test_expert_ffn_parity(moe, act_bits, D, I, counts):
     rng = np.random.default_rng(D + I + act_bits)
