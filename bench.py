@@ -150,9 +150,11 @@ def _setup(w: wl.Workload, device):
 
 
 def _ffn_pass(moe, w, layer, weights, x_dev, steps):
-    """Average duration of the expert-FFN call (schedule + gate/up + down stream
-    kernels) inside a layer step, timed with CUDA events on its stream; the step
-    is the same work as moe_layer_forward, issued stage by stage."""
+    """Average duration of the expert-FFN call (moe_expert_ffn_pairs: schedules,
+    stream and tensor-core kernels) inside a layer step, timed with CUDA events
+    on its stream; the step is the work of moe_layer_forward, issued stage by
+    stage through the C ABI (on the latent path the layer keeps y in fp32; this
+    replay writes bf16 y)."""
     lib = moe.lib
     dev = x_dev.device
     T, k, E, D, I = w.T, w.k, w.E, w.D, w.I
@@ -164,7 +166,7 @@ def _ffn_pass(moe, w, layer, weights, x_dev, steps):
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     rt, rs, inv = (torch.empty(R, dtype=torch.int32, device=dev) for _ in range(3))
-    xs = torch.empty(R, D, dtype=torch.bfloat16 if w.act_bits == 16 else torch.int8, device=dev)
+    xs = torch.empty(R, D, dtype=torch.float16 if w.act_bits == 16 else torch.int8, device=dev)
     xsc = torch.empty(R, dtype=torch.float32, device=dev) if w.act_bits == 8 else None
     y = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
     out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
@@ -172,7 +174,7 @@ def _ffn_pass(moe, w, layer, weights, x_dev, steps):
     if w.L:
         u = moe.linear_bf16(x_dev, weights["lat_down"])
     ws_n = max(lib.moe_route_workspace_size(T, w.H, E), lib.moe_dispatch_workspace_size(T, E, k),
-               lib.moe_expert_ffn_workspace_size(E, D, I, R, w.act_bits))
+               lib.moe_expert_ffn_pairs_workspace_size(E, D, I, R, w.act_bits))
     ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -180,15 +182,16 @@ def _ffn_pass(moe, w, layer, weights, x_dev, steps):
     def step(i=None):
         assert lib.moe_route(p(x_dev), p(weights["router_w"]), p(weights["router_bias"]), T, w.H, E,
                              k, int(w.renorm), p(idx), p(tw), p(ws), ws.numel(), s) == 0
-        assert lib.moe_dispatch(p(idx), p(u), T, D, E, k, w.act_bits, p(counts), p(offsets), p(rt),
-                                p(rs), p(inv), p(xs), p(xsc), p(ws), ws.numel(), s) == 0
+        assert lib.moe_dispatch_pairs(p(idx), p(u), T, D, E, k, w.act_bits, p(counts), p(offsets),
+                                      p(rt), p(rs), p(inv), p(xs), p(xsc), p(ws), ws.numel(),
+                                      s) == 0
         if i is not None:
             ev[i][0].record()
-        assert lib.moe_expert_ffn(p(xs), p(xsc), p(offsets), E, D, I, R, p(weights["gate_packed"]),
-                                  p(weights["gate_scale"]), p(weights["up_packed"]),
-                                  p(weights["up_scale"]), p(weights["down_packed"]),
-                                  p(weights["down_scale"]), w.act_bits, p(y), p(ws), ws.numel(),
-                                  s) == 0
+        assert lib.moe_expert_ffn_pairs(p(xs), p(xsc), p(offsets), E, D, I, R,
+                                        p(weights["gate_packed"]), p(weights["gate_scale"]),
+                                        p(weights["up_packed"]), p(weights["up_scale"]),
+                                        p(weights["down_packed"]), p(weights["down_scale"]),
+                                        w.act_bits, p(y), p(ws), ws.numel(), s) == 0
         if i is not None:
             ev[i][1].record()
         assert lib.moe_combine(p(y), p(inv), p(tw), T, D, k, p(out), s) == 0
@@ -351,8 +354,8 @@ def main(argv=None):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     roof.update({"traffic": _profiled_traffic(w.name),
-                 "kernel": "expert FFN call (schedule; ffn_stream_kernel for experts below 48 rows, "
-                           "to_f16_rows + ffn_tc_kernel gate/up and down above)",
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_kernel for "
+                           "experts of <= 16 rows, ffn_tc_kernel gate/up and down above)",
                  "kernel_ms": ffn_ms,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                  "active_experts": active, "peak_source": peaks["source"]})

@@ -135,6 +135,18 @@ int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E
                  int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* Same as moe_dispatch, but x_sorted is written in the expert kernels' "pair
+ * order": in every block of 8 columns the values are stored as columns
+ * 0 4 1 5 2 6 3 7 (the order in which a packed int32 word pairs its
+ * nibbles), as fp16 (act_bits 16; a bf16 value beyond the fp16 range records
+ * MOE_ERR_UNSUPPORTED) or int8 (act_bits 8).  These are the rows
+ * moe_expert_ffn_pairs reads; moe_layer_forward uses this pair of calls.
+ * No page has this layout: it is the GB300 kernels' operand order. */
+int moe_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                       int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                       int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                       void* ws, size_t ws_bytes, void* stream);
+
 /* Same as moe_dispatch, for callers that cannot provide device memory.
  *
  * No page has a counterpart of this call: it exists for host programs that
@@ -173,13 +185,30 @@ size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_
  *   weights   gate/up [E, I, D/8] + bf16 [E, I, D/32]; down [E, D, I/8] +
  *             bf16 [E, D, I/32]
  *   y_sorted  bf16 [rows_max, D] out (rows >= offsets[E] untouched)
- * The intermediate h = SiLU(G) * U is computed in fp32 and stored as bf16; in
- * act_bits 8 mode it is re-quantised per row before the down projection. */
+ * x_sorted is first copied into the kernels' pair order (see
+ * moe_dispatch_pairs).  The intermediate h = SiLU(G) * U is computed in fp32
+ * and stored as fp16 (bf16 in act_bits 8 mode, where it is re-quantised per
+ * row before the down projection).  A value beyond the fp16 range records
+ * MOE_ERR_UNSUPPORTED. */
 int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets, int E,
                    int D, int I, int rows_max, const int32_t* gate_packed,
                    const uint16_t* gate_scale, const int32_t* up_packed, const uint16_t* up_scale,
                    const int32_t* down_packed, const uint16_t* down_scale, int act_bits,
                    uint16_t* y_sorted, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of moe_expert_ffn_pairs (host only). */
+size_t moe_expert_ffn_pairs_workspace_size(int E, int D, int I, int rows_max, int act_bits);
+
+/* moe_expert_ffn over rows already in pair order, as moe_dispatch_pairs
+ * writes them (fp16, or int8 with act_bits 8); same weights, offsets, y and
+ * error behaviour, without the conversion pass of moe_expert_ffn.  The
+ * intermediate h is kept in fp16 (act_bits 16). */
+int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale, const int32_t* offsets, int E,
+                         int D, int I, int rows_max, const int32_t* gate_packed,
+                         const uint16_t* gate_scale, const int32_t* up_packed,
+                         const uint16_t* up_scale, const int32_t* down_packed,
+                         const uint16_t* down_scale, int act_bits, uint16_t* y_sorted, void* ws,
+                         size_t ws_bytes, void* stream);
 
 /* Workspace bytes of moe_int4_linear (host only). */
 size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);

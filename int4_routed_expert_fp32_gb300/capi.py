@@ -51,6 +51,9 @@ SIGNATURES = {
     "moe_dispatch": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_size_t, c_void_p]),
+    "moe_dispatch_pairs": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_dispatch_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p]),
@@ -58,6 +61,10 @@ SIGNATURES = {
     "moe_expert_ffn": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_expert_ffn_pairs_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "moe_expert_ffn_pairs": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_int4_linear_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_int4_linear": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                 c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -143,24 +150,33 @@ def route(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor, k: int, r
     return idx, w
 
 
-def dispatch(topk_idx: torch.Tensor, x: torch.Tensor, E: int, act_bits: int = 16) -> Dict[str, torch.Tensor]:
-    """Counts, offsets, the stable expert-major permutation and the gathered rows."""
-    _dev(topk_idx, torch.int32); _dev(x, torch.bfloat16)
-    T, k = topk_idx.shape
-    D = x.shape[1]
-    dev = x.device
+def _dispatch_out(T: int, k: int, D: int, E: int, act_bits: int, pairs: bool, dev):
     R = T * k
-    out = {
+    xdt = torch.int8 if act_bits == 8 else (torch.float16 if pairs else torch.bfloat16)
+    return {
         "counts": torch.empty(E, dtype=torch.int32, device=dev),
         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
         "row_token": torch.empty(R, dtype=torch.int32, device=dev),
         "row_slot": torch.empty(R, dtype=torch.int32, device=dev),
         "inv_row": torch.empty(R, dtype=torch.int32, device=dev),
-        "x_sorted": torch.empty(R, D, dtype=torch.bfloat16 if act_bits == 16 else torch.int8, device=dev),
+        "x_sorted": torch.empty(R, D, dtype=xdt, device=dev),
         "x_scale": torch.empty(R, dtype=torch.float32, device=dev) if act_bits == 8 else None,
     }
+
+
+def dispatch(topk_idx: torch.Tensor, x: torch.Tensor, E: int, act_bits: int = 16,
+             pairs: bool = False) -> Dict[str, torch.Tensor]:
+    """Counts, offsets, the stable expert-major permutation and the gathered
+    rows (pairs=True: moe_dispatch_pairs, rows in the expert kernels' pair
+    order, fp16 or int8)."""
+    _dev(topk_idx, torch.int32); _dev(x, torch.bfloat16)
+    T, k = topk_idx.shape
+    D = x.shape[1]
+    dev = x.device
+    out = _dispatch_out(T, k, D, E, act_bits, pairs, dev)
     ws = _ws(lib.moe_dispatch_workspace_size(T, E, k), dev)
-    _check("moe_dispatch", lib.moe_dispatch(
+    name = "moe_dispatch_pairs" if pairs else "moe_dispatch"
+    _check(name, getattr(lib, name)(
         _p(topk_idx), _p(x), T, D, E, k, act_bits, _p(out["counts"]), _p(out["offsets"]),
         _p(out["row_token"]), _p(out["row_slot"]), _p(out["inv_row"]), _p(out["x_sorted"]),
         _p(out["x_scale"]), _p(ws), ws.numel(), _stream()))
@@ -176,16 +192,7 @@ def dispatch_noalloc(topk_idx: torch.Tensor, x: torch.Tensor, E: int,
     T, k = topk_idx.shape
     D = x.shape[1]
     dev = x.device
-    R = T * k
-    out = {
-        "counts": torch.empty(E, dtype=torch.int32, device=dev),
-        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
-        "row_token": torch.empty(R, dtype=torch.int32, device=dev),
-        "row_slot": torch.empty(R, dtype=torch.int32, device=dev),
-        "inv_row": torch.empty(R, dtype=torch.int32, device=dev),
-        "x_sorted": torch.empty(R, D, dtype=torch.bfloat16 if act_bits == 16 else torch.int8, device=dev),
-        "x_scale": torch.empty(R, dtype=torch.float32, device=dev) if act_bits == 8 else None,
-    }
+    out = _dispatch_out(T, k, D, E, act_bits, False, dev)
     _check("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
         _p(topk_idx), _p(x), T, D, E, k, act_bits, _p(out["counts"]), _p(out["offsets"]),
         _p(out["row_token"]), _p(out["row_slot"]), _p(out["inv_row"]), _p(out["x_sorted"]),
@@ -194,14 +201,17 @@ def dispatch_noalloc(topk_idx: torch.Tensor, x: torch.Tensor, E: int,
 
 
 def expert_ffn(x_sorted: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.Tensor,
-               experts: Dict[str, torch.Tensor], act_bits: int = 16) -> torch.Tensor:
-    """y_sorted bf16 [rows, D] = down(SiLU(gate(x)) * up(x)) per expert segment."""
+               experts: Dict[str, torch.Tensor], act_bits: int = 16,
+               pairs: bool = False) -> torch.Tensor:
+    """y_sorted bf16 [rows, D] = down(SiLU(gate(x)) * up(x)) per expert segment
+    (pairs=True: moe_expert_ffn_pairs on rows from dispatch(..., pairs=True))."""
     _dev(x_sorted); _dev(offsets, torch.int32)
     rows, D = x_sorted.shape
     E, I = experts["gate_packed"].shape[0], experts["gate_packed"].shape[1]
     y = torch.empty(rows, D, dtype=torch.bfloat16, device=x_sorted.device)
-    ws = _ws(lib.moe_expert_ffn_workspace_size(E, D, I, rows, act_bits), x_sorted.device)
-    _check("moe_expert_ffn", lib.moe_expert_ffn(
+    name = "moe_expert_ffn_pairs" if pairs else "moe_expert_ffn"
+    ws = _ws(getattr(lib, name + "_workspace_size")(E, D, I, rows, act_bits), x_sorted.device)
+    _check(name, getattr(lib, name)(
         _p(x_sorted), _p(x_scale), _p(offsets), E, D, I, rows,
         _p(experts["gate_packed"]), _p(experts["gate_scale"]), _p(experts["up_packed"]),
         _p(experts["up_scale"]), _p(experts["down_packed"]), _p(experts["down_scale"]), act_bits,

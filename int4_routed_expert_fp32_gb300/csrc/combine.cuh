@@ -15,6 +15,11 @@ int launch_combine(const void* y, bool y_f32, const int32_t* inv_row, const floa
 // Gated expert MLP over expert-sorted rows (validated arguments); y is bf16
 // [rows_max, D] or, with y_f32, fp32.  No expert has more than
 // max_rows_per_expert rows (the token count when called from the layer).
+// Workspace bytes of launch_expert_ffn.
+size_t expert_ffn_ws_bytes(int E, int D, int I, int rows_max, int act_bits);
+
+// Expert FFN over expert-sorted rows x_sorted in pair order (fp16, or int8
+// with act_bits 8; see pair_pos), y in natural column order.
 int launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets, int E,
                       int D, int I, int rows_max, int max_rows_per_expert,
                       const int32_t* gate_packed,

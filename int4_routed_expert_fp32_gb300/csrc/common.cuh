@@ -28,6 +28,14 @@ void note_cuda_error(cudaError_t e);
 void count_launch();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Pair order of the activation rows the expert kernels read and write: in
+// every block of 8 columns, column j (j < 4) sits at position 2j and column
+// j + 4 at 2j + 1 (c0 c4 c1 c5 c2 c6 c3 c7), the order in which a packed
+// int32 word pairs its nibbles.
+__host__ __device__ __forceinline__ int pair_pos(int c) {
+  return (c & ~7) | ((c & 3) << 1) | ((c >> 2) & 1);
+}
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Encode a tiled tensor map (driver entry point looked up through the runtime).

@@ -5,6 +5,7 @@
 // expert" and "... sorted tokens").  The argsort is read as stable: the rows
 // of one expert ascend by token id.  In act_bits 8 mode each token row is
 // quantised to int8 on the way (per-row symmetric, IEEE fp32 steps).
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <mutex>
@@ -167,15 +168,37 @@ __device__ __forceinline__ float warp_row_scale(const uint4* row, int nv, int la
   return __fdiv_rn(m, 127.0f);
 }
 
+// bf16 x8 (natural order) -> fp16 x8 in pair order (c0 c4 c1 c5 c2 c6 c3 c7);
+// fin turns false for a value beyond the fp16 range.
+__device__ __forceinline__ uint4 bf16x8_to_f16_pairs(const uint4 x, bool& fin) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  float f[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    fin &= fabsf(f[j]) <= 65504.0f && fabsf(f[j + 4]) <= 65504.0f;
+    const __half2 h = __floats2half2_rn(f[j], f[j + 4]);
+    o[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // One warp per token: place its k (token, slot) pairs, then copy (or quantise
 // once and copy) the token row into each of its k expert-sorted rows.
-template <bool Q8>
+// PAIR: the rows are written in the expert kernels' pair order, fp16 (bf16
+// input beyond the fp16 range records MOE_ERR_UNSUPPORTED) or int8.
+template <bool Q8, bool PAIR>
 __global__ void __launch_bounds__(256) dispatch_place_kernel(
     const int32_t* __restrict__ idx, const uint16_t* __restrict__ x, int T, int D, int E, int k,
     const int32_t* __restrict__ hist, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
     int32_t* __restrict__ row_slot, int32_t* __restrict__ inv_row, void* __restrict__ x_sorted,
-    float* __restrict__ x_scale) {
+    float* __restrict__ x_scale, int* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -193,18 +216,21 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * D);
   if (!Q8) {
     uint4* dst = static_cast<uint4*>(x_sorted);
+    bool fin = true;
     for (int v = lane; v < nv; v += 32) {
-      const uint4 val = src[v];
+      const uint4 val = PAIR ? bf16x8_to_f16_pairs(src[v], fin) : src[v];
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, row, j);
         if (r >= 0) dst[(size_t)r * nv + v] = val;
       }
     }
+    if (PAIR && !fin) record_status(status, MOE_ERR_UNSUPPORTED);
   } else {
     const float sc = warp_row_scale(src, nv, lane);
     uint2* dst = static_cast<uint2*>(x_sorted);
     for (int v = lane; v < nv; v += 32) {
-      const uint2 q = quant8(src[v], sc);
+      uint2 q = quant8(src[v], sc);
+      if (PAIR) q = make_uint2(__byte_perm(q.x, q.y, 0x5140u), __byte_perm(q.x, q.y, 0x7362u));
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, row, j);
         if (r >= 0) dst[(size_t)r * nv + v] = q;
@@ -266,6 +292,51 @@ static int32_t* noalloc_scratch() {
   return g_noalloc_ptr[d];
 }
 
+// Count, scan and place kernels of one dispatch (T > 0, arguments checked).
+static int run_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                        int act_bits, bool pair, int32_t* counts, int32_t* offsets,
+                        int32_t* row_token, int32_t* row_slot, int32_t* inv_row, void* x_sorted,
+                        float* x_scale, int32_t* hist, int32_t* local_rank, cudaStream_t s) {
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  const int C = static_cast<int>(dispatch_chunks(T));
+  const size_t smem = (size_t)kCountWarps * (E + kChunkTokens * kMaxTopK) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    MOE_TRY_CUDA(cudaFuncSetAttribute(dispatch_count_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  }
+  dispatch_count_kernel<<<(C + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
+      topk_idx, T, E, k, hist, local_rank, status);
+  MOE_LAUNCH_CHECK();
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, counts, offsets);
+  MOE_LAUNCH_CHECK();
+  auto place = act_bits == 16 ? (pair ? dispatch_place_kernel<false, true>
+                                      : dispatch_place_kernel<false, false>)
+                              : (pair ? dispatch_place_kernel<true, true>
+                                      : dispatch_place_kernel<true, false>);
+  place<<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist, local_rank, offsets, row_token,
+                                     row_slot, inv_row, x_sorted, x_scale, status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+int launch_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                          int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                          int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                          void* ws, cudaStream_t s) {
+  if (T == 0) {
+    MOE_TRY_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
+    MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
+    return MOE_OK;
+  }
+  const size_t C = dispatch_chunks(T);
+  int32_t* hist = static_cast<int32_t*>(ws);
+  int32_t* local_rank =
+      reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align_up(C * E * sizeof(int32_t), 256));
+  return run_dispatch(topk_idx, x, T, D, E, k, act_bits, true, counts, offsets, row_token,
+                      row_slot, inv_row, x_sorted, x_scale, hist, local_rank, s);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -295,34 +366,33 @@ extern "C" int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, i
   if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
   if (!aligned(x, 16) || !aligned(x_sorted, 16)) return MOE_ERR_INVALID;
   if (ws_bytes < moe_dispatch_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  int* status = status_word();
-  if (!status) return MOE_ERR_CUDA;
-
-  const int C = static_cast<int>(dispatch_chunks(T));
+  const size_t C = dispatch_chunks(T);
   int32_t* hist = static_cast<int32_t*>(ws);
-  int32_t* local_rank = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
-                                                   align_up((size_t)C * E * sizeof(int32_t), 256));
-  const size_t smem = (size_t)kCountWarps * (E + kChunkTokens * kMaxTopK) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    MOE_TRY_CUDA(cudaFuncSetAttribute(dispatch_count_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int32_t* local_rank =
+      reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align_up(C * E * sizeof(int32_t), 256));
+  return run_dispatch(topk_idx, x, T, D, E, k, act_bits, false, counts, offsets, row_token,
+                      row_slot, inv_row, x_sorted, x_scale, hist, local_rank, s);
+}
+
+extern "C" int moe_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E,
+                                  int k, int act_bits, int32_t* counts, int32_t* offsets,
+                                  int32_t* row_token, int32_t* row_slot, int32_t* inv_row,
+                                  void* x_sorted, float* x_scale, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID;
+  if (T > 0) {
+    if (!topk_idx || !x || !row_token || !row_slot || !inv_row || !x_sorted || !ws)
+      return MOE_ERR_INVALID;
+    if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(x_sorted, 16)) return MOE_ERR_INVALID;
+    if (ws_bytes < moe_dispatch_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
   }
-  dispatch_count_kernel<<<(C + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
-      topk_idx, T, E, k, hist, local_rank, status);
-  MOE_LAUNCH_CHECK();
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, counts, offsets);
-  MOE_LAUNCH_CHECK();
-  if (act_bits == 16) {
-    dispatch_place_kernel<false><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
-                                                              local_rank, offsets, row_token,
-                                                              row_slot, inv_row, x_sorted, x_scale);
-  } else {
-    dispatch_place_kernel<true><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
-                                                             local_rank, offsets, row_token,
-                                                             row_slot, inv_row, x_sorted, x_scale);
-  }
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
+  return launch_dispatch_pairs(topk_idx, x, T, D, E, k, act_bits, counts, offsets, row_token,
+                               row_slot, inv_row, x_sorted, x_scale, ws,
+                               static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale,
@@ -358,30 +428,6 @@ extern "C" int moe_dispatch_noalloc(const int32_t* topk_idx, const uint16_t* x, 
     MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
     return MOE_OK;
   }
-  int* status = status_word();
-  if (!status) return MOE_ERR_CUDA;
-  int32_t* hist = scratch;
-  int32_t* local_rank = scratch + hist_ints;
-  const int Ci = static_cast<int>(C);
-  const size_t smem = (size_t)kCountWarps * (E + kChunkTokens * kMaxTopK) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    MOE_TRY_CUDA(cudaFuncSetAttribute(dispatch_count_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  }
-  dispatch_count_kernel<<<(Ci + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
-      topk_idx, T, E, k, hist, local_rank, status);
-  MOE_LAUNCH_CHECK();
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, Ci, E, counts, offsets);
-  MOE_LAUNCH_CHECK();
-  if (act_bits == 16) {
-    dispatch_place_kernel<false><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
-                                                              local_rank, offsets, row_token,
-                                                              row_slot, inv_row, x_sorted, x_scale);
-  } else {
-    dispatch_place_kernel<true><<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist,
-                                                             local_rank, offsets, row_token,
-                                                             row_slot, inv_row, x_sorted, x_scale);
-  }
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
+  return run_dispatch(topk_idx, x, T, D, E, k, act_bits, false, counts, offsets, row_token,
+                      row_slot, inv_row, x_sorted, x_scale, scratch, scratch + hist_ints, s);
 }

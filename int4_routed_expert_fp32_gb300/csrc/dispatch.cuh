@@ -11,4 +11,12 @@ namespace moe {
 int launch_quantize_rows(const uint16_t* v, int R, int C, const int32_t* row_count, int8_t* q,
                          float* scale, cudaStream_t s);
 
+// Dispatch whose x_sorted rows are in the expert kernels' pair order (fp16,
+// or int8 with act_bits 8); ws as for moe_dispatch.  Arguments are checked by
+// the caller.
+int launch_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, int T, int D, int E, int k,
+                          int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                          int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
+                          void* ws, cudaStream_t s);
+
 }  // namespace moe

@@ -9,24 +9,34 @@
 //     packed int4 weights and the matching bf16 group scales with 3-D TMA
 //     copies (128-byte swizzle for the weights), and the rows of the current
 //     token chunk (<= 16 expert-sorted rows) with 1-D bulk copies, into a
-//     4-stage shared-memory ring guarded by mbarriers.  When K is not a
-//     multiple of 256 the scale rows are not 16-byte aligned and the scales
-//     go through 4-byte cp.async instead;
+//     4-stage shared-memory ring guarded by mbarriers.  When the scale rows
+//     are not 16-byte aligned (K not a multiple of 256) the scales go through
+//     4-byte cp.async instead;
+//   * the activation rows arrive in "pair order": fp16 (int8 with act_bits 8)
+//     with each block of 8 columns stored as c0 c4 c1 c5 c2 c6 c3 c7, the
+//     order in which one packed int32 word pairs its nibbles.  A lane's
+//     16-byte load is then its MMA B fragments as they are;
 //   * sixteen consumer warps each own one 16-row block.  One ldmatrix gives a
-//     lane its packed words of two groups; each word becomes four bf16x2
-//     registers holding 136 + q exactly (nibble | 0x4300 magic), the A
-//     operand of m16n8k16 tensor-core MMAs against up to 2 blocks of 8 token
-//     rows.  The constant 136 is removed through the accumulator: each chain
-//     starts from the MMA of a constant -136 tile with the same activations,
-//     i.e. -136 * (sum of the group's activations).  The 32-column group's
-//     fp32 partial is then multiplied by its bf16 scale and accumulated in
-//     fp32, so the dequantised weight q * scale is never rounded;
+//     lane its packed words of two groups.  Each word becomes four fp16x2
+//     registers with one shift and four masks: the nibble pairs (0,4) and
+//     (2,6) land in the low mantissa bits of 1024 and hold 1032 + q, the pairs
+//     (1,5) and (3,7) in bits 4-7 and hold 1152 + 16 q, all exactly.  They
+//     are the A operands of two m16n8k16 fp16 MMAs per 32-column group (one
+//     per pair kind) against up to 2 blocks of 8 token rows.  The constants
+//     are removed through the accumulators: each chain starts from the MMA of
+//     a constant tile (-1032, or -1152) with the same activations.  The
+//     group's partial, low + high / 16, is then multiplied by its bf16 scale
+//     and accumulated in fp32, so the dequantised weight q * scale is never
+//     rounded;
 //   * in the gate/up variant warps 0-7 hold gate rows and warps 8-15 the up
 //     rows of the same outputs; the up partials go through shared memory and
-//     the gate warps write h = SiLU(G) * U (bf16).  The down variant writes y.
-// act_bits 8: the int8 activations become exact bf16 integers, the group
-// partials are exact integers (|P| <= 32*8*127 < 2^24) and the row scale is
-// applied in the epilogue.
+//     the gate warps write h = SiLU(G) * U in pair order (fp16; bf16 with
+//     act_bits 8, for its re-quantisation).  The down variant writes y.
+// act_bits 8: the int8 activations become exact fp16 integers; both chains
+// of a group stay exact integers (|sum| <= 16 * 1280 * 127 < 2^24), so the
+// group partial is the exact integer sum, and the row scale is applied in
+// the epilogue.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "combine.cuh"
@@ -44,6 +54,10 @@ constexpr int kFsTb = kFsMc / 8;           // token blocks of 8 (MMA N)
 #define FS_CWARPS 16
 #endif
 constexpr int kFsCWarps = FS_CWARPS;       // consumer warps, one 16-row block each
+#ifndef FS_UNROLL
+#define FS_UNROLL 4
+#endif
+constexpr int kFsUnroll = FS_UNROLL;       // group pairs unrolled with one token block
 constexpr int kFsThreads = (kFsCWarps + 1) * 32;
 constexpr int kFsRows = 16 * kFsCWarps;    // weight rows per stage tile
 constexpr int kFsStages = (FS_CWARPS <= 12) ? 5 : 4;
@@ -83,10 +97,10 @@ struct FsMaps {
   CUtensorMap s0, s1;     // scales (used when tma_scales)
 };
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1, const float (&c)[4]) {
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1, const float (&c)[4]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
@@ -99,43 +113,51 @@ __device__ __forceinline__ void ldsm_x4(const void* addr, uint32_t (&r)[4]) {
                : "r"(smem_u32(addr)));
 }
 
-// Eight two's-complement nibbles n -> four bf16x2 holding 128 + (n ^ 8), i.e.
-// 136 + value, exactly: out[i] = (nibble i, nibble i+4), low half = nibble i.
-// The constant 136 is removed through the MMA accumulator (see kNeg136).
+// Eight two's-complement nibbles n_0..n_7 of one packed word -> four fp16x2:
+//   out[0] = (n0, n4), out[2] = (n2, n6): 1024 + (n ^ 8) = 1032 + q;
+//   out[1] = (n1, n5), out[3] = (n3, n7): 1024 + 16 (n ^ 8) = 1152 + 16 q.
+// Low half = the lower nibble of the pair.  One shift and four mask-xor ops.
 __device__ __forceinline__ void dequant_magic(uint32_t w, uint32_t (&out)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) out[i] = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+  const uint32_t w8 = w >> 8;
+  out[0] = (w & 0x000F000Fu) ^ 0x64086408u;
+  out[1] = (w & 0x00F000F0u) ^ 0x64806480u;
+  out[2] = (w8 & 0x000F000Fu) ^ 0x64086408u;
+  out[3] = (w8 & 0x00F000F0u) ^ 0x64806480u;
 }
 
-// bf16x2 (-136, -136): A operand of the MMA that forms -136 * (sum of the
-// group's activations), the start value of every weight MMA chain.
-constexpr uint32_t kNeg136 = 0xC308C308u;
+// fp16x2 (-1032, -1032) and (-1152, -1152): A operands of the MMAs that form
+// the start value of each chain, -1032 (or -1152) * (sum of the activations
+// of those columns).
+constexpr uint32_t kNegLo = 0xE408E408u;
+constexpr uint32_t kNegHi = 0xE480E480u;
 
-__device__ __forceinline__ uint32_t i8pair_bf16x2(uint32_t lo_byte_word, int lo_shift,
-                                                  uint32_t hi_byte_word, int hi_shift) {
-  const float lo = static_cast<float>(static_cast<int8_t>((lo_byte_word >> lo_shift) & 0xffu));
-  const float hi = static_cast<float>(static_cast<int8_t>((hi_byte_word >> hi_shift) & 0xffu));
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+// Two int8 values (bytes selected by `sel` into the low byte of each half)
+// -> fp16x2, exactly: 1024 + (x + 128) via the 0x6480 xor, minus 1152.
+__device__ __forceinline__ uint32_t i8pair_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t m = __byte_perm(w, 0u, sel) ^ 0x64806480u;
+  __half2 h = *reinterpret_cast<const __half2*>(&m);
+  h = __hsub2(h, __floats2half2_rn(1152.0f, 1152.0f));
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// B fragments (8 tokens x 32 columns of one group) for the two K=16 halves.
-// Column permutation shared with the A side: MMA half j, logical k = 2t, 2t+1
-// <-> group columns 8t+2j, 8t+2j+4; logical 2t+8, 2t+9 <-> 8t+2j+1, 8t+2j+5.
+// B fragments (8 tokens x 32 columns of one group) from pair-ordered rows:
+// b[0] = (x0, x4), b[1] = (x1, x5), b[2] = (x2, x6), b[3] = (x3, x7) of the
+// lane's 8 columns 8t..8t+7 of group G.  The low-nibble MMA takes b[0], b[2],
+// the high-nibble MMA b[1], b[3].
 template <bool Q8>
 __device__ __forceinline__ void load_b_frag(const uint8_t* xrow, int G, int t, uint32_t (&b)[4]) {
   if (!Q8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xrow + G * 64 + t * 16);
-    b[0] = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
-    b[1] = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
-    b[2] = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
-    b[3] = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
+    b[0] = v.x;
+    b[1] = v.y;
+    b[2] = v.z;
+    b[3] = v.w;
   } else {
     const uint2 v = *reinterpret_cast<const uint2*>(xrow + G * 32 + t * 8);
-    b[0] = i8pair_bf16x2(v.x, 0, v.y, 0);    // (x0, x4)
-    b[1] = i8pair_bf16x2(v.x, 8, v.y, 8);    // (x1, x5)
-    b[2] = i8pair_bf16x2(v.x, 16, v.y, 16);  // (x2, x6)
-    b[3] = i8pair_bf16x2(v.x, 24, v.y, 24);  // (x3, x7)
+    b[0] = i8pair_f16x2(v.x, 0x4140u);
+    b[1] = i8pair_f16x2(v.x, 0x4342u);
+    b[2] = i8pair_f16x2(v.y, 0x4140u);
+    b[3] = i8pair_f16x2(v.y, 0x4342u);
   }
 }
 
@@ -154,12 +176,13 @@ template <bool Q8, int NTB, bool FULL>
 __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S, const uint8_t* X,
                                               int ng, const Lane& L, float (&acc)[NTB][4]) {
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
-  const uint32_t neg[4] = {kNeg136, kNeg136, kNeg136, kNeg136};
+  const uint32_t neg_lo[4] = {kNegLo, kNegLo, kNegLo, kNegLo};
+  const uint32_t neg_hi[4] = {kNegHi, kNegHi, kNegHi, kNegHi};
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
   const uint32_t* s_lo_row = reinterpret_cast<const uint32_t*>(S + L.rlo * 16);
   const uint32_t* s_hi_row = reinterpret_cast<const uint32_t*>(S + (L.rlo + 8) * 16);
   // two token blocks keep more values live: unroll less there
-#pragma unroll(NTB == 1 ? 4 : 1)
+#pragma unroll(NTB == 1 ? kFsUnroll : 1)
   for (int G2 = 0; G2 < kFsGroups; G2 += 2) {
     if (!FULL && G2 >= ng) break;
     uint32_t wr[4];  // (row g, row g+8) words of groups G2 and G2+1
@@ -169,30 +192,26 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
 #pragma unroll
     for (int gg = 0; gg < 2; ++gg) {
       const int G = G2 + gg;
-      uint32_t bfr[NTB][4];
-      float corr[NTB][4];
-#pragma unroll
-      for (int tb = 0; tb < NTB; ++tb) {
-        load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr[tb]);
-        mma_bf16_16816(corr[tb], neg, bfr[tb][0], bfr[tb][1], zero);
-        mma_bf16_16816(corr[tb], neg, bfr[tb][2], bfr[tb][3], corr[tb]);
-      }
       uint32_t P[4], Q[4];
-      dequant_magic(wr[2 * gg], P);
-      dequant_magic(wr[2 * gg + 1], Q);
-      const uint32_t a0[4] = {P[0], Q[0], P[1], Q[1]};
-      const uint32_t a1[4] = {P[2], Q[2], P[3], Q[3]};
+      dequant_magic(wr[2 * gg], P);      // row g
+      dequant_magic(wr[2 * gg + 1], Q);  // row g + 8
+      const uint32_t alo[4] = {P[0], Q[0], P[2], Q[2]};
+      const uint32_t ahi[4] = {P[1], Q[1], P[3], Q[3]};
       const float s_lo = __uint_as_float(gg ? (slo_w & 0xffff0000u) : (slo_w << 16));
       const float s_hi = __uint_as_float(gg ? (shi_w & 0xffff0000u) : (shi_w << 16));
 #pragma unroll
       for (int tb = 0; tb < NTB; ++tb) {
-        float c[4];
-        mma_bf16_16816(c, a0, bfr[tb][0], bfr[tb][1], corr[tb]);
-        mma_bf16_16816(c, a1, bfr[tb][2], bfr[tb][3], c);
-        acc[tb][0] = fmaf(s_lo, c[0], acc[tb][0]);
-        acc[tb][1] = fmaf(s_lo, c[1], acc[tb][1]);
-        acc[tb][2] = fmaf(s_hi, c[2], acc[tb][2]);
-        acc[tb][3] = fmaf(s_hi, c[3], acc[tb][3]);
+        uint32_t bfr[4];
+        load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr);
+        float clo[4], chi[4];
+        mma_f16_16816(clo, neg_lo, bfr[0], bfr[2], zero);
+        mma_f16_16816(chi, neg_hi, bfr[1], bfr[3], zero);
+        mma_f16_16816(clo, alo, bfr[0], bfr[2], clo);
+        mma_f16_16816(chi, ahi, bfr[1], bfr[3], chi);
+        acc[tb][0] = fmaf(s_lo, fmaf(chi[0], 0.0625f, clo[0]), acc[tb][0]);
+        acc[tb][1] = fmaf(s_lo, fmaf(chi[1], 0.0625f, clo[1]), acc[tb][1]);
+        acc[tb][2] = fmaf(s_hi, fmaf(chi[2], 0.0625f, clo[2]), acc[tb][2]);
+        acc[tb][3] = fmaf(s_hi, fmaf(chi[3], 0.0625f, clo[3]), acc[tb][3]);
       }
     }
   }
@@ -264,7 +283,13 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
         const float G = acc[tb][c] * xs;
         const float U = xch[rr * kFsMc + tok] * xs;
         const float h = G / (1.0f + expf(-G)) * U;
-        static_cast<uint16_t*>(p.out)[(size_t)row * N + n] = f32_to_bf16_bits(h);
+        uint16_t* hrow = static_cast<uint16_t*>(p.out) + (size_t)row * N;
+        if (Q8) {
+          hrow[pair_pos(n)] = f32_to_bf16_bits(h);
+        } else {
+          if (!(fabsf(h) <= 65504.0f)) record_status(p.status, MOE_ERR_UNSUPPORTED);
+          hrow[pair_pos(n)] = __half_as_ushort(__float2half_rn(h));
+        }
       }
     }
     }
@@ -638,17 +663,15 @@ static int check_width(int v) { return (v > 0 && v % 64 == 0) ? MOE_OK : MOE_ERR
 
 using namespace moe;
 
-extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_bits) {
-  if (E <= 0 || D <= 0 || I <= 0 || rows_max < 0) return 256;
+size_t moe::expert_ffn_ws_bytes(int E, int D, int I, int rows_max, int act_bits) {
   size_t b = schedule_bytes(E, rows_max);
-  b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);  // h (bf16)
+  b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);  // h (fp16, bf16 with act_bits 8)
   if (act_bits == 8) {
-    b += align_up((size_t)rows_max * I, 256);                // h as int8
-    b += align_up((size_t)rows_max * sizeof(float), 256);    // its row scales
+    b += align_up((size_t)rows_max * I, 256);                      // h as int8
+    b += align_up((size_t)rows_max * sizeof(float), 256);          // its row scales
+    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);   // fp16 of the int8 x (tensor cores)
+    b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);   // fp16 of the int8 h (tensor cores)
   }
-  // tensor-core path: fp16 copies of the activations and of h (or of its int8 form)
-  b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
-  b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   return b;
 }
 
@@ -668,15 +691,17 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   int8_t* hq = nullptr;
   float* hs = nullptr;
+  uint16_t* x16 = nullptr;
+  uint16_t* h16 = nullptr;
   if (q8) {
     hq = reinterpret_cast<int8_t*>(b);
     b += align_up((size_t)rows_max * I, 256);
     hs = reinterpret_cast<float*>(b);
     b += align_up((size_t)rows_max * sizeof(float), 256);
+    x16 = reinterpret_cast<uint16_t*>(b);
+    b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
+    h16 = reinterpret_cast<uint16_t*>(b);
   }
-  uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
-  b += align_up((size_t)rows_max * D * sizeof(uint16_t), 256);
-  uint16_t* h16 = reinterpret_cast<uint16_t*>(b);
 
   // experts with more than one chunk of rows go to the tensor-core kernels
   const bool use_tc = tc_path_supported(D) && tc_path_supported(I) &&
@@ -712,13 +737,17 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   rc = run_stream(kGateUp, q8, mgu, p, s);
   if (rc) return rc;
   if (use_tc) {
-    // act_bits 16: h of these rows in fp16 (h16); act_bits 8: in bf16 (h),
-    // re-quantised below with the stream kernel's rows
-    rc = launch_to_f16_rows(x_sorted, q8, rows_max, D, offsets + E, x16, s);
-    if (rc) return rc;
-    rc = launch_tc_gateup(x16, q8 ? x_scale : nullptr, rows_max, E, D, I, gate_packed, gate_scale,
-                          up_packed, up_scale, q8 ? h : h16, big.chunk_e, big.chunk_row0,
-                          big.chunk_rows, big.n_chunks, status, s);
+    // both kernels write h in pair order: fp16 (act_bits 16), or bf16 for
+    // the re-quantisation below (act_bits 8)
+    const uint16_t* xa = static_cast<const uint16_t*>(x_sorted);
+    if (q8) {
+      rc = launch_to_f16_rows(x_sorted, true, rows_max, D, offsets + E, x16, s);
+      if (rc) return rc;
+      xa = x16;
+    }
+    rc = launch_tc_gateup(xa, q8 ? x_scale : nullptr, rows_max, E, D, I, gate_packed, gate_scale,
+                          up_packed, up_scale, h, big.chunk_e, big.chunk_row0, big.chunk_rows,
+                          big.n_chunks, status, s);
     if (rc) return rc;
   }
 
@@ -740,16 +769,70 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   rc = run_stream(y_f32 ? kLinear : kDown, q8, md, pd, s);
   if (rc) return rc;
   if (use_tc) {
+    const uint16_t* ha = h;
     if (q8) {
       rc = launch_to_f16_rows(hq, true, rows_max, I, offsets + E, h16, s);
       if (rc) return rc;
+      ha = h16;
     }
-    rc = launch_tc_down(h16, q8 ? hs : nullptr, rows_max, E, D, I, down_packed, down_scale, y,
+    rc = launch_tc_down(ha, q8 ? hs : nullptr, rows_max, E, D, I, down_packed, down_scale, y,
                         y_f32, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status,
                         s);
     if (rc) return rc;
   }
   return MOE_OK;
+}
+
+// Argument checks shared by the two expert-FFN entry points.
+static int check_ffn_args(const void* x, const float* x_scale, const int32_t* offsets, int E, int D,
+                          int I, int rows_max, const int32_t* gate_packed,
+                          const uint16_t* gate_scale, const int32_t* up_packed,
+                          const uint16_t* up_scale, const int32_t* down_packed,
+                          const uint16_t* down_scale, int act_bits, const uint16_t* y, void* ws) {
+  if (E <= 0 || rows_max < 0) return MOE_ERR_INVALID;
+  if (check_width(D) || check_width(I) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (rows_max == 0) return MOE_OK;
+  if (!x || !offsets || !gate_packed || !gate_scale || !up_packed || !up_scale || !down_packed ||
+      !down_scale || !y || !ws)
+    return MOE_ERR_INVALID;
+  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(gate_packed, 16) || !aligned(up_packed, 16) ||
+      !aligned(down_packed, 16) || !aligned(gate_scale, 4) || !aligned(up_scale, 4) ||
+      !aligned(down_scale, 4) || !aligned(ws, 256))
+    return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+extern "C" size_t moe_expert_ffn_pairs_workspace_size(int E, int D, int I, int rows_max,
+                                                      int act_bits) {
+  if (E <= 0 || D <= 0 || I <= 0 || rows_max < 0) return 256;
+  return expert_ffn_ws_bytes(E, D, I, rows_max, act_bits);
+}
+
+extern "C" int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale,
+                                    const int32_t* offsets, int E, int D, int I, int rows_max,
+                                    const int32_t* gate_packed, const uint16_t* gate_scale,
+                                    const int32_t* up_packed, const uint16_t* up_scale,
+                                    const int32_t* down_packed, const uint16_t* down_scale,
+                                    int act_bits, uint16_t* y_sorted, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  const int rc = check_ffn_args(x_pairs, x_scale, offsets, E, D, I, rows_max, gate_packed,
+                                gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
+                                y_sorted, ws);
+  if (rc || rows_max == 0) return rc;
+  if (ws_bytes < moe_expert_ffn_pairs_workspace_size(E, D, I, rows_max, act_bits))
+    return MOE_ERR_WORKSPACE;
+  return launch_expert_ffn(x_pairs, x_scale, offsets, E, D, I, rows_max, rows_max, gate_packed,
+                           gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
+                           y_sorted, false, ws, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_bits) {
+  if (E <= 0 || D <= 0 || I <= 0 || rows_max < 0) return 256;
+  // + the pair-ordered copy of x_sorted
+  return expert_ffn_ws_bytes(E, D, I, rows_max, act_bits) +
+         align_up((size_t)rows_max * D * (act_bits == 8 ? 1 : 2), 256);
 }
 
 extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t* offsets,
@@ -758,29 +841,28 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
                               const uint16_t* up_scale, const int32_t* down_packed,
                               const uint16_t* down_scale, int act_bits, uint16_t* y_sorted,
                               void* ws, size_t ws_bytes, void* stream) {
-  if (E <= 0 || rows_max < 0) return MOE_ERR_INVALID;
-  if (check_width(D) || check_width(I) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
-  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
-  if (rows_max == 0) return MOE_OK;
-  if (!x_sorted || !offsets || !gate_packed || !gate_scale || !up_packed || !up_scale ||
-      !down_packed || !down_scale || !y_sorted || !ws)
-    return MOE_ERR_INVALID;
-  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
-  if (!aligned(x_sorted, 16) || !aligned(gate_packed, 16) || !aligned(up_packed, 16) ||
-      !aligned(down_packed, 16) || !aligned(gate_scale, 4) || !aligned(up_scale, 4) ||
-      !aligned(down_scale, 4))
-    return MOE_ERR_INVALID;
+  const int rc0 = check_ffn_args(x_sorted, x_scale, offsets, E, D, I, rows_max, gate_packed,
+                                 gate_scale, up_packed, up_scale, down_packed, down_scale,
+                                 act_bits, y_sorted, ws);
+  if (rc0 || rows_max == 0) return rc0;
   if (ws_bytes < moe_expert_ffn_workspace_size(E, D, I, rows_max, act_bits))
     return MOE_ERR_WORKSPACE;
-  return launch_expert_ffn(x_sorted, x_scale, offsets, E, D, I, rows_max, rows_max, gate_packed,
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* xp = static_cast<char*>(ws) + expert_ffn_ws_bytes(E, D, I, rows_max, act_bits);
+  int rc = launch_to_pair_rows(x_sorted, act_bits == 8, rows_max, D, offsets + E, xp, status, s);
+  if (rc) return rc;
+  return launch_expert_ffn(xp, x_scale, offsets, E, D, I, rows_max, rows_max, gate_packed,
                            gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
-                           y_sorted, false, ws, static_cast<cudaStream_t>(stream));
+                           y_sorted, false, ws, s);
 }
 
 extern "C" size_t moe_int4_linear_workspace_size(int E, int K, int rows_max) {
   if (E <= 0 || K <= 0 || rows_max < 0) return 256;
   return schedule_bytes(E, rows_max) +
-         align_up((size_t)rows_max * K * sizeof(uint16_t), 256);  // fp16 copy (tensor cores)
+         align_up((size_t)rows_max * K * sizeof(uint16_t), 256) +  // pair-ordered copy of x
+         align_up((size_t)rows_max * K * sizeof(uint16_t), 256);   // its fp16 form (int8 x)
 }
 
 extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E,
@@ -793,7 +875,8 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   if (rows_max == 0) return MOE_OK;
   if (!x || !offsets || !w_packed || !w_scale || !out || !ws) return MOE_ERR_INVALID;
   if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
-  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4) || !aligned(out, 16))
+  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4) || !aligned(out, 16) ||
+      !aligned(ws, 256))
     return MOE_ERR_INVALID;
   if (ws_bytes < moe_int4_linear_workspace_size(E, K, rows_max)) return MOE_ERR_WORKSPACE;
   int* status = status_word();
@@ -803,15 +886,19 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   char* b = static_cast<char*>(ws);
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
+  void* xp = b;
+  b += align_up((size_t)rows_max * K * sizeof(uint16_t), 256);
   uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
   const bool use_tc = tc_path_supported(K) && rows_max >= kTcMinBatchRows;
-  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max,
-                           small, status, s);
+  int rc = launch_to_pair_rows(x, q8, rows_max, K, offsets + E, xp, status, s);
+  if (rc) return rc;
+  rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max, small,
+                       status, s);
   if (rc) return rc;
   FsMaps m;
   if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
   FsParams p{};
-  p.x = x;
+  p.x = xp;
   p.x_scale = x_scale;
   p.scale0 = w_scale;
   p.out = out;
@@ -828,8 +915,12 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   if (rc || !use_tc) return rc;
   rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s);
   if (rc) return rc;
-  rc = launch_to_f16_rows(x, q8, rows_max, K, offsets + E, x16, s);
-  if (rc) return rc;
-  return launch_tc_down(x16, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale, out,
+  const uint16_t* xa = static_cast<const uint16_t*>(xp);
+  if (q8) {
+    rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
+    if (rc) return rc;
+    xa = x16;
+  }
+  return launch_tc_down(xa, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale, out,
                         true, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
 }

@@ -8,7 +8,9 @@
 //     4-stage ring;
 //   * warps 2-9: dequantisation, one weight row per thread, to fp16
 //     q * scale written in the K-major 128-byte-swizzle layout the MMA reads,
-//     then fence.proxy.async.  With a bf16 scale (8 significant bits) and
+//     then fence.proxy.async.  The activation rows are in pair order (each
+//     block of 8 columns stored c0 c4 c1 c5 c2 c6 c3 c7), so the weights are
+//     written in the same order, the order of the nibble pairs of a word;  With a bf16 scale (8 significant bits) and
 //     |q| <= 8, q * scale has at most 11 significant bits: it is exact in fp16
 //     for scales in [2^-17, 8188].  The activations arrive in fp16 (a copy
 //     made once per call; bf16 values are exact in fp16 for
@@ -260,17 +262,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         for (int c = 0; c < 8; ++c) {
           const uint32_t w = wv[c];
           const uint32_t sc = c < 4 ? s_lo : s_hi;
-          // pairs (n0,n4), (n1,n5) from w; (n2,n6), (n3,n7) from w >> 8
+          // (n0,n4), (n1,n5) from w; (n2,n6), (n3,n7) from w >> 8
           const uint32_t p04 = nib_lo_f16(w, sc), p15 = nib_hi_f16(w, sc);
           const uint32_t w8 = w >> 8;
           const uint32_t p26 = nib_lo_f16(w8, sc), p37 = nib_hi_f16(w8, sc);
-          // natural column order: (n0,n1), (n2,n3), (n4,n5), (n6,n7)
-          uint4 o;
-          o.x = __byte_perm(p04, p15, 0x5410);
-          o.y = __byte_perm(p26, p37, 0x5410);
-          o.z = __byte_perm(p04, p15, 0x7632);
-          o.w = __byte_perm(p26, p37, 0x7632);
-          *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
+          // pair order: (n0,n4), (n1,n5), (n2,n6), (n3,n7)
+          *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = make_uint4(p04, p15, p26, p37);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -308,33 +305,41 @@ __global__ void __launch_bounds__(kTxThreads, 1)
               fin &= fabsf(__uint_as_float(g[i])) <= 3.0e38f && fabsf(__uint_as_float(v[i])) <= 3.0e38f;
             if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
             uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
-            uint32_t hw[16];
+            float hv[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              float u0 = __uint_as_float(v[2 * i]), u1 = __uint_as_float(v[2 * i + 1]);
+            for (int i = 0; i < 32; ++i) {
+              float g0 = __uint_as_float(g[i]), u0 = __uint_as_float(v[i]);
               if (Q8) {
                 g0 *= xs;
-                g1 *= xs;
                 u0 *= xs;
-                u1 *= xs;
               }
-              const float h0 = g0 / (1.0f + expf(-g0)) * u0;
-              const float h1 = g1 / (1.0f + expf(-g1)) * u1;
-              if (Q8) {  // bf16 h, as the stream kernel writes it
-                hw[i] = static_cast<uint32_t>(f32_to_bf16_bits(h0)) |
-                        (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
-              } else {
-                const __half2 hh = __floats2half2_rn(h0, h1);
-                hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
-              }
+              hv[i] = g0 / (1.0f + expf(-g0)) * u0;
             }
+            // pair order: word 4b + j holds columns 8b + j and 8b + j + 4
+            uint32_t hw[16];
+            bool hfin = true;
+#pragma unroll
+            for (int b8 = 0; b8 < 4; ++b8)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float h0 = hv[8 * b8 + j], h1 = hv[8 * b8 + j + 4];
+                if (Q8) {  // bf16 h, as the stream kernel writes it
+                  hw[4 * b8 + j] = static_cast<uint32_t>(f32_to_bf16_bits(h0)) |
+                                   (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
+                } else {
+                  hfin &= fabsf(h0) <= 65504.0f && fabsf(h1) <= 65504.0f;
+                  const __half2 hh = __floats2half2_rn(h0, h1);
+                  hw[4 * b8 + j] = *reinterpret_cast<const uint32_t*>(&hh);
+                }
+              }
+            if (!hfin) record_status(p.status, MOE_ERR_UNSUPPORTED);
             if (col + 32 <= N && (N & 7) == 0) {
               uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 d4[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
             } else {
+              // N % 8 == 0 (K of the down projection): whole 8-column blocks
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (col + i < N) dst[i] = static_cast<uint16_t>((hw[i >> 1] >> (16 * (i & 1))) & 0xffffu);
@@ -450,6 +455,60 @@ __global__ void __launch_bounds__(256) to_f16_rows_kernel(const void* __restrict
                          i8x2_to_f16x2(q.y, 0, 8), i8x2_to_f16x2(q.y, 16, 24));
     }
   }
+}
+
+// Pair-ordered copy of natural-order rows below *row_count (one warp per
+// row): each 8-column block c0..c7 becomes c0 c4 c1 c5 c2 c6 c3 c7, bf16 ->
+// fp16 (I8 = false) or int8 -> int8 (I8 = true).
+template <bool I8>
+__global__ void __launch_bounds__(256) to_pair_rows_kernel(const void* __restrict__ src, int R,
+                                                           int C, const int32_t* row_count,
+                                                           void* __restrict__ dst, int* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= R || r >= *row_count) return;
+  if (!I8) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + (size_t)r * C);
+    uint4* d4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst) + (size_t)r * C);
+    bool fin = true;
+    for (int v = lane; v < C / 8; v += 32) {
+      const uint4 x = s4[v];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        fin &= fabsf(f[j]) <= 65504.0f && fabsf(f[j + 4]) <= 65504.0f;
+        const __half2 h = __floats2half2_rn(f[j], f[j + 4]);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      d4[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (!fin) record_status(status, MOE_ERR_UNSUPPORTED);
+  } else {
+    const uint2* s2 = reinterpret_cast<const uint2*>(static_cast<const int8_t*>(src) + (size_t)r * C);
+    uint2* d2 = reinterpret_cast<uint2*>(static_cast<int8_t*>(dst) + (size_t)r * C);
+    for (int v = lane; v < C / 8; v += 32) {
+      const uint2 q = s2[v];
+      d2[v] = make_uint2(__byte_perm(q.x, q.y, 0x5140u), __byte_perm(q.x, q.y, 0x7362u));
+    }
+  }
+}
+
+int launch_to_pair_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
+                        void* dst, int* status, cudaStream_t s) {
+  if (R == 0) return MOE_OK;
+  if (src_i8)
+    to_pair_rows_kernel<true><<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst, status);
+  else
+    to_pair_rows_kernel<false><<<(R + 7) / 8, 256, 0, s>>>(src, R, C, row_count, dst, status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }
 
 int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,

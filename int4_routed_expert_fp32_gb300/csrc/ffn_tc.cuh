@@ -39,8 +39,14 @@ bool tc_path_supported(int K);
 // Scale rows of [E, N, K/32] bf16 at `scale` start on 16-byte boundaries.
 bool scale_rows_16b(const uint16_t* scale, int K);
 
+// Pair-ordered copy (see pair_pos) of natural-order rows [R, C] below
+// *row_count: bf16 -> fp16 (src_i8 false; a value beyond the fp16 range
+// records MOE_ERR_UNSUPPORTED), or int8 -> int8 (src_i8 true).
+int launch_to_pair_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
+                        void* dst, int* status, cudaStream_t s);
+
 // fp16 copy of bf16 (src_i8 false) or int8 (src_i8 true) rows [R, C] below
-// *row_count.
+// *row_count (order kept).
 int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
                        uint16_t* dst, cudaStream_t s);
 

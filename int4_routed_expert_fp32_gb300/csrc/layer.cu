@@ -4,6 +4,7 @@
 // dispatch; experts; combine (+ RMSNorm and up-projection on the latent path).
 #include "combine.cuh"
 #include "common.cuh"
+#include "dispatch.cuh"
 
 namespace moe {
 
@@ -16,7 +17,7 @@ struct LayerWs {
   int32_t* row_slot;
   int32_t* inv_row;
   uint16_t* x_lat;     // [T, L] (latent)
-  void* x_sorted;      // [T*k, D] bf16 or int8
+  void* x_sorted;      // [T*k, D] fp16 or int8, pair order
   float* x_scale;      // [T*k] (act_bits 8)
   void* y_sorted;      // [T*k, D] bf16, or fp32 on the latent path
   bool y_f32;
@@ -33,7 +34,7 @@ static size_t scratch_need(const moe_config& c) {
   const int R = c.T * c.k;
   size_t a = moe_route_workspace_size(c.T, c.H, c.E);
   size_t b = moe_dispatch_workspace_size(c.T, c.E, c.k);
-  size_t f = moe_expert_ffn_workspace_size(c.E, D, c.I, R, c.act_bits);
+  size_t f = expert_ffn_ws_bytes(c.E, D, c.I, R, c.act_bits);
   size_t m = a > b ? a : b;
   return m > f ? m : f;
 }
@@ -106,9 +107,10 @@ static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x,
     if (rc) return rc;
     u = ws.x_lat;
   }
-  rc = moe_dispatch(ws.topk_idx, u, c.T, D, c.E, c.k, c.act_bits, ws.counts, ws.offsets,
-                    ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale, ws.scratch,
-                    ws.scratch_bytes, s);
+  // expert-sorted rows in the expert kernels' pair order (fp16 / int8)
+  rc = launch_dispatch_pairs(ws.topk_idx, u, c.T, D, c.E, c.k, c.act_bits, ws.counts, ws.offsets,
+                             ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale,
+                             ws.scratch, s);
   if (rc) return rc;
   rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, c.T, w.gate_packed,
                          w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,

@@ -149,6 +149,43 @@ def test_dispatch_parity(moe, name, act_bits):
         assert np.array_equal(got["x_scale"].view(np.uint32), sc[d.row_token].view(np.uint32))
 
 
+def _pair_columns(C):
+    """Natural column stored at each position of the pair order (blocks of 8:
+    0 4 1 5 2 6 3 7)."""
+    blk = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+    return (np.arange(C // 8)[:, None] * 8 + blk[None, :]).ravel()
+
+
+@pytest.mark.parametrize("name", ["random", "one_token", "zipf_prefill"])
+@pytest.mark.parametrize("act_bits", [16, 8])
+def test_dispatch_pairs_layout(moe, name, act_bits):
+    """moe_dispatch_pairs: the same permutation as moe_dispatch, rows in pair
+    order as fp16 (exact for these values) or int8, bit for bit."""
+    idx, x, E = _dispatch_case(name)
+    ti = torch.from_numpy(idx).to(DEV)
+    nat = moe.dispatch(ti, x.to(DEV), E, act_bits)
+    prs = moe.dispatch(ti, x.to(DEV), E, act_bits, pairs=True)
+    assert moe.check_error() == 0
+    for n in ("counts", "offsets", "row_token", "row_slot", "inv_row"):
+        assert torch.equal(nat[n], prs[n]), n
+    cols = _pair_columns(x.shape[1])
+    if act_bits == 16:
+        want = nat["x_sorted"].float().cpu().numpy().astype(np.float16)[:, cols]
+        assert np.array_equal(prs["x_sorted"].cpu().numpy().view(np.uint16), want.view(np.uint16))
+    else:
+        assert np.array_equal(prs["x_sorted"].cpu().numpy(), nat["x_sorted"].cpu().numpy()[:, cols])
+        assert torch.equal(prs["x_scale"], nat["x_scale"])
+
+
+def test_dispatch_pairs_reports_fp16_overflow(moe):
+    idx, x, E = _dispatch_case("random")
+    x = x.clone()
+    x[5, 17] = 1.0e5  # beyond the fp16 range
+    moe.dispatch(torch.from_numpy(idx).to(DEV), x.to(DEV), E, 16, pairs=True)
+    assert moe.check_error() == moe.capi.MOE_ERR_UNSUPPORTED
+    assert moe.check_error() == 0
+
+
 def test_quantize_rows_bit_exact(moe, golden_dir):
     import json
     import os
@@ -311,6 +348,29 @@ def test_expert_ffn_parity(moe, act_bits, D, I, counts):
         refs.append(O.expert_ffn(xf[a:b], exn, act_bits))
         gots.append(y[a:b])
     assert_close(np.concatenate(gots), np.concatenate(refs), what=f"ffn act{act_bits}")
+
+
+@pytest.mark.parametrize("act_bits", [16, 8])
+def test_expert_ffn_pairs_equals_expert_ffn(moe, act_bits):
+    """moe_dispatch_pairs + moe_expert_ffn_pairs (the layer's path) give the
+    bits of moe_dispatch + moe_expert_ffn (same kernels after the copy)."""
+    rng = np.random.default_rng(31)
+    T, k, E, D, I = 40, 4, 6, 320, 192
+    idx = random_topk(T, E, k, rng)       # ~27 rows per expert: most on the tensor cores
+    x = _bf16(rng.normal(size=(T, D)))
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    ti = torch.from_numpy(idx).to(DEV)
+    nat = moe.dispatch(ti, x.to(DEV), E, act_bits)
+    prs = moe.dispatch(ti, x.to(DEV), E, act_bits, pairs=True)
+    y0 = moe.expert_ffn(nat["x_sorted"], nat["x_scale"], nat["offsets"], ex, act_bits)
+    y1 = moe.expert_ffn(prs["x_sorted"], prs["x_scale"], prs["offsets"], ex, act_bits, pairs=True)
+    assert moe.check_error() == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
 def test_ffn_rejects_offsets_beyond_capacity(moe):
