@@ -116,6 +116,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to kSuspendNs while the phase
+// is incomplete; the thread resumes as soon as the phase completes, so a
+// waiting warp takes no issue slots from the working ones.
+constexpr uint32_t kSuspendNs = 100000;
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most limit_ns.
 // Gives up early when another thread has already recorded a status.  On
 // timeout records MOE_ERR_TIMEOUT.  Returns true when the phase completed.
@@ -125,8 +141,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_suspend(bar, parity)) return true;
     if (status_set(status)) return false;
     if (static_cast<int64_t>(global_timer_ns() - t0) > limit_ns) {
       record_status(status, MOE_ERR_TIMEOUT);

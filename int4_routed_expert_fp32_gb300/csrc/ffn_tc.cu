@@ -38,21 +38,24 @@
 
 namespace moe {
 
-constexpr int kTxBM = 128;                     // token rows per tile (MMA M)
-constexpr int kTxBN = 256;                     // weight rows per tile (MMA N)
-constexpr int kTxBK = 64;                      // K per stage (one swizzle atom of bf16)
-constexpr int kTxStages = 4;
-constexpr int kTxABytes = kTxBM * kTxBK * 2;   // 16 KiB activations
-constexpr int kTxBBytes = kTxBN * kTxBK * 2;   // 32 KiB dequantised weights
-constexpr int kTxQBytes = kTxBN * kTxBK / 2;   // 8 KiB packed int4
-constexpr int kTxStageBytes = kTxABytes + kTxBBytes + kTxQBytes;
+constexpr int kTxWM = 128;                     // weight rows per MMA block (M, TMEM lanes)
+constexpr int kTxTN = 128;                     // token rows per unit (largest MMA N)
+constexpr int kTxBK = 64;                      // K per stage (one swizzle atom of fp16)
+constexpr int kTxStages = 8;                   // shared-memory ring
+constexpr int kTxAStages = 4;                  // TMEM ring of dequantised weights
+constexpr int kTxXBytes = kTxTN * kTxBK * 2;   // 16 KiB token tile
+constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 8 KiB packed int4 (256 rows x 32 bytes)
+constexpr int kTxStageBytes = kTxXBytes + kTxQBytes;
 constexpr int kTxDqWarps = 8;
 constexpr int kTxEpWarps = 4;
 constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
-constexpr uint32_t kTxCols = 2 * kTxBN;        // two accumulators
+constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 4 x 64 A columns
+constexpr uint32_t kTxAcc1 = kTxTN;            // column of the second accumulator
+constexpr uint32_t kTxACol = 2 * kTxTN;        // first A column
 constexpr int kTxSmem = kTxStages * kTxStageBytes + 1024 + 256;
 static_assert(kTxStageBytes % 1024 == 0, "stage alignment");
-static_assert(kTxDqWarps * 32 == kTxBN, "one dequantisation thread per weight row");
+static_assert(kTxDqWarps * 32 == 2 * kTxWM, "one dequantisation thread per weight row");
+static_assert(kTxACol + kTxAStages * 2 * (kTxBK / 2) <= kTxCols, "TMEM budget");
 
 enum TxMode { kTxGateUp = 0, kTxDown = 1, kTxLinear = 2 };
 
@@ -98,23 +101,25 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTxStages * kTxStageBytes);
-  uint64_t* bready = full + kTxStages;
-  uint64_t* sfree = bready + kTxStages;
-  uint64_t* accfull = sfree + kTxStages;
-  uint64_t* accempty = accfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint64_t* sfree = full + kTxStages;
+  uint64_t* aready = sfree + kTxStages;
+  uint64_t* afree = aready + kTxAStages;
+  uint64_t* accfull = afree + kTxAStages;
+  uint64_t* accempty = accfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTxStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&bready[s], kTxDqWarps);
       mbar_init(&sfree[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accfull[b], 1);
-      mbar_init(&accempty[b], kTxEpWarps);
+    for (int a = 0; a < kTxAStages; ++a) {
+      mbar_init(&aready[a], kTxDqWarps);
+      mbar_init(&afree[a], 1);
     }
+    mbar_init(accfull, 1);
+    mbar_init(accempty, kTxEpWarps);
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const int K = p.K, N = p.N;
-  const int tile_n = (MODE == kTxGateUp) ? kTxBN / 2 : kTxBN;
+  const int tile_n = (MODE == kTxGateUp) ? kTxWM : 2 * kTxWM;  // outputs per unit
   const int n_tiles = (N + tile_n - 1) / tile_n;
   const int units = (*p.n_chunks) * n_tiles;
   const int ksteps = K / kTxBK;
@@ -153,8 +158,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             break;
           }
           uint8_t* st = smem + s * kTxStageBytes;
-          uint8_t* qd = st + kTxABytes + kTxBBytes;
-          mbar_arrive_expect_tx(&full[s], kTxABytes + kTxQBytes);
+          uint8_t* qd = st + kTxXBytes;
+          mbar_arrive_expect_tx(&full[s], kTxStageBytes);
           tma_g2s_2d(st, &maps.a, &full[s], ks * kTxBK, row0);
           if (MODE == kTxGateUp) {
             tma_g2s_3d(qd, &maps.q0, &full[s], ks * (kTxBK / 8), n0, e);
@@ -168,36 +173,44 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kTxBM, kTxBN);
       uint32_t it = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-        const uint32_t b = uc & 1u, uph = (uc >> 1) & 1u;
-        if (!mbar_wait(&accempty[b], uph ^ 1u, p.wait_ns, p.status)) break;
+        const int q = u / n_tiles;
+        const int rows = p.chunk_rows[q];
+        const int nn = rows <= 16 ? 16 : (rows + 15) / 16 * 16;  // MMA N: tokens, multiple of 16
+        const uint32_t idesc = idesc_f16(kTxWM, nn);
+        if (!mbar_wait(accempty, (uc & 1u) ^ 1u, p.wait_ns, p.status)) break;
         tc_fence_after();
-        const uint32_t dt = tbase + b * kTxBN;
         for (int ks = 0; ks < ksteps; ++ks, ++it) {
-          const int s = it % kTxStages;
-          const uint32_t ph = (it / kTxStages) & 1u;
-          if (!mbar_wait(&bready[s], ph, p.wait_ns, p.status)) {
+          const int s = it % kTxStages, a = it % kTxAStages;
+          if (!mbar_wait(&aready[a], (it / kTxAStages) & 1u, p.wait_ns, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint8_t* st = smem + s * kTxStageBytes;
-          const uint64_t da = smem_desc_sw128(st);
-          const uint64_t db = smem_desc_sw128(st + kTxABytes);
+          const uint64_t db = smem_desc_sw128(smem + s * kTxStageBytes);
+          const uint32_t ta = tbase + kTxACol + a * kTxBK;  // block 0; block 1 at +32
 #pragma unroll
-          for (int kk = 0; kk < kTxBK / 16; ++kk)
-            umma_f16(dt, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+          for (int kk = 0; kk < kTxBK / 16; ++kk) {
+            umma_f16_ts(tbase, ta + 8 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+            umma_f16_ts(tbase + kTxAcc1, ta + kTxBK / 2 + 8 * kk, db + 2 * kk, idesc,
+                        (ks | kk) != 0);
+          }
           umma_commit(&sfree[s]);
+          umma_commit(&afree[a]);
         }
-        if (ok) umma_commit(&accfull[b]);
+        if (ok) umma_commit(accfull);
       }
     }
   } else if (warp < 2 + kTxDqWarps) {
     // ----------------------------------------------------- dequantisation
-    const int r = threadIdx.x - 64;  // weight row of this thread within the tile
+    // TMEM lane quarter of this warp: warp % 4; block 0 = warps 2-5, block 1 = 6-9
+    const int qd = warp & 3;
+    const int blk = (warp - 2) >> 2;
+    const int m = 32 * qd + lane;        // TMEM lane = row within the block
+    const int r = blk * kTxWM + m;       // row within the 256-row tile
+    const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -207,8 +220,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       int n;
       const uint16_t* sb;
       if (MODE == kTxGateUp) {
-        n = n0 + (r & (kTxBN / 2 - 1));
-        sb = r < kTxBN / 2 ? p.scale0 : p.scale1;
+        n = n0 + m;
+        sb = blk == 0 ? p.scale0 : p.scale1;
       } else {
         n = n0 + r;
         sb = p.scale0;
@@ -241,166 +254,111 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           sw = scur.x;
           if (valid && ks + 1 < ksteps) scur.x = *reinterpret_cast<const uint32_t*>(srow + 2 * (ks + 1));
         }
-        const int s = it % kTxStages;
-        const uint32_t ph = (it / kTxStages) & 1u;
-        if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) {
+        const int s = it % kTxStages, a = it % kTxAStages;
+        // warp-uniform outcome: the tcgen05.st below needs the whole warp
+        const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, p.wait_ns, p.status) &&
+                         mbar_wait(&afree[a], ((it / kTxAStages) & 1u) ^ 1u, p.wait_ns, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * kTxStageBytes;
         // int4 rows of 32 bytes, stored with the 32-byte swizzle: 16-byte half
         // h of row r sits at half h ^ ((r >> 2) & 1)
-        const uint8_t* qrow = st + kTxABytes + kTxBBytes + r * 32;
+        const uint8_t* qrow = smem + s * kTxStageBytes + kTxXBytes + r * 32;
         const int qx = (r >> 2) & 1;
-        uint8_t* brow = st + kTxABytes + (r >> 3) * 1024 + (r & 7) * 128;
         const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + (qx << 4));
         const uint4 w1 = *reinterpret_cast<const uint4*>(qrow + ((qx ^ 1) << 4));
         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 2ks
         const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 2ks+1
+        uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t w = wv[c];
           const uint32_t sc = c < 4 ? s_lo : s_hi;
-          // (n0,n4), (n1,n5) from w; (n2,n6), (n3,n7) from w >> 8
-          const uint32_t p04 = nib_lo_f16(w, sc), p15 = nib_hi_f16(w, sc);
           const uint32_t w8 = w >> 8;
-          const uint32_t p26 = nib_lo_f16(w8, sc), p37 = nib_hi_f16(w8, sc);
-          // pair order: (n0,n4), (n1,n5), (n2,n6), (n3,n7)
-          *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = make_uint4(p04, p15, p26, p37);
+          av[4 * c + 0] = nib_lo_f16(w, sc);   // (n0, n4)
+          av[4 * c + 1] = nib_hi_f16(w, sc);   // (n1, n5)
+          av[4 * c + 2] = nib_lo_f16(w8, sc);  // (n2, n6)
+          av[4 * c + 3] = nib_hi_f16(w8, sc);  // (n3, n7)
         }
-        fence_proxy_async_smem();
+        tmem_st32(tbase + t_lane + kTxACol + a * kTxBK + blk * (kTxBK / 2), av);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bready[s]);
+        if (lane == 0) mbar_arrive(&aready[a]);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3;  // TMEM lane quarter of this warp
-    const int mrow = 32 * qd + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
     uint32_t uc = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
-      const uint32_t b = uc & 1u, uph = (uc >> 1) & 1u;
       const int q = u / n_tiles, jt = u - q * n_tiles;
       const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
       const int n0 = jt * tile_n;
-      if (!mbar_wait(&accfull[b], uph, p.wait_ns, p.status)) break;
+      // warp-uniform outcome: tcgen05.ld needs the whole warp
+      if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, p.wait_ns, p.status))) break;
       tc_fence_after();
-      const uint32_t ta = tbase + b * kTxBN + (static_cast<uint32_t>(32 * qd) << 16);
-      const bool vrow = mrow < rows;
-      const size_t orow = static_cast<size_t>(row0 + mrow) * N;
-      const float xs = (Q8 && vrow) ? p.x_scale[row0 + mrow] : 1.0f;
-      if (MODE == kTxGateUp) {
+      bool fin = true;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTxBN / 2; c0 += 32) {
-          uint32_t g[32], v[32];
-          tmem_ld32(ta + c0, g);
-          tmem_ld32(ta + kTxBN / 2 + c0, v);
-          tmem_ld_wait();
-          const int col = n0 + c0;
-          if (vrow && col < N) {
-            bool fin = true;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              fin &= fabsf(__uint_as_float(g[i])) <= 3.0e38f && fabsf(__uint_as_float(v[i])) <= 3.0e38f;
-            if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
-            float hv[32];
+      for (int c0 = 0; c0 < rows; c0 += 32) {
+        uint32_t g[32], v[32];
+        tmem_ld32(tbase + t_lane + c0, g);
+        tmem_ld32(tbase + t_lane + kTxAcc1 + c0, v);
+        tmem_ld_wait();
+        if (MODE == kTxGateUp) {
+          const int n = n0 + 32 * qd + lane;  // output feature of this lane
+          if (n < N) {
+            uint16_t* hcol = static_cast<uint16_t*>(p.out) + pair_pos(n);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              float g0 = __uint_as_float(g[i]), u0 = __uint_as_float(v[i]);
+              const int tok = c0 + i;
+              if (tok >= rows) continue;
+              float G = __uint_as_float(g[i]), U = __uint_as_float(v[i]);
+              fin &= fabsf(G) <= 3.0e38f && fabsf(U) <= 3.0e38f;
               if (Q8) {
-                g0 *= xs;
-                u0 *= xs;
+                const float xs = p.x_scale[row0 + tok];
+                G *= xs;
+                U *= xs;
               }
-              hv[i] = g0 / (1.0f + expf(-g0)) * u0;
-            }
-            // pair order: word 4b + j holds columns 8b + j and 8b + j + 4
-            uint32_t hw[16];
-            bool hfin = true;
-#pragma unroll
-            for (int b8 = 0; b8 < 4; ++b8)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float h0 = hv[8 * b8 + j], h1 = hv[8 * b8 + j + 4];
-                if (Q8) {  // bf16 h, as the stream kernel writes it
-                  hw[4 * b8 + j] = static_cast<uint32_t>(f32_to_bf16_bits(h0)) |
-                                   (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
-                } else {
-                  hfin &= fabsf(h0) <= 65504.0f && fabsf(h1) <= 65504.0f;
-                  const __half2 hh = __floats2half2_rn(h0, h1);
-                  hw[4 * b8 + j] = *reinterpret_cast<const uint32_t*>(&hh);
-                }
+              const float h = G / (1.0f + expf(-G)) * U;
+              uint16_t hb;
+              if (Q8) {  // bf16 h, as the stream kernel writes it
+                hb = f32_to_bf16_bits(h);
+              } else {
+                fin &= fabsf(h) <= 65504.0f;
+                hb = __half_as_ushort(__float2half_rn(h));
               }
-            if (!hfin) record_status(p.status, MOE_ERR_UNSUPPORTED);
-            if (col + 32 <= N && (N & 7) == 0) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d4[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
-            } else {
-              // N % 8 == 0 (K of the down projection): whole 8-column blocks
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col + i < N) dst[i] = static_cast<uint16_t>((hw[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+              hcol[(size_t)(row0 + tok) * N] = hb;
             }
           }
-        }
-      } else {
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTxBN; c0 += 32) {
-          uint32_t y[32];
-          tmem_ld32(ta + c0, y);
-          tmem_ld_wait();
-          const int col = n0 + c0;
-          if (vrow && col < N) {
-            bool fin = true;
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) fin &= fabsf(__uint_as_float(y[i])) <= 3.0e38f;
-            if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
-            if (Q8) {
+          for (int b2 = 0; b2 < 2; ++b2) {
+            const int n = n0 + b2 * kTxWM + 32 * qd + lane;
+            if (n >= N) continue;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * xs);
-            }
-            if (MODE == kTxDown) {
-              uint16_t* dst = static_cast<uint16_t*>(p.out) + orow + col;
-              if (col + 32 <= N && (N & 7) == 0) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  uint32_t w4[4];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    w4[j] = static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(y[8 * i + 2 * j]))) |
-                            (static_cast<uint32_t>(f32_to_bf16_bits(__uint_as_float(y[8 * i + 2 * j + 1])))
-                             << 16);
-                  d4[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col + i < N) dst[i] = f32_to_bf16_bits(__uint_as_float(y[i]));
-              }
-            } else {
-              float* dst = static_cast<float*>(p.out) + orow + col;
-              if (col + 32 <= N && (N & 3) == 0) {
-                float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  d4[i] = make_float4(__uint_as_float(y[4 * i]), __uint_as_float(y[4 * i + 1]),
-                                      __uint_as_float(y[4 * i + 2]), __uint_as_float(y[4 * i + 3]));
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col + i < N) dst[i] = __uint_as_float(y[i]);
-              }
+            for (int i = 0; i < 32; ++i) {
+              const int tok = c0 + i;
+              if (tok >= rows) continue;
+              float y = __uint_as_float(b2 ? v[i] : g[i]);
+              fin &= fabsf(y) <= 3.0e38f;
+              if (Q8) y *= p.x_scale[row0 + tok];
+              const size_t o = (size_t)(row0 + tok) * N + n;
+              if (MODE == kTxDown)
+                static_cast<uint16_t*>(p.out)[o] = f32_to_bf16_bits(y);
+              else
+                static_cast<float*>(p.out)[o] = y;
             }
           }
         }
       }
+      if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&accempty[b]);
+      if (lane == 0) mbar_arrive(accempty);
     }
   }
   tc_fence_before();
@@ -414,7 +372,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K) {
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
   const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
-  const uint32_t box[2] = {static_cast<uint32_t>(kTxBK), static_cast<uint32_t>(kTxBM)};
+  const uint32_t box[2] = {static_cast<uint32_t>(kTxBK), static_cast<uint32_t>(kTxTN)};
   return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -556,8 +514,8 @@ int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, in
                      int* status, cudaStream_t s) {
   TxMaps maps;
   if (!act_map(&maps.a, x16, rows_max, D) ||
-      !packed_map(&maps.q0, gate_packed, E, I, D, kTxBN / 2) ||
-      !packed_map(&maps.q1, up_packed, E, I, D, kTxBN / 2))
+      !packed_map(&maps.q0, gate_packed, E, I, D, kTxWM) ||
+      !packed_map(&maps.q1, up_packed, E, I, D, kTxWM))
     return MOE_ERR_CUDA;
   TxParams p{};
   p.scale0 = gate_scale;
@@ -581,7 +539,7 @@ int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int 
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s) {
   TxMaps maps;
-  if (!act_map(&maps.a, h16, rows_max, I) || !packed_map(&maps.q0, down_packed, E, D, I, kTxBN))
+  if (!act_map(&maps.a, h16, rows_max, I) || !packed_map(&maps.q0, down_packed, E, D, I, 2 * kTxWM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;
   TxParams p{};

@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
     const int row = m0 + 32 * q + lane;
-    if (mbar_wait(accf, 0, wait_ns, status)) {
+    // warp-uniform outcome: tcgen05.ld needs the whole warp
+    if (__all_sync(0xffffffffu, mbar_wait(accf, 0, wait_ns, status))) {
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < kTcBN; c0 += 32) {
