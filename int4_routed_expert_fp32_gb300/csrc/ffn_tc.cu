@@ -47,7 +47,7 @@ constexpr int kTxXBytes = kTxTN * kTxBK * 2;   // 16 KiB token tile
 constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 8 KiB packed int4 (256 rows x 32 bytes)
 constexpr int kTxStageBytes = kTxXBytes + kTxQBytes;
 constexpr int kTxDqWarps = 8;
-constexpr int kTxEpWarps = 4;
+constexpr int kTxEpWarps = 8;                  // two per TMEM lane quarter
 constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
 constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 4 x 64 A columns
 constexpr uint32_t kTxAcc1 = kTxTN;            // column of the second accumulator
@@ -213,6 +213,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
     uint32_t it = 0;
     bool ok = true;
+    // The TMEM store of stage i completes (and is signalled) after stage
+    // i + 1 has been computed, so its latency overlaps that work.
+    bool pend = false;
+    int pend_a = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int q = u / n_tiles, jt = u - q * n_tiles;
       const int e = p.chunk_e[q];
@@ -282,16 +286,29 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           av[4 * c + 2] = nib_lo_f16(w8, sc);  // (n2, n6)
           av[4 * c + 3] = nib_hi_f16(w8, sc);  // (n3, n7)
         }
+        if (pend) {  // the previous stage's store is complete: hand it to the MMA
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&aready[pend_a]);
+        }
         tmem_st32(tbase + t_lane + kTxACol + a * kTxBK + blk * (kTxBK / 2), av);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aready[a]);
+        pend = true;
+        pend_a = a;
       }
+    }
+    if (pend && ok) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aready[pend_a]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int qd = warp & 3;  // TMEM lane quarter of this warp
+    // two warps per TMEM lane quarter: half eh takes the 32-token chunks
+    // 32 eh, 32 eh + 64, ...
+    const int qd = warp & 3;
+    const int eh = (warp - 2 - kTxDqWarps) >> 2;
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
     uint32_t uc = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
@@ -303,7 +320,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       tc_fence_after();
       bool fin = true;
 #pragma unroll 1
-      for (int c0 = 0; c0 < rows; c0 += 32) {
+      for (int c0 = 32 * eh; c0 < rows; c0 += 64) {
         uint32_t g[32], v[32];
         tmem_ld32(tbase + t_lane + c0, g);
         tmem_ld32(tbase + t_lane + kTxAcc1 + c0, v);
@@ -323,7 +340,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 G *= xs;
                 U *= xs;
               }
-              const float h = G / (1.0f + expf(-G)) * U;
+              // SiLU(G) * U with the fast exponential and division (the
+              // quotient is 0 once 1 + exp(-G) overflows)
+              const float h = __fdividef(G, 1.0f + __expf(-G)) * U;
               uint16_t hb;
               if (Q8) {  // bf16 h, as the stream kernel writes it
                 hb = f32_to_bf16_bits(h);
