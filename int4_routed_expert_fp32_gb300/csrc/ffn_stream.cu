@@ -23,8 +23,9 @@
 //     (1,5) and (3,7) in bits 4-7 and hold 1152 + 16 q, all exactly.  They
 //     are the A operands of two m16n8k16 fp16 MMAs per 32-column group (one
 //     per pair kind) against up to 2 blocks of 8 token rows.  The constants
-//     are removed through the accumulators: each chain starts from the MMA of
-//     a constant tile (-1032, or -1152) with the same activations.  The
+//     are removed through the accumulators: each chain starts from -1032 (or
+//     -1152) times the sum of the token's activations of those columns,
+//     computed once per stage for the whole CTA by a start-value warp.  The
 //     group's partial, low + high / 16, is then multiplied by its bf16 scale
 //     and accumulated in fp32, so the dequantised weight q * scale is never
 //     rounded;
@@ -58,7 +59,7 @@ constexpr int kFsCWarps = FS_CWARPS;       // consumer warps, one 16-row block e
 #define FS_UNROLL 4
 #endif
 constexpr int kFsUnroll = FS_UNROLL;       // group pairs unrolled with one token block
-constexpr int kFsThreads = (kFsCWarps + 1) * 32;
+constexpr int kFsThreads = (kFsCWarps + 2) * 32;  // + TMA producer + start-value warp
 constexpr int kFsRows = 16 * kFsCWarps;    // weight rows per stage tile
 constexpr int kFsStages = (FS_CWARPS <= 12) ? 5 : 4;
 constexpr int kFsWBytes = kFsRows * 128;   // 32 KiB of packed int4 per stage
@@ -66,8 +67,9 @@ constexpr int kFsSBytes = kFsRows * 16;    // 8 bf16 scales per row per stage
 constexpr int kFsXStride16 = kFsKc * 2 + 64;  // bf16 row stride in shared memory
 constexpr int kFsXStride8 = kFsKc + 32;       // int8 row stride in shared memory
 constexpr int kFsXBytes = kFsMc * kFsXStride16;
+constexpr int kFsCBytes = kFsGroups * kFsMc * 2 * 4;  // chain start values [group][token][2]
 constexpr int kFsStageBytes =
-    (kFsWBytes + kFsSBytes + kFsXBytes + 1023) / 1024 * 1024;  // keeps 1024-byte alignment
+    (kFsWBytes + kFsSBytes + kFsXBytes + kFsCBytes + 1023) / 1024 * 1024;  // 1024-byte aligned
 constexpr int kFsXchBytes = (kFsRows / 2) * kFsMc * 4;          // up partials of one unit
 constexpr int kFsSmemBytes = kFsStages * kFsStageBytes + 2 * kFsXchBytes + 1024 + 256;
 static_assert(kFsStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -125,12 +127,6 @@ __device__ __forceinline__ void dequant_magic(uint32_t w, uint32_t (&out)[4]) {
   out[3] = (w8 & 0x00F000F0u) ^ 0x64806480u;
 }
 
-// fp16x2 (-1032, -1032) and (-1152, -1152): A operands of the MMAs that form
-// the start value of each chain, -1032 (or -1152) * (sum of the activations
-// of those columns).
-constexpr uint32_t kNegLo = 0xE408E408u;
-constexpr uint32_t kNegHi = 0xE480E480u;
-
 // Two int8 values (bytes selected by `sel` into the low byte of each half)
 // -> fp16x2, exactly: 1024 + (x + 128) via the 0x6480 xor, minus 1152.
 __device__ __forceinline__ uint32_t i8pair_f16x2(uint32_t w, uint32_t sel) {
@@ -174,13 +170,12 @@ struct Lane {
 // NTB blocks of 8 tokens.  FULL: all 8 groups present (no tail checks).
 template <bool Q8, int NTB, bool FULL>
 __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S, const uint8_t* X,
-                                              int ng, const Lane& L, float (&acc)[NTB][4]) {
+                                              const uint8_t* C, int ng, const Lane& L,
+                                              float (&acc)[NTB][4]) {
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
-  const uint32_t neg_lo[4] = {kNegLo, kNegLo, kNegLo, kNegLo};
-  const uint32_t neg_hi[4] = {kNegHi, kNegHi, kNegHi, kNegHi};
-  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
   const uint32_t* s_lo_row = reinterpret_cast<const uint32_t*>(S + L.rlo * 16);
   const uint32_t* s_hi_row = reinterpret_cast<const uint32_t*>(S + (L.rlo + 8) * 16);
+  const float4* cst = reinterpret_cast<const float4*>(C);  // [group][token pair]
   // two token blocks keep more values live: unroll less there
 #pragma unroll(NTB == 1 ? kFsUnroll : 1)
   for (int G2 = 0; G2 < kFsGroups; G2 += 2) {
@@ -203,9 +198,10 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
       for (int tb = 0; tb < NTB; ++tb) {
         uint32_t bfr[4];
         load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr);
-        float clo[4], chi[4];
-        mma_f16_16816(clo, neg_lo, bfr[0], bfr[2], zero);
-        mma_f16_16816(chi, neg_hi, bfr[1], bfr[3], zero);
+        // start values of tokens 8 tb + 2t and + 1: (-1032 S_lo, -1152 S_hi) each
+        const float4 c = cst[G * (kFsMc / 2) + tb * 4 + L.t];
+        float clo[4] = {c.x, c.z, c.x, c.z};
+        float chi[4] = {c.y, c.w, c.y, c.w};
         mma_f16_16816(clo, alo, bfr[0], bfr[2], clo);
         mma_f16_16816(chi, ahi, bfr[1], bfr[3], chi);
         acc[tb][0] = fmaf(s_lo, fmaf(chi[0], 0.0625f, clo[0]), acc[tb][0]);
@@ -217,6 +213,55 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
   }
 }
 
+// Start values of the MMA chains of one stage, for the chunk's token rows:
+// C[G][tok] = (-1032 * sum of the activations the low-nibble chain of group G
+// multiplies, -1152 * the same for the high-nibble chain).  In pair order
+// (c0 c4 c1 c5 c2 c6 c3 c7) the low chain takes positions 0, 1, 4, 5 of each
+// block of 8 (fragments b[0], b[2]: columns 0 4 2 6) and the high chain
+// positions 2, 3, 6, 7.  Lane l: token l % 16, groups 4 (l / 16) .. + 3.
+// With int8 activations the sums are exact integers.
+template <bool Q8>
+__device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int ng, int lane) {
+  const int tk = lane & 15;
+  float2* out = reinterpret_cast<float2*>(C);
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    const int G = 4 * (lane >> 4) + gi;
+    if (G >= ng) break;
+    float lo = 0.f, hi = 0.f;
+    if (!Q8) {
+      const uint4* xg = reinterpret_cast<const uint4*>(X + tk * kFsXStride16 + G * 64);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {  // one block of 8 per 16 bytes
+        const uint4 w = xg[v];
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));  // pos 0, 1
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));  // pos 2, 3
+        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&w.z));  // pos 4, 5
+        const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&w.w));  // pos 6, 7
+        lo += (f0.x + f0.y) + (f2.x + f2.y);
+        hi += (f1.x + f1.y) + (f3.x + f3.y);
+      }
+    } else {
+      const uint2* xg = reinterpret_cast<const uint2*>(X + tk * kFsXStride8 + G * 32);
+      int ilo = 0, ihi = 0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {  // one block of 8 per 8 bytes
+        const uint2 w = xg[v];
+        const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t b = ws[j];
+          ilo += static_cast<int8_t>(b & 0xffu) + static_cast<int8_t>((b >> 8) & 0xffu);
+          ihi += static_cast<int8_t>((b >> 16) & 0xffu) + static_cast<int8_t>(b >> 24);
+        }
+      }
+      lo = static_cast<float>(ilo);
+      hi = static_cast<float>(ihi);
+    }
+    out[G * kFsMc + tk] = make_float2(-1032.0f * lo, -1152.0f * hi);
+  }
+}
+
 __device__ __forceinline__ void consumer_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kFsCWarps * 32) : "memory");
 }
@@ -224,7 +269,7 @@ __device__ __forceinline__ void consumer_bar_sync() {
 // All K stages of one unit (expert chunk x row tile) for NTB token blocks,
 // then the epilogue.  Returns false when a wait gave up.
 template <int MODE, bool Q8, int NTB>
-__device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t* full,
+__device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t* ready,
                                              uint64_t* empty, uint32_t& it, int ksteps, int row0,
                                              int rows, int n0, int cw, int lane, const Lane& L,
                                              const FsParams& p) {
@@ -239,16 +284,17 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    if (ok && !mbar_wait(&full[s], ph, p.wait_ns, p.status)) ok = false;
+    if (ok && !mbar_wait(&ready[s], ph, p.wait_ns, p.status)) ok = false;
     if (ok) {
       const uint8_t* W = smem + s * kFsStageBytes;
       const uint8_t* S = W + kFsWBytes;
       const uint8_t* X = S + kFsSBytes;
+      const uint8_t* C = X + kFsXBytes;
       const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
       if (ng == kFsGroups)
-        stage_compute<Q8, NTB, true>(W, S, X, ng, L, acc);
+        stage_compute<Q8, NTB, true>(W, S, X, C, ng, L, acc);
       else
-        stage_compute<Q8, NTB, false>(W, S, X, ng, L, acc);
+        stage_compute<Q8, NTB, false>(W, S, X, C, ng, L, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -323,6 +369,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   float* xch = reinterpret_cast<float*>(smem + kFsStages * kFsStageBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFsStages * kFsStageBytes + 2 * kFsXchBytes);
   uint64_t* empty = full + kFsStages;
+  uint64_t* ready = empty + kFsStages;  // stage landed and its chain start values written
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool tma_s = p.tma_scales != 0;
@@ -330,7 +377,8 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     for (int s = 0; s < kFsStages; ++s) {
       // producer arrive.expect_tx (+ 32 cp.async arrivals when scales use cp.async)
       mbar_init(&full[s], tma_s ? 1 : 1 + 32);
-      mbar_init(&empty[s], kFsCWarps);  // one arrival per consumer warp
+      mbar_init(&empty[s], kFsCWarps + 1);  // one arrival per consumer warp + the start-value warp
+      mbar_init(&ready[s], 1);
     }
     fence_mbarrier_init();
   }
@@ -432,6 +480,28 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     return;
   }
 
+  if (warp == kFsCWarps + 1) {
+    // --------------------------------------------- chain start values
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const int s = it % kFsStages;
+        const uint32_t ph = (it / kFsStages) & 1u;
+        if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return;
+        uint8_t* st = smem + s * kFsStageBytes;
+        const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
+        stage_starts<Q8>(st + kFsWBytes + kFsSBytes, st + kFsWBytes + kFsSBytes + kFsXBytes, ng,
+                         lane);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ready[s]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   Lane L;
   L.g = lane >> 2;
@@ -454,10 +524,10 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     float* x = xch + parity * (kFsXchBytes / 4);
     bool ok;
     if (rows <= 8)
-      ok = consume_unit<MODE, Q8, 1>(smem, x, full, empty, it, ksteps, row0, rows, n0, warp, lane,
+      ok = consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
                                      L, p);
     else
-      ok = consume_unit<MODE, Q8, 2>(smem, x, full, empty, it, ksteps, row0, rows, n0, warp, lane,
+      ok = consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
                                      L, p);
     if (!ok) return;
   }

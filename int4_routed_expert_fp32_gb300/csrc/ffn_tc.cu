@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
       const int n0 = jt * tile_n;
       // warp-uniform outcome: tcgen05.ld needs the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, p.wait_ns, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, p.wait_ns, p.status, 256))) break;
       tc_fence_after();
       bool fin = true;
 #pragma unroll 1
