@@ -19,24 +19,24 @@
 //   * sixteen consumer warps each own one 16-row block.  One ldmatrix gives a
 //     lane its packed words of two groups.  Each word becomes four fp16x2
 //     registers with one shift and four masks: the nibble pairs (0,4) and
-//     (2,6) land in the low mantissa bits of 1024 and hold 1032 + q, the pairs
-//     (1,5) and (3,7) in bits 4-7 and hold 1152 + 16 q, all exactly.  They
-//     are the A operands of two m16n8k16 fp16 MMAs per 32-column group (one
-//     per pair kind) against up to 2 blocks of 8 token rows.  The constants
-//     are removed through the accumulators: each chain starts from -1032 (or
-//     -1152) times the sum of the token's activations of those columns,
-//     computed once per stage for the whole CTA by a start-value warp.  The
-//     group's partial, low + high / 16, is then multiplied by its bf16 scale
-//     and accumulated in fp32, so the dequantised weight q * scale is never
-//     rounded;
+//     (2,6) land in the low mantissa bits of 1024.0 and hold 1032 + q, the
+//     pairs (1,5) and (3,7) in bits 4-7 of 64.0 and hold 72 + q, all
+//     exactly.  They are the A operands of one chain of two m16n8k16 fp16
+//     MMAs per 32-column group against up to 2 blocks of 8 token rows.  The
+//     constants are removed through the accumulator: the chain starts from
+//     -(1032 S_lo + 72 S_hi), S the sums of the token's activations that the
+//     two kinds of values multiply, computed once per stage for the whole CTA
+//     by a start-value warp.  The group's partial is then multiplied by its
+//     bf16 scale and accumulated in fp32, so the dequantised weight q * scale
+//     is never rounded;
 //   * in the gate/up variant warps 0-7 hold gate rows and warps 8-15 the up
 //     rows of the same outputs; the up partials go through shared memory and
 //     the gate warps write h = SiLU(G) * U in pair order (fp16; bf16 with
 //     act_bits 8, for its re-quantisation).  The down variant writes y.
-// act_bits 8: the int8 activations become exact fp16 integers; both chains
-// of a group stay exact integers (|sum| <= 16 * 1280 * 127 < 2^24), so the
-// group partial is the exact integer sum, and the row scale is applied in
-// the epilogue.
+// act_bits 8: the int8 activations become exact fp16 integers; the chain of
+// a group stays an exact integer (|partial sums| <= 32 * 1040 * 127 < 2^24),
+// so the group partial is the exact integer sum, and the row scale is
+// applied in the epilogue.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -67,7 +67,7 @@ constexpr int kFsSBytes = kFsRows * 16;    // 8 bf16 scales per row per stage
 constexpr int kFsXStride16 = kFsKc * 2 + 64;  // bf16 row stride in shared memory
 constexpr int kFsXStride8 = kFsKc + 32;       // int8 row stride in shared memory
 constexpr int kFsXBytes = kFsMc * kFsXStride16;
-constexpr int kFsCBytes = kFsGroups * kFsMc * 2 * 4;  // chain start values [group][token][2]
+constexpr int kFsCBytes = kFsGroups * kFsMc * 4;  // chain start values [group][token]
 constexpr int kFsStageBytes =
     (kFsWBytes + kFsSBytes + kFsXBytes + kFsCBytes + 1023) / 1024 * 1024;  // 1024-byte aligned
 constexpr int kFsXchBytes = (kFsRows / 2) * kFsMc * 4;          // up partials of one unit
@@ -116,15 +116,18 @@ __device__ __forceinline__ void ldsm_x4(const void* addr, uint32_t (&r)[4]) {
 }
 
 // Eight two's-complement nibbles n_0..n_7 of one packed word -> four fp16x2:
-//   out[0] = (n0, n4), out[2] = (n2, n6): 1024 + (n ^ 8) = 1032 + q;
-//   out[1] = (n1, n5), out[3] = (n3, n7): 1024 + 16 (n ^ 8) = 1152 + 16 q.
-// Low half = the lower nibble of the pair.  One shift and four mask-xor ops.
+//   out[0] = (n0, n4), out[2] = (n2, n6): in the low mantissa bits of 1024.0
+//            (ulp 1): 1024 + (n ^ 8) = 1032 + q;
+//   out[1] = (n1, n5), out[3] = (n3, n7): in mantissa bits 4-7 of 64.0 (ulp
+//            1/16): 64 + (n ^ 8) = 72 + q.
+// Low half = the lower nibble of the pair.  One shift and four mask-xor ops;
+// every value is exact and carries q with weight 1.
 __device__ __forceinline__ void dequant_magic(uint32_t w, uint32_t (&out)[4]) {
   const uint32_t w8 = w >> 8;
   out[0] = (w & 0x000F000Fu) ^ 0x64086408u;
-  out[1] = (w & 0x00F000F0u) ^ 0x64806480u;
+  out[1] = (w & 0x00F000F0u) ^ 0x54805480u;
   out[2] = (w8 & 0x000F000Fu) ^ 0x64086408u;
-  out[3] = (w8 & 0x00F000F0u) ^ 0x64806480u;
+  out[3] = (w8 & 0x00F000F0u) ^ 0x54805480u;
 }
 
 // Two int8 values (bytes selected by `sel` into the low byte of each half)
@@ -175,7 +178,7 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
   const uint32_t* s_lo_row = reinterpret_cast<const uint32_t*>(S + L.rlo * 16);
   const uint32_t* s_hi_row = reinterpret_cast<const uint32_t*>(S + (L.rlo + 8) * 16);
-  const float4* cst = reinterpret_cast<const float4*>(C);  // [group][token pair]
+  const float2* cst = reinterpret_cast<const float2*>(C);  // [group][token pair]
   // two token blocks keep more values live: unroll less there
 #pragma unroll(NTB == 1 ? kFsUnroll : 1)
   for (int G2 = 0; G2 < kFsGroups; G2 += 2) {
@@ -198,32 +201,32 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
       for (int tb = 0; tb < NTB; ++tb) {
         uint32_t bfr[4];
         load_b_frag<Q8>(X + (tb * 8 + L.g) * xstride, G, L.t, bfr);
-        // start values of tokens 8 tb + 2t and + 1: (-1032 S_lo, -1152 S_hi) each
-        const float4 c = cst[G * (kFsMc / 2) + tb * 4 + L.t];
-        float clo[4] = {c.x, c.z, c.x, c.z};
-        float chi[4] = {c.y, c.w, c.y, c.w};
-        mma_f16_16816(clo, alo, bfr[0], bfr[2], clo);
-        mma_f16_16816(chi, ahi, bfr[1], bfr[3], chi);
-        acc[tb][0] = fmaf(s_lo, fmaf(chi[0], 0.0625f, clo[0]), acc[tb][0]);
-        acc[tb][1] = fmaf(s_lo, fmaf(chi[1], 0.0625f, clo[1]), acc[tb][1]);
-        acc[tb][2] = fmaf(s_hi, fmaf(chi[2], 0.0625f, clo[2]), acc[tb][2]);
-        acc[tb][3] = fmaf(s_hi, fmaf(chi[3], 0.0625f, clo[3]), acc[tb][3]);
+        // start value of tokens 8 tb + 2t and + 1: -(1032 S_lo + 72 S_hi)
+        const float2 c2 = cst[G * (kFsMc / 2) + tb * 4 + L.t];
+        float c[4] = {c2.x, c2.y, c2.x, c2.y};
+        mma_f16_16816(c, alo, bfr[0], bfr[2], c);
+        mma_f16_16816(c, ahi, bfr[1], bfr[3], c);
+        acc[tb][0] = fmaf(s_lo, c[0], acc[tb][0]);
+        acc[tb][1] = fmaf(s_lo, c[1], acc[tb][1]);
+        acc[tb][2] = fmaf(s_hi, c[2], acc[tb][2]);
+        acc[tb][3] = fmaf(s_hi, c[3], acc[tb][3]);
       }
     }
   }
 }
 
 // Start values of the MMA chains of one stage, for the chunk's token rows:
-// C[G][tok] = (-1032 * sum of the activations the low-nibble chain of group G
-// multiplies, -1152 * the same for the high-nibble chain).  In pair order
-// (c0 c4 c1 c5 c2 c6 c3 c7) the low chain takes positions 0, 1, 4, 5 of each
-// block of 8 (fragments b[0], b[2]: columns 0 4 2 6) and the high chain
-// positions 2, 3, 6, 7.  Lane l: token l % 16, groups 4 (l / 16) .. + 3.
-// With int8 activations the sums are exact integers.
+// C[G][tok] = -(1032 * S_lo + 72 * S_hi), where S_lo sums the token's
+// activations that the low-nibble values (1032 + q) of group G multiply and
+// S_hi those of the high-nibble values (72 + q).  In pair order (c0 c4 c1 c5
+// c2 c6 c3 c7) the low values take positions 0, 1, 4, 5 of each block of 8
+// (fragments b[0], b[2]: columns 0 4 2 6) and the high values positions 2,
+// 3, 6, 7.  Lane l: token l % 16, groups 4 (l / 16) .. + 3.  With int8
+// activations the sums, and the start values, are exact integers.
 template <bool Q8>
 __device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int ng, int lane) {
   const int tk = lane & 15;
-  float2* out = reinterpret_cast<float2*>(C);
+  float* out = reinterpret_cast<float*>(C);
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     const int G = 4 * (lane >> 4) + gi;
@@ -258,7 +261,7 @@ __device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int n
       lo = static_cast<float>(ilo);
       hi = static_cast<float>(ihi);
     }
-    out[G * kFsMc + tk] = make_float2(-1032.0f * lo, -1152.0f * hi);
+    out[G * kFsMc + tk] = -(1032.0f * lo + 72.0f * hi);
   }
 }
 

@@ -314,8 +314,9 @@ def test_int4_linear_exact_mode_scaled(moe):
     (320, 192, [0, 3, 40, 1, 0, 9]),
     (256, 128, [16, 16]),
     (1024, 512, [1, 2, 65, 0]),          # one expert on the tensor-core path (>= 17 rows)
-    (320, 192, [130, 5, 64, 0, 16, 17]), # ragged 128-row tails, ragged N tiles, threshold edges
+    (320, 192, [130, 5, 64, 0, 16, 17]), # ragged token tiles, ragged N tiles, threshold edges
     (256, 128, [16, 16, 16, 0, 3]),      # tensor-core kernels launched with no tile to do
+    (256, 192, [400, 3, 0, 193]),        # several 192-row chunks per expert, ragged last chunks
 ])
 def test_expert_ffn_parity(moe, act_bits, D, I, counts):
     rng = np.random.default_rng(D + I + act_bits)
