@@ -221,16 +221,16 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
 // S_hi those of the high-nibble values (72 + q).  In pair order (c0 c4 c1 c5
 // c2 c6 c3 c7) the low values take positions 0, 1, 4, 5 of each block of 8
 // (fragments b[0], b[2]: columns 0 4 2 6) and the high values positions 2,
-// 3, 6, 7.  Lane l: token l % 16, groups 4 (l / 16) .. + 3.  With int8
+// 3, 6, 7.  Only the chunk's rows are summed: lane l takes the (token,
+// group) pairs l, l + 32, ... of the rows x ng pairs.  With int8
 // activations the sums, and the start values, are exact integers.
 template <bool Q8>
-__device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int ng, int lane) {
-  const int tk = lane & 15;
+__device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int ng, int rows,
+                                             int lane) {
   float* out = reinterpret_cast<float*>(C);
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    const int G = 4 * (lane >> 4) + gi;
-    if (G >= ng) break;
+#pragma unroll 1
+  for (int idx = lane; idx < rows * ng; idx += 32) {
+    const int tk = idx / ng, G = idx - tk * ng;
     float lo = 0.f, hi = 0.f;
     if (!Q8) {
       const uint4* xg = reinterpret_cast<const uint4*>(X + tk * kFsXStride16 + G * 64);
@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     // --------------------------------------------- chain start values
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int rows = p.chunk_rows[u / n_tiles];
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
         const int s = it % kFsStages;
         const uint32_t ph = (it / kFsStages) & 1u;
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
         uint8_t* st = smem + s * kFsStageBytes;
         const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
         stage_starts<Q8>(st + kFsWBytes + kFsSBytes, st + kFsWBytes + kFsSBytes + kFsXBytes, ng,
-                         lane);
+                         rows, lane);
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&ready[s]);
