@@ -202,22 +202,29 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  // gridDim.y slices of the row's 16-byte vectors (few tokens: more CTAs);
+  // slice 0 also writes the permutation
+  const bool first = blockIdx.y == 0;
   int row = -1;
   if (lane < k) {
     const int e = idx[(size_t)t * k + lane];
     if (e >= 0 && e < E) {
       row = offsets[e] + hist[(size_t)(t / kChunkTokens) * E + e] + local_rank[(size_t)t * k + lane];
-      row_token[row] = t;
-      row_slot[row] = lane;
+      if (first) {
+        row_token[row] = t;
+        row_slot[row] = lane;
+      }
     }
-    inv_row[(size_t)t * k + lane] = row;
+    if (first) inv_row[(size_t)t * k + lane] = row;
   }
   const int nv = D / 8;
+  const int per = (nv + gridDim.y - 1) / gridDim.y;
+  const int v0 = blockIdx.y * per, v1 = min(nv, v0 + per);
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * D);
   if (!Q8) {
     uint4* dst = static_cast<uint4*>(x_sorted);
     bool fin = true;
-    for (int v = lane; v < nv; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
       const uint4 val = PAIR ? bf16x8_to_f16_pairs(src[v], fin) : src[v];
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, row, j);
@@ -226,9 +233,9 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
     }
     if (PAIR && !fin) record_status(status, MOE_ERR_UNSUPPORTED);
   } else {
-    const float sc = warp_row_scale(src, nv, lane);
+    const float sc = warp_row_scale(src, nv, lane);  // the whole row, in every slice
     uint2* dst = static_cast<uint2*>(x_sorted);
-    for (int v = lane; v < nv; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
       uint2 q = quant8(src[v], sc);
       if (PAIR) q = make_uint2(__byte_perm(q.x, q.y, 0x5140u), __byte_perm(q.x, q.y, 0x7362u));
       for (int j = 0; j < k; ++j) {
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
         if (r >= 0) dst[(size_t)r * nv + v] = q;
       }
     }
-    if (lane < k && row >= 0) x_scale[row] = sc;
+    if (first && lane < k && row >= 0) x_scale[row] = sc;
   }
 }
 
@@ -314,8 +321,14 @@ static int run_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D
                                       : dispatch_place_kernel<false, false>)
                               : (pair ? dispatch_place_kernel<true, true>
                                       : dispatch_place_kernel<true, false>);
-  place<<<(T + 7) / 8, 256, 0, s>>>(topk_idx, x, T, D, E, k, hist, local_rank, offsets, row_token,
-                                     row_slot, inv_row, x_sorted, x_scale, status);
+  // few tokens: split each row over CTAs so that about 4 CTAs per SM run
+  const int blocks = (T + 7) / 8;
+  const int max_slices = (D / 8 + 31) / 32;
+  int slices = (4 * num_sms() + blocks - 1) / blocks;
+  slices = slices < 1 ? 1 : (slices > max_slices ? max_slices : slices);
+  place<<<dim3(blocks, slices), 256, 0, s>>>(topk_idx, x, T, D, E, k, hist, local_rank, offsets,
+                                             row_token, row_slot, inv_row, x_sorted, x_scale,
+                                             status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
