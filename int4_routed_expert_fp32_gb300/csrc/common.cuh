@@ -140,6 +140,7 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_t limit_ns,
                                           int* status, uint32_t backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (status_set(status)) return false;  // fail fast once an error is recorded
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1

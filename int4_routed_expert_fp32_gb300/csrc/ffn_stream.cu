@@ -265,6 +265,10 @@ __device__ __forceinline__ void stage_starts(const uint8_t* X, uint8_t* C, int n
   }
 }
 
+__device__ __forceinline__ void named_bar_sync_n(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void consumer_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kFsCWarps * 32) : "memory");
 }
@@ -363,6 +367,112 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
   return ok;
 }
 
+// Producer side of one unit: for each K stage wait for a free slot, then
+// TMA the weight (and scale) tiles and bulk-copy the chunk's activation rows.
+// Returns false when a wait gave up.
+template <int MODE, bool Q8>
+__device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams& p, uint8_t* smem,
+                                             uint64_t* full, uint64_t* empty, uint32_t& it,
+                                             int e, int row0, int rows, int n0, int lane) {
+  constexpr int elem = Q8 ? 1 : 2;
+  constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
+  const int K = p.K, N = p.N;
+  const int ksteps = (K + kFsKc - 1) / kFsKc;
+  const int G_all = K / kGroup;
+  const bool tma_s = p.tma_scales != 0;
+  for (int ks = 0; ks < ksteps; ++ks, ++it) {
+    const int s = it % kFsStages;
+    const uint32_t ph = (it / kFsStages) & 1u;
+    if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, p.status)) return false;
+    uint8_t* st = smem + s * kFsStageBytes;
+    uint8_t* sdst = st + kFsWBytes;
+    const int k0 = ks * kFsKc;
+    const int ng = min(kFsGroups, (K - k0) / kGroup);
+    const uint32_t xrow_bytes = static_cast<uint32_t>(ng * kGroup * elem);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&full[s], kFsWBytes + (tma_s ? kFsSBytes : 0) +
+                                          static_cast<uint32_t>(rows) * xrow_bytes);
+      if (MODE == kGateUp) {
+        tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
+        tma_g2s_3d(st + kFsWBytes / 2, &maps.w1, &full[s], k0 / 8, n0, e);
+        if (tma_s) {
+          tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
+          tma_g2s_3d(sdst + kFsSBytes / 2, &maps.s1, &full[s], k0 / kGroup, n0, e);
+        }
+      } else {
+        tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
+        if (tma_s) tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
+      }
+    }
+    __syncwarp();
+    if (lane < rows) {
+      const uint8_t* src = static_cast<const uint8_t*>(p.x) + ((size_t)(row0 + lane) * K + k0) * elem;
+      bulk_g2s(st + kFsWBytes + kFsSBytes + lane * xstride, src, xrow_bytes, &full[s]);
+    }
+    if (!tma_s) {
+      // scales: row r of the tile, group pair pr (4 bytes)
+      const int g0 = k0 / kGroup;
+#pragma unroll 4
+      for (int i = 0; i < kFsRows * 4 / 32; ++i) {
+        const int c = lane + 32 * i;
+        const int r = c >> 2, pr = c & 3;
+        if (2 * pr >= ng) continue;
+        int n;
+        const uint16_t* sbase;
+        if (MODE == kGateUp) {
+          const bool up = r >= kFsRows / 2;
+          n = n0 + (up ? r - kFsRows / 2 : r);
+          sbase = up ? p.scale1 : p.scale0;
+        } else {
+          n = n0 + r;
+          sbase = p.scale0;
+        }
+        if (n >= N) continue;
+        cp_async_4(sdst + r * 16 + pr * 4, sbase + ((size_t)e * N + n) * G_all + g0 + 2 * pr);
+      }
+      cp_async_arrive_noinc(&full[s]);
+    }
+  }
+  return true;
+}
+
+// Let the copies a stopping producer already issued land before the CTA
+// exits (bounded).
+__device__ __forceinline__ void drain_copies(uint64_t* full, uint32_t it) {
+  const uint32_t first = it >= kFsStages ? it - kFsStages : 0;
+  for (uint32_t i = first; i < it; ++i) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(&full[i % kFsStages], (i / kFsStages) & 1u)) {
+      if (static_cast<int64_t>(global_timer_ns() - t0) > 100000000LL) break;
+    }
+  }
+}
+
+// Start-value side of one unit (see stage_starts).  Returns false when a wait
+// gave up.
+template <bool Q8>
+__device__ __forceinline__ bool starts_unit(const FsParams& p, uint8_t* smem, uint64_t* full,
+                                            uint64_t* empty, uint64_t* ready, uint32_t& it,
+                                            int rows, int lane) {
+  const int K = p.K;
+  const int ksteps = (K + kFsKc - 1) / kFsKc;
+  for (int ks = 0; ks < ksteps; ++ks, ++it) {
+    const int s = it % kFsStages;
+    const uint32_t ph = (it / kFsStages) & 1u;
+    if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return false;
+    uint8_t* st = smem + s * kFsStageBytes;
+    const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
+    stage_starts<Q8>(st + kFsWBytes + kFsSBytes, st + kFsWBytes + kFsSBytes + kFsXBytes, ng, rows,
+                     lane);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&ready[s]);
+      mbar_arrive(&empty[s]);
+    }
+  }
+  return true;
+}
+
 template <int MODE, bool Q8>
 __global__ void __launch_bounds__(kFsThreads, 1)
     ffn_stream_kernel(const __grid_constant__ FsMaps maps, const FsParams p) {
@@ -392,9 +502,6 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   const int n_tiles = (N + tile_n - 1) / tile_n;
   const int units = (*p.n_chunks) * n_tiles;
   const int ksteps = (K + kFsKc - 1) / kFsKc;
-  const int G_all = K / kGroup;
-  constexpr int elem = Q8 ? 1 : 2;
-  constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
 
   if (warp == kFsCWarps) {
     // ------------------------------------------------------------ producer
@@ -410,99 +517,18 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int q = u / n_tiles, jt = u - q * n_tiles;
-      const int e = p.chunk_e[q], row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
-      const int n0 = jt * tile_n;
-      for (int ks = 0; ks < ksteps; ++ks, ++it) {
-        const int s = it % kFsStages;
-        const uint32_t ph = (it / kFsStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, p.status)) {
-          ok = false;
-          break;
-        }
-        uint8_t* st = smem + s * kFsStageBytes;
-        uint8_t* sdst = st + kFsWBytes;
-        const int k0 = ks * kFsKc;
-        const int ng = min(kFsGroups, (K - k0) / kGroup);
-        const uint32_t xrow_bytes = static_cast<uint32_t>(ng * kGroup * elem);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], kFsWBytes + (tma_s ? kFsSBytes : 0) +
-                                              static_cast<uint32_t>(rows) * xrow_bytes);
-          if (MODE == kGateUp) {
-            tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
-            tma_g2s_3d(st + kFsWBytes / 2, &maps.w1, &full[s], k0 / 8, n0, e);
-            if (tma_s) {
-              tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
-              tma_g2s_3d(sdst + kFsSBytes / 2, &maps.s1, &full[s], k0 / kGroup, n0, e);
-            }
-          } else {
-            tma_g2s_3d(st, &maps.w0, &full[s], k0 / 8, n0, e);
-            if (tma_s) tma_g2s_3d(sdst, &maps.s0, &full[s], k0 / kGroup, n0, e);
-          }
-        }
-        __syncwarp();
-        if (lane < rows) {
-          const uint8_t* src = static_cast<const uint8_t*>(p.x) +
-                               ((size_t)(row0 + lane) * K + k0) * elem;
-          bulk_g2s(st + kFsWBytes + kFsSBytes + lane * xstride, src, xrow_bytes, &full[s]);
-        }
-        if (!tma_s) {
-          // scales: row r of the tile, group pair pr (4 bytes)
-          const int g0 = k0 / kGroup;
-#pragma unroll 4
-          for (int i = 0; i < kFsRows * 4 / 32; ++i) {
-            const int c = lane + 32 * i;
-            const int r = c >> 2, pr = c & 3;
-            if (2 * pr >= ng) continue;
-            int n;
-            const uint16_t* sbase;
-            if (MODE == kGateUp) {
-              const bool up = r >= kFsRows / 2;
-              n = n0 + (up ? r - kFsRows / 2 : r);
-              sbase = up ? p.scale1 : p.scale0;
-            } else {
-              n = n0 + r;
-              sbase = p.scale0;
-            }
-            if (n >= N) continue;
-            cp_async_4(sdst + r * 16 + pr * 4, sbase + ((size_t)e * N + n) * G_all + g0 + 2 * pr);
-          }
-          cp_async_arrive_noinc(&full[s]);
-        }
-      }
+      ok = produce_unit<MODE, Q8>(maps, p, smem, full, empty, it, p.chunk_e[q], p.chunk_row0[q],
+                                  p.chunk_rows[q], jt * tile_n, lane);
     }
-    if (!ok) {
-      // let copies already issued land before the CTA exits (bounded)
-      const uint32_t first = it >= kFsStages ? it - kFsStages : 0;
-      for (uint32_t i = first; i < it; ++i) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&full[i % kFsStages], (i / kFsStages) & 1u)) {
-          if (static_cast<int64_t>(global_timer_ns() - t0) > 100000000LL) break;
-        }
-      }
-    }
+    if (!ok) drain_copies(full, it);
     return;
   }
 
   if (warp == kFsCWarps + 1) {
     // --------------------------------------------- chain start values
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int rows = p.chunk_rows[u / n_tiles];
-      for (int ks = 0; ks < ksteps; ++ks, ++it) {
-        const int s = it % kFsStages;
-        const uint32_t ph = (it / kFsStages) & 1u;
-        if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return;
-        uint8_t* st = smem + s * kFsStageBytes;
-        const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
-        stage_starts<Q8>(st + kFsWBytes + kFsSBytes, st + kFsWBytes + kFsSBytes + kFsXBytes, ng,
-                         rows, lane);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ready[s]);
-          mbar_arrive(&empty[s]);
-        }
-      }
-    }
+    for (int u = blockIdx.x; u < units; u += gridDim.x)
+      if (!starts_unit<Q8>(p, smem, full, empty, ready, it, p.chunk_rows[u / n_tiles], lane)) return;
     return;
   }
 
@@ -526,14 +552,169 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
     const int n0 = jt * tile_n;
     float* x = xch + parity * (kFsXchBytes / 4);
-    bool ok;
+    // No early exit after a failed wait: the consumer warps meet at named
+    // barriers, so all of them walk every unit (the waits then return at once).
     if (rows <= 8)
-      ok = consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
-                                     L, p);
+      consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
     else
-      ok = consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
-                                     L, p);
-    if (!ok) return;
+      consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+  }
+}
+
+// Acquire-load of a completion counter (another CTA's release).
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Gate/up and down of the stream kernel in one persistent launch (act_bits
+// 16, scales by TMA).  Every CTA takes its gate/up units first, then its down
+// units, so the down phase starts on each SM as soon as that SM is done with
+// gate/up and no SM idles at the boundary.  A down unit of chunk q reads the
+// h rows of chunk q: its producer waits (bounded) until the gate/up units of
+// chunk q have all stored them, as counted in done[q].  Deadlock-free: a CTA
+// only waits after finishing all its gate/up units, and the gate/up units
+// wait on nothing but their own stages.
+template <int DMODE>
+__global__ void __launch_bounds__(kFsThreads, 1)
+    ffn_stream_fused_kernel(const __grid_constant__ FsMaps mgu, const __grid_constant__ FsMaps mdn,
+                            const FsParams pgu, const FsParams pdn, int32_t* done) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  float* xch = reinterpret_cast<float*>(smem + kFsStages * kFsStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFsStages * kFsStageBytes + 2 * kFsXchBytes);
+  uint64_t* empty = full + kFsStages;
+  uint64_t* ready = empty + kFsStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFsStages; ++s) {
+      mbar_init(&full[s], 1);               // both phases load their scales by TMA
+      mbar_init(&empty[s], kFsCWarps + 1);
+      mbar_init(&ready[s], 1);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  const int nt_gu = (pgu.N + kFsRows / 2 - 1) / (kFsRows / 2);
+  const int nt_dn = (pdn.N + kFsRows - 1) / kFsRows;
+  const int n_ch = *pgu.n_chunks;
+  const int units_gu = n_ch * nt_gu;
+  const int units = units_gu + n_ch * nt_dn;
+
+  if (warp == kFsCWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensor_map(&mgu.w0);
+      prefetch_tensor_map(&mgu.w1);
+      prefetch_tensor_map(&mgu.s0);
+      prefetch_tensor_map(&mgu.s1);
+      prefetch_tensor_map(&mdn.w0);
+      prefetch_tensor_map(&mdn.s0);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      if (u < units_gu) {
+        const int q = u / nt_gu, jt = u - q * nt_gu;
+        ok = produce_unit<kGateUp, false>(mgu, pgu, smem, full, empty, it, pgu.chunk_e[q],
+                                          pgu.chunk_row0[q], pgu.chunk_rows[q],
+                                          jt * (kFsRows / 2), lane);
+      } else {
+        const int d = u - units_gu;
+        const int q = d / nt_dn, jt = d - q * nt_dn;
+        // h rows of chunk q: wait for all of its gate/up units (bounded)
+        if (ld_acquire(done + q) < nt_gu) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire(done + q) < nt_gu) {
+            if (status_set(pdn.status)) {
+              ok = false;
+              break;
+            }
+            if (static_cast<int64_t>(global_timer_ns() - t0) > pdn.wait_ns) {
+              record_status(pdn.status, MOE_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        // the rows were stored through the generic proxy; the bulk copies
+        // read them through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        ok = produce_unit<DMODE, false>(mdn, pdn, smem, full, empty, it, pdn.chunk_e[q],
+                                        pdn.chunk_row0[q], pdn.chunk_rows[q], jt * kFsRows, lane);
+      }
+    }
+    if (!ok) drain_copies(full, it);
+    return;
+  }
+
+  if (warp == kFsCWarps + 1) {
+    // --------------------------------------------- chain start values
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const bool gu = u < units_gu;
+      const int q = gu ? u / nt_gu : (u - units_gu) / nt_dn;
+      if (!starts_unit<false>(gu ? pgu : pdn, smem, full, empty, ready, it, pgu.chunk_rows[q], lane))
+        return;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  Lane L;
+  L.g = lane >> 2;
+  L.t = lane & 3;
+  L.li = lane & 7;
+  {
+    const int m = lane >> 3;
+    const int rb = 16 * warp;
+    L.gsel = m >> 1;
+    L.lrow_off = static_cast<uint32_t>((rb + 8 * (m & 1) + L.li) * 128);
+    L.rlo = rb + L.g;
+  }
+  const int ks_gu = (pgu.K + kFsKc - 1) / kFsKc;
+  const int ks_dn = (pdn.K + kFsKc - 1) / kFsKc;
+  uint32_t it = 0;
+  int parity = 0;
+  // No early exit after a failed wait: the consumer warps meet at named
+  // barriers, so all of them walk every unit (the waits then return at once).
+  for (int u = blockIdx.x; u < units; u += gridDim.x, parity ^= 1) {
+    float* x = xch + parity * (kFsXchBytes / 4);
+    if (u < units_gu) {
+      const int q = u / nt_gu, jt = u - q * nt_gu;
+      const int row0 = pgu.chunk_row0[q], rows = pgu.chunk_rows[q];
+      if (rows <= 8)
+        consume_unit<kGateUp, false, 1>(smem, x, ready, empty, it, ks_gu, row0, rows,
+                                        jt * (kFsRows / 2), warp, lane, L, pgu);
+      else
+        consume_unit<kGateUp, false, 2>(smem, x, ready, empty, it, ks_gu, row0, rows,
+                                        jt * (kFsRows / 2), warp, lane, L, pgu);
+      if (warp < kFsCWarps / 2) {
+        // the gate warps stored this unit's h: publish it to the down units
+        __threadfence();
+        named_bar_sync_n(2, kFsCWarps / 2 * 32);
+        if (warp == 0 && lane == 0) atomicAdd(done + q, 1);
+      }
+    } else {
+      const int d = u - units_gu;
+      const int q = d / nt_dn, jt = d - q * nt_dn;
+      const int row0 = pdn.chunk_row0[q], rows = pdn.chunk_rows[q];
+      if (rows <= 8)
+        consume_unit<DMODE, false, 1>(smem, x, ready, empty, it, ks_dn, row0, rows, jt * kFsRows,
+                                      warp, lane, L, pdn);
+      else
+        consume_unit<DMODE, false, 2>(smem, x, ready, empty, it, ks_dn, row0, rows, jt * kFsRows,
+                                      warp, lane, L, pdn);
+    }
   }
 }
 
@@ -547,6 +728,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
                                                             int32_t* __restrict__ chunk_e,
                                                             int32_t* __restrict__ chunk_row0,
                                                             int32_t* __restrict__ chunk_rows,
+                                                            int32_t* __restrict__ done,
                                                             int32_t* __restrict__ n_chunks,
                                                             int* status) {
   __shared__ int32_t nch[kMaxExperts];
@@ -614,6 +796,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
       chunk_e[base + i] = e;
       chunk_row0[base + i] = a + i * mc;
       chunk_rows[base + i] = min(mc, cnt - i * mc);
+      done[base + i] = 0;
     }
   }
   if (threadIdx.x == 0) *n_chunks = total;
@@ -634,13 +817,14 @@ struct Schedule {
   int32_t* chunk_e;
   int32_t* chunk_row0;
   int32_t* chunk_rows;
+  int32_t* done;      // per chunk: gate/up units finished (fused kernel), zeroed here
   int32_t* n_chunks;
   int max_chunks;
 };
 
 static size_t schedule_bytes_one(int E, int rows_max, int mc) {
   const size_t n = static_cast<size_t>(max_chunks_for(E, rows_max, mc));
-  return 3 * align_up(n * sizeof(int32_t), 256) + 256;
+  return 4 * align_up(n * sizeof(int32_t), 256) + 256;
 }
 
 static Schedule carve_one(char*& b, int E, int rows_max, int mc) {
@@ -650,8 +834,9 @@ static Schedule carve_one(char*& b, int E, int rows_max, int mc) {
   s.chunk_e = reinterpret_cast<int32_t*>(b);
   s.chunk_row0 = reinterpret_cast<int32_t*>(b + arr);
   s.chunk_rows = reinterpret_cast<int32_t*>(b + 2 * arr);
-  s.n_chunks = reinterpret_cast<int32_t*>(b + 3 * arr);
-  b += 3 * arr + 256;
+  s.done = reinterpret_cast<int32_t*>(b + 3 * arr);
+  s.n_chunks = reinterpret_cast<int32_t*>(b + 4 * arr);
+  b += 4 * arr + 256;
   return s;
 }
 
@@ -663,8 +848,8 @@ static size_t schedule_bytes(int E, int rows_max) {
 static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
                            const Schedule& sc, int* status, cudaStream_t s) {
   ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, mc, lo, hi, sc.max_chunks,
-                                         sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks,
-                                         status);
+                                         sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.done,
+                                         sc.n_chunks, status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -731,6 +916,17 @@ static int run_stream(int mode, bool q8, const FsMaps& maps, const FsParams& p, 
   return q8 ? launch_stream<kLinear, true>(maps, p, s) : launch_stream<kLinear, false>(maps, p, s);
 }
 
+template <int DMODE>
+static int launch_fused(const FsMaps& mgu, const FsMaps& mdn, const FsParams& pgu,
+                        const FsParams& pdn, int32_t* done, cudaStream_t s) {
+  auto kern = ffn_stream_fused_kernel<DMODE>;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kFsSmemBytes));
+  kern<<<num_sms(), kFsThreads, kFsSmemBytes, s>>>(mgu, mdn, pgu, pdn, done);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
 static int check_width(int v) { return (v > 0 && v % 64 == 0) ? MOE_OK : MOE_ERR_UNSUPPORTED; }
 
 }  // namespace moe
@@ -794,6 +990,7 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
     return MOE_ERR_CUDA;
 
   FsParams p{};
+  FsParams pd{};
   p.x = x_sorted;
   p.x_scale = x_scale;
   p.scale0 = gate_scale;
@@ -808,7 +1005,23 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   p.K = D;
   p.N = I;
   p.tma_scales = tma_scales_ok(D, gate_scale, up_scale) ? 1 : 0;
-  rc = run_stream(kGateUp, q8, mgu, p, s);
+  pd = p;
+  pd.K = I;
+  pd.N = D;
+  pd.tma_scales = tma_scales_ok(I, down_scale, down_scale) ? 1 : 0;
+  pd.scale0 = down_scale;
+  pd.scale1 = nullptr;
+  pd.out = y;
+  pd.x = h;
+  // act_bits 16 with TMA-loaded scales: gate/up and down of the stream
+  // experts in one launch (no re-quantisation of h between them)
+  const bool fused = !q8 && p.tma_scales && pd.tma_scales;
+  if (fused) {
+    rc = y_f32 ? launch_fused<kLinear>(mgu, md, p, pd, small.done, s)
+               : launch_fused<kDown>(mgu, md, p, pd, small.done, s);
+  } else {
+    rc = run_stream(kGateUp, q8, mgu, p, s);
+  }
   if (rc) return rc;
   if (use_tc) {
     // both kernels write h in pair order: fp16 (act_bits 16), or bf16 for
@@ -825,23 +1038,16 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
     if (rc) return rc;
   }
 
-  FsParams pd = p;
-  pd.K = I;
-  pd.N = D;
-  pd.tma_scales = tma_scales_ok(I, down_scale, down_scale) ? 1 : 0;
-  pd.scale0 = down_scale;
-  pd.scale1 = nullptr;
-  pd.out = y;
   if (q8) {
     rc = launch_quantize_rows(h, rows_max, I, offsets + E, hq, hs, s);
     if (rc) return rc;
     pd.x = hq;
     pd.x_scale = hs;
-  } else {
-    pd.x = h;
   }
-  rc = run_stream(y_f32 ? kLinear : kDown, q8, md, pd, s);
-  if (rc) return rc;
+  if (!fused) {
+    rc = run_stream(y_f32 ? kLinear : kDown, q8, md, pd, s);
+    if (rc) return rc;
+  }
   if (use_tc) {
     const uint16_t* ha = h;
     if (q8) {

@@ -374,6 +374,30 @@ def test_expert_ffn_pairs_equals_expert_ffn(moe, act_bits):
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
+def test_expert_ffn_reports_fp16_overflow_and_recovers(moe):
+    """An intermediate h beyond the fp16 range, on both expert kernels (5 rows:
+    stream kernel; 60 rows: tensor cores), records MOE_ERR_UNSUPPORTED; the call
+    finishes and the next call is clean."""
+    rng = np.random.default_rng(41)
+    D, I, counts = 256, 128, [5, 60]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    big = _bf16(rng.normal(size=(R, D)) * 3000.0)
+    moe.expert_ffn(big.to(DEV), None, _t(off), ex, 16)
+    assert moe.check_error() == moe.capi.MOE_ERR_UNSUPPORTED
+    assert moe.check_error() == 0
+    small = _bf16(rng.normal(size=(R, D)))
+    moe.expert_ffn(small.to(DEV), None, _t(off), ex, 16)
+    assert moe.check_error() == 0
+
+
 def test_ffn_rejects_offsets_beyond_capacity(moe):
     rng = np.random.default_rng(1)
     E, D, I = 2, 128, 128
