@@ -354,8 +354,9 @@ def main(argv=None):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     roof.update({"traffic": _profiled_traffic(w.name),
-                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_kernel for "
-                           "experts of <= 16 rows, ffn_tc_kernel gate/up and down above)",
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_fused_kernel "
+                           "(gate/up + down) for experts of <= 16 rows, ffn_tc_kernel gate/up and "
+                           "down above)",
                  "kernel_ms": ffn_ms,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                  "active_experts": active, "peak_source": peaks["source"]})

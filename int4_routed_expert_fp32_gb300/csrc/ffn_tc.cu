@@ -46,7 +46,7 @@ constexpr int kTxAStages = 4;                  // TMEM ring of dequantised weigh
 constexpr int kTxXBytes = kTxTN * kTxBK * 2;   // 16 KiB token tile
 constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 8 KiB packed int4 (256 rows x 32 bytes)
 constexpr int kTxStageBytes = kTxXBytes + kTxQBytes;
-constexpr int kTxDqWarps = 8;
+constexpr int kTxDqWarps = 16;                 // (lane quarter, block, group of the stage)
 constexpr int kTxEpWarps = 8;                  // two per TMEM lane quarter
 constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
 constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 4 x 64 A columns
@@ -54,30 +54,33 @@ constexpr uint32_t kTxAcc1 = kTxTN;            // column of the second accumulat
 constexpr uint32_t kTxACol = 2 * kTxTN;        // first A column
 constexpr int kTxSmem = kTxStages * kTxStageBytes + 1024 + 256;
 static_assert(kTxStageBytes % 1024 == 0, "stage alignment");
-static_assert(kTxDqWarps * 32 == 2 * kTxWM, "one dequantisation thread per weight row");
+static_assert(kTxDqWarps * 32 == 2 * 2 * kTxWM, "one dequantisation thread per row and group");
 static_assert(kTxACol + kTxAStages * 2 * (kTxBK / 2) <= kTxCols, "TMEM budget");
 
 enum TxMode { kTxGateUp = 0, kTxDown = 1, kTxLinear = 2 };
 
 // Two nibbles n (bits 0-3 and 16-19 of v, two's complement) -> fp16x2 q * s,
-// exactly: (n ^ 8) lands in the low mantissa bits of 1024.0 (0x6400); minus
-// 1032 gives q; times the fp16 scale pair s2.
+// exactly: (n ^ 8) lands in the low mantissa bits of 1024.0 (0x6400), so the
+// half is 1032 + q; minus 1032 (0x6408) gives q; times the fp16 scale pair s2.
+// Written in PTX with the constants as immediates (bit patterns of fp16x2).
 __device__ __forceinline__ uint32_t nib_lo_f16(uint32_t v, uint32_t s2) {
-  const uint32_t m = (v & 0x000F000Fu) ^ 0x64086408u;
-  __half2 h = *reinterpret_cast<const __half2*>(&m);
-  h = __hsub2(h, __floats2half2_rn(1032.0f, 1032.0f));
-  h = __hmul2(h, *reinterpret_cast<const __half2*>(&s2));
-  return *reinterpret_cast<const uint32_t*>(&h);
+  uint32_t m, r;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64086408, 0x6a;" : "=r"(m) : "r"(v));  // (v & a) ^ b
+  asm("{\n .reg .b32 t;\n sub.rn.f16x2 t, %1, %2;\n mul.rn.f16x2 %0, t, %3;\n}"
+      : "=r"(r)
+      : "r"(m), "r"(0x64086408u), "r"(s2));
+  return r;
 }
 
-// Same for nibbles at bits 4-7 and 20-23: 1024 + 16 (n ^ 8), scaled by 1/16
-// and shifted by -72 (exact) to q, then times s2.
+// Same for nibbles at bits 4-7 and 20-23: the half is 1024 + 16 (n ^ 8);
+// times 1/16 (0x2C00) minus 72 (0xD480), exact, gives q; then times s2.
 __device__ __forceinline__ uint32_t nib_hi_f16(uint32_t v, uint32_t s2) {
-  const uint32_t m = (v & 0x00F000F0u) ^ 0x64806480u;
-  __half2 h = *reinterpret_cast<const __half2*>(&m);
-  h = __hfma2(h, __floats2half2_rn(0.0625f, 0.0625f), __floats2half2_rn(-72.0f, -72.0f));
-  h = __hmul2(h, *reinterpret_cast<const __half2*>(&s2));
-  return *reinterpret_cast<const uint32_t*>(&h);
+  uint32_t m, r;
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64806480, 0x6a;" : "=r"(m) : "r"(v));
+  asm("{\n .reg .b32 t;\n fma.rn.f16x2 t, %1, %2, %3;\n mul.rn.f16x2 %0, t, %4;\n}"
+      : "=r"(r)
+      : "r"(m), "r"(0x2C002C00u), "r"(0xD480D480u), "r"(s2));
+  return r;
 }
 
 // bf16x2 -> fp16x2 (exact for values in the fp16 range; beyond it: inf).
@@ -172,42 +175,47 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      uint32_t it = 0, uc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-        const int q = u / n_tiles;
-        const int rows = p.chunk_rows[q];
-        const int nn = rows <= 16 ? 16 : (rows + 15) / 16 * 16;  // MMA N: tokens, multiple of 16
-        const uint32_t idesc = idesc_f16(kTxWM, nn);
-        if (!mbar_wait(accempty, (uc & 1u) ^ 1u, p.wait_ns, p.status)) break;
-        tc_fence_after();
-        for (int ks = 0; ks < ksteps; ++ks, ++it) {
-          const int s = it % kTxStages, a = it % kTxAStages;
-          if (!mbar_wait(&aready[a], (it / kTxAStages) & 1u, p.wait_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t db = smem_desc_sw128(smem + s * kTxStageBytes);
-          const uint32_t ta = tbase + kTxACol + a * kTxBK;  // block 0; block 1 at +32
-#pragma unroll
-          for (int kk = 0; kk < kTxBK / 16; ++kk) {
-            umma_f16_ts(tbase, ta + 8 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
-            umma_f16_ts(tbase + kTxAcc1, ta + kTxBK / 2 + 8 * kk, db + 2 * kk, idesc,
-                        (ks | kk) != 0);
-          }
-          umma_commit(&sfree[s]);
-          umma_commit(&afree[a]);
+    // The whole warp walks the loop (uniform operands); one elected lane
+    // issues each MMA and commit.
+    uint32_t it = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+      const int q = u / n_tiles;
+      const int rows = p.chunk_rows[q];
+      const int nn = rows <= 16 ? 16 : (rows + 15) / 16 * 16;  // MMA N: tokens, multiple of 16
+      const uint32_t idesc = idesc_f16(kTxWM, nn);
+      if (!__all_sync(0xffffffffu, mbar_wait(accempty, (uc & 1u) ^ 1u, p.wait_ns, p.status)))
+        break;
+      tc_fence_after();
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const int s = it % kTxStages, a = it % kTxAStages;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&aready[a], (it / kTxAStages) & 1u, p.wait_ns, p.status))) {
+          ok = false;
+          break;
         }
-        if (ok) umma_commit(accfull);
+        tc_fence_after();
+        const uint64_t db = smem_desc_sw128(smem + s * kTxStageBytes);
+        const uint32_t ta = tbase + kTxACol + a * kTxBK;  // block 0; block 1 at +32
+#pragma unroll
+        for (int kk = 0; kk < kTxBK / 16; ++kk) {
+          umma_f16_ts_warp(tbase, ta + 8 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+          umma_f16_ts_warp(tbase + kTxAcc1, ta + kTxBK / 2 + 8 * kk, db + 2 * kk, idesc,
+                           (ks | kk) != 0);
+        }
+        umma_commit_warp(&sfree[s]);
+        umma_commit_warp(&afree[a]);
       }
+      if (ok) umma_commit_warp(accfull);
     }
   } else if (warp < 2 + kTxDqWarps) {
     // ----------------------------------------------------- dequantisation
-    // TMEM lane quarter of this warp: warp % 4; block 0 = warps 2-5, block 1 = 6-9
+    // TMEM lane quarter of this warp: warp % 4.  Warps 2-5: block 0, first
+    // scale group of each stage (K columns 0-31); 6-9: block 0, second group
+    // (32-63); 10-13 and 14-17: the same for block 1.
     const int qd = warp & 3;
-    const int blk = (warp - 2) >> 2;
+    const int blk = (warp - 2) >> 3;
+    const int gh = ((warp - 2) >> 2) & 1;  // group of the stage
     const int m = 32 * qd + lane;        // TMEM lane = row within the block
     const int r = blk * kTxWM + m;       // row within the 256-row tile
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         }
       }
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
-        uint32_t sw;  // bf16 scales of groups 2ks (low) and 2ks+1 (high)
+        uint32_t sw;  // bf16 scales of groups 2ks (low half) and 2ks+1 (high half)
         if (vec) {
           const int j = ks & 3;
           sw = (j & 2) ? ((j & 1) ? scur.w : scur.z) : ((j & 1) ? scur.y : scur.x);
@@ -267,19 +275,17 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           break;
         }
         // int4 rows of 32 bytes, stored with the 32-byte swizzle: 16-byte half
-        // h of row r sits at half h ^ ((r >> 2) & 1)
+        // h of row r sits at half h ^ ((r >> 2) & 1); half gh holds this
+        // warp's group
         const uint8_t* qrow = smem + s * kTxStageBytes + kTxXBytes + r * 32;
         const int qx = (r >> 2) & 1;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + (qx << 4));
-        const uint4 w1 = *reinterpret_cast<const uint4*>(qrow + ((qx ^ 1) << 4));
-        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 2ks
-        const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 2ks+1
-        uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
+        const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + ((gh ^ qx) << 4));
+        const uint32_t wv[4] = {w0.x, w0.y, w0.z, w0.w};
+        const uint32_t sc = scale_f16x2(gh ? (sw >> 16) : (sw & 0xffffu));
+        uint32_t av[16];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           const uint32_t w = wv[c];
-          const uint32_t sc = c < 4 ? s_lo : s_hi;
           const uint32_t w8 = w >> 8;
           av[4 * c + 0] = nib_lo_f16(w, sc);   // (n0, n4)
           av[4 * c + 1] = nib_hi_f16(w, sc);   // (n1, n5)
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&aready[pend_a]);
         }
-        tmem_st32(tbase + t_lane + kTxACol + a * kTxBK + blk * (kTxBK / 2), av);
+        tmem_st16(tbase + t_lane + kTxACol + a * kTxBK + blk * (kTxBK / 2) + gh * 16, av);
         pend = true;
         pend_a = a;
       }
@@ -305,8 +311,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // two warps per TMEM lane quarter: half eh takes the 32-token chunks
-    // 32 eh, 32 eh + 64, ...
+    // two warps per TMEM lane quarter: half eh takes the 16-token slices
+    // 16 eh, 16 eh + 32, ...
     const int qd = warp & 3;
     const int eh = (warp - 2 - kTxDqWarps) >> 2;
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
@@ -319,20 +325,26 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, p.wait_ns, p.status, 256))) break;
       tc_fence_after();
       bool fin = true;
-#pragma unroll 1
-      for (int c0 = 32 * eh; c0 < rows; c0 += 64) {
-        uint32_t g[32], v[32];
-        tmem_ld32(tbase + t_lane + c0, g);
-        tmem_ld32(tbase + t_lane + kTxAcc1 + c0, v);
-        tmem_ld_wait();
-        if (MODE == kTxGateUp) {
-          const int n = n0 + 32 * qd + lane;  // output feature of this lane
-          if (n < N) {
-            uint16_t* hcol = static_cast<uint16_t*>(p.out) + pair_pos(n);
+      if (MODE == kTxGateUp) {
+        // h of this lane's feature for the warp's (up to) four 16-token
+        // slices, packed in registers; the accumulator is released before the
+        // global stores, so the next unit's MMAs start meanwhile
+        const int n = n0 + 32 * qd + lane;  // output feature of this lane
+        uint32_t hb[4][8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+        for (int sl = 0; sl < 4; ++sl) {
+          const int c0 = 16 * eh + 32 * sl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hb[sl][i] = 0u;
+          if (c0 < rows) {  // warp-uniform
+            uint32_t g[16], v[16];
+            tmem_ld16(tbase + t_lane + c0, g);
+            tmem_ld16(tbase + t_lane + kTxAcc1 + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
               const int tok = c0 + i;
-              if (tok >= rows) continue;
+              if (tok >= rows || n >= N) continue;
               float G = __uint_as_float(g[i]), U = __uint_as_float(v[i]);
               fin &= fabsf(G) <= 3.0e38f && fabsf(U) <= 3.0e38f;
               if (Q8) {
@@ -343,23 +355,49 @@ __global__ void __launch_bounds__(kTxThreads, 1)
               // SiLU(G) * U with the fast exponential and division (the
               // quotient is 0 once 1 + exp(-G) overflows)
               const float h = __fdividef(G, 1.0f + __expf(-G)) * U;
-              uint16_t hb;
+              uint32_t hbits;
               if (Q8) {  // bf16 h, as the stream kernel writes it
-                hb = f32_to_bf16_bits(h);
+                hbits = f32_to_bf16_bits(h);
               } else {
                 fin &= fabsf(h) <= 65504.0f;
-                hb = __half_as_ushort(__float2half_rn(h));
+                hbits = __half_as_ushort(__float2half_rn(h));
               }
-              hcol[(size_t)(row0 + tok) * N] = hb;
+              hb[sl][i >> 1] |= hbits << (16 * (i & 1));
             }
           }
-        } else {
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accempty);
+        if (n < N) {
+          uint16_t* hcol = static_cast<uint16_t*>(p.out) + pair_pos(n);
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) {
+            const int c0 = 16 * eh + 32 * sl;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int tok = c0 + i;
+              if (tok < rows)
+                hcol[(size_t)(row0 + tok) * N] = static_cast<uint16_t>(hb[sl][i >> 1] >> (16 * (i & 1)));
+            }
+          }
+        }
+        if (!fin) record_status(p.status, MOE_ERR_UNSUPPORTED);
+        continue;
+      }
+#pragma unroll 1
+      for (int c0 = 16 * eh; c0 < rows; c0 += 32) {
+        uint32_t g[16], v[16];
+        tmem_ld16(tbase + t_lane + c0, g);
+        tmem_ld16(tbase + t_lane + kTxAcc1 + c0, v);
+        tmem_ld_wait();
+        {
 #pragma unroll
           for (int b2 = 0; b2 < 2; ++b2) {
             const int n = n0 + b2 * kTxWM + 32 * qd + lane;
             if (n >= N) continue;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               const int tok = c0 + i;
               if (tok >= rows) continue;
               float y = __uint_as_float(b2 ? v[i] : g[i]);

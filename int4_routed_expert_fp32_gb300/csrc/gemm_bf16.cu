@@ -5,7 +5,7 @@
 //
 // gemm_tc_kernel: 128 x 256 output tile per CTA on the 5th-generation tensor
 // cores: a TMA warp streams 128x64 (A) and 256x64 (B) bf16 tiles with the
-// 128-byte swizzle into a 4-stage ring, one thread issues tcgen05.mma
+// 128-byte swizzle into a 4-stage ring, one warp issues tcgen05.mma
 // (M=128, N=256, K=16) into a 256-column TMEM accumulator, and four epilogue
 // warps read it back with tcgen05.ld and store bf16.
 // gemm_bf16_kernel (mma.sync, 128x128x32) is the check kernel of the former.
@@ -191,27 +191,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
-      bool ok = true;
-      for (int kt = 0; kt < ktiles; ++kt) {
-        const int s = kt % kTcStages;
-        const uint32_t ph = (kt / kTcStages) & 1u;
-        if (!mbar_wait(&full[s], ph, wait_ns, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t* st = smem + s * kTcStageBytes;
-        const uint64_t da = smem_desc_sw128(st);
-        const uint64_t db = smem_desc_sw128(st + kTcABytes);
-#pragma unroll
-        for (int kk = 0; kk < kTcBK / 16; ++kk)
-          umma_f16(tbase, da + 2 * kk, db + 2 * kk, idesc, (kt | kk) != 0);
-        umma_commit(&empty[s]);
+    // the whole warp walks the loop; one elected lane issues (see umma_f16_warp)
+    constexpr uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
+    bool ok = true;
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const int s = kt % kTcStages;
+      const uint32_t ph = (kt / kTcStages) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wait_ns, status))) {
+        ok = false;
+        break;
       }
-      if (ok) umma_commit(accf);
+      tc_fence_after();
+      const uint8_t* st = smem + s * kTcStageBytes;
+      const uint64_t da = smem_desc_sw128(st);
+      const uint64_t db = smem_desc_sw128(st + kTcABytes);
+#pragma unroll
+      for (int kk = 0; kk < kTcBK / 16; ++kk)
+        umma_f16_warp(tbase, da + 2 * kk, db + 2 * kk, idesc, (kt | kk) != 0);
+      umma_commit_warp(&empty[s]);
     }
+    if (ok) umma_commit_warp(accf);
   } else {
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
