@@ -2,29 +2,35 @@
 // with many rows (prefill-shaped loads).  Same computation as the stream
 // kernel (Kimi exact-generator adaptation page, "The preserved forward form";
 // Kimi K2.5 donor-reference "SwiGLU-style gated feed-forward projection"),
-// with the weights dequantised once per 128-row token tile:
-//   * warp 0 (one thread): TMA of the 128 x 64 bf16 activation tile (128-byte
-//     swizzle) and of the 256-row x 64-column packed int4 weight tile into a
-//     4-stage ring;
-//   * warps 2-9: dequantisation, one weight row per thread, to fp16
-//     q * scale written in the K-major 128-byte-swizzle layout the MMA reads,
-//     then fence.proxy.async.  The activation rows are in pair order (each
-//     block of 8 columns stored c0 c4 c1 c5 c2 c6 c3 c7), so the weights are
-//     written in the same order, the order of the nibble pairs of a word;  With a bf16 scale (8 significant bits) and
-//     |q| <= 8, q * scale has at most 11 significant bits: it is exact in fp16
-//     for scales in [2^-17, 8188].  The activations arrive in fp16 (a copy
-//     made once per call; bf16 values are exact in fp16 for
-//     2^-17 <= |x| <= 65504), and the gate/up tiles write h in fp16 for the
-//     down tiles.  So, as in the stream kernel, the weights are never
-//     rounded; a value beyond the fp16 range makes its output row non-finite
-//     and records MOE_ERR_UNSUPPORTED;
-//   * warp 1 (one thread): tcgen05.mma kind::f16 (fp16 inputs), M=128, N=256,
-//     K=16, into one of two 256-column TMEM accumulators (the epilogue of a
-//     tile overlaps the main loop of the next);
-//   * warps 10-13: tcgen05.ld of the accumulator; gate/up tiles hold gate in
-//     columns 0-127 and up in 128-255 and store h = SiLU(G) * U (fp16); down
-//     tiles store y (bf16, or fp32).
-// act_bits 8 (Q8): the A operand is the fp16 copy of the int8 rows (exact);
+// with the weights dequantised once per 128-row token tile.  One persistent
+// CTA per SM walks units (token chunk x 256 weight rows: 128 gate + 128 up
+// outputs, or 256 down outputs) in K stages of 128 columns:
+//   * warp 0 (one thread): TMA of the fp16 activation tile (two 128 x 64
+//     boxes, 128-byte swizzle) and of the 256-row x 128-column packed int4
+//     tile (64-byte swizzle) into a 4-stage shared-memory ring;
+//   * warps 2-17: dequantisation, one weight row and half a stage (two scale
+//     groups) per thread, to fp16 q * scale written with tcgen05.st into a
+//     2-slot TMEM ring (the A operand).  The activation rows are in pair
+//     order (each block of 8 columns stored c0 c4 c1 c5 c2 c6 c3 c7), so the
+//     weights are written in the same order, the order of the nibble pairs
+//     of a word.  With a bf16 scale (8 significant bits) and |q| <= 8,
+//     q * scale has at most 11 significant bits: it is exact in fp16 for
+//     scales in [2^-17, 8188].  The activations arrive in fp16 (a copy made
+//     once per call; bf16 values are exact in fp16 for 2^-17 <= |x| <= 65504),
+//     and the gate/up tiles write h in fp16 for the down tiles.  So, as in
+//     the stream kernel, the weights are never rounded; a value beyond the
+//     fp16 range makes its output non-finite and records MOE_ERR_UNSUPPORTED;
+//   * warp 1 (whole warp, one elected lane issues): tcgen05.mma kind::f16,
+//     A from TMEM (M = 128 weight rows per block, two blocks), B the token
+//     tile (N = the chunk's rows rounded up to 16), K = 16, into two
+//     128-column fp32 accumulators;
+//   * warps 18-25: tcgen05.ld of the accumulators; gate/up units store
+//     h = SiLU(G) * U (fp16), releasing the accumulators before the stores;
+//     down units store y (bf16, or fp32).
+// K stages of 128 columns halve the per-stage barrier waits and handoffs
+// against 64-column stages (each mbarrier wait costs a dequantisation warp
+// ~130 cycles even on a completed phase).
+// act_bits 8 (Q8): the B operand is the fp16 copy of the int8 rows (exact);
 // every product q * scale * x_q is exact in fp32 and the accumulation is in
 // fp32 (with unit scales the integer sum itself, exact while |sum| < 2^24).
 // The epilogue applies the row scales; gate/up tiles store h in bf16 for the
@@ -40,22 +46,25 @@ namespace moe {
 
 constexpr int kTxWM = 128;                     // weight rows per MMA block (M, TMEM lanes)
 constexpr int kTxTN = 128;                     // token rows per unit (largest MMA N)
-constexpr int kTxBK = 64;                      // K per stage (one swizzle atom of fp16)
-constexpr int kTxStages = 8;                   // shared-memory ring
-constexpr int kTxAStages = 4;                  // TMEM ring of dequantised weights
-constexpr int kTxXBytes = kTxTN * kTxBK * 2;   // 16 KiB token tile
-constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 8 KiB packed int4 (256 rows x 32 bytes)
+constexpr int kTxBK = 128;                     // K per stage
+constexpr int kTxXK = 64;                      // K per activation box (one 128-byte swizzle atom)
+constexpr int kTxStages = 4;                   // shared-memory ring
+constexpr int kTxAStages = 2;                  // TMEM ring of dequantised weights
+constexpr int kTxXBoxBytes = kTxTN * kTxXK * 2;  // 16 KiB: 128 tokens x 64 columns
+constexpr int kTxXBytes = 2 * kTxXBoxBytes;    // 32 KiB token tile
+constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 16 KiB packed int4 (256 rows x 64 bytes)
 constexpr int kTxStageBytes = kTxXBytes + kTxQBytes;
-constexpr int kTxDqWarps = 16;                 // (lane quarter, block, group of the stage)
+constexpr int kTxDqWarps = 16;                 // (lane quarter, block, half of the stage)
 constexpr int kTxEpWarps = 8;                  // two per TMEM lane quarter
 constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
-constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 4 x 64 A columns
+constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 2 x 128 A columns
 constexpr uint32_t kTxAcc1 = kTxTN;            // column of the second accumulator
 constexpr uint32_t kTxACol = 2 * kTxTN;        // first A column
+constexpr uint32_t kTxASlot = 2 * (kTxBK / 2);  // A columns per stage: 2 blocks x 64
 constexpr int kTxSmem = kTxStages * kTxStageBytes + 1024 + 256;
 static_assert(kTxStageBytes % 1024 == 0, "stage alignment");
-static_assert(kTxDqWarps * 32 == 2 * 2 * kTxWM, "one dequantisation thread per row and group");
-static_assert(kTxACol + kTxAStages * 2 * (kTxBK / 2) <= kTxCols, "TMEM budget");
+static_assert(kTxDqWarps * 32 == 2 * 2 * kTxWM, "one dequantisation thread per row and half stage");
+static_assert(kTxACol + kTxAStages * kTxASlot <= kTxCols, "TMEM budget");
 
 enum TxMode { kTxGateUp = 0, kTxDown = 1, kTxLinear = 2 };
 
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   const int tile_n = (MODE == kTxGateUp) ? kTxWM : 2 * kTxWM;  // outputs per unit
   const int n_tiles = (N + tile_n - 1) / tile_n;
   const int units = (*p.n_chunks) * n_tiles;
-  const int ksteps = K / kTxBK;
+  const int ksteps = (K + kTxBK - 1) / kTxBK;
   const int G_all = K / kGroup;
 
   if (warp == 0) {
@@ -163,7 +172,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           uint8_t* st = smem + s * kTxStageBytes;
           uint8_t* qd = st + kTxXBytes;
           mbar_arrive_expect_tx(&full[s], kTxStageBytes);
+          // columns beyond K (a last half stage) read as zeros
           tma_g2s_2d(st, &maps.a, &full[s], ks * kTxBK, row0);
+          tma_g2s_2d(st + kTxXBoxBytes, &maps.a, &full[s], ks * kTxBK + kTxXK, row0);
           if (MODE == kTxGateUp) {
             tma_g2s_3d(qd, &maps.q0, &full[s], ks * (kTxBK / 8), n0, e);
             tma_g2s_3d(qd + kTxQBytes / 2, &maps.q1, &full[s], ks * (kTxBK / 8), n0, e);
@@ -195,13 +206,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t db = smem_desc_sw128(smem + s * kTxStageBytes);
-        const uint32_t ta = tbase + kTxACol + a * kTxBK;  // block 0; block 1 at +32
+        const uint64_t db0 = smem_desc_sw128(smem + s * kTxStageBytes);
+        const uint64_t db1 = smem_desc_sw128(smem + s * kTxStageBytes + kTxXBoxBytes);
+        const uint32_t ta = tbase + kTxACol + a * kTxASlot;  // block 0; block 1 at +64
 #pragma unroll
         for (int kk = 0; kk < kTxBK / 16; ++kk) {
-          umma_f16_ts_warp(tbase, ta + 8 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
-          umma_f16_ts_warp(tbase + kTxAcc1, ta + kTxBK / 2 + 8 * kk, db + 2 * kk, idesc,
-                           (ks | kk) != 0);
+          const uint64_t db = (kk < kTxXK / 16 ? db0 : db1) + 2 * (kk % (kTxXK / 16));
+          umma_f16_ts_warp(tbase, ta + 8 * kk, db, idesc, (ks | kk) != 0);
+          umma_f16_ts_warp(tbase + kTxAcc1, ta + kTxBK / 2 + 8 * kk, db, idesc, (ks | kk) != 0);
         }
         umma_commit_warp(&sfree[s]);
         umma_commit_warp(&afree[a]);
@@ -211,20 +223,23 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   } else if (warp < 2 + kTxDqWarps) {
     // ----------------------------------------------------- dequantisation
     // TMEM lane quarter of this warp: warp % 4.  Warps 2-5: block 0, first
-    // scale group of each stage (K columns 0-31); 6-9: block 0, second group
-    // (32-63); 10-13 and 14-17: the same for block 1.
+    // half of each stage (K columns 0-63, scale groups 0 and 1); 6-9: block 0,
+    // second half (64-127, groups 2 and 3); 10-13 and 14-17: the same for
+    // block 1.
     const int qd = warp & 3;
     const int blk = (warp - 2) >> 3;
-    const int gh = ((warp - 2) >> 2) & 1;  // group of the stage
+    const int gh = ((warp - 2) >> 2) & 1;  // half of the stage
     const int m = 32 * qd + lane;        // TMEM lane = row within the block
     const int r = blk * kTxWM + m;       // row within the 256-row tile
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
+    // int4 rows of 64 bytes, stored with the 64-byte swizzle: 16-byte chunk c
+    // of row r sits at chunk c ^ ((r >> 1) & 3); this thread reads chunks
+    // 2 gh and 2 gh + 1
+    const int qsw = (r >> 1) & 3;
+    const uint32_t qoff0 = static_cast<uint32_t>(r * 64 + (((2 * gh) ^ qsw) << 4));
+    const uint32_t qoff1 = static_cast<uint32_t>(r * 64 + (((2 * gh + 1) ^ qsw) << 4));
     uint32_t it = 0;
     bool ok = true;
-    // The TMEM store of stage i completes (and is signalled) after stage
-    // i + 1 has been computed, so its latency overlaps that work.
-    bool pend = false;
-    int pend_a = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int q = u / n_tiles, jt = u - q * n_tiles;
       const int e = p.chunk_e[q];
@@ -239,33 +254,21 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         sb = p.scale0;
       }
       const bool valid = n < N;
-      const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all;
-      // scales: 16 bytes (8 groups = 4 stages) per load, fetched 4 stages ahead
-      // when the rows are 16-byte aligned (checked on the host), else 4 bytes
-      // per stage
-      const bool vec = p.vec_scales != 0;
-      uint4 scur = make_uint4(0u, 0u, 0u, 0u), snxt = scur;
-      if (valid) {
-        if (vec) {
-          scur = *reinterpret_cast<const uint4*>(srow);
-          if (ksteps > 4) snxt = *reinterpret_cast<const uint4*>(srow + 8);
-        } else {
-          scur.x = *reinterpret_cast<const uint32_t*>(srow);
-        }
-      }
+      // bf16 scales of this thread's two groups of stage ks (4 ks + 2 gh and
+      // + 1: one 4-byte word), fetched three stages ahead; groups beyond K
+      // (a last half stage) are 0
+      const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all + 2 * gh;
+      auto scale_word = [&](int ks2) -> uint32_t {
+        return (valid && ks2 < ksteps && 4 * ks2 + 2 * gh < G_all)
+                   ? *reinterpret_cast<const uint32_t*>(srow + 4 * ks2)
+                   : 0u;
+      };
+      uint32_t s_a = scale_word(0), s_b = scale_word(1), s_c = scale_word(2);
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
-        uint32_t sw;  // bf16 scales of groups 2ks (low half) and 2ks+1 (high half)
-        if (vec) {
-          const int j = ks & 3;
-          sw = (j & 2) ? ((j & 1) ? scur.w : scur.z) : ((j & 1) ? scur.y : scur.x);
-          if (j == 3) {
-            scur = snxt;
-            if (valid && ks + 5 < ksteps) snxt = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 5));
-          }
-        } else {
-          sw = scur.x;
-          if (valid && ks + 1 < ksteps) scur.x = *reinterpret_cast<const uint32_t*>(srow + 2 * (ks + 1));
-        }
+        const uint32_t sw = s_a;
+        s_a = s_b;
+        s_b = s_c;
+        s_c = scale_word(ks + 3);
         const int s = it % kTxStages, a = it % kTxAStages;
         // warp-uniform outcome: the tcgen05.st below needs the whole warp
         const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, p.wait_ns, p.status) &&
@@ -274,40 +277,29 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           ok = false;
           break;
         }
-        // int4 rows of 32 bytes, stored with the 32-byte swizzle: 16-byte half
-        // h of row r sits at half h ^ ((r >> 2) & 1); half gh holds this
-        // warp's group
-        const uint8_t* qrow = smem + s * kTxStageBytes + kTxXBytes + r * 32;
-        const int qx = (r >> 2) & 1;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + ((gh ^ qx) << 4));
-        const uint32_t wv[4] = {w0.x, w0.y, w0.z, w0.w};
-        const uint32_t sc = scale_f16x2(gh ? (sw >> 16) : (sw & 0xffffu));
-        uint32_t av[16];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
+        const uint8_t* qt = smem + s * kTxStageBytes + kTxXBytes;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(qt + qoff0);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(qt + qoff1);
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 4 ks + 2 gh
+        const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 4 ks + 2 gh + 1
+        uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 8; ++c) {
           const uint32_t w = wv[c];
+          const uint32_t sc = c < 4 ? s_lo : s_hi;
           const uint32_t w8 = w >> 8;
           av[4 * c + 0] = nib_lo_f16(w, sc);   // (n0, n4)
           av[4 * c + 1] = nib_hi_f16(w, sc);   // (n1, n5)
           av[4 * c + 2] = nib_lo_f16(w8, sc);  // (n2, n6)
           av[4 * c + 3] = nib_hi_f16(w8, sc);  // (n3, n7)
         }
-        if (pend) {  // the previous stage's store is complete: hand it to the MMA
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&aready[pend_a]);
-        }
-        tmem_st16(tbase + t_lane + kTxACol + a * kTxBK + blk * (kTxBK / 2) + gh * 16, av);
-        pend = true;
-        pend_a = a;
+        tmem_st32(tbase + t_lane + kTxACol + a * kTxASlot + blk * (kTxBK / 2) + gh * 32, av);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aready[a]);
       }
-    }
-    if (pend && ok) {
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&aready[pend_a]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -429,7 +421,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K) {
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
   const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
-  const uint32_t box[2] = {static_cast<uint32_t>(kTxBK), static_cast<uint32_t>(kTxTN)};
+  const uint32_t box[2] = {static_cast<uint32_t>(kTxXK), static_cast<uint32_t>(kTxTN)};
   return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -543,9 +535,9 @@ static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
   const uint64_t strides[2] = {static_cast<uint64_t>(K / 8) * 4,
                                static_cast<uint64_t>(N) * (K / 8) * 4};
   const uint32_t box[3] = {static_cast<uint32_t>(kTxBK / 8), static_cast<uint32_t>(rows), 1};
-  // 32-byte rows with the 32-byte swizzle: conflict-free 16-byte reads per row
+  // 64-byte rows with the 64-byte swizzle: conflict-free 16-byte reads per row
   return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, w, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_32B);
+                           CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 template <int MODE, bool Q8>
@@ -557,11 +549,9 @@ static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
   return MOE_OK;
 }
 
-bool tc_path_supported(int K) { return K % kTxBK == 0; }
-
-bool scale_rows_16b(const uint16_t* scale, int K) {
-  return (K / kGroup) % 8 == 0 && aligned(scale, 16);
-}
+// K a multiple of 64: a last half stage reads zero weights and activations
+// beyond K.
+bool tc_path_supported(int K) { return K % kTxXK == 0; }
 
 int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
@@ -587,7 +577,6 @@ int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, in
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  p.vec_scales = scale_rows_16b(gate_scale, D) && scale_rows_16b(up_scale, D);
   return x_scale ? launch_tc<kTxGateUp, true>(maps, p, s) : launch_tc<kTxGateUp, false>(maps, p, s);
 }
 
@@ -612,7 +601,6 @@ int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int 
   p.wait_ns = kDefaultWaitNs;
   p.K = I;
   p.N = D;
-  p.vec_scales = scale_rows_16b(down_scale, I);
   if (h_scale)
     return y_f32 ? launch_tc<kTxLinear, true>(maps, p, s) : launch_tc<kTxDown, true>(maps, p, s);
   return y_f32 ? launch_tc<kTxLinear, false>(maps, p, s) : launch_tc<kTxDown, false>(maps, p, s);

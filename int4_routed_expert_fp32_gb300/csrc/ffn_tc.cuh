@@ -21,12 +21,11 @@ struct TxParams {
   long long wait_ns;
   int K;
   int N;
-  int vec_scales;  // scale rows 16-byte aligned: 8 groups per load
 };
 
 struct TxMaps {
-  CUtensorMap a;   // activations bf16 [rows_max, K], 128 x 64 box, 128-byte swizzle
-  CUtensorMap q0;  // packed weights [E, N, K/8], box 8 words x rows
+  CUtensorMap a;   // activations fp16 [rows_max, K], 128 x 64 box, 128-byte swizzle
+  CUtensorMap q0;  // packed weights [E, N, K/8], box 16 words x rows, 64-byte swizzle
   CUtensorMap q1;
 };
 
@@ -35,9 +34,6 @@ constexpr int kTcChunkRows = 128;
 
 // K of the tensor-core path must be a multiple of 64.
 bool tc_path_supported(int K);
-
-// Scale rows of [E, N, K/32] bf16 at `scale` start on 16-byte boundaries.
-bool scale_rows_16b(const uint16_t* scale, int K);
 
 // Pair-ordered copy (see pair_pos) of natural-order rows [R, C] below
 // *row_count: bf16 -> fp16 (src_i8 false; a value beyond the fp16 range
