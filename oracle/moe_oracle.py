@@ -207,6 +207,35 @@ def quantize_rows_int8(v):
     return q, scale
 
 
+Q4_MAX = 7           # symmetric int4 weight range used by the quantiser
+
+
+def quantize_weight_int4(w):
+    """bf16 weight [N, K] -> (packed int32 [N, K/8], bf16 scale bits [N, K/32]).
+
+    The conversion the "Kimi exact-generator adaptation" page names (section
+    "The proposed substitution": the to_exact path calls ExactLinear.from_weight
+    with a four-bit choice and group size 32; the page gives no rounding
+    rule).  Reading, per row and 32-column group, every step in IEEE float32:
+    a = max|w| (exact); s = bf16(a / 7) (the division rounded to nearest, then
+    rounded to bf16, ties to even); q = clamp(rint(w / s), -8, 7) with the
+    stored (bf16) s and rint rounding half to even; s = 0 gives q = 0.  The
+    values are packed as in ``pack_int4``."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 32")
+    g = w.reshape(N, K // GROUP, GROUP)
+    amax = np.max(np.abs(g), axis=-1)
+    s_bits = f32_to_bf16_bits((amax / np.float32(Q4_MAX)).astype(np.float32))
+    s = (s_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(g / s[..., None])
+    q = np.where(s[..., None] > 0, q, np.float32(0))
+    q = np.clip(q, -8, Q4_MAX).astype(np.int64).reshape(N, K)
+    return pack_int4(q), s_bits
+
+
 def int4_group_partials(qx, packed) -> np.ndarray:
     """Exact integer partial sums P[r, n, g] = sum_{c in group g} qx[r, c] * qw[n, c].
 

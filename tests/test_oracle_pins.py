@@ -448,3 +448,56 @@ def test_latent_projection_orientation():
     x = O.round_bf16(RNG.normal(size=(2, H)))
     u = O.expert_input(x, p)
     assert np.array_equal(u, x[:, np.arange(L) % H])
+
+
+# ----------------------------------------------------------------------------
+# int4 weight quantiser (ExactLinear.from_weight with four bits, group 32)
+# ----------------------------------------------------------------------------
+
+def _bf16_exact(v):
+    """The float32 values of v, asserting each is exactly a bf16."""
+    v = np.asarray(v, dtype=np.float32)
+    assert np.array_equal(O.round_bf16(v).astype(np.float32), v)
+    return v
+
+
+def test_weight_quantiser_recovers_exact_codes():
+    # scales with at most 5 significant bits times codes of at most 3 bits are
+    # exact bf16 values; a group whose largest |code| is 7 recovers (q, s)
+    N, K = 6, 128
+    q = RNG.integers(-7, 8, size=(N, K))
+    q[:, ::32] = np.where(RNG.random((N, K // 32)) < 0.5, 7, -7)
+    mant = RNG.integers(16, 32, size=(N, K // 32))
+    expo = RNG.integers(-14, -3, size=(N, K // 32))
+    s = np.ldexp(mant.astype(np.float64), expo)
+    w = _bf16_exact(q * np.repeat(s, 32, axis=1))
+    packed, s_bits = O.quantize_weight_int4(w)
+    assert np.array_equal(O.unpack_int4(packed), q)
+    assert np.array_equal(O.bf16_bits_to_f64(s_bits), s)
+
+
+def test_weight_quantiser_error_bound_and_range():
+    w = O.round_bf16(RNG.normal(size=(16, 256)) * RNG.uniform(1e-3, 10, size=(16, 1))).astype(np.float32)
+    packed, s_bits = O.quantize_weight_int4(w)
+    q = O.unpack_int4(packed)
+    s = np.repeat(O.bf16_bits_to_f64(s_bits), 32, axis=1)
+    assert q.min() >= -8 and q.max() <= 7
+    # every code is within half a step of w / s (s is the stored bf16 scale)
+    assert np.all(np.abs(w / s - q) <= 0.5 + 2.0 ** -20)  # fp32 division, ulp(8) = 2^-20
+    # the scale is a/7 rounded to bf16: within 2^-8 relative of the group's max/7
+    amax = np.abs(w).reshape(16, 8, 32).max(axis=-1)
+    rel = np.abs(O.bf16_bits_to_f64(s_bits) * 7 / amax - 1)
+    assert rel.max() <= 2.0 ** -8
+    # the largest magnitude of each group maps to +-7
+    assert np.all(np.abs(q).reshape(16, 8, 32).max(axis=-1) == 7)
+
+
+def test_weight_quantiser_zero_group_and_half_ties():
+    w = np.zeros((2, 64), dtype=np.float32)
+    # group 1 of row 0: max 7 (s = 1), values on half steps round to even codes
+    w[0, 32:40] = [7.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, -3.5]
+    packed, s_bits = O.quantize_weight_int4(w)
+    q = O.unpack_int4(packed)
+    assert s_bits.tolist() == [[0, 0x3F80], [0, 0]]
+    assert q[0, 32:40].tolist() == [7, 0, 2, 2, 0, -2, -2, -4]
+    assert not q[1].any() and not q[0, :32].any()
