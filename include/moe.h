@@ -230,6 +230,24 @@ int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets,
  * v bf16 [R, C] -> q int8 [R, C], scale fp32 [R].  R rows, C % 64 == 0. */
 int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale, void* stream);
 
+/* int4 weight quantiser (the conversion the "Kimi exact-generator adaptation"
+ * page names in section "The proposed substitution": ExactLinear.from_weight
+ * with a four-bit choice and group size 32; the page gives no rounding rule).
+ * Reading, per row and 32-column group, in IEEE float32: a = max|w|;
+ * s = bf16(a / 7) (division rounded to nearest, then to bf16, ties to even);
+ * q = clamp(rint(w / s), -8, 7) with the stored s, ties to even; s = 0 gives
+ * q = 0.
+ *   w       bf16 [N, K] row-major, device, 16-byte aligned (stacked experts
+ *           [E, N, K] are rows E*N);
+ *   packed  int32 [N, K/8] out, device, 16-byte aligned: nibble j (bits
+ *           4j..4j+3) of word i is column 8i+j, two's complement;
+ *   scale   bf16 [N, K/32] out, device.
+ * K % 32 == 0 (else MOE_ERR_UNSUPPORTED).  A non-finite weight records
+ * MOE_ERR_UNSUPPORTED in the device status word (moe_check_error); its group
+ * gets s = 0.  Caller-owned buffers; stream-ordered, no host sync. */
+int moe_quantize_int4(const uint16_t* w, int N, int K, int32_t* packed, uint16_t* scale,
+                      void* stream);
+
 /* --------------------------------------------------------------- combine -- */
 
 /* Un-permute and weighted sum (moe_infer listing; donor-reference "Sum the

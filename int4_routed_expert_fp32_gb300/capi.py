@@ -69,6 +69,7 @@ SIGNATURES = {
     "moe_int4_linear": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                 c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_quantize_int4": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_linear_bf16": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_rmsnorm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_float, c_void_p, c_void_p]),
@@ -241,6 +242,18 @@ def quantize_rows(v: torch.Tensor):
     s = torch.empty(R, dtype=torch.float32, device=v.device)
     _check("moe_quantize_rows", lib.moe_quantize_rows(_p(v), R, C, _p(q), _p(s), _stream()))
     return q, s
+
+
+def quantize_int4(w: torch.Tensor):
+    """bf16 weight [..., N, K] -> (packed int32 [..., N, K/8], bf16 scale [..., N, K/32])."""
+    _dev(w, torch.bfloat16)
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    packed = torch.empty(*w.shape[:-1], K // 8, dtype=torch.int32, device=w.device)
+    scale = torch.empty(*w.shape[:-1], K // 32, dtype=torch.bfloat16, device=w.device)
+    _check("moe_quantize_int4", lib.moe_quantize_int4(_p(w), rows, K, _p(packed), _p(scale),
+                                                      _stream()))
+    return packed, scale
 
 
 def combine(y_sorted: torch.Tensor, inv_row: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:

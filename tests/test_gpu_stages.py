@@ -231,6 +231,66 @@ def _t(a, dtype=None):
     return t.to(DEV)
 
 
+# ------------------------------------------------------------ int4 weight quantiser
+
+@pytest.mark.parametrize("shape", [(3, 40, 96), (1, 7, 32), (2, 513, 7168)])
+def test_quantize_int4_bit_exact(moe, shape):
+    """Codes and bf16 scales equal the oracle's bit for bit (float32 steps on
+    both sides), over magnitudes from 1e-4 to 1e3, zero groups and ties."""
+    rng = np.random.default_rng(sum(shape))
+    E, N, K = shape
+    w = rng.normal(size=shape) * rng.uniform(1e-4, 1e3, size=(E, N, 1))
+    w[:, :, :32] *= rng.random((E, N, 1)) < 0.8        # some all-zero groups
+    if K >= 64:
+        w[0, 0, 32:64] = np.concatenate([np.arange(29) * 0.5 - 7, [0, 0, 0]])  # s = 1: ties
+    wb = _bf16(w)
+    packed, scale = moe.quantize_int4(wb.to(DEV))
+    assert moe.check_error() == 0
+    ref_p, ref_s = O.quantize_weight_int4(wb.float().numpy().reshape(E * N, K))
+    assert np.array_equal(packed.cpu().numpy().reshape(E * N, K // 8), ref_p)
+    assert np.array_equal(bf16_bits(scale.cpu()).reshape(E * N, K // 32), ref_s)
+
+
+def test_quantize_int4_feeds_int4_linear(moe):
+    """Quantised bf16 weights run through the expert GEMM: the result equals
+    the oracle's product with the dequantised weights."""
+    rng = np.random.default_rng(11)
+    E, N, K, counts = 3, 256, 1024, [5, 0, 60]
+    off = _segments(counts)
+    R = int(off[-1])
+    w = _bf16(rng.normal(size=(E, N, K)) * 0.02)
+    packed, scale = moe.quantize_int4(w.to(DEV))
+    x = _bf16(rng.normal(size=(R, K)))
+    got = moe.int4_linear(x.to(DEV), None, _t(off), packed, scale, 16)
+    assert moe.check_error() == 0
+    got = got.cpu().numpy()
+    pk = packed.cpu().numpy()
+    sb = bf16_bits(scale.cpu())
+    xf = oi.x_f64(x)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a < b:
+            ref = O.int4_linear(xf[a:b], pk[e], sb[e], 16)
+            assert rel_l2(got[a:b], ref) <= 1e-5
+    # and the dequantised weights are within half a step of the bf16 weights
+    wq = O.dequantize(pk.reshape(E * N, K // 8), sb.reshape(E * N, K // 32))
+    step = np.repeat(O.bf16_bits_to_f64(sb.reshape(E * N, K // 32)), 32, axis=1)
+    assert np.all(np.abs(wq - w.float().numpy().reshape(E * N, K)) <= 0.5 * step * (1 + 2.0 ** -20))
+
+
+def test_quantize_int4_reports_nonfinite_weights(moe):
+    w = torch.zeros(4, 64, dtype=torch.bfloat16)
+    w[2, 40] = float("inf")
+    w[3, 3] = float("nan")
+    packed, scale = moe.quantize_int4(w.to(DEV))
+    assert moe.check_error() == moe.capi.MOE_ERR_UNSUPPORTED
+    s = bf16_bits(scale.cpu())
+    assert s[2, 1] == 0 and s[3, 0] == 0
+    # the next call is clean
+    moe.quantize_int4(torch.ones(2, 32, dtype=torch.bfloat16, device=DEV))
+    assert moe.check_error() == 0
+
+
 @pytest.mark.parametrize("K,N,counts", [
     (320, 300, [0, 1, 33, 70, 8]),        # ragged K tail, ragged N tile, multi-chunk experts
     (2048, 512, [5, 0, 0, 64, 2]),
