@@ -301,6 +301,25 @@ def expert_ffn(u, ex: Mapping[str, np.ndarray], act_bits: int = 16) -> np.ndarra
     return int4_linear(h, ex["down_packed"], ex["down_scale"], act_bits)
 
 
+def shared_expert(x, gate_bits, up_bits, down_bits) -> np.ndarray:
+    """The always-active shared expert: down( SiLU(gate(x)) * up(x) ) with bf16
+    nn.Linear weights and no bias, on the full-width input ("Kimi K3 latent
+    up-projection" page, KimiSparseMoeBlock listing: ``self.shared_experts =
+    KimiMLP(...)`` of moe_intermediate_size * num_shared_experts features and
+    ``y = y + self.shared_experts(identity)``; "Kimi K2.5 donor reference"
+    page, "Add an always-active shared expert"; the exact-generator page keeps
+    shared experts as ordinary bf16 linear modules).
+
+    gate_bits, up_bits bf16 bits [I, H]; down_bits [H, I].  The intermediate h
+    is stored in bf16 (the module's dtype) before the down projection; the
+    rest is fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    g = x @ bf16_bits_to_f64(gate_bits).T
+    u = x @ bf16_bits_to_f64(up_bits).T
+    h = round_bf16(silu(g) * u)
+    return h @ bf16_bits_to_f64(down_bits).T
+
+
 def rmsnorm(v, gain_bits, eps: float) -> np.ndarray:
     """v / sqrt(mean(v**2) + eps) * gain, over the last axis."""
     v = np.asarray(v, dtype=np.float64)
@@ -328,6 +347,16 @@ class LayerParams:
     lat_norm: Optional[np.ndarray] = None   # bf16 bits [L] (None: no norm)
     lat_up: Optional[np.ndarray] = None     # bf16 bits [H, L]
     eps: float = 1e-6
+    shared_gate: Optional[np.ndarray] = None  # bf16 bits [Is, H] (None: no shared expert)
+    shared_up: Optional[np.ndarray] = None    # bf16 bits [Is, H]
+    shared_down: Optional[np.ndarray] = None  # bf16 bits [H, Is]
+
+
+def add_shared(out, x, p: "LayerParams") -> np.ndarray:
+    """Routed output plus the shared expert on the full-width x (when present)."""
+    if p.shared_gate is None:
+        return out
+    return out + shared_expert(x, p.shared_gate, p.shared_up, p.shared_down)
 
 
 def expert_input(x, p: LayerParams) -> np.ndarray:
@@ -366,7 +395,7 @@ def moe_forward(x, p: LayerParams, tokens=None) -> np.ndarray:
             if e not in cache:
                 cache[e] = p.expert(e)
             out[i] += rt.weight[i, j] * expert_ffn(u[i:i + 1], cache[e], p.act_bits)[0]
-    return latent_out(out, p)
+    return add_shared(latent_out(out, p), xs, p)
 
 
 @dataclass
@@ -394,4 +423,4 @@ def moe_forward_sorted(x, p: LayerParams) -> SortedResult:
         outs[a:b] = expert_ffn(sorted_u[a:b], p.expert(e), p.act_bits)
     new_x = outs[d.inv_row]                      # new_x[t*k + j] = outs[row of (t, j)]
     y = (new_x.reshape(T, p.k, -1) * rt.weight[:, :, None]).sum(axis=1)
-    return SortedResult(out=latent_out(y, p), route=rt, disp=d, y_sorted=outs)
+    return SortedResult(out=add_shared(latent_out(y, p), x, p), route=rt, disp=d, y_sorted=outs)

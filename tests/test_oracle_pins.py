@@ -501,3 +501,44 @@ def test_weight_quantiser_zero_group_and_half_ties():
     assert s_bits.tolist() == [[0, 0x3F80], [0, 0]]
     assert q[0, 32:40].tolist() == [7, 0, 2, 2, 0, -2, -2, -4]
     assert not q[1].any() and not q[0, :32].any()
+
+
+# ----------------------------------------------------------------------------
+# shared expert
+# ----------------------------------------------------------------------------
+
+def test_shared_expert_closed_form_special_case():
+    """x = e_0, up(x) = 1 for every feature, gate(x) = v, down a permutation:
+    out = P bf16(SiLU(v)), with SiLU written out from the exponential."""
+    H = I = 8
+    v = np.array([-3.0, -1.0, -0.5, 0.0, 0.25, 1.0, 2.0, 5.0])
+    gate = np.zeros((I, H)); gate[:, 0] = v
+    up = np.zeros((I, H)); up[:, 0] = 1.0
+    perm = [3, 0, 7, 1, 6, 2, 5, 4]
+    down = np.zeros((H, I))
+    for r, c in enumerate(perm):
+        down[r, c] = 1.0
+    x = np.zeros((1, H)); x[0, 0] = 1.0
+    bits = lambda a: O.f32_to_bf16_bits(a.astype(np.float32))
+    out = O.shared_expert(x, bits(gate), bits(up), bits(down))
+    silu = np.array([t / (1.0 + math.exp(-t)) for t in v])
+    want = O.round_bf16(silu)[perm]
+    assert np.array_equal(out[0], want)
+    # gate and up swapped: SiLU(1) * v instead (a transposed role fails here)
+    out2 = O.shared_expert(x, bits(up), bits(gate), bits(down))
+    assert np.array_equal(out2[0], O.round_bf16(v * (1.0 / (1.0 + math.exp(-1.0))))[perm])
+
+
+def test_shared_expert_hidden_order_and_down_scaling():
+    rng = np.random.default_rng(5)
+    H, I = 64, 48
+    bits = lambda a: O.f32_to_bf16_bits(a.astype(np.float32))
+    gate, up, down = (bits(rng.normal(size=s) * 0.1) for s in [(I, H), (I, H), (H, I)])
+    x = rng.normal(size=(5, H))
+    ref = O.shared_expert(x, gate, up, down)
+    # reordering the hidden features consistently changes nothing
+    p = rng.permutation(I)
+    assert np.allclose(O.shared_expert(x, gate[p], up[p], down[:, p]), ref, rtol=1e-12, atol=1e-14)
+    # doubling the down weights (exact in bf16) doubles the output exactly
+    d2 = O.f32_to_bf16_bits(2 * O.bf16_bits_to_f64(down).astype(np.float32))
+    assert np.array_equal(O.shared_expert(x, gate, up, d2), 2 * ref)
