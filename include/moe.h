@@ -80,6 +80,7 @@ typedef struct moe_config {
   int32_t act_bits; /* 16 or 8 */
   int32_t renorm;   /* 1: divide the top-k affinities by their sum + 1e-20 */
   float eps;        /* RMSNorm epsilon (latent path) */
+  int32_t I_shared; /* shared-expert intermediate width; 0 = no shared expert */
 } moe_config;
 
 /* Weights of one layer.  D = L if L > 0 else H. */
@@ -95,6 +96,9 @@ typedef struct moe_weights {
   const uint16_t* lat_down;    /* bf16 [L, H]  (latent only) */
   const uint16_t* lat_norm;    /* bf16 [L] RMSNorm gain, NULL = no norm (latent only) */
   const uint16_t* lat_up;      /* bf16 [H, L]  (latent only) */
+  const uint16_t* shared_gate; /* bf16 [I_shared, H]  (shared expert only) */
+  const uint16_t* shared_up;   /* bf16 [I_shared, H] */
+  const uint16_t* shared_down; /* bf16 [H, I_shared] */
 } moe_weights;
 
 /* ---------------------------------------------------------------- router -- */
@@ -270,6 +274,28 @@ int moe_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, u
  * (donor-reference RMSNorm equations).  x, y bf16 [M, N]; gain bf16 [N]. */
 int moe_rmsnorm(const uint16_t* x, const uint16_t* gain, int M, int N, float eps, uint16_t* y,
                 void* stream);
+
+/* --------------------------------------------------------- shared expert -- */
+
+/* Workspace bytes of moe_shared_expert. */
+size_t moe_shared_expert_workspace_size(int T, int H, int I);
+
+/* The always-active shared expert, added to an output ("Kimi K3 latent
+ * up-projection" page, KimiSparseMoeBlock listing: shared_experts = KimiMLP
+ * of moe_intermediate_size * num_shared_experts features and
+ * y = y + shared_experts(identity); "Kimi K2.5 donor reference" page, "Add an
+ * always-active shared expert"; the exact-generator page keeps shared experts
+ * as ordinary bf16 linear modules):
+ *   out = bf16( (accumulate ? out : 0) + down( bf16(SiLU(gate(x)) * up(x)) ) )
+ * with fp32 accumulation of every product and h stored in bf16.
+ *   x       bf16 [T, H] (the full-width layer input), 16-byte aligned
+ *   gate_w, up_w  bf16 [I, H];  down_w bf16 [H, I]  (nn.Linear [out, in])
+ *   out     bf16 [T, H], read when accumulate != 0, written
+ * H % 64 == 0 and I % 64 == 0 (else MOE_ERR_UNSUPPORTED).  Caller-owned
+ * device buffers and workspace (256-byte aligned); stream-ordered. */
+int moe_shared_expert(const uint16_t* x, int T, int H, int I, const uint16_t* gate_w,
+                      const uint16_t* up_w, const uint16_t* down_w, int accumulate, uint16_t* out,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------- layer -- */
 

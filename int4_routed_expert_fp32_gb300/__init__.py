@@ -9,7 +9,7 @@ import importlib
 
 _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "combine",
             "dispatch", "dispatch_noalloc", "expert_ffn", "int4_linear", "launch_count", "lib", "linear_bf16", "quantize_int4",
-            "quantize_rows",
+            "quantize_rows", "shared_expert",
             "rmsnorm", "route", "status_string", "wait_selftest", "capi")
 
 

@@ -33,13 +33,15 @@ class MoeError(RuntimeError):
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", c_int32), ("H", c_int32), ("E", c_int32), ("k", c_int32), ("I", c_int32),
-                ("L", c_int32), ("act_bits", c_int32), ("renorm", c_int32), ("eps", c_float)]
+                ("L", c_int32), ("act_bits", c_int32), ("renorm", c_int32), ("eps", c_float),
+                ("I_shared", c_int32)]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in (
         "router_w", "router_bias", "gate_packed", "gate_scale", "up_packed", "up_scale",
-        "down_packed", "down_scale", "lat_down", "lat_norm", "lat_up")]
+        "down_packed", "down_scale", "lat_down", "lat_norm", "lat_up", "shared_gate", "shared_up",
+        "shared_down")]
 
 
 # name -> (restype, argtypes); mirrors include/moe.h
@@ -70,6 +72,9 @@ SIGNATURES = {
                                 c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_quantize_int4": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_shared_expert_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "moe_shared_expert": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                  c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_linear_bf16": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_rmsnorm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_float, c_void_p, c_void_p]),
@@ -256,6 +261,24 @@ def quantize_int4(w: torch.Tensor):
     return packed, scale
 
 
+def shared_expert(x: torch.Tensor, gate_w: torch.Tensor, up_w: torch.Tensor,
+                  down_w: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out (+)= down(SiLU(gate x) * up x) with bf16 weights; a new output when
+    ``out`` is None, else added to it in place."""
+    for t in (x, gate_w, up_w, down_w):
+        _dev(t, torch.bfloat16)
+    T, H = x.shape
+    I = gate_w.shape[0]
+    acc = out is not None
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    ws = _ws(lib.moe_shared_expert_workspace_size(T, H, I), x.device)
+    _check("moe_shared_expert", lib.moe_shared_expert(
+        _p(x), T, H, I, _p(gate_w), _p(up_w), _p(down_w), int(acc), _p(out), _p(ws), ws.numel(),
+        _stream()))
+    return out
+
+
 def combine(y_sorted: torch.Tensor, inv_row: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:
     _dev(y_sorted, torch.bfloat16); _dev(inv_row, torch.int32); _dev(topk_w, torch.float32)
     T, k = topk_w.shape
@@ -298,8 +321,9 @@ class MoeLayer:
     """One routed int4 MoE layer: configuration, device weights and a workspace."""
 
     def __init__(self, T: int, H: int, E: int, k: int, I: int, weights: Dict[str, torch.Tensor],
-                 L: int = 0, act_bits: int = 16, renorm: bool = True, eps: float = 1e-6):
-        self.cfg = MoeConfig(T, H, E, k, I, L, act_bits, int(renorm), eps)
+                 L: int = 0, act_bits: int = 16, renorm: bool = True, eps: float = 1e-6,
+                 I_shared: int = 0):
+        self.cfg = MoeConfig(T, H, E, k, I, L, act_bits, int(renorm), eps, I_shared)
         self.weights = weights
         self.device = weights["router_w"].device
         for name, t in weights.items():

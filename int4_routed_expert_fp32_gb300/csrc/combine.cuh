@@ -39,4 +39,11 @@ int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                        cudaStream_t s);
 
+// Shared expert (validated arguments): out = bf16((accumulate ? out : 0) +
+// down(SiLU(gate x) * up x)), bf16 weights gate/up [I, H], down [H, I].
+size_t shared_expert_ws_bytes(int T, int H, int I);
+int launch_shared_expert(const uint16_t* x, int T, int H, int I, const uint16_t* gate_w,
+                         const uint16_t* up_w, const uint16_t* down_w, int accumulate,
+                         uint16_t* out, void* ws, cudaStream_t s);
+
 }  // namespace moe

@@ -1,7 +1,8 @@
 // The whole routed int4 MoE layer on one stream (Kimi K3 latent up-projection
-// page, KimiSparseMoeBlock.forward listing, without the shared expert): the
-// router sees the full-width x; the latent down-projection (if any) feeds the
-// dispatch; experts; combine (+ RMSNorm and up-projection on the latent path).
+// page, KimiSparseMoeBlock.forward listing): the router sees the full-width x;
+// the latent down-projection (if any) feeds the dispatch; experts; combine
+// (+ RMSNorm and up-projection on the latent path); then, when configured,
+// the shared expert on the full-width x is added to the output.
 #include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
@@ -36,7 +37,10 @@ static size_t scratch_need(const moe_config& c) {
   size_t b = moe_dispatch_workspace_size(c.T, c.E, c.k);
   size_t f = expert_ffn_ws_bytes(c.E, D, c.I, R, c.act_bits);
   size_t m = a > b ? a : b;
-  return m > f ? m : f;
+  m = m > f ? m : f;
+  // the shared expert runs last and reuses the scratch
+  const size_t sh = c.I_shared > 0 ? shared_expert_ws_bytes(c.T, c.H, c.I_shared) : 0;
+  return m > sh ? m : sh;
 }
 
 // Carve the workspace; with base == nullptr only the total size is computed.
@@ -91,11 +95,18 @@ static int validate(const moe_config* c, const moe_weights* w) {
   if (c->L > 0 && (!aligned(w->lat_down, 16) || !aligned(w->lat_up, 16) ||
                    (w->lat_norm && !aligned(w->lat_norm, 16))))
     return MOE_ERR_INVALID;
+  if (c->I_shared < 0) return MOE_ERR_INVALID;
+  if (c->I_shared > 0) {
+    if (c->I_shared % 64) return MOE_ERR_UNSUPPORTED;
+    if (!w->shared_gate || !w->shared_up || !w->shared_down || !aligned(w->shared_gate, 16) ||
+        !aligned(w->shared_up, 16) || !aligned(w->shared_down, 16))
+      return MOE_ERR_INVALID;
+  }
   return MOE_OK;
 }
 
-static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x, uint16_t* out,
-                   const LayerWs& ws, cudaStream_t s) {
+static int routed(const moe_config& c, const moe_weights& w, const uint16_t* x, uint16_t* out,
+                  const LayerWs& ws, cudaStream_t s) {
   const int D = c.L > 0 ? c.L : c.H;
   const int R = c.T * c.k;
   int rc = moe_route(x, w.router_w, w.router_bias, c.T, c.H, c.E, c.k, c.renorm, ws.topk_idx,
@@ -124,6 +135,14 @@ static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x,
   }
   return launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.H, c.k, nullptr, 0.f,
                         out, s);
+}
+
+static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x, uint16_t* out,
+                   const LayerWs& ws, cudaStream_t s) {
+  const int rc = routed(c, w, x, out, ws, s);
+  if (rc || c.I_shared == 0) return rc;
+  return launch_shared_expert(x, c.T, c.H, c.I_shared, w.shared_gate, w.shared_up, w.shared_down,
+                              1, out, ws.scratch, s);
 }
 
 }  // namespace moe

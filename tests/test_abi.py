@@ -39,9 +39,23 @@ def test_every_declared_symbol_is_exported_and_bound(capi):
     assert set(capi.SIGNATURES) == set(declared_functions())
 
 
+def _header_struct_fields(name):
+    """Field names, in order, of ``typedef struct name { ... } name;`` in moe.h."""
+    import re
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (name, name), text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    return [re.findall(r"(\w+)\s*$", d.strip())[0] for d in body.split(";") if d.strip()]
+
+
 def test_struct_layouts_match_header(capi):
-    assert ctypes.sizeof(capi.MoeConfig) == 9 * 4
-    assert ctypes.sizeof(capi.MoeWeights) == 11 * ctypes.sizeof(ctypes.c_void_p)
+    cfg = _header_struct_fields("moe_config")
+    wts = _header_struct_fields("moe_weights")
+    assert [n for n, _ in capi.MoeConfig._fields_] == cfg
+    assert [n for n, _ in capi.MoeWeights._fields_] == wts
+    assert ctypes.sizeof(capi.MoeConfig) == len(cfg) * 4            # int32 / float fields
+    assert ctypes.sizeof(capi.MoeWeights) == len(wts) * ctypes.sizeof(ctypes.c_void_p)
 
 
 def test_status_strings(capi):

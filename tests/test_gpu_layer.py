@@ -113,3 +113,54 @@ def test_layer_zero_tokens(moe):
     out = layer.forward(torch.empty(0, w.H, dtype=torch.bfloat16, device=DEV))
     assert out.shape == (0, w.H)
     assert moe.check_error() == 0
+
+
+# ----------------------------------------------------------- shared expert
+
+def _shared_weights(rng, H, Is, std=0.02):
+    mk = lambda *s: O.f32_to_bf16_bits((rng.normal(size=s) * std).astype(np.float32))
+    return mk(Is, H), mk(Is, H), mk(H, Is)
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16).to(DEV)
+
+
+@pytest.mark.parametrize("T,H,Is,acc", [(5, 512, 256, False), (32, 1024, 320, True),
+                                        (300, 768, 192, True), (1, 7168, 2048, False)])
+def test_shared_expert_parity(moe, T, H, Is, acc):
+    """out (+)= down(bf16(SiLU(gate x) * up x)) against the fp64 oracle; the
+    split-K slices (many when T is small) are summed in fp32."""
+    rng = np.random.default_rng(T + H + Is)
+    g, u, d = _shared_weights(rng, H, Is)
+    x = torch.from_numpy(rng.normal(size=(T, H)).astype(np.float32)).to(torch.bfloat16)
+    base = torch.from_numpy(rng.normal(size=(T, H)).astype(np.float32) * 0.1).to(torch.bfloat16)
+    out = base.to(DEV) if acc else None
+    got = moe.shared_expert(x.to(DEV), _bf16_dev(g), _bf16_dev(u), _bf16_dev(d), out)
+    assert moe.check_error() == 0
+    ref = O.shared_expert(oi.x_f64(x), g, u, d)
+    if acc:
+        ref = ref + base.double().numpy()
+    assert_close(got.float().cpu().numpy(), ref, what=f"shared {T}x{H}x{Is}")
+
+
+@pytest.mark.parametrize("case", ["tiny", "small_latent"])
+def test_layer_with_shared_expert(moe, case):
+    w = SMALL[case]
+    Is = 192
+    rng = np.random.default_rng(31)
+    g, u, d = _shared_weights(rng, w.H, Is)
+    x = wl.gen_x(w, attempts=conditioned_attempts(w))
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    weights = device_weights(w, DEV, router, lat)
+    weights.update({"shared_gate": _bf16_dev(g), "shared_up": _bf16_dev(u),
+                    "shared_down": _bf16_dev(d)})
+    layer = moe.MoeLayer(w.T, w.H, w.E, w.k, w.I, weights, L=w.L, act_bits=w.act_bits,
+                         renorm=w.renorm, eps=w.eps, I_shared=Is)
+    out = layer.forward(x.to(DEV))
+    assert moe.check_error() == 0
+    p = oi.layer_params(w, router=router, latent=lat)
+    p.shared_gate, p.shared_up, p.shared_down = g, u, d
+    ref = O.moe_forward(oi.x_f64(x), p)
+    assert_close(out.float().cpu().numpy(), ref, what=case + "+shared")
