@@ -234,6 +234,22 @@ def _cpu_baseline(w: wl.Workload, budget_s: float = 20.0):
                       f"definition, expert weights generated per token ({dt:.1f} s)"}
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of the ranks' values (a replicated job takes as long as its
+    slowest rank); the value itself with one rank (dist None)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own tokens_per_rank
+    tokens per step, in ms (the max over ranks)."""
+    return world * tokens_per_rank / (ms / 1000.0)
+
+
 def run_reference(args):
     rank, world, _ = _env_rank()
     if rank != 0:
@@ -323,15 +339,11 @@ def main(argv=None):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, device)
     rc = moe.check_error()
     if rc != 0:
         raise RuntimeError(f"device status after timing: {moe.status_string(rc)}")
-    value = world * w.T / (ms / 1000.0)
+    value = job_tokens_per_s(world, w.T, ms)
 
     # dominant kernel: the expert FFN stream kernels
     ffn_ms, counts = _ffn_pass(moe, w, layer, weights, x_dev, min(args.steps, 100))
@@ -389,12 +401,8 @@ def _e2e_pass(layer, x, w, world, dist, device, e_steps):
     e1.record()
     torch.cuda.synchronize()
     wall = (time.perf_counter() - t0) / e_steps
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return {"value": world * w.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, device)
+    return {"value": job_tokens_per_s(world, w.T, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
             "host_wall_ms_per_step": wall * 1000.0}
 

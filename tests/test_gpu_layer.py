@@ -164,3 +164,29 @@ def test_layer_with_shared_expert(moe, case):
     p.shared_gate, p.shared_up, p.shared_down = g, u, d
     ref = O.moe_forward(oi.x_f64(x), p)
     assert_close(out.float().cpu().numpy(), ref, what=case + "+shared")
+
+
+@pytest.mark.parametrize("case", ["tiny", "small_latent", "small_adversarial"])
+def test_layer_forward_replays_from_a_cuda_graph(moe, case):
+    """The layer call allocates nothing and never synchronises the host, so a
+    captured CUDA graph of it replays to the same bits as stream launches."""
+    w = SMALL[case]
+    x = wl.gen_x(w, attempts=conditioned_attempts(w)).to(DEV)
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    layer = _layer(moe, w, device_weights(w, DEV, router, lat))
+    ref = layer.forward(x)
+    out = torch.zeros_like(ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, out)  # warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, out)
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert moe.check_error() == 0
+    assert torch.equal(out, ref)
