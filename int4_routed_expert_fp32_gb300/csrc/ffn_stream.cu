@@ -51,17 +51,11 @@ constexpr int kFsKc = 256;                 // K columns per stage
 constexpr int kFsGroups = kFsKc / kGroup;  // 8 scale groups per stage
 constexpr int kFsMc = 16;                  // token rows per chunk
 constexpr int kFsTb = kFsMc / 8;           // token blocks of 8 (MMA N)
-#ifndef FS_CWARPS
-#define FS_CWARPS 16
-#endif
-constexpr int kFsCWarps = FS_CWARPS;       // consumer warps, one 16-row block each
-#ifndef FS_UNROLL
-#define FS_UNROLL 4
-#endif
-constexpr int kFsUnroll = FS_UNROLL;       // group pairs unrolled with one token block
+constexpr int kFsCWarps = 16;              // consumer warps, one 16-row block each
+constexpr int kFsUnroll = 4;               // group pairs unrolled with one token block
 constexpr int kFsThreads = (kFsCWarps + 2) * 32;  // + TMA producer + start-value warp
 constexpr int kFsRows = 16 * kFsCWarps;    // weight rows per stage tile
-constexpr int kFsStages = (FS_CWARPS <= 12) ? 5 : 4;
+constexpr int kFsStages = 4;
 constexpr int kFsWBytes = kFsRows * 128;   // 32 KiB of packed int4 per stage
 constexpr int kFsSBytes = kFsRows * 16;    // 8 bf16 scales per row per stage
 constexpr int kFsXStride16 = kFsKc * 2 + 64;  // bf16 row stride in shared memory

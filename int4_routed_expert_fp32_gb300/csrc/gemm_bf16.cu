@@ -8,127 +8,11 @@
 // 128-byte swizzle into a 4-stage ring, one warp issues tcgen05.mma
 // (M=128, N=256, K=16) into a 256-column TMEM accumulator, and four epilogue
 // warps read it back with tcgen05.ld and store bf16.
-// gemm_bf16_kernel (mma.sync, 128x128x32) is the check kernel of the former.
 #include "combine.cuh"
 #include "common.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
-
-constexpr int kGbBM = 128, kGbBN = 128, kGbBK = 32, kGbStages = 3;
-constexpr int kGbLd = kGbBK + 8;  // padded row (80 bytes): conflict-free ldmatrix
-constexpr int kGbTileElems = kGbBM * kGbLd;
-constexpr int kGbSmem = kGbStages * 2 * kGbTileElems * 2;
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__global__ void __launch_bounds__(256) gemm_bf16_kernel(const uint16_t* __restrict__ A,
-                                                        const uint16_t* __restrict__ B,
-                                                        uint16_t* __restrict__ C, int M, int N,
-                                                        int K) {
-  extern __shared__ __align__(16) uint16_t gsm[];
-  uint16_t* As = gsm;
-  uint16_t* Bs = gsm + kGbStages * kGbTileElems;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wm = warp >> 2, wn = warp & 3;
-  const int m0 = blockIdx.y * kGbBM, n0 = blockIdx.x * kGbBN;
-  const int ktiles = K / kGbBK;
-
-  auto load_stage = [&](int st, int kt) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int c = tid + 256 * i;
-      const int row = c >> 2, kc = c & 3;
-      const int ga = m0 + row, gb = n0 + row;
-      const uint16_t* sa = ga < M ? A + (size_t)ga * K + kt * kGbBK + kc * 8 : A;
-      const uint16_t* sb = gb < N ? B + (size_t)gb * K + kt * kGbBK + kc * 8 : B;
-      cp_async_16(smem_u32(As + st * kGbTileElems + row * kGbLd + kc * 8), sa, ga < M ? 16 : 0);
-      cp_async_16(smem_u32(Bs + st * kGbTileElems + row * kGbLd + kc * 8), sb, gb < N ? 16 : 0);
-    }
-  };
-
-  float acc[4][4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
-
-#pragma unroll
-  for (int st = 0; st < kGbStages - 1; ++st) {
-    if (st < ktiles) load_stage(st, st);
-    cp_async_commit();
-  }
-  for (int kt = 0; kt < ktiles; ++kt) {
-    cp_async_wait<kGbStages - 2>();
-    __syncthreads();
-    const int nk = kt + kGbStages - 1;
-    if (nk < ktiles) load_stage(nk % kGbStages, nk);
-    cp_async_commit();
-    const int st = kt % kGbStages;
-    const uint16_t* as = As + st * kGbTileElems;
-    const uint16_t* bs = Bs + st * kGbTileElems;
-#pragma unroll
-    for (int kk = 0; kk < kGbBK; kk += 16) {
-      uint32_t af[4][4], bf[2][4];
-#pragma unroll
-      for (int mi = 0; mi < 4; ++mi)
-        ldmatrix_x4(smem_u32(as + (wm * 64 + mi * 16 + (lane & 15)) * kGbLd + kk + (lane >> 4) * 8),
-                    af[mi]);
-#pragma unroll
-      for (int nj = 0; nj < 2; ++nj)
-        ldmatrix_x4(smem_u32(bs + (wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3)) * kGbLd + kk +
-                             ((lane >> 3) & 1) * 8),
-                    bf[nj]);
-#pragma unroll
-      for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
-          mma16816(acc[mi][ni], af[mi], bf[ni >> 1][(ni & 1) * 2], bf[ni >> 1][(ni & 1) * 2 + 1]);
-    }
-  }
-  cp_async_wait<0>();
-
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int mi = 0; mi < 4; ++mi) {
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) {
-      const int col = n0 + wn * 32 + ni * 8 + 2 * t;
-      if (col >= N) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = m0 + wm * 64 + mi * 16 + g + 8 * h;
-        if (row >= M) continue;
-        const uint32_t v = static_cast<uint32_t>(f32_to_bf16_bits(acc[mi][ni][2 * h])) |
-                           (static_cast<uint32_t>(f32_to_bf16_bits(acc[mi][ni][2 * h + 1])) << 16);
-        *reinterpret_cast<uint32_t*>(C + (size_t)row * N + col) = v;
-      }
-    }
-  }
-}
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KiB
@@ -303,17 +187,6 @@ int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int
                                 float* y, cudaStream_t s) {
   const int splits = (K + kc - 1) / kc;
   return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, y, s);
-}
-
-int launch_linear_mma(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
-                      cudaStream_t s) {
-  if (M == 0) return MOE_OK;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kGbSmem));
-  dim3 grid((N + kGbBN - 1) / kGbBN, (M + kGbBM - 1) / kGbBM);
-  gemm_bf16_kernel<<<grid, 256, kGbSmem, s>>>(x, w, y, M, N, K);
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
 }
 
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
