@@ -47,6 +47,8 @@ SMALL = {
     "one_token": wl.workload("tiny", name="one", T=1, H=256, E=8, k=2, I=128, seed=12),
     "multi_chunk": wl.workload("tiny", name="multi", T=200, H=256, E=4, k=2, I=128, seed=13),
     "no_renorm": wl.workload("tiny", name="nr", T=40, H=256, E=24, k=3, I=64, renorm=False, seed=6),
+    # the library's limits: 2048 experts, top-32
+    "max_E_k": wl.workload("tiny", name="max_E_k", T=20, H=256, E=2048, k=32, I=64, seed=21),
 }
 
 

@@ -53,6 +53,8 @@ ROUTE_CASES = {
     # from 512 tokens the logits come from the tensor cores: ragged in both
     # the 128-token and the 256-logit tiles
     "tc_ragged": wl.workload("tiny", name="tc_ragged", T=601, H=512, E=100, k=6, seed=7),
+    # the library's limits: 2048 experts, top-32
+    "max_E_k": wl.workload("tiny", name="max_E_k", T=24, H=256, E=2048, k=32, seed=21),
 }
 
 
@@ -512,4 +514,16 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     assert moe.check_error() == 0   # cleared
     q, s = moe.quantize_rows(torch.ones(2, 64, dtype=torch.bfloat16, device=DEV))
     assert float(s[0]) == float(np.float32(1.0) / np.float32(127.0))
+    assert moe.check_error() == 0
+
+
+def test_limits_are_enforced(moe):
+    """One past each limit (2048 experts, top-32) is rejected before any launch."""
+    x = torch.zeros(4, 256, dtype=torch.bfloat16, device=DEV)
+    for E, k in [(2049, 8), (64, 33)]:
+        W = torch.zeros(E, 256, device=DEV)
+        b = torch.zeros(E, device=DEV)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.route(x, W, b, k, True)
+        assert "UNSUPPORTED" in str(ei.value)
     assert moe.check_error() == 0
