@@ -134,9 +134,12 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
 
 // Quantise the 8 values of one 16-byte bf16 vector with a row scale: IEEE
 // division, round half to even, clamp to [-127, 127]; packs 8 int8 in a uint2.
-__device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
+// F16: also the fp16 values of the eight codes (exact: |q| <= 127).
+template <bool F16 = false>
+__device__ __forceinline__ uint2 quant8(const uint4 v, float sc, uint4* f16 = nullptr) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t out[2] = {0u, 0u};
+  uint32_t h[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
@@ -145,7 +148,9 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float sc) {
     q = fminf(fmaxf(q, -127.f), 127.f);
     const uint32_t b = static_cast<uint32_t>(static_cast<int>(q)) & 0xffu;
     out[i >> 2] |= b << (8 * (i & 3));
+    if (F16) h[i >> 1] |= static_cast<uint32_t>(__half_as_ushort(__float2half_rn(q))) << (16 * (i & 1));
   }
+  if (F16) *f16 = make_uint4(h[0], h[1], h[2], h[3]);
   return make_uint2(out[0], out[1]);
 }
 
@@ -249,10 +254,14 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
 
 // Per-row int8 quantisation of R rows of C bf16 values (one warp per row).
 // Rows at or beyond *row_count (when given) are skipped.
+// With q16 (F16) the kernel also writes the fp16 values of the codes, the
+// operand copy the tensor-core kernels read.
+template <bool F16>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ v, int R,
                                                             int C, const int32_t* row_count,
                                                             int8_t* __restrict__ q,
-                                                            float* __restrict__ scale) {
+                                                            float* __restrict__ scale,
+                                                            uint16_t* __restrict__ q16) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= R) return;
@@ -261,14 +270,23 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
   const uint4* src = reinterpret_cast<const uint4*>(v + (size_t)r * C);
   const float sc = warp_row_scale(src, nv, lane);
   uint2* dst = reinterpret_cast<uint2*>(q + (size_t)r * C);
-  for (int i = lane; i < nv; i += 32) dst[i] = quant8(src[i], sc);
+  uint4* d16 = F16 ? reinterpret_cast<uint4*>(q16 + (size_t)r * C) : nullptr;
+  for (int i = lane; i < nv; i += 32) {
+    if (F16)
+      dst[i] = quant8<true>(src[i], sc, d16 + i);
+    else
+      dst[i] = quant8(src[i], sc);
+  }
   if (lane == 0) scale[r] = sc;
 }
 
 int launch_quantize_rows(const uint16_t* v, int R, int C, const int32_t* row_count, int8_t* q,
-                         float* scale, cudaStream_t s) {
+                         float* scale, cudaStream_t s, uint16_t* q16) {
   if (R == 0) return MOE_OK;
-  quantize_rows_kernel<<<(R + 7) / 8, 256, 0, s>>>(v, R, C, row_count, q, scale);
+  if (q16)
+    quantize_rows_kernel<true><<<(R + 7) / 8, 256, 0, s>>>(v, R, C, row_count, q, scale, q16);
+  else
+    quantize_rows_kernel<false><<<(R + 7) / 8, 256, 0, s>>>(v, R, C, row_count, q, scale, nullptr);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

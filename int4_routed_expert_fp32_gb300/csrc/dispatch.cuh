@@ -7,9 +7,10 @@
 namespace moe {
 
 // Per-row int8 quantisation of R rows of C bf16 values on stream s; rows at or
-// beyond *row_count (device pointer, may be null) are skipped.
+// beyond *row_count (device pointer, may be null) are skipped.  With q16 the
+// fp16 values of the codes are written too (16-byte aligned, [R, C]).
 int launch_quantize_rows(const uint16_t* v, int R, int C, const int32_t* row_count, int8_t* q,
-                         float* scale, cudaStream_t s);
+                         float* scale, cudaStream_t s, uint16_t* q16 = nullptr);
 
 // Dispatch whose x_sorted rows are in the expert kernels' pair order (fp16,
 // or int8 with act_bits 8); ws as for moe_dispatch.  Arguments are checked by

@@ -1033,7 +1033,9 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   }
 
   if (q8) {
-    rc = launch_quantize_rows(h, rows_max, I, offsets + E, hq, hs, s);
+    // the tensor-core down kernel reads the fp16 copy of the codes, written
+    // in the same pass
+    rc = launch_quantize_rows(h, rows_max, I, offsets + E, hq, hs, s, use_tc ? h16 : nullptr);
     if (rc) return rc;
     pd.x = hq;
     pd.x_scale = hs;
@@ -1043,12 +1045,7 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
     if (rc) return rc;
   }
   if (use_tc) {
-    const uint16_t* ha = h;
-    if (q8) {
-      rc = launch_to_f16_rows(hq, true, rows_max, I, offsets + E, h16, s);
-      if (rc) return rc;
-      ha = h16;
-    }
+    const uint16_t* ha = q8 ? h16 : h;
     rc = launch_tc_down(ha, q8 ? hs : nullptr, rows_max, E, D, I, down_packed, down_scale, y,
                         y_f32, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status,
                         s);
