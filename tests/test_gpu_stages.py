@@ -379,6 +379,9 @@ def test_int4_linear_exact_mode_scaled(moe):
     (320, 192, [130, 5, 64, 0, 16, 17]), # ragged token tiles, ragged N tiles, threshold edges
     (256, 128, [16, 16, 16, 0, 3]),      # tensor-core kernels launched with no tile to do
     (256, 192, [400, 3, 0, 193]),        # several 192-row chunks per expert, ragged last chunks
+    # many experts of 17..70 rows on the tensor cores (partial 128-row tiles)
+    (320, 192, [40, 3, 64, 17, 33, 0]),
+    (256, 128, [70, 40, 40, 40, 40, 40, 40, 40]),
 ])
 def test_expert_ffn_parity(moe, act_bits, D, I, counts):
     rng = np.random.default_rng(D + I + act_bits)
