@@ -127,10 +127,11 @@ __global__ void router_split_kernel(const float* __restrict__ W, size_t n, uint1
 }
 
 // One CTA per token.  Its threads reduce the partial logits of the token in
-// order (partial p of (t, e) at part[p * sp + t * st + e]), then take the
-// sigmoid and add the bias; warp 0 runs k rounds of warp arg-max (equal
-// scores: lower expert id) and renormalises.
-constexpr int kTopkThreads = 128;
+// order (partial p of (t, e) at part[p * sp + t * st + e]; one thread per
+// expert at E <= 384, so that all the partial loads are in flight at once),
+// then take the sigmoid and add the bias; warp 0 runs k rounds of warp
+// arg-max (equal scores: lower expert id) and renormalises.
+constexpr int kTopkThreads = 384;
 
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
     const float* __restrict__ part, int S, size_t sp, size_t st, const float* __restrict__ bias,
