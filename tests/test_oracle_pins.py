@@ -221,6 +221,27 @@ def test_quantizer_golden(golden_dir):
         assert float(s[0]) == c["scale"]
 
 
+def _f32_half_ulp(x) -> Fraction:
+    """Half the spacing of the float32 values around x (normal range)."""
+    return Fraction(2) ** (math.floor(math.log2(abs(float(x)))) - 24)
+
+
+def test_quantizer_float32_tie_case_by_exact_arithmetic(golden_dir):
+    # The golden row [a, a/2, -a/2] that separates float32 from float64
+    # quantisation, checked with exact rationals: the stored scale is the
+    # float32 nearest a/127; the exact quotient (a/2)/s is not a tie, but the
+    # float32 nearest to it is the tie 63.5, so rint gives the even code 64.
+    with open(os.path.join(golden_dir, "quantizer_cases.json")) as f:
+        c = json.load(f)["cases"][4]
+    a, v, s = Fraction(c["v"][0]), Fraction(c["v"][1]), Fraction(c["scale"])
+    assert float(np.float32(c["scale"])) == c["scale"]          # s is a float32 value
+    assert abs(s - a / 127) <= _f32_half_ulp(s)
+    tie = Fraction(127, 2)
+    quo = v / s
+    assert quo < tie and tie - quo < _f32_half_ulp(tie)
+    assert c["q"] == [127, 64, -64]
+
+
 def test_quantizer_identity_on_int8_rows():
     x = RNG.integers(-127, 128, size=(20, 96)).astype(np.float32)
     x[:, 5] = 127.0
@@ -342,6 +363,51 @@ def test_expert_matches_brute_force_loops():
         assert np.allclose(y[r], _brute_expert(u[r], ex), rtol=1e-12, atol=1e-12)
 
 
+def _brute_q8(vals):
+    """Per-row int8 codes and scale of a list of values, one float32 operation at a time."""
+    a = np.float32(0.0)
+    for v in vals:
+        a = max(a, abs(np.float32(v)))
+    s = np.float32(a / np.float32(127))
+    if s == 0:
+        return [0] * len(vals), s
+    return [int(min(max(np.rint(np.float32(np.float32(v) / s)), -127), 127)) for v in vals], s
+
+
+def _brute_expert_exact(u, ex):
+    """Plain loops of the act_bits=8 expert: each linear takes the bf16 value
+    of its input, quantises it per row to int8, sums integer products per
+    32-column group, and scales by the group scale and the row scale."""
+    def lin(vec, packed, scale):
+        q, sx = _brute_q8(O.round_bf16(np.array(vec, dtype=np.float64)).tolist())
+        N, K8 = packed.shape
+        out = []
+        for n in range(N):
+            acc = 0.0
+            for g in range(K8 * 8 // 32):
+                P = 0
+                for c in range(32 * g, 32 * g + 32):
+                    code = (int(packed[n, c // 8]) & 0xFFFFFFFF) >> (4 * (c % 8)) & 0xF
+                    P += q[c] * (code - 16 if code >= 8 else code)
+                acc += float(O.bf16_bits_to_f64(scale[n, g])) * P
+            out.append(float(sx) * acc)
+        return out
+    g = lin(u, ex["gate_packed"], ex["gate_scale"])
+    up = lin(u, ex["up_packed"], ex["up_scale"])
+    h = [gv / (1.0 + math.exp(-gv)) * uv for gv, uv in zip(g, up)]
+    return lin(h, ex["down_packed"], ex["down_scale"])
+
+
+def test_exact_expert_matches_brute_force_loops():
+    # u is not bf16-valued (as after the latent projection): both the input
+    # and h are rounded to bf16 before their int8 quantisation
+    ex = _random_expert(64, 32)
+    u = RNG.normal(size=(3, 64))
+    y = O.expert_ffn(u, ex, 8)
+    for r in range(3):
+        assert np.allclose(y[r], _brute_expert_exact(u[r], ex), rtol=1e-12, atol=1e-12)
+
+
 def test_expert_closed_form_swiglu():
     # u = 1, every gate/up weight 1 * 2^-5 over 32 inputs -> G = U = 1;
     # down weights 1 * 2^-5 over 32 hidden -> y = SiLU(1) * 1 = 1 / (1 + e^-1).
@@ -436,6 +502,23 @@ def test_latent_identity_projections_reduce_to_rmsnorm_of_moe():
     p_plain = O.LayerParams(k=p.k, renorm=p.renorm, act_bits=16, w_router=p.w_router, bias=p.bias,
                             expert=p.expert, E=p.E)
     want = O.rmsnorm(O.moe_forward(x, p_plain), gain, p.eps)
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_latent_norm_precedes_up_projection():
+    # down = I and up = 2 I (2.0 is exact in bf16): out = 2 RMSNorm(moe(x)).
+    # Normalising after the up-projection would give RMSNorm(2 moe(x)) = RMSNorm(moe(x)).
+    D = 64
+    eye = np.where(np.eye(D) > 0, ONE, 0).astype(np.uint16)
+    two = np.where(np.eye(D) > 0, 0x4000, 0).astype(np.uint16)
+    gain = np.full(D, ONE, np.uint16)
+    p = _small_params(latent=(eye, gain, two))
+    x = O.round_bf16(RNG.normal(size=(3, D)))
+    y = O.moe_forward(x, p)
+    p_plain = O.LayerParams(k=p.k, renorm=p.renorm, act_bits=16, w_router=p.w_router, bias=p.bias,
+                            expert=p.expert, E=p.E)
+    m = O.moe_forward(x, p_plain)
+    want = 2.0 * m / np.sqrt(np.mean(m * m, axis=1, keepdims=True) + p.eps)
     assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
 
 
@@ -542,3 +625,30 @@ def test_shared_expert_hidden_order_and_down_scaling():
     # doubling the down weights (exact in bf16) doubles the output exactly
     d2 = O.f32_to_bf16_bits(2 * O.bf16_bits_to_f64(down).astype(np.float32))
     assert np.array_equal(O.shared_expert(x, gate, up, d2), 2 * ref)
+
+
+def test_layer_adds_the_shared_expert_on_the_full_width_input():
+    # Latent layer (H = 8 -> L = 32) with a shared expert on the full width H.
+    H, L, Is = 8, 32, 16
+    rng = np.random.default_rng(11)
+    bits = lambda a: O.f32_to_bf16_bits(a.astype(np.float32))
+    down = np.zeros((L, H), np.uint16)
+    down[np.arange(L), np.arange(L) % H] = ONE
+    up = bits(rng.normal(size=(H, L)) * 0.1)
+    p = _small_params(D=L, latent=(down, np.full(L, ONE, np.uint16), up))
+    p.w_router = rng.normal(size=(p.E, H)) * 0.2
+    sg, su, sd = (bits(rng.normal(size=s) * 0.2) for s in [(Is, H), (Is, H), (H, Is)])
+    x = O.round_bf16(rng.normal(size=(4, H)))
+    routed = O.moe_forward(x, p)
+    shared = O.shared_expert(x, sg, su, sd)
+    assert np.abs(routed).max() > 0 and np.abs(shared).max() > 0
+    p.shared_gate, p.shared_up, p.shared_down = sg, su, sd
+    # a shared expert with zero down weights changes nothing
+    p.shared_down = np.zeros_like(sd)
+    assert np.array_equal(O.moe_forward(x, p), routed)
+    # routed experts with zero codes leave exactly the shared expert
+    p.shared_down = sd
+    zero = {key: (np.zeros_like(v) if key.endswith("_packed") else v) for key, v in p.expert(0).items()}
+    p.expert = lambda e: zero
+    assert np.array_equal(O.moe_forward(x, p), shared)
+    assert np.array_equal(O.moe_forward_sorted(x, p).out, shared)
