@@ -132,25 +132,62 @@ def _ws(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def _dev(t: torch.Tensor, dtype=None) -> None:
-    if not t.is_cuda:
-        raise ValueError("tensor must live on a CUDA device")
-    if not t.is_contiguous():
-        raise ValueError("tensor must be contiguous")
+def _arg(name: str, t: Optional[torch.Tensor], shape=None, dtype=None) -> torch.Tensor:
+    """Check one tensor argument against the layout its C entry point reads
+    (``include/moe.h``) before its pointer is passed on: the library trusts
+    the sizes it is given, so a short or strided buffer would be read or
+    written out of bounds.  ``shape`` entries of None match any size.  Only
+    metadata is checked here; ``_placed`` checks where the tensors live."""
+    if t is None:
+        raise ValueError(f"{name} is required")
     if dtype is not None and t.dtype != dtype:
-        raise ValueError(f"expected {dtype}, got {t.dtype}")
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and (t.dim() != len(shape) or any(
+            want is not None and int(got) != int(want) for got, want in zip(t.shape, shape))):
+        want = tuple("*" if w is None else int(w) for w in shape)
+        raise ValueError(f"{name}: expected shape {want}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _placed(**tensors: Optional[torch.Tensor]) -> torch.device:
+    """Every given tensor (None skipped) lives on the current CUDA device, the
+    one whose stream the call is enqueued on; returns that device."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must live on a CUDA device")
+        if dev is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}; the call runs on {dev}")
+    return dev
+
+
+EXPERT_NAMES = ("gate_packed", "gate_scale", "up_packed", "up_scale", "down_packed", "down_scale")
+
+
+def _experts(experts: Dict[str, torch.Tensor], E: int, D: int, I: int) -> None:
+    """Gate/up [E, I, D/8] + [E, I, D/32]; down [E, D, I/8] + [E, D, I/32]."""
+    for proj, (N, K) in (("gate", (I, D)), ("up", (I, D)), ("down", (D, I))):
+        _arg(f"{proj}_packed", experts.get(f"{proj}_packed"), (E, N, K // 8), torch.int32)
+        _arg(f"{proj}_scale", experts.get(f"{proj}_scale"), (E, N, K // 32), torch.bfloat16)
 
 
 # ------------------------------------------------------------------ stages
 
 def route(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor, k: int, renorm: bool = True):
     """topk_idx int32 [T, k], topk_w fp32 [T, k] for bf16 x [T, H]."""
-    _dev(x, torch.bfloat16); _dev(w_router, torch.float32); _dev(bias, torch.float32)
-    T, H = x.shape
-    E = w_router.shape[0]
-    idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
-    w = torch.empty(T, k, dtype=torch.float32, device=x.device)
-    ws = _ws(lib.moe_route_workspace_size(T, H, E), x.device)
+    T, H = _arg("x", x, (None, None), torch.bfloat16).shape
+    E = _arg("w_router", w_router, (None, H), torch.float32).shape[0]
+    _arg("bias", bias, (E,), torch.float32)
+    dev = _placed(x=x, w_router=w_router, bias=bias)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    ws = _ws(lib.moe_route_workspace_size(T, H, E), dev)
     _check("moe_route", lib.moe_route(_p(x), _p(w_router), _p(bias), T, H, E, k, int(renorm),
                                       _p(idx), _p(w), _p(ws), ws.numel(), _stream()))
     return idx, w
@@ -170,15 +207,19 @@ def _dispatch_out(T: int, k: int, D: int, E: int, act_bits: int, pairs: bool, de
     }
 
 
+def _dispatch_args(topk_idx: torch.Tensor, x: torch.Tensor):
+    """T, k, D and the device of topk_idx int32 [T, k] and x bf16 [T, D]."""
+    T, k = _arg("topk_idx", topk_idx, (None, None), torch.int32).shape
+    D = _arg("x", x, (T, None), torch.bfloat16).shape[1]
+    return T, k, D, _placed(topk_idx=topk_idx, x=x)
+
+
 def dispatch(topk_idx: torch.Tensor, x: torch.Tensor, E: int, act_bits: int = 16,
              pairs: bool = False) -> Dict[str, torch.Tensor]:
     """Counts, offsets, the stable expert-major permutation and the gathered
     rows (pairs=True: moe_dispatch_pairs, rows in the expert kernels' pair
     order, fp16 or int8)."""
-    _dev(topk_idx, torch.int32); _dev(x, torch.bfloat16)
-    T, k = topk_idx.shape
-    D = x.shape[1]
-    dev = x.device
+    T, k, D, dev = _dispatch_args(topk_idx, x)
     out = _dispatch_out(T, k, D, E, act_bits, pairs, dev)
     ws = _ws(lib.moe_dispatch_workspace_size(T, E, k), dev)
     name = "moe_dispatch_pairs" if pairs else "moe_dispatch"
@@ -194,10 +235,7 @@ def dispatch_noalloc(topk_idx: torch.Tensor, x: torch.Tensor, E: int,
     """moe_dispatch without a workspace: the library's fixed device scratch is
     used instead (for callers that cannot allocate device memory; calls must
     not overlap on the GPU)."""
-    _dev(topk_idx, torch.int32); _dev(x, torch.bfloat16)
-    T, k = topk_idx.shape
-    D = x.shape[1]
-    dev = x.device
+    T, k, D, dev = _dispatch_args(topk_idx, x)
     out = _dispatch_out(T, k, D, E, act_bits, False, dev)
     _check("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
         _p(topk_idx), _p(x), T, D, E, k, act_bits, _p(out["counts"]), _p(out["offsets"]),
@@ -206,17 +244,33 @@ def dispatch_noalloc(topk_idx: torch.Tensor, x: torch.Tensor, E: int,
     return out
 
 
+def _rows_args(x: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.Tensor,
+               act_bits: int, dtype16, E: int) -> Optional[torch.Tensor]:
+    """Expert-sorted rows x (int8 with act_bits 8, else ``dtype16``), their
+    fp32 scales (act_bits 8 only; returned, None otherwise) and the E + 1
+    segment offsets."""
+    rows = _arg("x", x, (None, None), torch.int8 if act_bits == 8 else dtype16).shape[0]
+    _arg("offsets", offsets, (E + 1,), torch.int32)
+    if act_bits != 8:
+        return None
+    return _arg("x_scale", x_scale, (rows,), torch.float32)
+
+
 def expert_ffn(x_sorted: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.Tensor,
                experts: Dict[str, torch.Tensor], act_bits: int = 16,
                pairs: bool = False) -> torch.Tensor:
     """y_sorted bf16 [rows, D] = down(SiLU(gate(x)) * up(x)) per expert segment
     (pairs=True: moe_expert_ffn_pairs on rows from dispatch(..., pairs=True))."""
-    _dev(x_sorted); _dev(offsets, torch.int32)
+    E, I = _arg("gate_packed", experts.get("gate_packed"), (None, None, None), torch.int32).shape[:2]
+    x_scale = _rows_args(x_sorted, x_scale, offsets, act_bits,
+                         torch.float16 if pairs else torch.bfloat16, E)
     rows, D = x_sorted.shape
-    E, I = experts["gate_packed"].shape[0], experts["gate_packed"].shape[1]
-    y = torch.empty(rows, D, dtype=torch.bfloat16, device=x_sorted.device)
+    _experts(experts, E, D, I)
+    dev = _placed(x_sorted=x_sorted, x_scale=x_scale, offsets=offsets,
+                  **{n: experts[n] for n in EXPERT_NAMES})
+    y = torch.empty(rows, D, dtype=torch.bfloat16, device=dev)
     name = "moe_expert_ffn_pairs" if pairs else "moe_expert_ffn"
-    ws = _ws(getattr(lib, name + "_workspace_size")(E, D, I, rows, act_bits), x_sorted.device)
+    ws = _ws(getattr(lib, name + "_workspace_size")(E, D, I, rows, act_bits), dev)
     _check(name, getattr(lib, name)(
         _p(x_sorted), _p(x_scale), _p(offsets), E, D, I, rows,
         _p(experts["gate_packed"]), _p(experts["gate_scale"]), _p(experts["up_packed"]),
@@ -228,11 +282,14 @@ def expert_ffn(x_sorted: torch.Tensor, x_scale: Optional[torch.Tensor], offsets:
 def int4_linear(x: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.Tensor,
                 w_packed: torch.Tensor, w_scale: torch.Tensor, act_bits: int = 16) -> torch.Tensor:
     """fp32 [rows, N] = x W_e^T per expert segment (one grouped PackedInt4Linear)."""
-    _dev(x); _dev(offsets, torch.int32); _dev(w_packed, torch.int32)
+    E, N = _arg("w_packed", w_packed, (None, None, None), torch.int32).shape[:2]
+    x_scale = _rows_args(x, x_scale, offsets, act_bits, torch.bfloat16, E)
     rows, K = x.shape
-    E, N = w_packed.shape[0], w_packed.shape[1]
-    out = torch.empty(rows, N, dtype=torch.float32, device=x.device)
-    ws = _ws(lib.moe_int4_linear_workspace_size(E, K, rows), x.device)
+    _arg("w_packed", w_packed, (E, N, K // 8), torch.int32)
+    _arg("w_scale", w_scale, (E, N, K // 32), torch.bfloat16)
+    dev = _placed(x=x, x_scale=x_scale, offsets=offsets, w_packed=w_packed, w_scale=w_scale)
+    out = torch.empty(rows, N, dtype=torch.float32, device=dev)
+    ws = _ws(lib.moe_int4_linear_workspace_size(E, K, rows), dev)
     _check("moe_int4_linear", lib.moe_int4_linear(
         _p(x), _p(x_scale), _p(offsets), E, K, N, rows, _p(w_packed), _p(w_scale), act_bits,
         _p(out), _p(ws), ws.numel(), _stream()))
@@ -241,21 +298,23 @@ def int4_linear(x: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch
 
 def quantize_rows(v: torch.Tensor):
     """Per-row int8 quantisation: (q int8 [R, C], scale fp32 [R])."""
-    _dev(v, torch.bfloat16)
-    R, C = v.shape
-    q = torch.empty(R, C, dtype=torch.int8, device=v.device)
-    s = torch.empty(R, dtype=torch.float32, device=v.device)
+    R, C = _arg("v", v, (None, None), torch.bfloat16).shape
+    dev = _placed(v=v)
+    q = torch.empty(R, C, dtype=torch.int8, device=dev)
+    s = torch.empty(R, dtype=torch.float32, device=dev)
     _check("moe_quantize_rows", lib.moe_quantize_rows(_p(v), R, C, _p(q), _p(s), _stream()))
     return q, s
 
 
 def quantize_int4(w: torch.Tensor):
     """bf16 weight [..., N, K] -> (packed int32 [..., N, K/8], bf16 scale [..., N, K/32])."""
-    _dev(w, torch.bfloat16)
+    if _arg("w", w, None, torch.bfloat16).dim() < 1:
+        raise ValueError("w: expected at least one dimension")
+    dev = _placed(w=w)
     K = w.shape[-1]
     rows = w.numel() // K if K else 0
-    packed = torch.empty(*w.shape[:-1], K // 8, dtype=torch.int32, device=w.device)
-    scale = torch.empty(*w.shape[:-1], K // 32, dtype=torch.bfloat16, device=w.device)
+    packed = torch.empty(*w.shape[:-1], K // 8, dtype=torch.int32, device=dev)
+    scale = torch.empty(*w.shape[:-1], K // 32, dtype=torch.bfloat16, device=dev)
     _check("moe_quantize_int4", lib.moe_quantize_int4(_p(w), rows, K, _p(packed), _p(scale),
                                                       _stream()))
     return packed, scale
@@ -265,14 +324,17 @@ def shared_expert(x: torch.Tensor, gate_w: torch.Tensor, up_w: torch.Tensor,
                   down_w: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """out (+)= down(SiLU(gate x) * up x) with bf16 weights; a new output when
     ``out`` is None, else added to it in place."""
-    for t in (x, gate_w, up_w, down_w):
-        _dev(t, torch.bfloat16)
-    T, H = x.shape
-    I = gate_w.shape[0]
+    T, H = _arg("x", x, (None, None), torch.bfloat16).shape
+    I = _arg("gate_w", gate_w, (None, H), torch.bfloat16).shape[0]
+    _arg("up_w", up_w, (I, H), torch.bfloat16)
+    _arg("down_w", down_w, (H, I), torch.bfloat16)
     acc = out is not None
-    if out is None:
-        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
-    ws = _ws(lib.moe_shared_expert_workspace_size(T, H, I), x.device)
+    if acc:
+        _arg("out", out, (T, H), torch.bfloat16)
+    dev = _placed(x=x, gate_w=gate_w, up_w=up_w, down_w=down_w, out=out)
+    if not acc:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws = _ws(lib.moe_shared_expert_workspace_size(T, H, I), dev)
     _check("moe_shared_expert", lib.moe_shared_expert(
         _p(x), T, H, I, _p(gate_w), _p(up_w), _p(down_w), int(acc), _p(out), _p(ws), ws.numel(),
         _stream()))
@@ -280,27 +342,33 @@ def shared_expert(x: torch.Tensor, gate_w: torch.Tensor, up_w: torch.Tensor,
 
 
 def combine(y_sorted: torch.Tensor, inv_row: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:
-    _dev(y_sorted, torch.bfloat16); _dev(inv_row, torch.int32); _dev(topk_w, torch.float32)
-    T, k = topk_w.shape
-    D = y_sorted.shape[1]
-    out = torch.empty(T, D, dtype=torch.bfloat16, device=y_sorted.device)
+    """out bf16 [T, D] = sum over the k slots of topk_w * y_sorted[inv_row]."""
+    T, k = _arg("topk_w", topk_w, (None, None), torch.float32).shape
+    D = _arg("y_sorted", y_sorted, (T * k, None), torch.bfloat16).shape[1]
+    if _arg("inv_row", inv_row, None, torch.int32).numel() != T * k:
+        raise ValueError(f"inv_row: expected {T * k} entries, got {inv_row.numel()}")
+    dev = _placed(y_sorted=y_sorted, inv_row=inv_row, topk_w=topk_w)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
     _check("moe_combine", lib.moe_combine(_p(y_sorted), _p(inv_row), _p(topk_w), T, D, k, _p(out),
                                           _stream()))
     return out
 
 
 def linear_bf16(x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
-    _dev(x, torch.bfloat16); _dev(w, torch.bfloat16)
-    M, K = x.shape
-    N = w.shape[0]
-    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    """y bf16 [M, N] = x [M, K] w^T, w bf16 [N, K]."""
+    M, K = _arg("x", x, (None, None), torch.bfloat16).shape
+    N = _arg("w", w, (None, K), torch.bfloat16).shape[0]
+    dev = _placed(x=x, w=w)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     _check("moe_linear_bf16", lib.moe_linear_bf16(_p(x), _p(w), M, N, K, _p(y), _stream()))
     return y
 
 
 def rmsnorm(x: torch.Tensor, gain: torch.Tensor, eps: float) -> torch.Tensor:
-    _dev(x, torch.bfloat16); _dev(gain, torch.bfloat16)
-    M, N = x.shape
+    """Row-wise RMSNorm of bf16 x [M, N] with bf16 gain [N]."""
+    M, N = _arg("x", x, (None, None), torch.bfloat16).shape
+    _arg("gain", gain, (N,), torch.bfloat16)
+    _placed(x=x, gain=gain)
     y = torch.empty_like(x)
     _check("moe_rmsnorm", lib.moe_rmsnorm(_p(x), _p(gain), M, N, float(eps), _p(y), _stream()))
     return y
@@ -325,15 +393,19 @@ class MoeLayer:
                  I_shared: int = 0):
         self.cfg = MoeConfig(T, H, E, k, I, L, act_bits, int(renorm), eps, I_shared)
         self.weights = weights
-        self.device = weights["router_w"].device
-        for name, t in weights.items():
-            if t is not None:
-                _dev(t)
+        _check_layer_weights(weights, H, E, I, L, I_shared)
+        self.device = _placed(**{n: t for n, t in weights.items() if t is not None})
         self.wstruct = MoeWeights(*[_p(weights.get(n)) for n, _ in MoeWeights._fields_])
         self.ws = _ws(lib.moe_workspace_size(ctypes.byref(self.cfg)), self.device)
 
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        _dev(x, torch.bfloat16)
+        shape = (self.cfg.T, self.cfg.H)
+        _arg("x", x, shape, torch.bfloat16)
+        if out is not None:
+            _arg("out", out, shape, torch.bfloat16)
+        dev = _placed(x=x, out=out)
+        if dev != self.device:
+            raise ValueError(f"x is on {dev}; the layer's weights are on {self.device}")
         if out is None:
             out = torch.empty_like(x)
         _check("moe_layer_forward", lib.moe_layer_forward(
@@ -343,8 +415,32 @@ class MoeLayer:
 
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor) -> None:
         """x_host / out_host: CPU bf16 [T, H] (pinned for asynchronous copies)."""
-        if x_host.is_cuda or out_host.is_cuda:
-            raise ValueError("forward_host takes host tensors")
+        shape = (self.cfg.T, self.cfg.H)
+        for name, t in (("x_host", x_host), ("out_host", out_host)):
+            if _arg(name, t, shape, torch.bfloat16).is_cuda:
+                raise ValueError(f"{name} must be a host tensor")
         _check("moe_layer_forward_host", lib.moe_layer_forward_host(
             ctypes.byref(self.cfg), ctypes.byref(self.wstruct), _p(x_host), _p(out_host),
             _p(self.ws), self.ws.numel(), _stream()))
+
+
+def _check_layer_weights(w: Dict[str, torch.Tensor], H: int, E: int, I: int, L: int,
+                         I_shared: int) -> None:
+    """Every pointer of moe_weights against the layout the configuration
+    implies (the experts read the latent width L when L > 0)."""
+    bf16 = torch.bfloat16
+    extra = set(w) - {n for n, _ in MoeWeights._fields_}
+    if extra:
+        raise ValueError(f"unknown weight names: {sorted(extra)}")
+    _arg("router_w", w.get("router_w"), (E, H), torch.float32)
+    _arg("router_bias", w.get("router_bias"), (E,), torch.float32)
+    _experts(w, E, L if L else H, I)
+    if L:
+        _arg("lat_down", w.get("lat_down"), (L, H), bf16)
+        _arg("lat_up", w.get("lat_up"), (H, L), bf16)
+        if w.get("lat_norm") is not None:
+            _arg("lat_norm", w["lat_norm"], (L,), bf16)
+    if I_shared:
+        _arg("shared_gate", w.get("shared_gate"), (I_shared, H), bf16)
+        _arg("shared_up", w.get("shared_up"), (I_shared, H), bf16)
+        _arg("shared_down", w.get("shared_down"), (H, I_shared), bf16)
