@@ -42,6 +42,10 @@ SMALL = {
                                 act_bits=8),
     "small_latent": wl.workload("tiny", name="small_latent", T=50, H=512, L=256, E=16, k=4,
                                 I=128, seed=9, norm_gain_std=0.1),
+    # exact mode on the latent width: the int8 rows are the bf16 latent
+    # projection's, and the expert outputs stay fp32 into the RMSNorm
+    "small_latent_exact": wl.workload("tiny", name="small_latent_exact", T=50, H=512, L=256,
+                                      E=16, k=4, I=128, seed=9, norm_gain_std=0.1, act_bits=8),
     "small_adversarial": wl.workload("tiny", name="small_adv", T=60, H=512, E=16, k=4, I=192,
                                      seed=10, act_bits=8, routing="adversarial"),
     "one_token": wl.workload("tiny", name="one", T=1, H=256, E=8, k=2, I=128, seed=12),
@@ -49,6 +53,8 @@ SMALL = {
     "no_renorm": wl.workload("tiny", name="nr", T=40, H=256, E=24, k=3, I=64, renorm=False, seed=6),
     # the library's limits: 2048 experts, top-32
     "max_E_k": wl.workload("tiny", name="max_E_k", T=20, H=256, E=2048, k=32, I=64, seed=21),
+    "max_E_k_exact": wl.workload("tiny", name="max_E_k_exact", T=20, H=256, E=2048, k=32, I=64,
+                                 seed=21, act_bits=8),
 }
 
 
@@ -146,7 +152,7 @@ def test_shared_expert_parity(moe, T, H, Is, acc):
     assert_close(got.float().cpu().numpy(), ref, what=f"shared {T}x{H}x{Is}")
 
 
-@pytest.mark.parametrize("case", ["tiny", "small_latent"])
+@pytest.mark.parametrize("case", ["tiny", "small_latent", "tiny_exact", "small_latent_exact"])
 def test_layer_with_shared_expert(moe, case):
     w = SMALL[case]
     Is = 192
@@ -192,3 +198,22 @@ def test_layer_forward_replays_from_a_cuda_graph(moe, case):
     torch.cuda.synchronize()
     assert moe.check_error() == 0
     assert torch.equal(out, ref)
+
+
+def test_layer_rejects_mis_sized_buffers_before_any_launch(moe):
+    w = SMALL["tiny"]
+    layer = _layer(moe, w, device_weights(w, DEV))
+    n0 = moe.launch_count()
+    for x, out in [(torch.zeros(w.T - 1, w.H, dtype=torch.bfloat16, device=DEV), None),
+                   (torch.zeros(w.T, w.H, dtype=torch.bfloat16, device=DEV),
+                    torch.zeros(w.T, w.H // 2, dtype=torch.bfloat16, device=DEV)),
+                   (torch.zeros(w.T, 2 * w.H, dtype=torch.bfloat16, device=DEV)[:, ::2], None),
+                   (torch.zeros(w.T, w.H, dtype=torch.bfloat16), None)]:
+        with pytest.raises(ValueError):
+            layer.forward(x, out)
+    with pytest.raises(ValueError):
+        moe.combine(torch.zeros(w.T * w.k - 1, w.H, dtype=torch.bfloat16, device=DEV),
+                    torch.zeros(w.T * w.k, dtype=torch.int32, device=DEV),
+                    torch.zeros(w.T, w.k, dtype=torch.float32, device=DEV))
+    assert moe.launch_count() == n0
+    assert moe.check_error() == 0
