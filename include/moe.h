@@ -331,6 +331,13 @@ int moe_wait_selftest(int64_t limit_ns, void* stream);
 /* Human-readable name of a status code. */
 const char* moe_status_string(int status);
 
+/* Name of the CUDA runtime error (e.g. "cudaErrorInvalidValue") that last
+ * made a call of this library return MOE_ERR_CUDA on the calling thread, or
+ * "cudaSuccess" when none has.  A MOE_ERR_CUDA from a failed tensor-map
+ * encoding (a driver call) records no runtime error.  Host only; never
+ * synchronises; the returned string is static. */
+const char* moe_last_cuda_error(void);
+
 /* Library version string. */
 const char* moe_version(void);
 

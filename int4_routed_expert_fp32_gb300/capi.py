@@ -27,7 +27,10 @@ MOE_ERR_TIMEOUT = -5
 
 class MoeError(RuntimeError):
     def __init__(self, name: str, code: int):
-        super().__init__(f"{name} returned {code} ({status_string(code)})")
+        what = status_string(code)
+        if code == MOE_ERR_CUDA:
+            what += f": {last_cuda_error()}"
+        super().__init__(f"{name} returned {code} ({what})")
         self.code = code
 
 
@@ -86,6 +89,7 @@ SIGNATURES = {
     "moe_check_error": (c_int, [c_void_p]),
     "moe_wait_selftest": (c_int, [c_int64, c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [c_int]),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_version": (ctypes.c_char_p, []),
     "moe_launch_count": (ctypes.c_uint64, []),
 }
@@ -108,6 +112,11 @@ lib = _load()
 
 def status_string(code: int) -> str:
     return lib.moe_status_string(code).decode()
+
+
+def last_cuda_error() -> str:
+    """Name of the CUDA runtime error behind this thread's last MOE_ERR_CUDA."""
+    return lib.moe_last_cuda_error().decode()
 
 
 def launch_count() -> int:

@@ -28,12 +28,21 @@ int current_device() {
 }  // namespace
 
 int* status_word() {
-  int d = current_device();
-  if (d < 0) return nullptr;
+  int d = 0;
+  const cudaError_t ed = cudaGetDevice(&d);
+  if (ed != cudaSuccess) {
+    note_cuda_error(ed);
+    return nullptr;
+  }
+  if (d < 0 || d >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_status_ptr[d]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      return nullptr;
+    }
     g_status_ptr[d] = static_cast<int*>(p);
   }
   return g_status_ptr[d];
@@ -141,6 +150,8 @@ const char* moe_status_string(int status) {
     default: return "MOE_ERR_UNKNOWN";
   }
 }
+
+const char* moe_last_cuda_error(void) { return cudaGetErrorName(moe::g_last_cuda_error); }
 
 const char* moe_version(void) { return "int4-routed-moe sm_103a 0.1"; }
 

@@ -108,3 +108,21 @@ def test_workspace_too_small_is_reported(capi):
     fake = ctypes.c_void_p(0x10000)
     rc = capi.lib.moe_route(fake, fake, fake, 4, 64, 8, 2, 1, fake, fake, fake, 16, None)
     assert rc == capi.MOE_ERR_WORKSPACE
+
+
+def test_last_cuda_error_is_named_per_thread(capi):
+    import threading
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a usable CUDA device")
+    # without a device the runtime refuses the synchronisation: MOE_ERR_CUDA,
+    # and the runtime error behind it is named for this thread only
+    assert capi.lib.moe_check_error(None) == capi.MOE_ERR_CUDA
+    name = capi.last_cuda_error()
+    assert name.startswith("cudaError") and name != "cudaSuccess"
+    assert name in str(capi.MoeError("moe_check_error", capi.MOE_ERR_CUDA))
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(capi.last_cuda_error()))
+    t.start()
+    t.join()
+    assert seen == ["cudaSuccess"]
