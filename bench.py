@@ -452,7 +452,7 @@ def _report(args, rank, world, w, value, ms, roof, cpu, e2e, clocks, launches):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8" if w.act_bits == 8 else "bf16", "data": "synthetic",
+            "dtype": "f16", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
                        "L": w.L, "act_bits": w.act_bits, "weights": "int4 g32 bf16 scales",
                        "l2": l2,
