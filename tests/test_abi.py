@@ -126,3 +126,30 @@ def test_last_cuda_error_is_named_per_thread(capi):
     t.start()
     t.join()
     assert seen == ["cudaSuccess"]
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """A copy of the package without libmoe.so imports, but its first use of
+    any binding name raises ImportError: there is no CPU fallback."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "int4_routed_expert_fp32_gb300")
+    dst = tmp_path / "int4_routed_expert_fp32_gb300"
+    dst.mkdir()
+    for name in os.listdir(src):
+        if name.endswith(".py"):
+            shutil.copy(os.path.join(src, name), dst / name)
+    code = (
+        "import int4_routed_expert_fp32_gb300 as m\n"
+        "for name in ('MoeLayer', 'route', 'expert_ffn', 'lib'):\n"
+        "    try:\n"
+        "        getattr(m, name)\n"
+        "    except ImportError as e:\n"
+        "        assert 'libmoe.so is missing' in str(e), e\n"
+        "    else:\n"
+        "        raise SystemExit(name + ' did not fail')\n"
+        "print('ok')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True,
+                       env={**os.environ, "PYTHONPATH": str(tmp_path)}, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
