@@ -184,6 +184,7 @@ using namespace moe;
 
 extern "C" int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, const float* topk_w,
                            int T, int D, int k, uint16_t* out, void* stream) {
+  moe::Range range_("moe_combine");
   if (T < 0 || D <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (D % 64 != 0 || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
@@ -195,6 +196,7 @@ extern "C" int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, con
 
 extern "C" int moe_rmsnorm(const uint16_t* x, const uint16_t* gain, int M, int N, float eps,
                            uint16_t* y, void* stream) {
+  moe::Range range_("moe_rmsnorm");
   if (M < 0 || N <= 0 || !(eps >= 0.f)) return MOE_ERR_INVALID;
   if (N % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (M == 0) return MOE_OK;

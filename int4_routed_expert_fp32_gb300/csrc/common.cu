@@ -115,6 +115,7 @@ __global__ void wait_selftest_kernel(int64_t limit_ns, int* status) {
 extern "C" {
 
 int moe_check_error(void* stream) {
+  moe::Range range_("moe_check_error");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
@@ -131,6 +132,7 @@ int moe_check_error(void* stream) {
 }
 
 int moe_wait_selftest(int64_t limit_ns, void* stream) {
+  moe::Range range_("moe_wait_selftest");
   if (limit_ns < 1000 || limit_ns > 5000000000LL) return MOE_ERR_INVALID;
   int* w = moe::status_word();
   if (!w) return MOE_ERR_CUDA;

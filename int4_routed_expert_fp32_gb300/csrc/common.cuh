@@ -9,6 +9,13 @@
 
 #include "../../include/moe.h"
 
+#if defined(__has_include)
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+#define MOE_HAVE_NVTX 1
+#endif
+#endif
+
 namespace moe {
 
 constexpr int kGroup = 32;          // columns per weight scale
@@ -28,6 +35,28 @@ void note_cuda_error(cudaError_t e);
 void count_launch();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Names a stretch of host code (one C-ABI call, or one stage of the layer) in
+// a profiler's timeline: an NVTX range on the calling thread, open for the
+// object's lifetime.  Without an attached tool NVTX calls return at once;
+// without the NVTX headers this is empty.
+class Range {
+ public:
+  explicit Range(const char* name) {
+#ifdef MOE_HAVE_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~Range() {
+#ifdef MOE_HAVE_NVTX
+    nvtxRangePop();
+#endif
+  }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 
 // Pair order of the activation rows the expert kernels read and write: in
 // every block of 8 columns, column j (j < 4) sits at position 2j and column

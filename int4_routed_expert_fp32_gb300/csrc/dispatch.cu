@@ -382,6 +382,7 @@ extern "C" int moe_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, i
                             int act_bits, int32_t* counts, int32_t* offsets, int32_t* row_token,
                             int32_t* row_slot, int32_t* inv_row, void* x_sorted, float* x_scale,
                             void* ws, size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_dispatch");
   if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
@@ -410,6 +411,7 @@ extern "C" int moe_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, in
                                   int32_t* row_token, int32_t* row_slot, int32_t* inv_row,
                                   void* x_sorted, float* x_scale, void* ws, size_t ws_bytes,
                                   void* stream) {
+  moe::Range range_("moe_dispatch_pairs");
   if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
@@ -428,6 +430,7 @@ extern "C" int moe_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, in
 
 extern "C" int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale,
                                  void* stream) {
+  moe::Range range_("moe_quantize_rows");
   if (R < 0 || C <= 0) return MOE_ERR_INVALID;
   if (C % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (R == 0) return MOE_OK;
@@ -439,6 +442,7 @@ extern "C" int moe_dispatch_noalloc(const int32_t* topk_idx, const uint16_t* x, 
                                     int k, int act_bits, int32_t* counts, int32_t* offsets,
                                     int32_t* row_token, int32_t* row_slot, int32_t* inv_row,
                                     void* x_sorted, float* x_scale, void* stream) {
+  moe::Range range_("moe_dispatch_noalloc");
   if (T < 0 || D <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (D % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;

@@ -200,6 +200,7 @@ using namespace moe;
 
 extern "C" int moe_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K,
                                uint16_t* y, void* stream) {
+  moe::Range range_("moe_linear_bf16");
   if (M < 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID;
   if (K % 32 != 0 || N % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (M == 0) return MOE_OK;

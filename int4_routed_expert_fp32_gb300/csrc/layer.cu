@@ -114,25 +114,37 @@ static int routed(const moe_config& c, const moe_weights& w, const uint16_t* x, 
   if (rc) return rc;
   const uint16_t* u = x;
   if (c.L > 0) {
+    Range r("latent_down");
     rc = launch_linear_bf16(x, w.lat_down, c.T, c.L, c.H, ws.x_lat, s);
     if (rc) return rc;
     u = ws.x_lat;
   }
   // expert-sorted rows in the expert kernels' pair order (fp16 / int8)
-  rc = launch_dispatch_pairs(ws.topk_idx, u, c.T, D, c.E, c.k, c.act_bits, ws.counts, ws.offsets,
-                             ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted, ws.x_scale,
-                             ws.scratch, s);
+  {
+    Range r("dispatch");
+    rc = launch_dispatch_pairs(ws.topk_idx, u, c.T, D, c.E, c.k, c.act_bits, ws.counts,
+                               ws.offsets, ws.row_token, ws.row_slot, ws.inv_row, ws.x_sorted,
+                               ws.x_scale, ws.scratch, s);
+  }
   if (rc) return rc;
-  rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, c.T, w.gate_packed,
-                         w.gate_scale, w.up_packed, w.up_scale, w.down_packed, w.down_scale,
-                         c.act_bits, ws.y_sorted, ws.y_f32, ws.scratch, s);
+  {
+    Range r("expert_ffn");
+    rc = launch_expert_ffn(ws.x_sorted, ws.x_scale, ws.offsets, c.E, D, c.I, R, c.T,
+                           w.gate_packed, w.gate_scale, w.up_packed, w.up_scale, w.down_packed,
+                           w.down_scale, c.act_bits, ws.y_sorted, ws.y_f32, ws.scratch, s);
+  }
   if (rc) return rc;
   if (c.L > 0) {
-    rc = launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.L, c.k, w.lat_norm,
-                        c.eps, ws.comb, s);
+    {
+      Range r("combine_rmsnorm");
+      rc = launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.L, c.k, w.lat_norm,
+                          c.eps, ws.comb, s);
+    }
     if (rc) return rc;
+    Range r("latent_up");
     return launch_linear_bf16(ws.comb, w.lat_up, c.T, c.H, c.L, out, s);
   }
+  Range r("combine");
   return launch_combine(ws.y_sorted, ws.y_f32, ws.inv_row, ws.topk_w, c.T, c.H, c.k, nullptr, 0.f,
                         out, s);
 }
@@ -141,6 +153,7 @@ static int forward(const moe_config& c, const moe_weights& w, const uint16_t* x,
                    const LayerWs& ws, cudaStream_t s) {
   const int rc = routed(c, w, x, out, ws, s);
   if (rc || c.I_shared == 0) return rc;
+  Range r("shared_expert");
   return launch_shared_expert(x, c.T, c.H, c.I_shared, w.shared_gate, w.shared_up, w.shared_down,
                               1, out, ws.scratch, s);
 }
@@ -156,6 +169,7 @@ extern "C" size_t moe_workspace_size(const moe_config* cfg) {
 
 extern "C" int moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
                                  uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_layer_forward");
   int rc = validate(cfg, w);
   if (rc) return rc;
   if (cfg->T == 0) return MOE_OK;
@@ -169,6 +183,7 @@ extern "C" int moe_layer_forward(const moe_config* cfg, const moe_weights* w, co
 extern "C" int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
                                       const uint16_t* x_host, uint16_t* out_host, void* ws,
                                       size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_layer_forward_host");
   int rc = validate(cfg, w);
   if (rc) return rc;
   if (cfg->T == 0) return MOE_OK;

@@ -214,6 +214,7 @@ extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
 extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
                          int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
                          size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_route");
   if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (H % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;

@@ -160,6 +160,7 @@ extern "C" size_t moe_shared_expert_workspace_size(int T, int H, int I) {
 extern "C" int moe_shared_expert(const uint16_t* x, int T, int H, int I, const uint16_t* gate_w,
                                  const uint16_t* up_w, const uint16_t* down_w, int accumulate,
                                  uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_shared_expert");
   if (T < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID;
   if (H % 64 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;

@@ -63,6 +63,7 @@ using namespace moe;
 
 extern "C" int moe_quantize_int4(const uint16_t* w, int N, int K, int32_t* packed,
                                  uint16_t* scale, void* stream) {
+  moe::Range range_("moe_quantize_int4");
   if (N < 0 || K <= 0) return MOE_ERR_INVALID;
   if (K % kGroup != 0) return MOE_ERR_UNSUPPORTED;
   if (N == 0) return MOE_OK;
