@@ -87,6 +87,48 @@ def _profiled_traffic(config: str):
     return None
 
 
+def visible_gpu_id(visible, local_rank: int, current: int) -> str:
+    """The id nvidia-smi knows this rank's GPU by: its entry in
+    CUDA_VISIBLE_DEVICES (an index or a UUID), else the current device."""
+    if visible:
+        ids = [v.strip() for v in visible.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(current)
+
+
+def roofline(w: wl.Workload, ffn_ms: float, active: int, peaks: dict) -> dict:
+    """The expert-FFN call against its binding roofline.
+
+    Algorithmic bytes: the int4 weights and bf16 scales of every active expert
+    once, plus the sorted activation rows read (fp16, or int8 with act_bits 8),
+    h written and read (fp16), and y written (bf16).  Algorithmic flops:
+    2 * rows * 3 * D * I.  The bound is the one their ratio selects against the
+    ridge of the measured HBM and sustained bf16 peaks."""
+    R = w.T * w.k
+    act_bytes = R * w.D * (1 if w.act_bits == 8 else 2) + 2 * R * w.I * 2 + R * w.D * 2
+    alg_bytes = active * expert_bytes(w) + act_bytes
+    flops = 2.0 * R * 3 * w.D * w.I
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / alg_bytes < ridge:
+        achieved = alg_bytes / (ffn_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = flops / (ffn_ms / 1000.0) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    roof.update({"traffic": None,
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_fused_kernel "
+                           "(gate/up + down) for experts of <= 16 rows, ffn_tc_kernel gate/up and "
+                           "down above)",
+                 "kernel_ms": ffn_ms,
+                 "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
+                 "active_experts": active, "peak_source": peaks["source"]})
+    return roof
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -94,8 +136,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id):
+        self.gpu = str(gpu_id)  # an index or a GPU UUID, as nvidia-smi --id takes
         self.proc = None
         self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
 
@@ -357,8 +399,8 @@ def main(argv=None):
     if rc != 0:
         raise RuntimeError(f"device status after warm-up: {moe.status_string(rc)}")
 
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = ClockSampler(visible_gpu_id(os.environ.get("CUDA_VISIBLE_DEVICES"), local,
+                                          torch.cuda.current_device()))
     sampler.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
@@ -382,31 +424,8 @@ def main(argv=None):
 
     # dominant kernel: the expert FFN stream kernels
     ffn_ms, counts = _ffn_pass(moe, w, layer, weights, x_dev, min(args.steps, 100))
-    active = int((counts > 0).sum())
-    R = w.T * w.k
-    act_bytes = R * w.D * (1 if w.act_bits == 8 else 2) + 2 * R * w.I * 2 + R * w.D * 2
-    alg_bytes = active * expert_bytes(w) + act_bytes
-    flops = 2.0 * R * 3 * w.D * w.I
-    peaks = _peaks()
-    # bound: flops per algorithmic byte against the ridge of the two peaks
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    hbm_bound = flops / alg_bytes < ridge
-    if hbm_bound:
-        achieved = alg_bytes / (ffn_ms / 1000.0) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    else:
-        achieved = flops / (ffn_ms / 1000.0) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak}
-    roof.update({"traffic": _profiled_traffic(w.name),
-                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_fused_kernel "
-                           "(gate/up + down) for experts of <= 16 rows, ffn_tc_kernel gate/up and "
-                           "down above)",
-                 "kernel_ms": ffn_ms,
-                 "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
-                 "active_experts": active, "peak_source": peaks["source"]})
+    roof = roofline(w, ffn_ms, int((counts > 0).sum()), _peaks())
+    roof["traffic"] = _profiled_traffic(w.name)
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     e2e = None
