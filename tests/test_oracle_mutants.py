@@ -69,6 +69,16 @@ MUTANTS = [
      'order = np.asarray(r).shape[-1] - 1 - np.argsort(-np.asarray(r)[..., ::-1], axis=-1, kind="stable")'),
     ("gap_off_by_one", "gap taken between the (k-1)-th and k-th scores",
      "srt[:, k - 1] - srt[:, k]", "srt[:, k - 2] - srt[:, k - 1]"),
+    ("gap_k_equals_E", "no gap case when k equals E",
+     "if k >= r.shape[1]:", "if k > r.shape[1]:"),
+    ("renorm_ignores_flag", "renormalisation applied with renorm off",
+     "    if renorm:\n        w = w /", "    if True:\n        w = w /"),
+    ("router_on_latent", "the router fed the latent input",
+     "    rt = route(xs, p.w_router, p.bias, p.k, p.renorm)\n    u = expert_input(xs, p)",
+     "    u = expert_input(xs, p)\n    rt = route(u, p.w_router, p.bias, p.k, p.renorm)"),
+    ("token_subset_ignored", "the token subset ignored",
+     "rows = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)",
+     "rows = np.arange(x.shape[0])"),
     # sorted dispatch
     ("scan_inclusive", "offsets from an inclusive scan",
      "offsets[1:] = np.cumsum(counts)", "offsets[:-1] = np.cumsum(counts)"),
@@ -78,6 +88,10 @@ MUTANTS = [
      "inv_row[order] = np.arange(T * k, dtype=np.int64)", "inv_row[:] = order"),
     ("token_from_remainder", "row token taken as order mod k",
      "row_token=order // k,", "row_token=order % k,"),
+    ("unstable_sort", "an unstable sort of the expert ids",
+     'np.argsort(idx.reshape(-1), kind="stable")', 'np.argsort(idx.reshape(-1), kind="quicksort")'),
+    ("single_row_experts_skipped", "sorted path skipping experts with one row",
+     "        if a == b:\n            continue", "        if b - a < 2:\n            continue"),
     # act_bits = 8 activation quantiser
     ("q8_divisor_128", "activation scale max/128",
      "(amax / np.float32(Q8_MAX))", "(amax / np.float32(128))"),
@@ -85,6 +99,10 @@ MUTANTS = [
      "q = np.rint(v / scale[..., None])", "q = np.trunc(v / scale[..., None])"),
     ("q8_in_float64", "activation quantiser evaluated in float64",
      "v = np.asarray(v, dtype=np.float32)", "v = np.asarray(v, dtype=np.float64)"),
+    ("q8_clip_126", "activation codes clamped to +-126",
+     "q = np.clip(q, -Q8_MAX, Q8_MAX)", "q = np.clip(q, -Q8_MAX + 1, Q8_MAX - 1)"),
+    ("int32_bound_loosened", "accumulator bound checked against 2^32",
+     "if K * 8 * Q8_MAX >= 2 ** 31:", "if K * 8 * Q8_MAX > 2 ** 32:"),
     ("q8_row_scale_dropped", "activation row scale left out of the output",
      "sx.astype(np.float64)[:, None] * np.einsum", "np.einsum"),
     ("partials_group_strided", "weight groups taken as strided columns",
@@ -97,6 +115,10 @@ MUTANTS = [
      "q = np.rint(g / s[..., None])", "q = np.rint(g / (amax / np.float32(Q4_MAX))[..., None])"),
     ("q4_truncate", "weight codes truncated instead of rounded",
      "q = np.rint(g / s[..., None])", "q = np.trunc(g / s[..., None])"),
+    ("q4_zero_group_unguarded", "a zero group divided by its zero scale",
+     "q = np.where(s[..., None] > 0, q, np.float32(0))", "pass"),
+    ("pack_range_unchecked", "out-of-range codes packed silently",
+     "if q.size and (q.min() < -8 or q.max() > 7):", "if False:"),
     # expert
     ("silu_sign", "SiLU written as g * sigmoid(-g)",
      "return np.asarray(g, dtype=np.float64) * sigmoid(g)",
@@ -112,6 +134,8 @@ MUTANTS = [
      "h = round_bf16(silu(g) * u)", "h = silu(g) * u"),
     ("shared_gate_up_swapped", "shared-expert SiLU applied to up",
      "h = round_bf16(silu(g) * u)", "h = round_bf16(g * silu(u))"),
+    ("shared_down_rows_reversed", "shared down projection rows reversed",
+     "return h @ bf16_bits_to_f64(down_bits).T", "return h @ bf16_bits_to_f64(down_bits).T[::-1]"),
     ("shared_never_added", "the shared expert left out of the layer",
      "if p.shared_gate is None:\n        return out", "if True:\n        return out"),
     ("shared_on_expert_input", "the shared expert fed the experts' (latent) input",
@@ -121,6 +145,11 @@ MUTANTS = [
      "v / np.sqrt(ms + eps)", "v / (np.sqrt(ms) + eps)"),
     ("rms_mean_abs", "mean |v| squared instead of the mean square",
      "ms = np.mean(v * v, axis=-1, keepdims=True)", "ms = np.mean(np.abs(v), axis=-1, keepdims=True) ** 2"),
+    ("rms_over_rows", "mean square taken over the rows instead of the features",
+     "ms = np.mean(v * v, axis=-1, keepdims=True)", "ms = np.mean(v * v, axis=0, keepdims=True)"),
+    ("latent_norm_skipped", "the latent RMSNorm left out",
+     "    if p.lat_norm is not None:\n        y = rmsnorm(y, p.lat_norm, p.eps)",
+     "    if False:\n        y = rmsnorm(y, p.lat_norm, p.eps)"),
     ("rms_gain_dropped", "RMSNorm gain left out",
      "np.sqrt(ms + eps) * bf16_bits_to_f64(gain_bits)", "np.sqrt(ms + eps)"),
     ("latent_down_untransposed", "lat_down applied as [H, L]",
@@ -188,7 +217,9 @@ def _failing_pins(src: str, stop_at_first: bool) -> list:
         for name, fn, kwargs in _cases(_pins(mod)):
             try:
                 fn(**kwargs)
-            except Exception as e:  # an assertion, or the mistake breaking a shape
+            # an assertion, the mistake breaking a shape, or a pytest.raises
+            # that saw no exception (pytest's Failed is not an Exception)
+            except (Exception, pytest.fail.Exception) as e:
                 failed.append(f"{name}: {type(e).__name__}")
                 if stop_at_first:
                     break

@@ -462,6 +462,17 @@ def test_sorted_dispatch_equals_per_token_definition(act_bits):
     assert np.allclose(sub, a[[3, 11, 0]], rtol=1e-12, atol=1e-14)
 
 
+def test_sorted_dispatch_with_single_row_and_idle_experts():
+    # 10 rows over 24 experts: most experts hold one row or none, so the
+    # sorted path must neither skip a one-row segment nor touch an empty one
+    p = _small_params(E=24, k=2)
+    x = O.round_bf16(RNG.normal(size=(5, 64)))
+    counts = O.dispatch(O.route(x, p.w_router, p.bias, p.k).idx, p.E).counts
+    assert (counts == 1).any() and (counts == 0).any()
+    a = O.moe_forward(x, p)
+    assert np.allclose(O.moe_forward_sorted(x, p).out, a, rtol=1e-12, atol=1e-12 * np.abs(a).max())
+
+
 def test_single_expert_layer_is_the_textbook_mlp():
     p = _small_params(E=1, k=1)
     x = O.round_bf16(RNG.normal(size=(3, 64)))
