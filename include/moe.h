@@ -302,9 +302,10 @@ int moe_shared_expert(const uint16_t* x, int T, int H, int I, const uint16_t* ga
 /* Workspace bytes of moe_layer_forward / moe_layer_forward_host. */
 size_t moe_workspace_size(const moe_config* cfg);
 
-/* The whole layer (KimiSparseMoeBlock.forward listing without the shared
- * expert): route on x, optional latent down-projection, dispatch, experts,
- * combine (+ RMSNorm and up-projection when cfg->L > 0).
+/* The whole layer (KimiSparseMoeBlock.forward listing): route on x, optional
+ * latent down-projection, dispatch, experts, combine (+ RMSNorm and
+ * up-projection when cfg->L > 0), then, when cfg->I_shared > 0, the shared
+ * expert on x added to the routed output (summed in fp32, one bf16 rounding).
  *   x bf16 [T, H] in, out bf16 [T, H] out.  All intermediates live in ws. */
 int moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
                       uint16_t* out, void* ws, size_t ws_bytes, void* stream);
