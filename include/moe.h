@@ -22,7 +22,12 @@
  *     outputs with their routing weights"; moe_infer listing);
  *   - optional latent wrap: bf16 down-projection, RMSNorm, bf16
  *     up-projection (KimiSparseMoeBlock.forward listing, "Latent
- *     up-projection" section; donor-reference RMSNorm equations).
+ *     up-projection" section; donor-reference RMSNorm equations);
+ *   - optional shared expert: a bf16 gated MLP on the full-width x added to
+ *     the routed output (KimiSparseMoeBlock listing; donor-reference "Add an
+ *     always-active shared expert");
+ *   - weight preparation: bf16 weights to packed int4 with bf16 group-32
+ *     scales (exact-generator page, "The proposed substitution").
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller unless the
