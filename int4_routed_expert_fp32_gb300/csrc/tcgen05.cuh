@@ -34,35 +34,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory writes by threads, made visible to the async proxy (MMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- MMA
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 inputs here).
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M x 16) is read from
-// tensor memory, one row per lane, two 16-bit values per 32-bit column.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// umma_f16 issued by a whole converged warp (see umma_f16_ts_warp).
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16, issued by a whole
+// converged warp (see umma_f16_ts_warp).
 __device__ __forceinline__ void umma_f16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -72,8 +47,10 @@ __device__ __forceinline__ void umma_f16_warp(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-// umma_f16_ts issued by a whole converged warp: the warp computes the
-// (uniform) operands and one lane, elected in the instruction, executes it.
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M x 16) is read from
+// tensor memory, one row per lane, two 16-bit values per 32-bit column.
+// Issued by a whole converged warp: the warp computes the (uniform) operands
+// and one lane, elected in the instruction, executes it.
 // Measured on GB300 (M=128, N=128 MMAs, 8 per K stage of 64, with an mbarrier
 // wait, a tcgen05 fence and two commits per stage): the tensor pipe idles
 // ~220 cycles per stage when one lane runs the loop alone, ~50 when the whole
@@ -88,20 +65,13 @@ __device__ __forceinline__ void umma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
-// Commit issued by a whole converged warp (one elected lane, the same lane
-// as the MMAs above: the lowest active one).
+// Arrive (once) on `bar` when every MMA issued so far by the issuing lane is
+// done; issued by a whole converged warp (one elected lane, the same lane as
+// the MMAs above: the lowest active one).
 __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// Arrive (once) on `bar` when every MMA issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
 }
@@ -180,16 +150,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 // 32 lanes x 16 consecutive columns.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
