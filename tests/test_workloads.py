@@ -97,3 +97,31 @@ def test_prefill_load_is_zipf_with_idle_experts():
     # heavier rank -> larger load, on the head of the distribution
     order = np.argsort(-target)[:10]
     assert np.all(np.diff(counts[order]) < 0)
+
+
+def test_oracle_input_adapters():
+    """oracle.inputs hands the oracle exactly the generator's values."""
+    from oracle import inputs as oi
+    w = wl.workload("tiny", name="adapt", L=128, I=128, norm_gain_std=0.1)
+    x = wl.gen_x(w)
+    assert np.array_equal(O.bf16_bits_to_f64(oi.bf16_bits(x)), oi.x_f64(x))
+    ex = wl.gen_expert(w, 3, "cpu")
+    arr = oi.expert_arrays(w, 3)
+    assert set(arr) == set(ex)
+    for name, t in ex.items():
+        want = oi.bf16_bits(t) if t.dtype == torch.bfloat16 else t.numpy()
+        assert arr[name].dtype == want.dtype and np.array_equal(arr[name], want), name
+    assert np.array_equal(O.unpack_int4(arr["gate_packed"]).shape, (w.I, w.D))
+    # the lazy cache evicts and regenerates the same arrays
+    lazy = oi.LazyExperts(w, keep=2)
+    first = {e: lazy(e)["down_scale"].copy() for e in range(4)}
+    assert len(lazy._cache) == 2
+    for e in range(4):
+        assert np.array_equal(lazy(e)["down_scale"], first[e])
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    p = oi.layer_params(w, router=router, latent=lat)
+    assert (p.k, p.renorm, p.act_bits, p.E, p.eps) == (w.k, w.renorm, w.act_bits, w.E, w.eps)
+    assert np.array_equal(p.w_router, router[0].numpy().astype(np.float64))
+    assert np.array_equal(p.lat_up, oi.bf16_bits(lat["lat_up"])) and p.lat_up.shape == (w.H, w.L)
+    assert p.lat_down.shape == (w.L, w.H) and p.lat_norm.shape == (w.L,)
