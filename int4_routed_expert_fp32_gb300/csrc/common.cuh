@@ -162,23 +162,21 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 }
 
 // Wait for the phase with the given parity to complete, for at most limit_ns.
-// Gives up early, after one round of suspended polls, when another thread has
-// already recorded a status.  On timeout records MOE_ERR_TIMEOUT.  Returns
-// true when the phase completed.  The status word is a global load (an L2
-// round trip), so it is read only after a round of polls: a wait whose phase
-// completes during that round never pays for it.
+// Gives up early when another thread has already recorded a status.  On
+// timeout records MOE_ERR_TIMEOUT.  Returns true when the phase completed.
 // backoff_ns > 0: sleep that long between rounds of polls (for waits that
 // last long, so that the waiting warps leave the issue slots to others).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_t limit_ns,
                                           int* status, uint32_t backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (status_set(status)) return false;  // fail fast once an error is recorded
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_suspend(bar, parity)) return true;
     if (backoff_ns) __nanosleep(backoff_ns);
-    if (status_set(status)) return false;  // fail fast once an error is recorded
+    if (status_set(status)) return false;
     if (static_cast<int64_t>(global_timer_ns() - t0) > limit_ns) {
       record_status(status, MOE_ERR_TIMEOUT);
       return false;
