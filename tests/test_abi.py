@@ -153,3 +153,46 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True,
                        env={**os.environ, "PYTHONPATH": str(tmp_path)}, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_header_is_plain_c_and_links(capi, tmp_path):
+    """include/moe.h compiles as strict C99 and a C program links against
+    libmoe.so and calls it: the entry points that need no GPU answer, and
+    argument errors come back before any CUDA call."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_moe.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+
+int main(void) {
+  moe_config cfg;
+  moe_weights w;
+  memset(&cfg, 0, sizeof cfg);
+  memset(&w, 0, sizeof w);
+  cfg.T = 4; cfg.H = 64; cfg.E = 8; cfg.k = 2; cfg.I = 64; cfg.act_bits = 16; cfg.renorm = 1;
+  if (moe_workspace_size(&cfg) == 0) return 1;
+  if (moe_layer_forward(&cfg, &w, NULL, NULL, NULL, 0, NULL) != MOE_ERR_INVALID) return 2;
+  if (moe_route(NULL, NULL, NULL, 4, 64, 8, 2, 1, NULL, NULL, NULL, 0, NULL) != MOE_ERR_INVALID)
+    return 3;
+  if (strcmp(moe_status_string(MOE_ERR_TIMEOUT), "MOE_ERR_TIMEOUT") != 0) return 4;
+  printf("%s\n", moe_version());
+  return 0;
+}
+''')
+    from int4_routed_expert_fp32_gb300.build import LIB_PATH
+    libdir = os.path.dirname(LIB_PATH)
+    exe = tmp_path / "use_moe"
+    r = subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-l:libmoe.so", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.startswith("int4-routed-moe")
