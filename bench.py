@@ -1,19 +1,22 @@
 """Benchmark of the routed int4 MoE layer (tokens/s per layer and roofline).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill]
+                [--workloads decode,latent,exact] [--impl reference]
 
-One step = one full layer forward (router, dispatch, experts, combine) over one
-batch of seeded synthetic tokens of the named workload, through
-``moe_layer_forward``.  Default workload: one decode step of the K2.5-shaped
-layer (T=32, H=7168, 384 experts, top-8, I=2048, int4 g32).  The expert
-weights read per step (~4.5 GB) are far larger than L2, so no L2 flush is
-needed between steps.
+One step = one full layer forward (router, dispatch, experts, combine, and the
+latent projections on the latent workload) over one batch of seeded synthetic
+tokens, through ``moe_layer_forward``.  The headline workload is prefill: 8192
+tokens through the K2.5-shaped layer (H=7168, 384 experts, top-8, I=2048, int4
+g32) with a Zipf(1.1) expert load.  The same JSON line carries, under
+``workloads``, the decode (T=32), latent (T=2048, L=3584) and exact (act_bits 8,
+T=1024) results, each timed the same way.  Every step reads gigabytes of
+distinct expert weights, far more than L2, so no L2 flush is needed.
 
 For N > 1 (torchrun) every rank runs an independent replica of the layer on its
 own GPU (no data-path collective); value = total tokens / max-over-ranks time.
 
---impl reference times the fp64 CPU oracle on the host cores on a bounded
-sample of the same workload (the oracle is the reference of this build).
+--impl reference times the fp64 CPU oracle on the host cores on bounded
+samples of the same workload (the oracle is the reference of this build).
 """
 from __future__ import annotations
 
@@ -251,9 +254,12 @@ def _ffn_pass(moe, w, layer, weights, x_dev, steps):
 class OracleSampler:
     """The fp64 oracle on the host cores over a fixed token order of the
     workload, one (token, expert slot) pair at a time: the token's routing and
-    expert input when its first slot comes up, one expert's gated MLP per slot
-    (its weights generated for that slot, so every slot pays for its own
-    expert), the latent output after the last slot."""
+    expert input when its first slot comes up, one expert's gated MLP per slot,
+    the latent output after the last slot.
+
+    The expert weights of the pairs about to be timed are generated before the
+    clock starts (``prepare``), so the timed region holds oracle arithmetic
+    only."""
 
     def __init__(self, w: wl.Workload):
         import oracle
@@ -267,44 +273,69 @@ class OracleSampler:
         self.order = np.random.default_rng(0).permutation(w.T)
         self.pair = 0
         self.cur = None
+        self.experts = {}
+
+    def _token(self, pair):
+        return int(self.order[(pair // self.w.k) % self.w.T])
+
+    def prepare(self, n: int):
+        """Generate (untimed) the expert arrays the next n pairs use; keeps
+        only those."""
+        O, w, p = self.O, self.w, self.params
+        need = set()
+        for t in sorted({self._token(i) for i in range(self.pair, self.pair + n)}):
+            need.update(int(e) for e in O.route(self.xf[t:t + 1], p.w_router, p.bias, w.k,
+                                                p.renorm).idx[0])
+        self.experts = {e: self.experts[e] if e in self.experts else self.oi.expert_arrays(w, e)
+                        for e in need}
 
     def _one_pair(self):
         O, w, p = self.O, self.w, self.params
-        i, j = divmod(self.pair, w.k)
-        t = int(self.order[i % w.T])
-        if j == 0:
+        j = self.pair % w.k
+        t = self._token(self.pair)
+        if j == 0 or self.cur is None:
             xt = self.xf[t:t + 1]
             rt = O.route(xt, p.w_router, p.bias, w.k, p.renorm)
             self.cur = (rt, O.expert_input(xt, p), None)
         rt, u, acc = self.cur
-        ex = self.oi.expert_arrays(w, int(rt.idx[0, j]))
-        y = rt.weight[0, j] * O.expert_ffn(u, ex, p.act_bits)
+        y = rt.weight[0, j] * O.expert_ffn(u, self.experts[int(rt.idx[0, j])], p.act_bits)
         acc = y if acc is None else acc + y
         if j == w.k - 1:
             O.latent_out(acc, p)
         self.cur = (rt, u, acc)
         self.pair += 1
 
-    def sample(self, budget_s: float):
-        """Pairs until budget_s has passed (at least one); tokens/s = pairs / k / time."""
+    def run(self, n: int) -> float:
+        """Time exactly n prepared pairs; returns seconds."""
         t0 = time.perf_counter()
-        n = 0
-        while True:
+        for _ in range(n):
             self._one_pair()
-            n += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        dt = time.perf_counter() - t0
-        cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-        return {"value": n / self.w.k / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                "sample": f"{n} (token, expert) pairs = {n / self.w.k:.2f} of {self.w.T} tokens of "
-                          f"the {self.w.name} workload, fp64 oracle per pair (routing, expert "
-                          f"weights generated per pair, gated MLP), {dt:.1f} s"}
+        return time.perf_counter() - t0
+
+    def pairs_for(self, budget_s: float) -> int:
+        """Pairs that take about budget_s (from one untimed calibration pair)."""
+        self.prepare(1)
+        dt = self.run(1)
+        return max(1, int(budget_s / max(dt, 1e-9)))
+
+    def describe(self, n: int, dt: float) -> str:
+        return (f"{n} (token, expert) pairs = {n / self.w.k:.2f} of {self.w.T} tokens of the "
+                f"{self.w.name} workload, fp64 oracle per pair (routing, gated MLP, weighted sum; "
+                f"expert weights generated before timing), {dt:.1f} s")
+
+
+def _cores() -> int:
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
 def _cpu_baseline(w: wl.Workload, budget_s: float = 20.0):
     """A bounded sample of the workload on the oracle (see OracleSampler)."""
-    return OracleSampler(w).sample(budget_s)
+    sampler = OracleSampler(w)
+    n = sampler.pairs_for(budget_s)
+    sampler.prepare(n)
+    dt = sampler.run(n)
+    return {"value": n / w.k / dt, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": sampler.describe(n, dt)}
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -324,70 +355,46 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
 
 
 def run_reference(args):
+    """The oracle as the reference arm.  One step = one bounded sample of n
+    (token, expert) pairs of the workload, n chosen so that all warm-up and
+    timed steps take about a minute; ms_per_step is the measured duration of
+    those n pairs, and value = n / k tokens per second over the timed steps."""
     rank, world, _ = _env_rank()
     if rank != 0:
         return 0
     w = wl.WORKLOADS[args.config]
     sampler = OracleSampler(w)
-    # about a minute of oracle work over all steps; a step is at least one
-    # (token, expert) pair
-    budget = 60.0 / max(1, args.warmup + args.steps)
-    steps = []
+    n = sampler.pairs_for(60.0 / max(1, args.warmup + args.steps))
+    times = []
     for i in range(args.warmup + args.steps):
-        r = sampler.sample(budget)
+        sampler.prepare(n)
+        dt = sampler.run(n)
         if i >= args.warmup:
-            steps.append(r)
-    value = statistics.mean(s["value"] for s in steps)
+            times.append(dt)
+    step_s = statistics.mean(times)
+    value = n / w.k / step_s
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * w.T / value, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1000.0 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "sampled": True,
+        "step": f"{n} (token, expert) pairs of the {w.name} workload ({n / w.k:.3f} tokens)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
                    "L": w.L, "act_bits": w.act_bits},
-        "cpu_baseline": {**steps[-1], "value": value},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                         "sample": sampler.describe(n * args.steps, sum(times))},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
 
-def main(argv=None):
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="decode", choices=list(wl.WORKLOADS))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--experts", type=int, default=0,
-                    help="profiling case: replace the workload's expert count (routing uncalibrated)")
-    ap.add_argument("--tokens", type=int, default=0,
-                    help="profiling case: replace the workload's token count")
-    args = ap.parse_args(argv)
-    if args.impl == "reference":
-        return run_reference(args)
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
-
-    rank, world, local = _env_rank()
-    device = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(device)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-
-    w = wl.WORKLOADS[args.config]
-    if args.experts or args.tokens:
-        w = wl.workload(args.config, name=f"{args.config}_small", E=args.experts or w.E,
-                        T=args.tokens or w.T)
-    from int4_routed_expert_fp32_gb300.build import build
-    if rank == 0 or world == 1:
-        build()
-    if dist:
-        dist.barrier()
+def _measure(args, w, device, dist, world, local):
+    """Time one workload on this rank: the layer steps (value, ms_per_step,
+    clocks, launches), the expert-FFN call (roofline) and the host-buffer
+    path (e2e).  Returns the fields of its JSON entry."""
+    import gc
     moe, x, layer, weights = _setup(w, device)
     x_dev = x.to(device)
     out = torch.empty_like(x_dev)
@@ -397,7 +404,7 @@ def main(argv=None):
     torch.cuda.synchronize()
     rc = moe.check_error()
     if rc != 0:
-        raise RuntimeError(f"device status after warm-up: {moe.status_string(rc)}")
+        raise RuntimeError(f"{w.name}: device status after warm-up: {moe.status_string(rc)}")
 
     sampler = ClockSampler(visible_gpu_id(os.environ.get("CUDA_VISIBLE_DEVICES"), local,
                                           torch.cuda.current_device()))
@@ -419,10 +426,9 @@ def main(argv=None):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, device)
     rc = moe.check_error()
     if rc != 0:
-        raise RuntimeError(f"device status after timing: {moe.status_string(rc)}")
-    value = job_tokens_per_s(world, w.T, ms)
+        raise RuntimeError(f"{w.name}: device status after timing: {moe.status_string(rc)}")
 
-    # dominant kernel: the expert FFN stream kernels
+    # dominant kernel: the expert FFN call
     ffn_ms, counts = _ffn_pass(moe, w, layer, weights, x_dev, min(args.steps, 100))
     roof = roofline(w, ffn_ms, int((counts > 0).sum()), _peaks())
     roof["traffic"] = _profiled_traffic(w.name)
@@ -431,11 +437,84 @@ def main(argv=None):
     e2e = None
     if not args.no_e2e:
         e2e = _e2e_pass(layer, x, w, world, dist, device, min(args.steps, 100))
+    res = {"value": job_tokens_per_s(world, w.T, ms), "ms_per_step": ms, "roofline": roof,
+           "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "config": _config(w, world, roof)}
+    del layer, weights, x_dev, out
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
+def _config(w: wl.Workload, world: int, roof: dict) -> dict:
+    wbytes = roof["active_experts"] * expert_bytes(w)
+    l2 = (f"no flush: {wbytes / 1e9:.2f} GB of expert weights read per step exceed the "
+          f"{L2_BYTES / 1e6:.0f} MB L2" if wbytes > L2_BYTES else
+          f"WARNING: {wbytes / 1e6:.0f} MB of expert weights fit in L2 (not flushed)")
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I, "L": w.L,
+            "act_bits": w.act_bits, "weights": "int4 g32 bf16 scales", "l2": l2,
+            "parallelism": f"replicas x{world}"}
+
+
+def _parser() -> argparse.ArgumentParser:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="prefill", choices=list(wl.WORKLOADS),
+                    help="headline workload of the JSON line")
+    ap.add_argument("--workloads", default="decode,latent,exact",
+                    help="further workloads reported under 'workloads' (comma list, or 'none')")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling case: replace the workload's expert count (routing uncalibrated)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling case: replace the workload's token count")
+    return ap
+
+
+def main(argv=None):
+    ap = _parser()
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    extra = [] if args.workloads in ("", "none") else args.workloads.split(",")
+    for name in extra:
+        if name not in wl.WORKLOADS:
+            ap.error(f"unknown workload {name}")
+    extra = [n for n in extra if n != args.config]
+
+    rank, world, local = _env_rank()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    w = wl.WORKLOADS[args.config]
+    if args.experts or args.tokens:
+        w = wl.workload(args.config, name=f"{args.config}_small", E=args.experts or w.E,
+                        T=args.tokens or w.T)
+        extra = []
+    from int4_routed_expert_fp32_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if dist:
+        dist.barrier()
+
+    head = _measure(args, w, device, dist, world, local)
+    others = {name: _measure(args, wl.WORKLOADS[name], device, dist, world, local)
+              for name in extra}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = _cpu_baseline(w)
-    _report(args, rank, world, w, value, ms, roof, cpu, e2e, clocks, launches)
+    if rank == 0:
+        _report(args, world, head, others, cpu)
     if dist:
         dist.destroy_process_group()
     return 0
@@ -461,28 +540,22 @@ def _e2e_pass(layer, x, w, world, dist, device, e_steps):
             "host_wall_ms_per_step": wall * 1000.0}
 
 
-def _report(args, rank, world, w, value, ms, roof, cpu, e2e, clocks, launches):
-    if rank == 0:
-        wbytes = roof["active_experts"] * expert_bytes(w)
-        l2 = (f"no flush: {wbytes / 1e9:.2f} GB of expert weights read per step exceed the "
-              f"{L2_BYTES / 1e6:.0f} MB L2" if wbytes > L2_BYTES else
-              f"WARNING: {wbytes / 1e6:.0f} MB of expert weights fit in L2 (not flushed)")
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16", "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
-                       "L": w.L, "act_bits": w.act_bits, "weights": "int4 g32 bf16 scales",
-                       "l2": l2,
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clocks,
-        }
-        print(json.dumps(line))
+def _report(args, world, head, others, cpu):
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": head["config"],
+        "roofline": head["roofline"],
+        "cpu_baseline": cpu,
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "workloads": {name: {**r, "unit": "tokens/s", "steps": args.steps, "warmup": args.warmup}
+                      for name, r in others.items()},
+    }
+    print(json.dumps(line))
 
 
 if __name__ == "__main__":

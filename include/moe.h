@@ -40,7 +40,7 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous and stream-ordered; they never synchronise the host, so a
  *     sequence of calls may be captured in a CUDA graph after one warm-up
- *     call per device (the warm-up resolves per-device symbols).
+ *     call per device (the warm-up loads the library's device code).
  *   - Packed int4 weights: int32 [E, N, K/8]; column 8*i + j of row n is
  *     nibble j (bits 4j..4j+3) of word i, a two's-complement value in
  *     [-8, 7].  Scales: bf16 [E, N, K/32], one per output row and 32-column
@@ -51,9 +51,14 @@
  *     scale), -127, 127), IEEE fp32), integer products are summed exactly per
  *     32-column weight group, y = scale_x * sum_g scale_w[n, g] * P[g] in fp32.
  *   - Return value: MOE_OK or a negative MOE_ERR_* code.  Argument errors are
- *     detected on the host before any launch.  Device-side problems (a
- *     bounded wait that ran out, offsets that exceed the stated capacity) are
- *     recorded in a per-device status word read by moe_check_error().
+ *     detected on the host before any launch.  Device-side problems are
+ *     recorded in a per-device status word that moe_check_error() reads and
+ *     clears: a bounded wait that ran out (MOE_ERR_TIMEOUT), offsets or row
+ *     indices outside the stated capacity (MOE_ERR_INVALID), a value outside
+ *     the range the kernels compute exactly (MOE_ERR_UNSUPPORTED).  The word
+ *     keeps the first such error since the last check.  It is a report only:
+ *     the kernels never read it, so an error recorded by one call does not
+ *     change what later calls compute, whether or not anyone checks it.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -168,8 +173,10 @@ int moe_dispatch_pairs(const int32_t* topk_idx, const uint16_t* x, int T, int D,
  *   Limit: ceil(T/32)*E rounded up to 64, plus T*k, must not exceed 524288
  *   (for example T = 16384 with E = 384, k = 8); larger requests return
  *   MOE_ERR_WORKSPACE before any launch.
- *   The first call on a device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   Each call looks up the array's device address in the current device's
+ *   context (so the address stays right after a device reset); the first
+ *   call on a device may load the library's device code, so make one call
+ *   before any stream capture.
  *   All calls share the one array: calls whose executions overlap on the GPU
  *   (different streams, or several host threads) race and give wrong
  *   results.  Nothing in the array needs to start at zero.
@@ -263,7 +270,8 @@ int moe_quantize_int4(const uint16_t* w, int N, int K, int32_t* packed, uint16_t
  * selected expert outputs with their routing weights"):
  *   out[t] = bf16( sum_j fp32(y_sorted[inv_row[t*k + j]]) * topk_w[t*k + j] ),
  * j ascending.  y_sorted bf16 [T*k, D], inv_row int32 [T*k], topk_w fp32
- * [T*k], out bf16 [T, D]. */
+ * [T*k], out bf16 [T, D].  A row index outside [0, T*k) is skipped (the slot
+ * adds nothing) and records MOE_ERR_INVALID. */
 int moe_combine(const uint16_t* y_sorted, const int32_t* inv_row, const float* topk_w, int T,
                 int D, int k, uint16_t* out, void* stream);
 
@@ -323,9 +331,13 @@ int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w, const ui
 
 /* ------------------------------------------------------------ status etc -- */
 
-/* Synchronises `stream`, returns and clears the current device's status word
- * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_INVALID), or MOE_ERR_CUDA if the stream
- * reports a CUDA error.  Test and harness use only: it blocks the host. */
+/* Synchronises `stream`, then returns and clears the current device's
+ * status word: MOE_OK, or the first of MOE_ERR_TIMEOUT, MOE_ERR_INVALID and
+ * MOE_ERR_UNSUPPORTED recorded on the device since the last check (see the
+ * conventions above).  Returns MOE_ERR_CUDA if the stream reports a CUDA
+ * error.  It blocks the host, so a serving loop calls it off the hot path
+ * (for instance once per batch of steps); not checking is harmless, since
+ * no kernel reads the word. */
 int moe_check_error(void* stream);
 
 /* Launches a kernel that waits on a barrier nothing completes, with a limit

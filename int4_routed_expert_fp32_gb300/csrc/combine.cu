@@ -68,14 +68,20 @@ template <typename YT, bool NORM>
 __global__ void __launch_bounds__(kCbThreads) combine_kernel(
     const YT* __restrict__ y, const int32_t* __restrict__ inv_row, const float* __restrict__ w,
     int T, int D, int k, const uint16_t* __restrict__ gain, float eps,
-    uint16_t* __restrict__ out) {
+    uint16_t* __restrict__ out, int* status) {
   extern __shared__ float rowbuf[];  // NORM: D floats
   __shared__ int32_t rows[kMaxTopK];
   __shared__ float wts[kMaxTopK];
   __shared__ float red[32];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
-    rows[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
+    // y holds T * k rows: a row index outside them is skipped and recorded
+    int r = inv_row[(size_t)t * k + threadIdx.x];
+    if (r < 0 || r >= T * k) {
+      record_status(status, MOE_ERR_INVALID);
+      r = -1;
+    }
+    rows[threadIdx.x] = r;
     wts[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
@@ -152,19 +158,23 @@ __global__ void __launch_bounds__(kCbThreads) rmsnorm_kernel(const uint16_t* __r
 template <typename YT>
 static int launch_combine_t(const YT* y, const int32_t* inv_row, const float* w, int T, int D,
                             int k, const uint16_t* gain, float eps, uint16_t* out, cudaStream_t s) {
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
   if (gain) {
     const size_t smem = (size_t)D * sizeof(float);
     if (smem > 48 * 1024)
       MOE_TRY_CUDA(cudaFuncSetAttribute(combine_kernel<YT, true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    combine_kernel<YT, true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out);
+    combine_kernel<YT, true><<<T, kCbThreads, smem, s>>>(y, inv_row, w, T, D, k, gain, eps, out,
+                                                         status);
   } else {
     // few tokens: split each row over CTAs so that about 4 CTAs per SM run
     const int nv = D / 8;
     const int max_split = (nv + kCbThreads - 1) / kCbThreads;
     const int want = (4 * num_sms() + T - 1) / T;
     const dim3 grid(T, want < 1 ? 1 : (want > max_split ? max_split : want));
-    combine_kernel<YT, false><<<grid, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps, out);
+    combine_kernel<YT, false><<<grid, kCbThreads, 0, s>>>(y, inv_row, w, T, D, k, nullptr, eps,
+                                                           out, status);
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;

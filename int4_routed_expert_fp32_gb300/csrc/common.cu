@@ -14,7 +14,6 @@ __device__ int g_status_word;
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_status_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
@@ -27,25 +26,17 @@ int current_device() {
 }
 }  // namespace
 
+// Looked up on every call, with the caller's device current: the address
+// belongs to the current context, so it stays right after a device reset or
+// a new primary context, which a cache keyed by device would not.
 int* status_word() {
-  int d = 0;
-  const cudaError_t ed = cudaGetDevice(&d);
-  if (ed != cudaSuccess) {
-    note_cuda_error(ed);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
     return nullptr;
   }
-  if (d < 0 || d >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[d]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
-    if (e != cudaSuccess) {
-      note_cuda_error(e);
-      return nullptr;
-    }
-    g_status_ptr[d] = static_cast<int*>(p);
-  }
-  return g_status_ptr[d];
+  return static_cast<int*>(p);
 }
 
 int num_sms() {
@@ -98,14 +89,16 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 // A barrier that nothing completes: the bounded wait must run out.
 __global__ void wait_selftest_kernel(int64_t limit_ns, int* status) {
   __shared__ __align__(8) uint64_t bar;
+  __shared__ int cta_abort;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
+    cta_abort = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     // The phase with parity 0 never completes (no arrival is ever made).
-    mbar_wait(&bar, 0, limit_ns, status);
+    mbar_wait(&bar, 0, Waiter{&cta_abort, status, limit_ns});
   }
   __syncthreads();
 }

@@ -25,7 +25,8 @@ constexpr int64_t kDefaultWaitNs = 2000000000LL;  // 2 s per wait before giving 
 
 // ------------------------------------------------------------------ host side
 
-// Device address of the per-device status word (resolved once per device).
+// Device address of the status word on the current device (null after a
+// failed lookup, whose CUDA error is recorded for moe_last_cuda_error).
 int* status_word();
 // Number of SMs of the current device (cached).
 int num_sms();
@@ -104,10 +105,6 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ bool status_set(const int* status) {
-  return *reinterpret_cast<const volatile int*>(status) != 0;
-}
-
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
@@ -161,27 +158,77 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most limit_ns.
-// Gives up early when another thread has already recorded a status.  On
-// timeout records MOE_ERR_TIMEOUT.  Returns true when the phase completed.
-// backoff_ns > 0: sleep that long between rounds of polls (for waits that
-// last long, so that the waiting warps leave the issue slots to others).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_t limit_ns,
-                                          int* status, uint32_t backoff_ns = 0) {
+// Bounded waits.  Every wait on an mbarrier (or on another CTA's counter)
+// is bounded by %globaltimer.  Each CTA keeps an abort flag in shared
+// memory: a wait that runs out records MOE_ERR_TIMEOUT in the device status
+// word and sets the flag, and every later wait of the same CTA then gives up
+// at once, so a CTA whose pipeline stopped leaves after one time-out rather
+// than one per wait.  Kernels only ever write the status word: an error that
+// an earlier call recorded does not change what a later call computes.
+struct Waiter {
+  int* abort;        // the CTA's flag (shared memory)
+  int* status;       // the device status word (written, never read)
+  int64_t limit_ns;  // per wait
+};
+
+__device__ __forceinline__ bool aborted(const Waiter& w) {
+  return *reinterpret_cast<const volatile int*>(w.abort) != 0;
+}
+
+__device__ __forceinline__ void give_up(const Waiter& w) {
+  *reinterpret_cast<volatile int*>(w.abort) = 1;
+  record_status(w.status, MOE_ERR_TIMEOUT);
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// w.limit_ns; gives up at once when the CTA has aborted.  Returns true when
+// the phase completed.  backoff_ns > 0: sleep that long between rounds of
+// polls (for waits that last long, so that the waiting warps leave the issue
+// slots to others).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waiter& w,
+                                          uint32_t backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (status_set(status)) return false;  // fail fast once an error is recorded
+  if (aborted(w)) return false;  // a shared-memory read: cheap on the fast path
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_suspend(bar, parity)) return true;
     if (backoff_ns) __nanosleep(backoff_ns);
-    if (status_set(status)) return false;
-    if (static_cast<int64_t>(global_timer_ns() - t0) > limit_ns) {
+    if (aborted(w)) return false;
+    if (static_cast<int64_t>(global_timer_ns() - t0) > w.limit_ns) {
+      give_up(w);
+      return false;
+    }
+  }
+}
+
+// Time a CTA's exit path waits, per barrier, for work it issued itself
+// (copies in flight, MMAs) before it leaves anyway.
+constexpr int64_t kDrainNs = 100000000LL;
+
+// Wait for a phase on the exit path: ignores the abort flag (the work it
+// waits for was issued and completes by itself), bounded by kDrainNs.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, int* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (static_cast<int64_t>(global_timer_ns() - t0) > kDrainNs) {
       record_status(status, MOE_ERR_TIMEOUT);
       return false;
     }
   }
+  return true;
+}
+
+// Let the last copies a producer issued into a `stages`-slot ring land:
+// `issued` fills in total, fill i completing phase i / stages of barrier
+// full[i % stages].  Called on every exit of a producer, so that no copy is
+// still writing the CTA's shared memory when it leaves; on the normal path
+// these phases have completed and the waits return at once.
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, uint32_t stages,
+                                          int* status) {
+  const uint32_t first = issued >= stages ? issued - stages : 0;
+  for (uint32_t i = first; i < issued; ++i) mbar_drain(&full[i % stages], (i / stages) & 1u, status);
 }
 
 // ---- asynchronous copies

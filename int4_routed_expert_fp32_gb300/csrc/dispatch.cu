@@ -8,7 +8,6 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
-#include <mutex>
 
 #include "common.cuh"
 #include "dispatch.cuh"
@@ -296,25 +295,22 @@ static size_t dispatch_chunks(int T) { return (size_t)(T + kChunkTokens - 1) / k
 // Scratch of moe_dispatch_noalloc: the per-chunk expert histograms followed by
 // the in-chunk ranks.  Every GPU that loads the library holds these 2 MiB
 // until the process exits.  Host code must not use the symbol as a device
-// address; noalloc_scratch() resolves the address per device.
+// address; noalloc_scratch() resolves the address on the current device.
 constexpr size_t kNoAllocScratchInts = 512 * 1024;
 static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchInts];
 
-static std::mutex g_noalloc_mu;
-static int32_t* g_noalloc_ptr[64] = {};
-
-// Device address of g_dispatch_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Device address of g_dispatch_scratch in the current device's context,
+// looked up on every call (so it stays right after a device reset or a new
+// primary context).  On failure records the CUDA error for
+// moe_last_cuda_error and returns null.
 static int32_t* noalloc_scratch() {
-  int d = 0;
-  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[d]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return nullptr;
-    g_noalloc_ptr[d] = static_cast<int32_t*>(p);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    return nullptr;
   }
-  return g_noalloc_ptr[d];
+  return static_cast<int32_t*>(p);
 }
 
 // Count, scan and place kernels of one dispatch (T > 0, arguments checked).

@@ -273,7 +273,7 @@ template <int MODE, bool Q8, int NTB>
 __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t* ready,
                                              uint64_t* empty, uint32_t& it, int ksteps, int row0,
                                              int rows, int n0, int cw, int lane, const Lane& L,
-                                             const FsParams& p) {
+                                             const FsParams& p, const Waiter& wt) {
   const int K = p.K, N = p.N;
   float acc[NTB][4];
 #pragma unroll
@@ -285,7 +285,8 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    if (ok && !mbar_wait(&ready[s], ph, p.wait_ns, p.status)) ok = false;
+    // warp-uniform outcome: the MMAs below need the whole warp
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ready[s], ph, wt));
     if (ok) {
       const uint8_t* W = smem + s * kFsStageBytes;
       const uint8_t* S = W + kFsWBytes;
@@ -367,7 +368,8 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
 template <int MODE, bool Q8>
 __device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams& p, uint8_t* smem,
                                              uint64_t* full, uint64_t* empty, uint32_t& it,
-                                             int e, int row0, int rows, int n0, int lane) {
+                                             int e, int row0, int rows, int n0, int lane,
+                                             const Waiter& wt) {
   constexpr int elem = Q8 ? 1 : 2;
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
   const int K = p.K, N = p.N;
@@ -377,7 +379,7 @@ __device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams&
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, p.status)) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1u, wt))) return false;  // warp-uniform
     uint8_t* st = smem + s * kFsStageBytes;
     uint8_t* sdst = st + kFsWBytes;
     const int k0 = ks * kFsKc;
@@ -430,30 +432,18 @@ __device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams&
   return true;
 }
 
-// Let the copies a stopping producer already issued land before the CTA
-// exits (bounded).
-__device__ __forceinline__ void drain_copies(uint64_t* full, uint32_t it) {
-  const uint32_t first = it >= kFsStages ? it - kFsStages : 0;
-  for (uint32_t i = first; i < it; ++i) {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(&full[i % kFsStages], (i / kFsStages) & 1u)) {
-      if (static_cast<int64_t>(global_timer_ns() - t0) > 100000000LL) break;
-    }
-  }
-}
-
 // Start-value side of one unit (see stage_starts).  Returns false when a wait
 // gave up.
 template <bool Q8>
 __device__ __forceinline__ bool starts_unit(const FsParams& p, uint8_t* smem, uint64_t* full,
                                             uint64_t* empty, uint64_t* ready, uint32_t& it,
-                                            int rows, int lane) {
+                                            int rows, int lane, const Waiter& wt) {
   const int K = p.K;
   const int ksteps = (K + kFsKc - 1) / kFsKc;
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    if (!mbar_wait(&full[s], ph, p.wait_ns, p.status)) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wt))) return false;  // warp-uniform
     uint8_t* st = smem + s * kFsStageBytes;
     const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
     stage_starts<Q8>(st + kFsWBytes + kFsSBytes, st + kFsWBytes + kFsSBytes + kFsXBytes, ng, rows,
@@ -478,6 +468,8 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   uint64_t* empty = full + kFsStages;
   uint64_t* ready = empty + kFsStages;  // stage landed and its chain start values written
 
+  __shared__ int cta_abort;
+  const Waiter wt{&cta_abort, p.status, p.wait_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool tma_s = p.tma_scales != 0;
   if (threadIdx.x == 0) {
@@ -487,6 +479,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
       mbar_init(&empty[s], kFsCWarps + 1);  // one arrival per consumer warp + the start-value warp
       mbar_init(&ready[s], 1);
     }
+    cta_abort = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
@@ -512,9 +505,12 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int q = u / n_tiles, jt = u - q * n_tiles;
       ok = produce_unit<MODE, Q8>(maps, p, smem, full, empty, it, p.chunk_e[q], p.chunk_row0[q],
-                                  p.chunk_rows[q], jt * tile_n, lane);
+                                  p.chunk_rows[q], jt * tile_n, lane, wt);
     }
-    if (!ok) drain_copies(full, it);
+    // on every exit (a wait that gave up included) the issued copies land
+    // before the producer leaves, so none is still writing shared memory
+    // when the CTA exits
+    drain_ring(full, it, kFsStages, p.status);
     return;
   }
 
@@ -522,7 +518,8 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     // --------------------------------------------- chain start values
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x)
-      if (!starts_unit<Q8>(p, smem, full, empty, ready, it, p.chunk_rows[u / n_tiles], lane)) return;
+      if (!starts_unit<Q8>(p, smem, full, empty, ready, it, p.chunk_rows[u / n_tiles], lane, wt))
+        return;
     return;
   }
 
@@ -549,9 +546,11 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     // No early exit after a failed wait: the consumer warps meet at named
     // barriers, so all of them walk every unit (the waits then return at once).
     if (rows <= 8)
-      consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+      consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p,
+                                wt);
     else
-      consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p);
+      consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p,
+                                wt);
   }
 }
 
@@ -582,6 +581,8 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   uint64_t* empty = full + kFsStages;
   uint64_t* ready = empty + kFsStages;
 
+  __shared__ int cta_abort;
+  const Waiter wt{&cta_abort, pgu.status, pgu.wait_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFsStages; ++s) {
@@ -589,6 +590,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
       mbar_init(&empty[s], kFsCWarps + 1);
       mbar_init(&ready[s], 1);
     }
+    cta_abort = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
         const int q = u / nt_gu, jt = u - q * nt_gu;
         ok = produce_unit<kGateUp, false>(mgu, pgu, smem, full, empty, it, pgu.chunk_e[q],
                                           pgu.chunk_row0[q], pgu.chunk_rows[q],
-                                          jt * (kFsRows / 2), lane);
+                                          jt * (kFsRows / 2), lane, wt);
       } else {
         const int d = u - units_gu;
         const int q = d / nt_dn, jt = d - q * nt_dn;
@@ -624,12 +626,12 @@ __global__ void __launch_bounds__(kFsThreads, 1)
         if (ld_acquire(done + q) < nt_gu) {
           const uint64_t t0 = global_timer_ns();
           while (ld_acquire(done + q) < nt_gu) {
-            if (status_set(pdn.status)) {
+            if (aborted(wt)) {
               ok = false;
               break;
             }
-            if (static_cast<int64_t>(global_timer_ns() - t0) > pdn.wait_ns) {
-              record_status(pdn.status, MOE_ERR_TIMEOUT);
+            if (static_cast<int64_t>(global_timer_ns() - t0) > wt.limit_ns) {
+              give_up(wt);
               ok = false;
               break;
             }
@@ -644,10 +646,11 @@ __global__ void __launch_bounds__(kFsThreads, 1)
         // read them through the async proxy
         asm volatile("fence.proxy.async.global;" ::: "memory");
         ok = produce_unit<DMODE, false>(mdn, pdn, smem, full, empty, it, pdn.chunk_e[q],
-                                        pdn.chunk_row0[q], pdn.chunk_rows[q], jt * kFsRows, lane);
+                                        pdn.chunk_row0[q], pdn.chunk_rows[q], jt * kFsRows, lane,
+                                        wt);
       }
     }
-    if (!ok) drain_copies(full, it);
+    drain_ring(full, it, kFsStages, pgu.status);
     return;
   }
 
@@ -657,7 +660,8 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const bool gu = u < units_gu;
       const int q = gu ? u / nt_gu : (u - units_gu) / nt_dn;
-      if (!starts_unit<false>(gu ? pgu : pdn, smem, full, empty, ready, it, pgu.chunk_rows[q], lane))
+      if (!starts_unit<false>(gu ? pgu : pdn, smem, full, empty, ready, it, pgu.chunk_rows[q], lane,
+                              wt))
         return;
     }
     return;
@@ -688,10 +692,10 @@ __global__ void __launch_bounds__(kFsThreads, 1)
       const int row0 = pgu.chunk_row0[q], rows = pgu.chunk_rows[q];
       if (rows <= 8)
         consume_unit<kGateUp, false, 1>(smem, x, ready, empty, it, ks_gu, row0, rows,
-                                        jt * (kFsRows / 2), warp, lane, L, pgu);
+                                        jt * (kFsRows / 2), warp, lane, L, pgu, wt);
       else
         consume_unit<kGateUp, false, 2>(smem, x, ready, empty, it, ks_gu, row0, rows,
-                                        jt * (kFsRows / 2), warp, lane, L, pgu);
+                                        jt * (kFsRows / 2), warp, lane, L, pgu, wt);
       if (warp < kFsCWarps / 2) {
         // the gate warps stored this unit's h: publish it to the down units
         __threadfence();
@@ -704,10 +708,10 @@ __global__ void __launch_bounds__(kFsThreads, 1)
       const int row0 = pdn.chunk_row0[q], rows = pdn.chunk_rows[q];
       if (rows <= 8)
         consume_unit<DMODE, false, 1>(smem, x, ready, empty, it, ks_dn, row0, rows, jt * kFsRows,
-                                      warp, lane, L, pdn);
+                                      warp, lane, L, pdn, wt);
       else
         consume_unit<DMODE, false, 2>(smem, x, ready, empty, it, ks_dn, row0, rows, jt * kFsRows,
-                                      warp, lane, L, pdn);
+                                      warp, lane, L, pdn, wt);
     }
   }
 }

@@ -118,7 +118,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   uint64_t* afree = aready + kTxAStages;
   uint64_t* accfull = afree + kTxAStages;
   uint64_t* accempty = accfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 1);
+  uint64_t* mma_done = accempty + 1;  // the MMA warp's last commit (exit path)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  __shared__ int cta_abort;
+  const Waiter wt{&cta_abort, p.status, p.wait_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -132,6 +135,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     }
     mbar_init(accfull, 1);
     mbar_init(accempty, kTxEpWarps);
+    mbar_init(mma_done, 1);
+    cta_abort = 0;
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -165,7 +170,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         for (int ks = 0; ks < ksteps; ++ks, ++it) {
           const int s = it % kTxStages;
           const uint32_t ph = (it / kTxStages) & 1u;
-          if (!mbar_wait(&sfree[s], ph ^ 1u, p.wait_ns, p.status)) {
+          if (!mbar_wait(&sfree[s], ph ^ 1u, wt)) {
             ok = false;
             break;
           }
@@ -183,6 +188,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
           }
         }
       }
+      // on every exit (a wait that gave up included) let the issued copies
+      // land before the CTA can leave
+      drain_ring(full, it, kTxStages, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -195,13 +203,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const int rows = p.chunk_rows[q];
       const int nn = rows <= 16 ? 16 : (rows + 15) / 16 * 16;  // MMA N: tokens, multiple of 16
       const uint32_t idesc = idesc_f16(kTxWM, nn);
-      if (!__all_sync(0xffffffffu, mbar_wait(accempty, (uc & 1u) ^ 1u, p.wait_ns, p.status)))
+      if (!__all_sync(0xffffffffu, mbar_wait(accempty, (uc & 1u) ^ 1u, wt)))
         break;
       tc_fence_after();
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
         const int s = it % kTxStages, a = it % kTxAStages;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&aready[a], (it / kTxAStages) & 1u, p.wait_ns, p.status))) {
+                        mbar_wait(&aready[a], (it / kTxAStages) & 1u, wt))) {
           ok = false;
           break;
         }
@@ -220,6 +228,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       }
       if (ok) umma_commit_warp(accfull);
     }
+    // every MMA issued (reading shared memory and TMEM) completes before the
+    // CTA frees its TMEM or leaves, on the error path too
+    umma_commit_warp(mma_done);
+    mbar_drain(mma_done, 0, p.status);
   } else if (warp < 2 + kTxDqWarps) {
     // ----------------------------------------------------- dequantisation
     // TMEM lane quarter of this warp: warp % 4.  Warps 2-5: block 0, first
@@ -271,8 +283,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         s_c = scale_word(ks + 3);
         const int s = it % kTxStages, a = it % kTxAStages;
         // warp-uniform outcome: the tcgen05.st below needs the whole warp
-        const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, p.wait_ns, p.status) &&
-                         mbar_wait(&afree[a], ((it / kTxAStages) & 1u) ^ 1u, p.wait_ns, p.status);
+        const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, wt) &&
+                         mbar_wait(&afree[a], ((it / kTxAStages) & 1u) ^ 1u, wt);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const int row0 = p.chunk_row0[q], rows = p.chunk_rows[q];
       const int n0 = jt * tile_n;
       // warp-uniform outcome: tcgen05.ld needs the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, p.wait_ns, p.status, 256))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(accfull, uc & 1u, wt, 256))) break;
       tc_fence_after();
       bool fin = true;
       if (MODE == kTxGateUp) {

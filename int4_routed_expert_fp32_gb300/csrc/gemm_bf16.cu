@@ -36,7 +36,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
   uint64_t* accf = empty + kTcStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* mma_done = accf + 1;  // the MMA warp's last commit (exit path)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  __shared__ int cta_abort;
+  const Waiter wt{&cta_abort, status, wait_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -45,6 +48,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accf, 1);
+    mbar_init(mma_done, 1);
+    cta_abort = 0;
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -64,15 +69,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       prefetch_tensor_map(&ma);
       prefetch_tensor_map(&mb);
-      for (int kt = 0; kt < ktiles; ++kt) {
+      int kt = 0;
+      for (; kt < ktiles; ++kt) {
         const int s = kt % kTcStages;
         const uint32_t ph = (kt / kTcStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, wait_ns, status)) break;
+        if (!mbar_wait(&empty[s], ph ^ 1u, wt)) break;
         uint8_t* st = smem + s * kTcStageBytes;
         mbar_arrive_expect_tx(&full[s], kTcStageBytes);
         tma_g2s_2d(st, &ma, &full[s], kbase + kt * kTcBK, m0);
         tma_g2s_2d(st + kTcABytes, &mb, &full[s], kbase + kt * kTcBK, n0);
       }
+      // the issued copies land before the CTA can leave (error path included)
+      drain_ring(full, static_cast<uint32_t>(kt), kTcStages, status);
     }
   } else if (warp == 1) {
     // the whole warp walks the loop; one elected lane issues (see umma_f16_warp)
@@ -81,7 +89,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int kt = 0; kt < ktiles; ++kt) {
       const int s = kt % kTcStages;
       const uint32_t ph = (kt / kTcStages) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wait_ns, status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wt))) {
         ok = false;
         break;
       }
@@ -95,12 +103,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit_warp(&empty[s]);
     }
     if (ok) umma_commit_warp(accf);
+    // every issued MMA completes before TMEM is freed, on the error path too
+    umma_commit_warp(mma_done);
+    mbar_drain(mma_done, 0, status);
   } else {
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
     const int row = m0 + 32 * q + lane;
     // warp-uniform outcome: tcgen05.ld needs the whole warp
-    if (__all_sync(0xffffffffu, mbar_wait(accf, 0, wait_ns, status))) {
+    if (__all_sync(0xffffffffu, mbar_wait(accf, 0, wt))) {
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < kTcBN; c0 += 32) {

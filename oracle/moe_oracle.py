@@ -23,7 +23,7 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).  Page references:
   up-projection; moe_infer: one-hot counts, argsort, gather, per-expert loop,
   scatter back, fp32 weighted sum) and the "Latent up-projection" shapes.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   - one expert group, so group-limited masking is the identity;
   - rank by s + b, weight by the unbiased s; ties go to the lower expert id;
   - argsort is stable (rows of one expert ascend by token id);

@@ -91,23 +91,57 @@ def test_peaks_are_positive_with_a_source():
     assert p["hbm_gbs"] > 0 and p["bf16_tflops"] > 0 and p["bf16_tflops_sustained"] > 0
 
 
-def test_json_line_has_the_contract_fields(capsys):
-    w = wl.WORKLOADS["decode"]
-    args = types.SimpleNamespace(steps=5, warmup=3)
-    roof = bench.roofline(w, 0.9, 180, PEAKS)
+def _entry(w, ms, active):
+    roof = bench.roofline(w, ms, active, PEAKS)
     e2e = {"value": 1.0, "unit": "tokens/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1}
-    cpu = {"value": 0.3, "unit": "tokens/s", "cores": 4, "kind": "oracle", "sample": "s"}
     clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
-    bench._report(args, 0, 1, w, 32000.0, 1.0, roof, cpu, e2e, clocks, 12)
+    return {"value": w.T / ms * 1e3, "ms_per_step": ms, "roofline": roof, "e2e": e2e,
+            "gpu_launches": 12, "clocks": clocks, "config": bench._config(w, 1, roof)}
+
+
+def test_json_line_has_the_contract_fields(capsys):
+    args = types.SimpleNamespace(steps=5, warmup=3)
+    head = _entry(wl.WORKLOADS["prefill"], 5.7, 368)
+    others = {"decode": _entry(wl.WORKLOADS["decode"], 0.99, 181),
+              "exact": _entry(wl.WORKLOADS["exact"], 0.7, 8)}
+    cpu = {"value": 0.3, "unit": "tokens/s", "cores": 4, "kind": "oracle", "sample": "s"}
+    bench._report(args, 1, head, others, cpu)
     line = json.loads(capsys.readouterr().out.strip())
     for key in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
-                "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"]:
+                "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks", "workloads"]:
         assert key in line, key
-    assert line["config"]["workload"] == "decode" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "prefill" and line["higher_is_better"] is True
     assert line["scaling"] == "weak" and line["vs_baseline"] is None and line["steps"] == 5
     for key in ["bound", "achieved", "peak", "unit", "frac", "traffic"]:
         assert key in line["roofline"], key
-    # other ranks print nothing
-    bench._report(args, 1, 2, w, 32000.0, 1.0, roof, None, e2e, clocks, 12)
-    assert capsys.readouterr().out == ""
+    assert set(line["workloads"]) == {"decode", "exact"}
+    for name, entry in line["workloads"].items():
+        assert entry["config"]["workload"] == name
+        for key in ["value", "ms_per_step", "roofline", "e2e", "clocks", "gpu_launches"]:
+            assert key in entry, (name, key)
+
+
+def test_bench_defaults_to_the_largest_workload():
+    """The headline line is the prefill workload, the largest configuration;
+    the other three are reported beside it."""
+    args = bench._parser().parse_args([])
+    assert args.config == "prefill"
+    assert max(wl.WORKLOADS.values(), key=lambda w: w.T * w.k).name == "prefill"
+    assert set(args.workloads.split(",")) == {"decode", "latent", "exact"}
+
+
+def test_cpu_baseline_times_oracle_arithmetic_only(monkeypatch):
+    """The sampler generates the expert weights of the pairs it is about to
+    time before the clock starts: inside run() nothing is generated."""
+    w = wl.workload("tiny", name="tiny")
+    sampler = bench.OracleSampler(w)
+    n = 5
+    sampler.prepare(n)
+
+    def no_generation(*a, **k):
+        raise AssertionError("expert weights generated inside the timed region")
+
+    monkeypatch.setattr(sampler.oi, "expert_arrays", no_generation)
+    dt = sampler.run(n)
+    assert dt > 0 and sampler.pair == n

@@ -463,6 +463,40 @@ def test_expert_ffn_reports_fp16_overflow_and_recovers(moe):
     assert moe.check_error() == 0
 
 
+def test_status_word_is_a_report_only(moe):
+    """An error that one call records (an fp16 overflow on both expert
+    kernels, a bounded wait that ran out) leaves later calls unchanged, with
+    no moe_check_error in between: they give the bits of a clean call, and
+    the status word keeps the first error until it is read."""
+    rng = np.random.default_rng(43)
+    D, I, counts = 256, 128, [5, 60]
+    E = len(counts)
+    off = _t(_segments(counts))
+    R = sum(counts)
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    small = _bf16(rng.normal(size=(R, D))).to(DEV)
+    big = _bf16(rng.normal(size=(R, D)) * 3000.0).to(DEV)
+    clean = moe.expert_ffn(small, None, off, ex, 16)
+    assert moe.check_error() == 0
+    moe.expert_ffn(big, None, off, ex, 16)          # records UNSUPPORTED
+    after_unsupported = moe.expert_ffn(small, None, off, ex, 16)
+    moe.wait_selftest(20_000_000)                   # a wait runs out (TIMEOUT, not kept)
+    after_timeout = moe.expert_ffn(small, None, off, ex, 16)
+    assert moe.check_error() == moe.capi.MOE_ERR_UNSUPPORTED   # the first error
+    assert torch.equal(after_unsupported.view(torch.int16), clean.view(torch.int16))
+    assert torch.equal(after_timeout.view(torch.int16), clean.view(torch.int16))
+    moe.wait_selftest(20_000_000)
+    again = moe.expert_ffn(small, None, off, ex, 16)
+    assert moe.check_error() == moe.capi.MOE_ERR_TIMEOUT
+    assert torch.equal(again.view(torch.int16), clean.view(torch.int16))
+    assert moe.check_error() == 0
+
+
 def test_ffn_rejects_offsets_beyond_capacity(moe):
     rng = np.random.default_rng(1)
     E, D, I = 2, 128, 128
@@ -478,6 +512,27 @@ def test_ffn_rejects_offsets_beyond_capacity(moe):
 
 
 # ---------------------------------------------------------------- combine
+
+def test_combine_rejects_rows_outside_y(moe):
+    """A row index outside [0, T*k) is skipped and recorded (MOE_ERR_INVALID);
+    the other slots of the token still add up."""
+    rng = np.random.default_rng(5)
+    T, k, D = 4, 2, 128
+    y = _bf16(rng.normal(size=(T * k, D)))
+    inv = np.arange(T * k, dtype=np.int32)
+    inv[3] = T * k          # one past the last row
+    inv[6] = -1
+    w = np.full((T, k), 0.5, np.float32)
+    out = moe.combine(y.to(DEV), _t(inv), _t(w))
+    assert moe.check_error() == moe.capi.MOE_ERR_INVALID
+    assert moe.check_error() == 0
+    got = out.float().cpu().numpy()
+    yf = oi.x_f64(y)
+    assert np.array_equal(got[1], (0.5 * yf[2]).astype(np.float32))   # slot 1 skipped
+    assert np.array_equal(got[3], (0.5 * yf[7]).astype(np.float32))   # slot 0 skipped
+    ref0 = 0.5 * yf[0] + 0.5 * yf[1]
+    assert np.all(np.abs(got[0] - ref0) <= 2 ** -8 * np.abs(ref0) + 1e-6)
+
 
 def test_combine_parity(moe):
     rng = np.random.default_rng(3)
