@@ -235,12 +235,39 @@ size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);
  *   w_packed  int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
  *   out       fp32 [rows_max, N], 16-byte aligned
  * Experts with up to 16 rows run on the stream kernel, larger ones (when
- * rows_max >= 48 and K % 64 == 0) on the tensor-core kernel.  With unit
- * weight scales and an int8 input of scale 1 the output equals the integer
- * accumulator sum_c q_x * q_w exactly on both (|sum| <= K*8*127 < 2^24). */
+ * rows_max >= 48 and K % 64 == 0) on the tensor-core kernel.  With
+ * act_bits 8 both kernels form the exact integer partial P_g of every
+ * 32-column weight group and give the same bits: y = x_scale * acc, acc the
+ * fp32 chain fma(scale[n, g], P_g, acc) over the groups in K order. */
 int moe_int4_linear(const void* x, const float* x_scale, const int32_t* offsets, int E, int K,
                     int N, int rows_max, const int32_t* w_packed, const uint16_t* w_scale,
                     int act_bits, float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of moe_int4_linear_partials (host only). */
+size_t moe_int4_linear_partials_workspace_size(int E, int K, int rows_max);
+
+/* For tests: the exact-mode integer accumulators of one grouped
+ * PackedInt4Linear (exact-generator adaptation page, "Sources & provenance":
+ * the exact int4 multiply-accumulate; "The preserved forward form":
+ * accumulator bounds).  Runs moe_int4_linear's act_bits 8 computation for
+ * every expert on the kernel `kernel` names -- 0: the stream kernel (chunks
+ * of <= 16 rows), 1: the tensor-core kernel (chunks of <= 128 rows) --
+ * whatever the row counts, and also stores the integer partial of every
+ * 32-column weight group:
+ *   partials  int32 [rows_max, N, K/32] out:
+ *             P[r, n, g] = sum_{c in group g} x[r, c] * q_w[n, c], exact
+ *             (|P| <= 32 * 8 * 127);
+ *   out       fp32 [rows_max, N] out: y[r, n] = x_scale[r] * acc, acc the
+ *             fp32 chain acc = fma(scale[n, g], P[r, n, g], acc) over g in
+ *             K order from 0 -- the bits moe_int4_linear gives on either
+ *             kernel.
+ * x int8 [rows_max, K] (16-byte aligned), x_scale fp32 [rows_max]; weights,
+ * offsets, K % 64 == 0 and the error codes as moe_int4_linear.  Rows
+ * outside every expert are left untouched. */
+int moe_int4_linear_partials(const int8_t* x, const float* x_scale, const int32_t* offsets, int E,
+                             int K, int N, int rows_max, const int32_t* w_packed,
+                             const uint16_t* w_scale, int kernel, float* out, int32_t* partials,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* Per-row symmetric int8 quantisation (the act_bits 8 input step):
  * v bf16 [R, C] -> q int8 [R, C], scale fp32 [R].  R rows, C % 64 == 0. */

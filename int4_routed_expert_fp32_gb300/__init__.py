@@ -8,7 +8,8 @@ no fallback).  ``int4_routed_expert_fp32_gb300.build`` compiles it.
 import importlib
 
 _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "combine",
-            "dispatch", "dispatch_noalloc", "expert_ffn", "int4_linear", "last_cuda_error", "launch_count",
+            "dispatch", "dispatch_noalloc", "expert_ffn", "int4_linear", "int4_linear_partials",
+            "last_cuda_error", "launch_count",
             "lib", "linear_bf16", "quantize_int4",
             "quantize_rows", "shared_expert",
             "rmsnorm", "route", "status_string", "wait_selftest", "capi")

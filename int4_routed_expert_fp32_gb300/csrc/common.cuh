@@ -111,6 +111,32 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// SiLU(g) * u, with SiLU(g) = g / 2 + (g / 2) tanh(g / 2) (the logistic
+// function through the hardware tanh approximation, relative error ~2^-11).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  float th;
+  const float hg = 0.5f * g;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hg));
+  return fmaf(hg, th, hg) * u;
+}
+
+// Two independent fp32 FMAs in one instruction: y0 = fma(s, p0, y0) and
+// y1 = fma(s, p1, y1), each rounded as fmaf (the packed form halves the
+// issue slots; the FMA pipe rate is the same).  s2 is s in both halves
+// (pair_f32).
+__device__ __forceinline__ uint64_t pair_f32(float s) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
+}
+
+__device__ __forceinline__ void fma_f32x2(float& y0, float& y1, uint64_t s2, float p0, float p1) {
+  asm("{\n .reg .b64 a, c;\n mov.b64 a, {%2, %3};\n mov.b64 c, {%0, %1};\n"
+      " fma.rn.f32x2 c, %4, a, c;\n mov.b64 {%0, %1}, c;\n}"
+      : "+f"(y0), "+f"(y1)
+      : "f"(p0), "f"(p1), "l"(s2));
+}
+
 // ---- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

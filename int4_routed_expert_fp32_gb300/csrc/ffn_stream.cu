@@ -86,6 +86,19 @@ struct FsParams {
   int K;
   int N;
   int tma_scales;         // 1: scales by TMA (K % 256 == 0), 0: 4-byte cp.async
+  int32_t* partials;      // act_bits 8, tests only: int32 [rows_max, N, K/32] or null
+};
+
+// Where a consumer thread stores the integer group partials of its MMA
+// chains (tests only): token rows tok0, tok0 + 1 of each 8-token block and
+// weight rows n, n + 8, K/32 groups per (row, output) pair.
+struct PartialsOut {
+  int32_t* base;  // partials at (row0 + 2t, n0 + 16 cw + g, group ks * 8)
+  int N;          // outputs per row
+  int G_all;      // groups per output
+  int rows;       // rows of the chunk
+  int t2;         // 2t: first token of the thread's pair in each 8-token block
+  bool n_ok0, n_ok8;  // weight rows n and n + 8 exist
 };
 
 struct FsMaps {
@@ -165,10 +178,11 @@ struct Lane {
 
 // One K stage: up to 8 groups of 32 columns for this warp's 16-row block and
 // NTB blocks of 8 tokens.  FULL: all 8 groups present (no tail checks).
-template <bool Q8, int NTB, bool FULL>
+template <bool Q8, int NTB, bool FULL, bool WP = false>
 __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S, const uint8_t* X,
                                               const uint8_t* C, int ng, const Lane& L,
-                                              float (&acc)[NTB][4]) {
+                                              float (&acc)[NTB][4],
+                                              const PartialsOut& po = PartialsOut{}) {
   constexpr int xstride = Q8 ? kFsXStride8 : kFsXStride16;
   const uint32_t* s_lo_row = reinterpret_cast<const uint32_t*>(S + L.rlo * 16);
   const uint32_t* s_hi_row = reinterpret_cast<const uint32_t*>(S + (L.rlo + 8) * 16);
@@ -200,6 +214,17 @@ __device__ __forceinline__ void stage_compute(const uint8_t* W, const uint8_t* S
         float c[4] = {c2.x, c2.y, c2.x, c2.y};
         mma_f16_16816(c, alo, bfr[0], bfr[2], c);
         mma_f16_16816(c, ahi, bfr[1], bfr[3], c);
+        if (WP) {
+          // c holds the exact integer partials of group G: rows n, n + 8 x
+          // tokens 8 tb + 2t, + 1
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = tb * 8 + po.t2 + (i & 1);
+            if (tk < po.rows && ((i & 2) ? po.n_ok8 : po.n_ok0))
+              po.base[((size_t)(tb * 8 + (i & 1)) * po.N + ((i & 2) ? 8 : 0)) * po.G_all + G] =
+                  static_cast<int32_t>(c[i]);
+          }
+        }
         acc[tb][0] = fmaf(s_lo, c[0], acc[tb][0]);
         acc[tb][1] = fmaf(s_lo, c[1], acc[tb][1]);
         acc[tb][2] = fmaf(s_hi, c[2], acc[tb][2]);
@@ -269,7 +294,7 @@ __device__ __forceinline__ void consumer_bar_sync() {
 
 // All K stages of one unit (expert chunk x row tile) for NTB token blocks,
 // then the epilogue.  Returns false when a wait gave up.
-template <int MODE, bool Q8, int NTB>
+template <int MODE, bool Q8, int NTB, bool WP = false>
 __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t* ready,
                                              uint64_t* empty, uint32_t& it, int ksteps, int row0,
                                              int rows, int n0, int cw, int lane, const Lane& L,
@@ -293,10 +318,20 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
       const uint8_t* X = S + kFsSBytes;
       const uint8_t* C = X + kFsXBytes;
       const int ng = min(kFsGroups, (K - ks * kFsKc) / kGroup);
-      if (ng == kFsGroups)
+      if (WP) {
+        const int G_all = K / kGroup;
+        const int n = n0 + cw * 16 + L.g;
+        PartialsOut po{p.partials + ((size_t)(row0 + 2 * L.t) * N + n) * G_all + ks * kFsGroups,
+                       N, G_all, rows, 2 * L.t, n < N, n + 8 < N};
+        if (ng == kFsGroups)
+          stage_compute<Q8, NTB, true, true>(W, S, X, C, ng, L, acc, po);
+        else
+          stage_compute<Q8, NTB, false, true>(W, S, X, C, ng, L, acc, po);
+      } else if (ng == kFsGroups) {
         stage_compute<Q8, NTB, true>(W, S, X, C, ng, L, acc);
-      else
+      } else {
         stage_compute<Q8, NTB, false>(W, S, X, C, ng, L, acc);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -330,7 +365,9 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
         const float xs = Q8 ? p.x_scale[row] : 1.0f;
         const float G = acc[tb][c] * xs;
         const float U = xch[rr * kFsMc + tok] * xs;
-        const float h = G / (1.0f + expf(-G)) * U;
+        // act_bits 8: the tanh form the tensor-core exact kernel uses, so that
+        // both give the same h
+        const float h = Q8 ? silu_mul(G, U) : G / (1.0f + expf(-G)) * U;
         uint16_t* hrow = static_cast<uint16_t*>(p.out) + (size_t)row * N;
         if (Q8) {
           hrow[pair_pos(n)] = f32_to_bf16_bits(h);
@@ -457,7 +494,7 @@ __device__ __forceinline__ bool starts_unit(const FsParams& p, uint8_t* smem, ui
   return true;
 }
 
-template <int MODE, bool Q8>
+template <int MODE, bool Q8, bool WP = false>
 __global__ void __launch_bounds__(kFsThreads, 1)
     ffn_stream_kernel(const __grid_constant__ FsMaps maps, const FsParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -546,11 +583,11 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     // No early exit after a failed wait: the consumer warps meet at named
     // barriers, so all of them walk every unit (the waits then return at once).
     if (rows <= 8)
-      consume_unit<MODE, Q8, 1>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p,
-                                wt);
+      consume_unit<MODE, Q8, 1, WP>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
+                                    L, p, wt);
     else
-      consume_unit<MODE, Q8, 2>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane, L, p,
-                                wt);
+      consume_unit<MODE, Q8, 2, WP>(smem, x, ready, empty, it, ksteps, row0, rows, n0, warp, lane,
+                                    L, p, wt);
   }
 }
 
@@ -896,9 +933,9 @@ static bool make_maps(FsMaps* m, const int32_t* w0, const uint16_t* s0, const in
   return true;
 }
 
-template <int MODE, bool Q8>
+template <int MODE, bool Q8, bool WP = false>
 static int launch_stream(const FsMaps& maps, const FsParams& p, cudaStream_t s) {
-  auto kern = ffn_stream_kernel<MODE, Q8>;
+  auto kern = ffn_stream_kernel<MODE, Q8, WP>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kFsSmemBytes));
   kern<<<num_sms(), kFsThreads, kFsSmemBytes, s>>>(maps, p);
@@ -1030,9 +1067,12 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
       if (rc) return rc;
       xa = x16;
     }
-    rc = launch_tc_gateup(xa, q8 ? x_scale : nullptr, rows_max, E, D, I, gate_packed, gate_scale,
-                          up_packed, up_scale, h, big.chunk_e, big.chunk_row0, big.chunk_rows,
-                          big.n_chunks, status, s);
+    rc = q8 ? launch_tc_q8_gateup(xa, x_scale, rows_max, E, D, I, gate_packed, gate_scale,
+                                  up_packed, up_scale, h, big.chunk_e, big.chunk_row0,
+                                  big.chunk_rows, big.n_chunks, status, s)
+            : launch_tc_gateup(xa, rows_max, E, D, I, gate_packed, gate_scale, up_packed, up_scale,
+                               h, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks,
+                               status, s);
     if (rc) return rc;
   }
 
@@ -1050,9 +1090,11 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   }
   if (use_tc) {
     const uint16_t* ha = q8 ? h16 : h;
-    rc = launch_tc_down(ha, q8 ? hs : nullptr, rows_max, E, D, I, down_packed, down_scale, y,
-                        y_f32, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status,
-                        s);
+    rc = q8 ? launch_tc_q8_down(ha, hs, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
+                                big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status,
+                                s, nullptr)
+            : launch_tc_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
+                             big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
     if (rc) return rc;
   }
   return MOE_OK;
@@ -1133,6 +1175,70 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
                            y_sorted, false, ws, s);
 }
 
+extern "C" size_t moe_int4_linear_partials_workspace_size(int E, int K, int rows_max) {
+  if (E <= 0 || K <= 0 || rows_max < 0) return 256;
+  return schedule_bytes(E, rows_max) +
+         align_up((size_t)rows_max * K, 256) +                     // pair-ordered int8 x
+         align_up((size_t)rows_max * K * sizeof(uint16_t), 256);   // its fp16 form
+}
+
+extern "C" int moe_int4_linear_partials(const int8_t* x, const float* x_scale,
+                                        const int32_t* offsets, int E, int K, int N, int rows_max,
+                                        const int32_t* w_packed, const uint16_t* w_scale,
+                                        int kernel, float* out, int32_t* partials, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (E <= 0 || rows_max < 0 || N <= 0) return MOE_ERR_INVALID;
+  if (kernel != 0 && kernel != 1) return MOE_ERR_INVALID;
+  if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (rows_max == 0) return MOE_OK;
+  if (!x || !x_scale || !offsets || !w_packed || !w_scale || !out || !partials || !ws)
+    return MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4) || !aligned(out, 16) ||
+      !aligned(partials, 4) || !aligned(ws, 256))
+    return MOE_ERR_INVALID;
+  if (ws_bytes < moe_int4_linear_partials_workspace_size(E, K, rows_max)) return MOE_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* b = static_cast<char*>(ws);
+  Schedule sc = carve_one(b, E, rows_max, kernel == 0 ? kFsMc : kTcChunkRows);
+  b = static_cast<char*>(ws) + schedule_bytes(E, rows_max);
+  void* xp = b;
+  b += align_up((size_t)rows_max * K, 256);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
+  int rc = launch_to_pair_rows(x, true, rows_max, K, offsets + E, xp, status, s);
+  if (rc) return rc;
+  // every expert with rows on the chosen kernel
+  rc = launch_schedule(offsets, E, rows_max, kernel == 0 ? kFsMc : kTcChunkRows, 1, rows_max, sc,
+                       status, s);
+  if (rc) return rc;
+  if (kernel == 0) {
+    FsMaps m;
+    if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
+    FsParams p{};
+    p.x = xp;
+    p.x_scale = x_scale;
+    p.scale0 = w_scale;
+    p.out = out;
+    p.partials = partials;
+    p.chunk_e = sc.chunk_e;
+    p.chunk_row0 = sc.chunk_row0;
+    p.chunk_rows = sc.chunk_rows;
+    p.n_chunks = sc.n_chunks;
+    p.status = status;
+    p.wait_ns = kDefaultWaitNs;
+    p.K = K;
+    p.N = N;
+    p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
+    return launch_stream<kLinear, true, true>(m, p, s);
+  }
+  rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
+  if (rc) return rc;
+  return launch_tc_q8_down(x16, x_scale, rows_max, E, N, K, w_packed, w_scale, out, true,
+                           sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks, status, s,
+                           partials);
+}
+
 extern "C" size_t moe_int4_linear_workspace_size(int E, int K, int rows_max) {
   if (E <= 0 || K <= 0 || rows_max < 0) return 256;
   return schedule_bytes(E, rows_max) +
@@ -1196,6 +1302,10 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
     if (rc) return rc;
     xa = x16;
   }
-  return launch_tc_down(xa, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale, out,
-                        true, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+  if (q8)
+    return launch_tc_q8_down(xa, x_scale, rows_max, E, N, K, w_packed, w_scale, out, true,
+                             big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s,
+                             nullptr);
+  return launch_tc_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big.chunk_e,
+                        big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
 }

@@ -30,11 +30,8 @@
 // K stages of 128 columns halve the per-stage barrier waits and handoffs
 // against 64-column stages (each mbarrier wait costs a dequantisation warp
 // ~130 cycles even on a completed phase).
-// act_bits 8 (Q8): the B operand is the fp16 copy of the int8 rows (exact);
-// every product q * scale * x_q is exact in fp32 and the accumulation is in
-// fp32 (with unit scales the integer sum itself, exact while |sum| < 2^24).
-// The epilogue applies the row scales; gate/up tiles store h in bf16 for the
-// per-row re-quantisation of the down input.
+// act_bits 8 has its own kernel (ffn_tc_q8.cu), which keeps the integer
+// partial of every weight group.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -106,7 +103,7 @@ __device__ __forceinline__ uint32_t scale_f16x2(uint32_t bf16_bits) {
   return u | (u << 16);
 }
 
-template <int MODE, bool Q8>
+template <int MODE>
 __global__ void __launch_bounds__(kTxThreads, 1)
     ffn_tc_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -349,26 +346,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const int tok = c0 + i;
               if (tok >= rows || n >= N) continue;
-              float G = __uint_as_float(g[i]), U = __uint_as_float(v[i]);
-              if (Q8) {
-                const float xs = p.x_scale[row0 + tok];
-                G *= xs;
-                U *= xs;
-              }
-              // SiLU(G) * U with SiLU(G) = G/2 + (G/2) tanh(G/2) (the
-              // logistic function through the hardware tanh approximation,
-              // relative error ~2^-11, the size of h's fp16 rounding)
-              float th;
-              const float hg = 0.5f * G;
-              asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hg));
-              const float h = fmaf(hg, th, hg) * U;
-              uint32_t hbits;
-              if (Q8) {  // bf16 h, as the stream kernel writes it
-                hbits = f32_to_bf16_bits(h);
-              } else {
-                fin &= fabsf(h) <= 65504.0f;
-                hbits = __half_as_ushort(__float2half_rn(h));
-              }
+              const float G = __uint_as_float(g[i]), U = __uint_as_float(v[i]);
+              // SiLU through the hardware tanh approximation (relative error
+              // ~2^-11, the size of h's fp16 rounding)
+              const float h = silu_mul(G, U);
+              fin &= fabsf(h) <= 65504.0f;
+              const uint32_t hbits = __half_as_ushort(__float2half_rn(h));
               hb[sl][i >> 1] |= hbits << (16 * (i & 1));
             }
           }
@@ -408,8 +391,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 #pragma unroll
               for (int i = 0; i < 16; ++i, o += N) {
                 if (c0 + i >= rows) break;
-                float y = __uint_as_float(b2 ? v[i] : g[i]);
-                if (Q8) y *= p.x_scale[row0 + c0 + i];
+                const float y = __uint_as_float(b2 ? v[i] : g[i]);
                 if (MODE == kTxDown)
                   static_cast<uint16_t*>(p.out)[o] = f32_to_bf16_bits(y);
                 else
@@ -554,9 +536,9 @@ static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
                            CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int MODE, bool Q8>
+template <int MODE>
 static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
-  auto kern = ffn_tc_kernel<MODE, Q8>;
+  auto kern = ffn_tc_kernel<MODE>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTxSmem));
   kern<<<num_sms(), kTxThreads, kTxSmem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
@@ -567,7 +549,7 @@ static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
 // beyond K.
 bool tc_path_supported(int K) { return K % kTxXK == 0; }
 
-int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D, int I,
+int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
                      const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e,
@@ -581,7 +563,6 @@ int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, in
   TxParams p{};
   p.scale0 = gate_scale;
   p.scale1 = up_scale;
-  p.x_scale = x_scale;
   p.out = h;
   p.chunk_e = chunk_e;
   p.chunk_row0 = chunk_row0;
@@ -591,10 +572,10 @@ int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, in
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  return x_scale ? launch_tc<kTxGateUp, true>(maps, p, s) : launch_tc<kTxGateUp, false>(maps, p, s);
+  return launch_tc<kTxGateUp>(maps, p, s);
 }
 
-int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int E, int D, int I,
+int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s) {
@@ -605,7 +586,6 @@ int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int 
   TxParams p{};
   p.scale0 = down_scale;
   p.scale1 = down_scale;
-  p.x_scale = h_scale;
   p.out = y;
   p.chunk_e = chunk_e;
   p.chunk_row0 = chunk_row0;
@@ -615,9 +595,7 @@ int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int 
   p.wait_ns = kDefaultWaitNs;
   p.K = I;
   p.N = D;
-  if (h_scale)
-    return y_f32 ? launch_tc<kTxLinear, true>(maps, p, s) : launch_tc<kTxDown, true>(maps, p, s);
-  return y_f32 ? launch_tc<kTxLinear, false>(maps, p, s) : launch_tc<kTxDown, false>(maps, p, s);
+  return y_f32 ? launch_tc<kTxLinear>(maps, p, s) : launch_tc<kTxDown>(maps, p, s);
 }
 
 }  // namespace moe

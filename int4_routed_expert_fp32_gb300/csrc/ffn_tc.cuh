@@ -11,8 +11,9 @@ namespace moe {
 struct TxParams {
   const uint16_t* scale0;  // bf16 [E, N, K/32] (gate, or the single matrix)
   const uint16_t* scale1;  // bf16 [E, N, K/32] (up)
-  const float* x_scale;    // act_bits 8: row scales of the int8 rows, else null
+  const float* x_scale;    // act_bits 8: row scales of the int8 rows
   void* out;               // fp16 h (bf16 h in act_bits 8) / bf16 y / fp32 y  [rows_max, N]
+  int32_t* partials;       // act_bits 8, tests only: int32 [rows_max, N, K/32] or null
   const int32_t* chunk_e;
   const int32_t* chunk_row0;
   const int32_t* chunk_rows;
@@ -46,19 +47,36 @@ int launch_to_pair_rows(const void* src, bool src_i8, int R, int C, const int32_
 int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t* row_count,
                        uint16_t* dst, cudaStream_t s);
 
-// h[rows] = SiLU(x W_gate^T) * (x W_up^T) for the listed 128-row chunks; x16
-// is the fp16 copy of the activations.  x_scale null: bf16 activations, h in
-// fp16.  x_scale set: int8 activations with these row scales, h in bf16.
-int launch_tc_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D, int I,
+// h[rows] = SiLU(x W_gate^T) * (x W_up^T) for the listed 128-row chunks
+// (act_bits 16); x16 is the fp16 copy of the activations (pair order), h is
+// written in fp16, pair order.
+int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
                      const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e, const int32_t* chunk_row0,
                      const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
                      cudaStream_t s);
 
-// y[rows] = h16 W_down^T (times h_scale[row] when given: int8 rows) for the
-// listed chunks; bf16 y, or fp32 with y_f32.
-int launch_tc_down(const uint16_t* h16, const float* h_scale, int rows_max, int E, int D, int I,
+// act_bits 8 on the tensor cores (ffn_tc_q8.cu): exact int4 x int8 group
+// partials, y = sc_x * (fp32 chain of fma(s_w[g], P[g], .) in group order).
+// x16 / h16: fp16 copies of the int8 rows.  Gate/up stores h in bf16 (pair
+// order) for its re-quantisation.  partials (tests only, down / linear): also
+// store every P as int32 [rows_max, N, K/32] (then y is fp32).
+int launch_tc_q8_gateup(const uint16_t* x16, const float* x_scale, int rows_max, int E, int D,
+                        int I, const int32_t* gate_packed, const uint16_t* gate_scale,
+                        const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
+                        const int32_t* chunk_e, const int32_t* chunk_row0,
+                        const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                        cudaStream_t s);
+int launch_tc_q8_down(const uint16_t* h16, const float* h_scale, int rows_max, int E, int D, int I,
+                      const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
+                      const int32_t* chunk_e, const int32_t* chunk_row0,
+                      const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                      cudaStream_t s, int32_t* partials);
+
+// y[rows] = h16 W_down^T for the listed chunks (act_bits 16); bf16 y, or fp32
+// with y_f32.
+int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s);

@@ -82,3 +82,20 @@ def random_topk(T: int, E: int, k: int, rng: np.random.Generator, hot=None) -> n
     for t in range(T):
         out[t] = rng.choice(E, size=k, replace=False, p=p)
     return out
+
+
+def fp32_group_chain(P, scale_bits, x_scale) -> np.ndarray:
+    """The fp32 evaluation the library states for act_bits 8 (include/moe.h,
+    moe_int4_linear): acc = fma(scale[n, g], P[r, n, g], acc) over the groups
+    g in K order from acc = 0, then y = x_scale[r] * acc, all IEEE fp32.
+
+    P [R, N, G] exact integers (int64), scale_bits bf16 [N, G], x_scale fp32
+    [R].  Every product scale * P is exact in fp32 (8 significant bits times
+    at most 15), so each fma is one fp32 addition of the exact product."""
+    P = np.asarray(P)
+    s = O.bf16_bits_to_f64(scale_bits).astype(np.float32)  # exact
+    acc = np.zeros(P.shape[:2], dtype=np.float32)
+    for g in range(P.shape[2]):
+        prod = s[None, :, g] * P[:, :, g].astype(np.float32)  # exact in fp32
+        acc = (acc + prod).astype(np.float32)
+    return (acc * np.asarray(x_scale, dtype=np.float32)[:, None]).astype(np.float32)

@@ -11,7 +11,8 @@ import torch
 import oracle as O
 import workloads as wl
 from oracle import inputs as oi
-from tests._helpers import assert_close, bf16_bits, conditioned_attempts, random_topk, rel_l2
+from tests._helpers import (assert_close, bf16_bits, conditioned_attempts, fp32_group_chain,
+                            random_topk, rel_l2)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -349,24 +350,68 @@ def test_int4_linear_exact_integer_accumulators(moe, K, N, counts):
         assert np.all(got[a:b] == P)   # exactly integral in fp32
 
 
-def test_int4_linear_exact_mode_scaled(moe):
-    rng = np.random.default_rng(8)
-    K, N, counts = 512, 384, [9, 0, 41]
+@pytest.mark.parametrize("K,N,counts", [
+    (512, 384, [9, 0, 41, 70]),      # 41 and 70 rows on the tensor cores
+    (7168, 300, [5, 17, 0, 40, 130]),  # full width, ragged N tile, one expert of two chunks
+])
+def test_int4_linear_exact_mode_scaled(moe, K, N, counts):
+    """Real (non-unit) scales: the output is the fp32 chain of the exact group
+    partials that the header states, bit for bit, on the library's own
+    choice of kernel per expert; and within fp32 rounding of the fp64
+    oracle's sum."""
+    rng = np.random.default_rng(8 + K)
     E = len(counts)
     off = _segments(counts)
     R = int(off[-1])
-    packed, scale = _random_int4(rng, E, N, K)
+    packed, scale = _random_int4(rng, E, N, K, 0.002, 0.02)
     x = _bf16(rng.normal(size=(R, K)) * 3)
     q, sx = O.quantize_rows_int8(x.float().numpy())
     got = moe.int4_linear(_t(q), _t(sx), _t(off), _t(packed), _t(scale, torch.bfloat16), 8)
+    assert moe.check_error() == 0
     got = got.cpu().numpy()
     for e in range(E):
         a, b = off[e], off[e + 1]
         if a == b:
             continue
+        P = O.int4_group_partials(q[a:b], packed[e])
+        assert np.array_equal(got[a:b], fp32_group_chain(P, scale[e], sx[a:b])), e
         ref = O.int4_linear(oi.x_f64(x)[a:b], packed[e], scale[e], 8)
-        # exact integer partials; fp32 scaling and group sum only
         assert rel_l2(got[a:b], ref) <= 1e-6
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_int4_linear_exact_group_partials(moe, kernel):
+    """The int32 group partials of the exact mode, read out of either kernel
+    (0: stream, 1: tensor cores), equal the oracle's int64 partials bit for
+    bit at K = 7168 with non-unit scales, for experts of 5, 17, 40 and 130
+    rows (one 128-row tile plus a ragged one) and a ragged output tile; the
+    output is their fp32 chain, the same bits on both kernels."""
+    rng = np.random.default_rng(11)
+    K, N, counts = 7168, 300, [5, 17, 0, 40, 130]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed, scale = _random_int4(rng, E, N, K, 0.002, 0.02)
+    packed[:, :, :4] = np.int32(-2004318072)   # 0x88888888: every nibble -8
+    packed[:, 7, 8:12] = np.int32(0x77777777)  # every nibble +7
+    q = rng.integers(-127, 128, size=(R, K)).astype(np.int8)
+    q[:, :32] = -127                            # extreme products in the first group
+    q[:, 64:96] = 127
+    xs = rng.uniform(1e-3, 1e-1, size=R).astype(np.float32)
+    out, P = moe.int4_linear_partials(_t(q), _t(xs), _t(off), _t(packed),
+                                      _t(scale, torch.bfloat16), kernel)
+    assert moe.check_error() == 0
+    out, P = out.cpu().numpy(), P.cpu().numpy()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        ref = O.int4_group_partials(q[a:b], packed[e])
+        assert np.array_equal(P[a:b].astype(np.int64), ref), e
+        assert np.array_equal(out[a:b], fp32_group_chain(ref, scale[e], xs[a:b])), e
+    # the library's own routing of the same call gives the same bits
+    lib = moe.int4_linear(_t(q), _t(xs), _t(off), _t(packed), _t(scale, torch.bfloat16), 8)
+    assert np.array_equal(lib.cpu().numpy(), out)
 
 
 # ------------------------------------------------------------- expert FFN
