@@ -28,14 +28,13 @@
 //     (the MMA's A operand, M = 128 weight rows);
 //   * warp 1 (whole warp, one elected lane issues): per group two MMAs into
 //     one of three 128-column TMEM group buffers, committed per group;
-//   * warps 6-21: per group, tcgen05.ld of the partials (lane = weight row,
-//     column = token) in two halves, the second in flight while the first
-//     is accumulated, release of the buffer, then y = fma(s_w, P, y) in
-//     registers (32 tokens per thread, four warps per lane quarter).  After
-//     the last group a gate/up unit pairs each gate lane with its up lane
-//     (lanes i and i + 16 of a lane quarter) and stores h = SiLU(G) * U in
-//     bf16, pair order; a down unit stores y (bf16, or fp32 for the plain
-//     linear).
+//   * warps 6-13: per group, tcgen05.ld of the partials (lane = weight row,
+//     column = token) in four 16-token pieces, each accumulated as
+//     y = fma(s_w, P, y) in registers (64 tokens per thread, two warps per
+//     lane quarter), and release of the buffer after the last piece is read.  After the last group a gate/up unit pairs each gate
+//     lane with its up lane (lanes i and i + 16 of a lane quarter) and stores
+//     h = SiLU(G) * U in bf16, pair order; a down unit stores y (bf16, or
+//     fp32 for the plain linear).
 // WP (tests only): every partial P is also stored, as int32, to p.partials
 // [rows_max, N, K/32].
 #include <cuda_fp16.h>
@@ -59,13 +58,13 @@ constexpr int kQXBytes = 2 * kQXBoxBytes;       // 32 KiB token tile
 constexpr int kQQBytes = kQM * kQBK / 2;        // 8 KiB packed int4 (128 rows x 64 bytes)
 constexpr int kQStageBytes = kQXBytes + kQQBytes;
 constexpr int kQDqWarps = 4;                    // one per lane quarter, a whole stage per row
-constexpr int kQEpWarps = 16;                   // (lane quarter, quarter of the tokens)
+constexpr int kQEpWarps = 8;                    // (lane quarter, half of the tokens)
 constexpr int kQThreads = (2 + kQDqWarps + kQEpWarps) * 32;
 constexpr uint32_t kQCols = 512;
 constexpr uint32_t kQACol = kQGBufs * kQTN;     // A ring after the group buffers
 constexpr uint32_t kQASlot = kQBK / 2;          // 64 columns: 128 fp16 per row
 constexpr int kQSmem = kQStages * kQStageBytes + 1024 + 256;
-constexpr int kQEpCols = kQTN / 4;              // tokens per epilogue thread
+constexpr int kQEpCols = kQTN / 2;              // tokens per epilogue thread
 static_assert(kQStageBytes % 1024 == 0, "stage alignment");
 static_assert(kQDqWarps * 32 == kQM, "one conversion thread per row");
 static_assert(kQACol + kQAStages * kQASlot <= kQCols, "TMEM budget");
@@ -267,7 +266,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3;
-    const int eh = (warp - 2 - kQDqWarps) >> 2;  // tokens 32 eh .. 32 eh + 31
+    const int eh = (warp - 2 - kQDqWarps) >> 2;  // tokens 64 eh .. 64 eh + 63
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
     // output of this lane: gate/up units pair lane i (gate) with lane i + 16
     // (up) of the same quarter
@@ -311,30 +310,30 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         tc_fence_after();
         if (any) {
-          // two 16-token halves: the second load is in flight while the first
-          // half is accumulated; the buffer is released once both are read
-          uint32_t v0[16], v1[16];
+          // four 16-token pieces; the buffer is released once all are read
           const uint32_t ta = tbase + t_lane + b * kQTN + c0;
-          tmem_ld16(ta, v0);
-          tmem_ld_wait();
-          tmem_ld16(ta + 16, v1);
 #pragma unroll
-          for (int j = 0; j < 16; j += 2)
-            fma_f32x2(y[j], y[j + 1], sg2, __uint_as_float(v0[j]), __uint_as_float(v0[j + 1]));
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&gempty[b]);
+          for (int pc = 0; pc < 4; ++pc) {
+            uint32_t vc[16];
+            tmem_ld16(ta + 16 * pc, vc);
+            tmem_ld_wait();
+            if (pc == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&gempty[b]);
+            }
 #pragma unroll
-          for (int j = 0; j < 16; j += 2)
-            fma_f32x2(y[16 + j], y[17 + j], sg2, __uint_as_float(v1[j]), __uint_as_float(v1[j + 1]));
-          if (WP) {
+            for (int j = 0; j < 16; j += 2)
+              fma_f32x2(y[16 * pc + j], y[16 * pc + j + 1], sg2, __uint_as_float(vc[j]),
+                        __uint_as_float(vc[j + 1]));
+            if (WP) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c0 + j;
-              if (valid && col < rows)
-                p.partials[((size_t)(row0 + col) * N + o) * G_all + g] =
-                    static_cast<int32_t>(__uint_as_float(j < 16 ? v0[j] : v1[j - 16]));
+              for (int j = 0; j < 16; ++j) {
+                const int col = c0 + 16 * pc + j;
+                if (valid && col < rows)
+                  p.partials[((size_t)(row0 + col) * N + o) * G_all + g] =
+                      static_cast<int32_t>(__uint_as_float(vc[j]));
+              }
             }
           }
         } else {
@@ -345,18 +344,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       if (!ok || !any) continue;
       if (MODE == kQGateUp) {
-        // lanes i and i + 16 hold G and U of output o for the warp's 32
-        // tokens; the gate lane finishes tokens 0-15, the up lane 16-31
+        // lanes i and i + 16 hold G and U of output o for the warp's 64
+        // tokens; the gate lane finishes tokens 0-31, the up lane 32-63
         uint16_t* hcol = static_cast<uint16_t*>(p.out) + pair_pos(o);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float mine = up_lane ? y[j] : y[16 + j];
+        for (int j = 0; j < 32; ++j) {
+          const float mine = up_lane ? y[j] : y[32 + j];
           const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-          const int col = c0 + (up_lane ? 16 + j : j);
+          const int col = c0 + (up_lane ? 32 + j : j);
           if (!valid || col >= rows) continue;
           const float xs = p.x_scale[row0 + col];
           const float G = (up_lane ? other : y[j]) * xs;
-          const float U = (up_lane ? y[16 + j] : other) * xs;
+          const float U = (up_lane ? y[32 + j] : other) * xs;
           hcol[(size_t)(row0 + col) * N] = f32_to_bf16_bits(silu_mul(G, U));
         }
       } else if (valid) {
