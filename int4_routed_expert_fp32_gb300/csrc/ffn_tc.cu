@@ -15,11 +15,13 @@
 //     weights are written in the same order, the order of the nibble pairs
 //     of a word.  With a bf16 scale (8 significant bits) and |q| <= 8,
 //     q * scale has at most 11 significant bits: it is exact in fp16 for
-//     scales in [2^-17, 8188].  The activations arrive in fp16 (a copy made
-//     once per call; bf16 values are exact in fp16 for 2^-17 <= |x| <= 65504),
-//     and the gate/up tiles write h in fp16 for the down tiles.  So, as in
-//     the stream kernel, the weights are never rounded; a value beyond the
-//     fp16 range makes its output non-finite and records MOE_ERR_UNSUPPORTED;
+//     scales in [2^-17, 8160] (and zero); a scale outside that range records
+//     MOE_ERR_UNSUPPORTED (the stream kernel, which applies scales in fp32,
+//     takes any scale).  The activations arrive in fp16 (a copy made once per
+//     call; bf16 values are exact in fp16 for 2^-17 <= |x| <= 65504), and the
+//     gate/up tiles write h in fp16 for the down tiles.  So, as in the stream
+//     kernel, the weights are never rounded silently; a value beyond the fp16
+//     range makes its output non-finite and records MOE_ERR_UNSUPPORTED;
 //   * warp 1 (whole warp, one elected lane issues): tcgen05.mma kind::f16,
 //     A from TMEM (M = 128 weight rows per block, two blocks), B the token
 //     tile (N = the chunk's rows rounded up to 16), K = 16, into two
@@ -101,6 +103,19 @@ __device__ __forceinline__ uint32_t scale_f16x2(uint32_t bf16_bits) {
   const __half h = __float2half_rn(__uint_as_float(bf16_bits << 16));
   const uint32_t u = __half_as_ushort(h);
   return u | (u << 16);
+}
+
+// Whether q * scale is exact in fp16 for every q in [-8, 7], for the two bf16
+// scales of a word.  A bf16 scale m * 2^(e-7) (m the 8-bit significand)
+// times q has at most 11 significant bits and its lowest set bit is at least
+// 2^(e-7); fp16 holds it exactly when that bit is at least 2^-24 (e >= -17,
+// exponent field >= 110) and |8 * scale| <= 65504 (e <= 12, field <= 139:
+// the largest such bf16 is 8160).  Zero is exact; subnormal, infinite and
+// NaN scales are not.
+__device__ __forceinline__ bool scales_exact_f16(uint32_t w) {
+  const uint32_t f0 = (w >> 7) & 0xFFu, f1 = (w >> 23) & 0xFFu;
+  const bool z0 = (w & 0x7FFFu) == 0, z1 = (w & 0x7FFF0000u) == 0;
+  return (z0 || (f0 - 110u) <= 29u) && (z1 || (f1 - 110u) <= 29u);
 }
 
 template <int MODE>
@@ -273,6 +288,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                    : 0u;
       };
       uint32_t s_a = scale_word(0), s_b = scale_word(1), s_c = scale_word(2);
+      bool exact = true;  // every scale of this unit's row converts exactly
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
         const uint32_t sw = s_a;
         s_a = s_b;
@@ -290,6 +306,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const uint4 w0 = *reinterpret_cast<const uint4*>(qt + qoff0);
         const uint4 w1 = *reinterpret_cast<const uint4*>(qt + qoff1);
         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        exact &= scales_exact_f16(sw);
         const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 4 ks + 2 gh
         const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 4 ks + 2 gh + 1
         uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
@@ -309,6 +326,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&aready[a]);
       }
+      if (!exact) record_status(p.status, MOE_ERR_UNSUPPORTED);
     }
   } else {
     // ------------------------------------------------------------ epilogue

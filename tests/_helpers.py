@@ -99,3 +99,69 @@ def fp32_group_chain(P, scale_bits, x_scale) -> np.ndarray:
         prod = s[None, :, g] * P[:, :, g].astype(np.float32)  # exact in fp32
         acc = (acc + prod).astype(np.float32)
     return (acc * np.asarray(x_scale, dtype=np.float32)[:, None]).astype(np.float32)
+
+
+def _expert_rows(job):
+    """Worker: one expert's gated MLP on its rows (oracle, fp64)."""
+    w, e, u, act_bits = job
+    return O.expert_ffn(u, oi.expert_arrays(w, e), act_bits)
+
+
+def oracle_tokens(w: wl.Workload, x, router, latent, tokens, workers: int = 8) -> np.ndarray:
+    """The oracle's layer output for the listed tokens of workload ``w``.
+
+    Same arithmetic as ``oracle.moe_forward(x, params, tokens)`` (routing,
+    expert input, per-slot expert outputs summed in slot order, latent
+    wrap), with the rows of each selected expert evaluated together and the
+    experts spread over a pool of processes (started with spawn, so it is
+    safe after CUDA has been initialised).  Every row is independent in the
+    definition, so grouping changes no value."""
+    import multiprocessing as mp
+    p = oi.layer_params(w, router=router, latent=latent)
+    xs = oi.x_f64(x)[np.asarray(tokens)]
+    rt = O.route(xs, p.w_router, p.bias, w.k, w.renorm)
+    u = O.expert_input(xs, p)
+    experts = sorted({int(e) for e in rt.idx.ravel()})
+    rows = {e: np.nonzero((rt.idx == e).any(axis=1))[0] for e in experts}
+    jobs = [(w, e, u[rows[e]], w.act_bits) for e in experts]
+    if workers > 1 and len(jobs) > 1:
+        with mp.get_context("spawn").Pool(min(workers, len(jobs))) as pool:
+            outs = pool.map(_expert_rows, jobs, chunksize=1)
+    else:
+        outs = [_expert_rows(j) for j in jobs]
+    y = {e: dict(zip(rows[e].tolist(), o)) for e, o in zip(experts, outs)}
+    out = np.zeros_like(u)
+    for i in range(len(xs)):
+        for j in range(w.k):
+            e = int(rt.idx[i, j])
+            out[i] += rt.weight[i, j] * y[e][i]
+    return O.latent_out(out, p)
+
+
+def targeted_tokens(w: wl.Workload, x, router, n: int = 32, seed: int = 2024) -> list:
+    """n tokens of workload ``w`` chosen to reach the expert kernels' edge
+    cases: the last token, the rows of the hottest experts' last (ragged)
+    128-row chunk, every 128-row chunk boundary of the hottest experts,
+    experts of exactly 16 and 17 rows (the last stream-kernel size and the
+    first tensor-core size), then random tokens.  Routing is the oracle's."""
+    if w.T <= n:
+        return list(range(w.T))
+    W, b = router
+    rt = O.route(oi.x_f64(x), W.numpy(), b.numpy(), w.k, w.renorm)
+    toks = {w.T - 1}
+    counts = np.bincount(rt.idx.ravel(), minlength=w.E)
+    rows_of = lambda e: np.nonzero((rt.idx == e).any(axis=1))[0]   # ascending token ids
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        r = rows_of(e)
+        last0 = (len(r) - 1) // 128 * 128                 # first row of the last chunk
+        toks.update(int(t) for t in (r[last0], r[-1]))
+        toks.update(int(r[c]) for c in range(127, len(r), 128)[:3])   # chunk edges
+        toks.update(int(r[c]) for c in range(128, len(r), 128)[:3])
+    for size in (16, 17):
+        for e in np.nonzero(counts == size)[0][:2]:
+            r = rows_of(e)
+            toks.update(int(t) for t in (r[0], r[-1]))
+    rng = np.random.default_rng(seed)
+    while len(toks) < n:
+        toks.add(int(rng.integers(w.T)))
+    return sorted(toks)[: max(n, len(toks))]

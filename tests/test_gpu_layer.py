@@ -12,7 +12,8 @@ import torch
 import oracle as O
 import workloads as wl
 from oracle import inputs as oi
-from tests._helpers import assert_close, conditioned_attempts, device_weights
+from tests._helpers import (assert_close, conditioned_attempts, device_weights, oracle_tokens,
+                            targeted_tokens)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -73,18 +74,11 @@ def test_layer_small_all_tokens(moe, case):
 
 # ----------------------------------------------------------- full sizes
 
-FULL_SAMPLE = {"decode": 8, "prefill": 4, "latent": 4, "exact": 4}
-
-
-def _sample_tokens(w, n, counts_hot=True):
-    rng = np.random.default_rng(2024)
-    toks = set(rng.choice(w.T, size=n - 1, replace=False).tolist())
-    toks.add(w.T - 1)   # the ragged end of the last chunk
-    return sorted(toks)
-
-
 @pytest.mark.parametrize("name", ["decode", "prefill", "latent", "exact"])
 def test_layer_full_size_sampled(moe, name):
+    """The full workloads against the oracle on at least 32 tokens each (all
+    32 at decode), chosen to reach the hottest experts' last ragged chunks,
+    128-row chunk boundaries and experts of exactly 16 and 17 rows."""
     w = wl.WORKLOADS[name]
     x = wl.gen_x(w)
     router = wl.gen_router(w)
@@ -94,8 +88,9 @@ def test_layer_full_size_sampled(moe, name):
     assert moe.check_error() == 0
     out = out.float().cpu().numpy()
     assert np.all(np.isfinite(out))
-    toks = _sample_tokens(w, FULL_SAMPLE[name])
-    ref = O.moe_forward(oi.x_f64(x), oi.layer_params(w, router=router, latent=lat), tokens=toks)
+    toks = targeted_tokens(w, x, router)
+    assert len(toks) >= min(32, w.T)
+    ref = oracle_tokens(w, x, router, lat, toks)
     assert_close(out[toks], ref, what=name)
 
 

@@ -319,6 +319,93 @@ def test_int4_linear_w4a16(moe, K, N, counts):
         assert rel_l2(got[a:b], ref) <= 1e-5
 
 
+def _extreme_scales(rng, E, N, K, lo=1e-30, tiny=1e-7, big=1e2, huge=2e4, small=3e-6):
+    """bf16 group scales spanning ``lo`` .. ``huge`` in chosen weight rows:
+    all tiny, tiny and large mixed, all large, huge (q * s beyond 65504 when
+    huge > 8160), just below 2^-17 (``small``), zero, extremely small, six
+    decades in one row; the other rows U(0.002, 0.01)."""
+    G = K // 32
+    s = rng.uniform(0.002, 0.01, size=(E, N, G)).astype(np.float32)
+    s[:, 0] = tiny
+    s[:, 1, 0::2], s[:, 1, 1::2] = tiny, big
+    s[:, 2] = big
+    s[:, 3] = huge
+    s[:, 4] = small
+    s[:, 5] = 0.0
+    s[:, 6] = lo
+    s[:, 7] = rng.choice([tiny * 10, 1e-3, 1.0, big / 4], size=(E, G))
+    return O.f32_to_bf16_bits(s)
+
+
+def _check_columns(got, ref, what):
+    """Every weight row (output column) against the oracle on its own, so a
+    row of tiny scales cannot hide behind rows of large ones."""
+    for n in range(ref.shape[1]):
+        g, r = got[:, n], ref[:, n]
+        if not np.any(r):
+            assert not np.any(g), (what, n)
+            continue
+        assert rel_l2(g, r) <= 3e-5, (what, n, rel_l2(g, r))
+
+
+@pytest.mark.parametrize("act_bits", [16, 8])
+def test_int4_linear_extreme_scales_both_kernels(moe, act_bits):
+    """Weight scales from 1e-30 to 2e4 on both expert kernels (9 rows: stream
+    kernel; 40 rows: tensor cores), each weight row checked on its own:
+    relative L2 <= 3e-5 per column, and the exact mode's fp32 chain bit for
+    bit.  The bound: fp32 accumulation of exact products, plus, on the stream
+    kernel, the start value -(1032 S_lo + 72 S_hi) of each group's fp16
+    chain, which leaves an absolute error of about 2^-24 * 1040 * sum|x| per
+    group (~1e-5 relative on one column; 1e-5 over a whole matrix, as
+    test_int4_linear_w4a16 checks).
+
+    The stream kernel and the exact mode apply scales in fp32 and take any
+    scale.  The act_bits 16 tensor-core kernel multiplies q * scale in fp16,
+    exact for scales in [2^-17, 8160]: outside that range it records
+    MOE_ERR_UNSUPPORTED (checked here), and inside it (scales 1e-5 .. 8000)
+    it matches like the stream kernel."""
+    rng = np.random.default_rng(17 + act_bits)
+    K, N, counts = 2048, 136, [9, 40]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed = rng.integers(0, 2 ** 32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    x = _bf16(rng.normal(size=(R, K)))
+    xf = oi.x_f64(x)
+    q, sx = O.quantize_rows_int8(x.float().numpy())
+
+    def run(scale):
+        if act_bits == 16:
+            return moe.int4_linear(x.to(DEV), None, _t(off), _t(packed),
+                                   _t(scale, torch.bfloat16), 16).cpu().numpy()
+        return moe.int4_linear(_t(q), _t(sx), _t(off), _t(packed), _t(scale, torch.bfloat16),
+                               8).cpu().numpy()
+
+    scale = _extreme_scales(rng, E, N, K)
+    got = run(scale)
+    status = moe.check_error()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if act_bits == 16 and e == 1:
+            continue   # out-of-range scales on the fp16 tensor-core path: reported below
+        ref = O.int4_linear(xf[a:b], packed[e], scale[e], act_bits)
+        if act_bits == 8:
+            P = O.int4_group_partials(q[a:b], packed[e])
+            assert np.array_equal(got[a:b], fp32_group_chain(P, scale[e], sx[a:b])), e
+        _check_columns(got[a:b], ref, f"expert {e}")
+    if act_bits == 8:
+        assert status == 0
+        return
+    assert status == moe.capi.MOE_ERR_UNSUPPORTED
+    # the tensor-core kernel's exact range: 2^-17 (7.6e-6) .. 8160
+    scale = _extreme_scales(rng, E, N, K, lo=8e-6, tiny=1e-5, big=64.0, huge=8000.0, small=7.7e-6)
+    got = run(scale)
+    assert moe.check_error() == 0
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        _check_columns(got[a:b], O.int4_linear(xf[a:b], packed[e], scale[e], 16), f"expert {e}")
+
+
 @pytest.mark.parametrize("K,N,counts", [
     (320, 300, [0, 1, 33, 70, 8]),   # 33 and 70 rows on the tensor cores
     (7168, 256, [2, 40]),            # all on the stream kernel (fewer than 48 rows)
