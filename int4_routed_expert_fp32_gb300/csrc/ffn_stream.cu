@@ -310,9 +310,12 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
-    // warp-uniform outcome: the MMAs below need the whole warp
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ready[s], ph, wt));
-    if (ok) {
+    if (ok && !mbar_wait(&ready[s], ph, wt)) ok = false;
+    // The stage is computed whatever the wait's outcome, so every lane runs
+    // the warp-collective ldmatrix and MMAs (after a wait that gave up, on
+    // data that may be stale, all inside this CTA's ring; the epilogue then
+    // stores nothing).
+    {
       const uint8_t* W = smem + s * kFsStageBytes;
       const uint8_t* S = W + kFsWBytes;
       const uint8_t* X = S + kFsSBytes;

@@ -5,9 +5,10 @@
 // "Bias the choice of experts while retaining original affinities",
 // "MoEGate.forward: topk weight" and "Normalize the selected routing
 // affinities").  One expert group: group-limited masking is the identity.
-// Few tokens: split-K fp32 SIMT logits (the weight read dominates).  Many
-// tokens: the fp32 weight is split exactly into three bf16 terms and the
-// logits come from tcgen05 GEMMs with fp32 accumulation.
+// Few tokens: split-K fp32 SIMT logits (the weight read dominates); up to 32
+// tokens one lane per token.  Many tokens: the fp32 weight is split exactly
+// into three bf16 terms and the logits come from tcgen05 GEMMs with fp32
+// accumulation.
 #include <math.h>
 
 #include <algorithm>
@@ -97,6 +98,89 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
       const int e = e0 + tx * 4 + j;
       if (e < E) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i][j];
     }
+  }
+}
+
+// Decode-sized batches (T <= 32): one lane per token.  A CTA of eight warps
+// takes 32 experts x 512 columns: the fp32 weight tile and the tokens' bf16
+// x slice are copied to shared memory up front (16-byte cp.async, all in
+// flight at once; x rows padded by 16 bytes so that the lanes' 16-byte reads
+// of 32 different rows hit distinct banks), then each lane accumulates its
+// token against the four experts of its warp, the weights read as
+// shared-memory broadcasts (one 16-byte read per four FMAs).
+// part[z, t, e] = the z-th 512-column slice's dot product, in column order.
+constexpr int kRwExperts = 32;               // experts per CTA (4 per warp)
+constexpr int kRwK = 512;                    // K columns per CTA
+constexpr int kRwMaxTokens = 32;             // one lane per token
+constexpr int kRwXStride = kRwK * 2 + 16;    // bytes per x row in shared memory
+constexpr int kRwSmem = kRwExperts * kRwK * 4 + kRwMaxTokens * kRwXStride;  // 97 KiB
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(256) router_logits_warp_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ W,
+                                                                 int T, int H, int E,
+                                                                 float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  float* wsm = reinterpret_cast<float*>(rsm);              // [kRwExperts][kRwK]
+  uint8_t* xsm = rsm + kRwExperts * kRwK * 4;              // [kRwMaxTokens][kRwXStride]
+  const int e0 = blockIdx.x * kRwExperts;
+  const int k0 = blockIdx.y * kRwK;
+  const int kn = min(kRwK, H - k0);  // multiple of 64 (H % 64 == 0)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // weight tile (rows of experts beyond E are zeros) and x slice (rows of
+  // tokens beyond T are never read)
+  for (int i = threadIdx.x; i < kRwExperts * (kRwK / 4); i += 256) {
+    const int r = i / (kRwK / 4), c4 = i % (kRwK / 4);
+    float* dst = wsm + r * kRwK + 4 * c4;
+    if (e0 + r < E && 4 * c4 < kn)
+      cp_async_16(dst, W + (size_t)(e0 + r) * H + k0 + 4 * c4);
+    else
+      *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = threadIdx.x; i < T * (kRwK / 8); i += 256) {
+    const int t = i / (kRwK / 8), c8 = i % (kRwK / 8);
+    if (8 * c8 < kn) cp_async_16(xsm + t * kRwXStride + 16 * c8, x + (size_t)t * H + k0 + 8 * c8);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int t = lane;
+  if (t >= T) return;  // no barrier follows
+  const uint8_t* xr = xsm + t * kRwXStride;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const float* wr = wsm + (warp * 4) * kRwK;
+  for (int c0 = 0; c0 < kn; c0 += 32) {
+    float xv[32];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 q = *reinterpret_cast<const uint4*>(xr + 2 * c0 + 16 * v);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv[8 * v + 2 * i] = bf16_bits_to_f32(w4[i] & 0xffffu);
+        xv[8 * v + 2 * i + 1] = bf16_bits_to_f32(w4[i] >> 16);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4* w4 = reinterpret_cast<const float4*>(wr + j * kRwK + c0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 wv = w4[v];  // broadcast: every lane reads the same address
+        acc[j] = fmaf(xv[4 * v], wv.x, acc[j]);
+        acc[j] = fmaf(xv[4 * v + 1], wv.y, acc[j]);
+        acc[j] = fmaf(xv[4 * v + 2], wv.z, acc[j]);
+        acc[j] = fmaf(xv[4 * v + 3], wv.w, acc[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = e0 + warp * 4 + j;
+    if (e < E) part[((size_t)blockIdx.y * T + t) * E + e] = acc[j];
   }
 }
 
@@ -207,6 +291,8 @@ extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
   if (T >= kRtTcMinTokens)  // split weights [3E, H] bf16 + partials [T, splits * 3E] fp32
     return align_up((size_t)3 * E * H * sizeof(uint16_t), 256) +
            align_up((size_t)T * router_tc_splits(H) * 3 * E * sizeof(float), 256);
+  if (T <= kRwMaxTokens)
+    return align_up((size_t)((H + kRwK - 1) / kRwK) * T * E * sizeof(float), 256);
   const RouterSplit sp = router_split(T, H, E);
   return align_up((size_t)sp.splits * T * E * sizeof(float), 256);
 }
@@ -240,6 +326,17 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
     S = 3 * splits;
     sp_stride = E;
     st_stride = (size_t)S * E;
+  } else if (T <= kRwMaxTokens) {
+    if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_INVALID;
+    part = static_cast<float*>(ws);
+    S = (H + kRwK - 1) / kRwK;
+    MOE_TRY_CUDA(cudaFuncSetAttribute(router_logits_warp_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kRwSmem));
+    dim3 grid((E + kRwExperts - 1) / kRwExperts, S);
+    router_logits_warp_kernel<<<grid, 256, kRwSmem, s>>>(x, w_router, T, H, E, part);
+    MOE_LAUNCH_CHECK();
+    sp_stride = (size_t)T * E;
+    st_stride = E;
   } else {
     const RouterSplit spl = router_split(T, H, E);
     part = static_cast<float*>(ws);
