@@ -373,6 +373,24 @@ int moe_check_error(void* stream);
  * Exercises the bounded-wait path of the pipelined kernels. */
 int moe_wait_selftest(int64_t limit_ns, void* stream);
 
+/* For tests: the exit paths of the pipelined expert kernels.  Runs
+ * moe_int4_linear (same arguments, workspace of
+ * moe_int4_linear_workspace_size) on the kernel `kernel` names -- 0: the
+ * stream kernel (chunks of <= 16 rows), 1: the tensor-core kernel (the
+ * act_bits 16 one, or the exact one for act_bits 8; chunks of <= 128 rows)
+ * -- in a build of it whose producer stops before its copy stage
+ * `stall_stage` (counted per CTA from 0), as if those copies never arrived,
+ * with every bounded wait limited to `limit_ns` (1e3 .. 5e9).  The other
+ * roles' waits then run out: the kernel records MOE_ERR_TIMEOUT, lets every
+ * copy and MMA it issued complete, frees its tensor memory and returns;
+ * moe_check_error() reports the time-out and later calls run normally.  The
+ * production kernels do not contain the stop. */
+int moe_int4_linear_stall_selftest(const void* x, const float* x_scale, const int32_t* offsets,
+                                   int E, int K, int N, int rows_max, const int32_t* w_packed,
+                                   const uint16_t* w_scale, int act_bits, int kernel,
+                                   int stall_stage, int64_t limit_ns, float* out, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* Human-readable name of a status code. */
 const char* moe_status_string(int status);
 

@@ -77,6 +77,9 @@ SIGNATURES = {
     "moe_int4_linear_partials": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                          c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
                                          c_size_t, c_void_p]),
+    "moe_int4_linear_stall_selftest": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                               c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                                               c_int64, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_quantize_int4": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_shared_expert_workspace_size": (c_size_t, [c_int, c_int, c_int]),
@@ -327,6 +330,25 @@ def int4_linear_partials(x: torch.Tensor, x_scale: torch.Tensor, offsets: torch.
         _p(x), _p(x_scale), _p(offsets), E, K, N, rows, _p(w_packed), _p(w_scale), kernel,
         _p(out), _p(partials), _p(ws), ws.numel(), _stream()))
     return out, partials
+
+
+def int4_linear_stall_selftest(x: torch.Tensor, x_scale: Optional[torch.Tensor],
+                               offsets: torch.Tensor, w_packed: torch.Tensor, w_scale: torch.Tensor,
+                               act_bits: int, kernel: int, stall_stage: int, limit_ns: int) -> None:
+    """Run int4_linear on a kernel build whose producer stops before stage
+    ``stall_stage`` (tests of the exit paths; the device records
+    MOE_ERR_TIMEOUT, read with check_error())."""
+    E, N = _arg("w_packed", w_packed, (None, None, None), torch.int32).shape[:2]
+    x_scale = _rows_args(x, x_scale, offsets, act_bits, torch.bfloat16, E)
+    rows, K = x.shape
+    _arg("w_packed", w_packed, (E, N, K // 8), torch.int32)
+    _arg("w_scale", w_scale, (E, N, K // 32), torch.bfloat16)
+    dev = _placed(x=x, x_scale=x_scale, offsets=offsets, w_packed=w_packed, w_scale=w_scale)
+    out = torch.empty(rows, N, dtype=torch.float32, device=dev)
+    ws = _ws(lib.moe_int4_linear_workspace_size(E, K, rows), dev)
+    _check("moe_int4_linear_stall_selftest", lib.moe_int4_linear_stall_selftest(
+        _p(x), _p(x_scale), _p(offsets), E, K, N, rows, _p(w_packed), _p(w_scale), act_bits,
+        kernel, stall_stage, limit_ns, _p(out), _p(ws), ws.numel(), _stream()))
 
 
 def quantize_rows(v: torch.Tensor):

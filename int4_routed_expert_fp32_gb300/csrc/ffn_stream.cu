@@ -87,6 +87,7 @@ struct FsParams {
   int N;
   int tma_scales;         // 1: scales by TMA (K % 256 == 0), 0: 4-byte cp.async
   int32_t* partials;      // act_bits 8, tests only: int32 [rows_max, N, K/32] or null
+  int stall_at;           // tests only (STALL instantiation): the producer stops at this stage
 };
 
 // Where a consumer thread stores the integer group partials of its MMA
@@ -405,7 +406,7 @@ __device__ __forceinline__ bool consume_unit(uint8_t* smem, float* xch, uint64_t
 // Producer side of one unit: for each K stage wait for a free slot, then
 // TMA the weight (and scale) tiles and bulk-copy the chunk's activation rows.
 // Returns false when a wait gave up.
-template <int MODE, bool Q8>
+template <int MODE, bool Q8, bool STALL = false>
 __device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams& p, uint8_t* smem,
                                              uint64_t* full, uint64_t* empty, uint32_t& it,
                                              int e, int row0, int rows, int n0, int lane,
@@ -419,6 +420,7 @@ __device__ __forceinline__ bool produce_unit(const FsMaps& maps, const FsParams&
   for (int ks = 0; ks < ksteps; ++ks, ++it) {
     const int s = it % kFsStages;
     const uint32_t ph = (it / kFsStages) & 1u;
+    if (STALL && static_cast<int>(it) == p.stall_at) return false;  // tests only
     if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1u, wt))) return false;  // warp-uniform
     uint8_t* st = smem + s * kFsStageBytes;
     uint8_t* sdst = st + kFsWBytes;
@@ -497,7 +499,9 @@ __device__ __forceinline__ bool starts_unit(const FsParams& p, uint8_t* smem, ui
   return true;
 }
 
-template <int MODE, bool Q8, bool WP = false>
+// STALL (tests only): the producer stops before stage p.stall_at, as if its
+// copies never arrived, so that the other roles' waits run out.
+template <int MODE, bool Q8, bool WP = false, bool STALL = false>
 __global__ void __launch_bounds__(kFsThreads, 1)
     ffn_stream_kernel(const __grid_constant__ FsMaps maps, const FsParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int q = u / n_tiles, jt = u - q * n_tiles;
-      ok = produce_unit<MODE, Q8>(maps, p, smem, full, empty, it, p.chunk_e[q], p.chunk_row0[q],
+      ok = produce_unit<MODE, Q8, STALL>(maps, p, smem, full, empty, it, p.chunk_e[q], p.chunk_row0[q],
                                   p.chunk_rows[q], jt * tile_n, lane, wt);
     }
     // on every exit (a wait that gave up included) the issued copies land
@@ -936,9 +940,9 @@ static bool make_maps(FsMaps* m, const int32_t* w0, const uint16_t* s0, const in
   return true;
 }
 
-template <int MODE, bool Q8, bool WP = false>
+template <int MODE, bool Q8, bool WP = false, bool STALL = false>
 static int launch_stream(const FsMaps& maps, const FsParams& p, cudaStream_t s) {
-  auto kern = ffn_stream_kernel<MODE, Q8, WP>;
+  auto kern = ffn_stream_kernel<MODE, Q8, WP, STALL>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kFsSmemBytes));
   kern<<<num_sms(), kFsThreads, kFsSmemBytes, s>>>(maps, p);
@@ -1240,6 +1244,70 @@ extern "C" int moe_int4_linear_partials(const int8_t* x, const float* x_scale,
   return launch_tc_q8_down(x16, x_scale, rows_max, E, N, K, w_packed, w_scale, out, true,
                            sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks, status, s,
                            partials);
+}
+
+extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scale,
+                                              const int32_t* offsets, int E, int K, int N,
+                                              int rows_max, const int32_t* w_packed,
+                                              const uint16_t* w_scale, int act_bits, int kernel,
+                                              int stall_stage, int64_t limit_ns, float* out,
+                                              void* ws, size_t ws_bytes, void* stream) {
+  if (E <= 0 || rows_max <= 0 || N <= 0 || stall_stage < 0) return MOE_ERR_INVALID;
+  if (kernel != 0 && kernel != 1) return MOE_ERR_INVALID;
+  if (limit_ns < 1000 || limit_ns > 5000000000LL) return MOE_ERR_INVALID;
+  if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!x || !offsets || !w_packed || !w_scale || !out || !ws) return MOE_ERR_INVALID;
+  if (act_bits == 8 && !x_scale) return MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scale, 4) || !aligned(out, 16) ||
+      !aligned(ws, 256))
+    return MOE_ERR_INVALID;
+  if (ws_bytes < moe_int4_linear_workspace_size(E, K, rows_max)) return MOE_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool q8 = act_bits == 8;
+  const int mc = kernel == 0 ? kFsMc : kTcChunkRows;
+  char* b = static_cast<char*>(ws);
+  Schedule sc = carve_one(b, E, rows_max, mc);
+  b = static_cast<char*>(ws) + schedule_bytes(E, rows_max);
+  void* xp = b;
+  b += align_up((size_t)rows_max * K * sizeof(uint16_t), 256);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
+  int rc = launch_to_pair_rows(x, q8, rows_max, K, offsets + E, xp, status, s);
+  if (rc) return rc;
+  rc = launch_schedule(offsets, E, rows_max, mc, 1, rows_max, sc, status, s);
+  if (rc) return rc;
+  if (kernel == 0) {
+    FsMaps m;
+    if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
+    FsParams p{};
+    p.x = xp;
+    p.x_scale = x_scale;
+    p.scale0 = w_scale;
+    p.out = out;
+    p.chunk_e = sc.chunk_e;
+    p.chunk_row0 = sc.chunk_row0;
+    p.chunk_rows = sc.chunk_rows;
+    p.n_chunks = sc.n_chunks;
+    p.status = status;
+    p.wait_ns = limit_ns;
+    p.stall_at = stall_stage;
+    p.K = K;
+    p.N = N;
+    p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
+    return q8 ? launch_stream<kLinear, true, false, true>(m, p, s)
+              : launch_stream<kLinear, false, false, true>(m, p, s);
+  }
+  const uint16_t* xa = static_cast<const uint16_t*>(xp);
+  if (q8) {
+    rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
+    if (rc) return rc;
+    xa = x16;
+  }
+  return launch_tc_linear_stalled(xa, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale,
+                                  out, sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks,
+                                  status, limit_ns, stall_stage, s);
 }
 
 extern "C" size_t moe_int4_linear_workspace_size(int E, int K, int rows_max) {

@@ -118,7 +118,9 @@ __device__ __forceinline__ bool scales_exact_f16(uint32_t w) {
   return (z0 || (f0 - 110u) <= 29u) && (z1 || (f1 - 110u) <= 29u);
 }
 
-template <int MODE>
+// STALL (tests only): the producer stops before stage p.stall_at, as if its
+// copies never arrived, so that the other roles' waits run out.
+template <int MODE, bool STALL = false>
 __global__ void __launch_bounds__(kTxThreads, 1)
     ffn_tc_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         for (int ks = 0; ks < ksteps; ++ks, ++it) {
           const int s = it % kTxStages;
           const uint32_t ph = (it / kTxStages) & 1u;
-          if (!mbar_wait(&sfree[s], ph ^ 1u, wt)) {
+          if ((STALL && static_cast<int>(it) == p.stall_at) || !mbar_wait(&sfree[s], ph ^ 1u, wt)) {
             ok = false;
             break;
           }
@@ -554,9 +556,9 @@ static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
                            CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int MODE>
+template <int MODE, bool STALL = false>
 static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
-  auto kern = ffn_tc_kernel<MODE>;
+  auto kern = ffn_tc_kernel<MODE, STALL>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTxSmem));
   kern<<<num_sms(), kTxThreads, kTxSmem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
@@ -614,6 +616,41 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
   p.K = I;
   p.N = D;
   return y_f32 ? launch_tc<kTxLinear>(maps, p, s) : launch_tc<kTxDown>(maps, p, s);
+}
+
+int launch_tc_q8_linear_stalled(const uint16_t* x16, const float* x_scale, int rows_max, int E,
+                                int N, int K, const int32_t* w_packed, const uint16_t* w_scale,
+                                float* y, const int32_t* chunk_e, const int32_t* chunk_row0,
+                                const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                                long long wait_ns, int stall_at, cudaStream_t s);
+
+int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows_max, int E, int N,
+                             int K, const int32_t* w_packed, const uint16_t* w_scale, float* y,
+                             const int32_t* chunk_e, const int32_t* chunk_row0,
+                             const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                             long long wait_ns, int stall_at, cudaStream_t s) {
+  if (x_scale)
+    return launch_tc_q8_linear_stalled(x16, x_scale, rows_max, E, N, K, w_packed, w_scale, y,
+                                       chunk_e, chunk_row0, chunk_rows, n_chunks, status, wait_ns,
+                                       stall_at, s);
+  TxMaps maps;
+  if (!act_map(&maps.a, x16, rows_max, K) || !packed_map(&maps.q0, w_packed, E, N, K, 2 * kTxWM))
+    return MOE_ERR_CUDA;
+  maps.q1 = maps.q0;
+  TxParams p{};
+  p.scale0 = w_scale;
+  p.scale1 = w_scale;
+  p.out = y;
+  p.chunk_e = chunk_e;
+  p.chunk_row0 = chunk_row0;
+  p.chunk_rows = chunk_rows;
+  p.n_chunks = n_chunks;
+  p.status = status;
+  p.wait_ns = wait_ns;
+  p.stall_at = stall_at;
+  p.K = K;
+  p.N = N;
+  return launch_tc<kTxLinear, true>(maps, p, s);
 }
 
 }  // namespace moe

@@ -22,6 +22,7 @@ struct TxParams {
   long long wait_ns;
   int K;
   int N;
+  int stall_at;            // tests only (STALL instantiation): the producer stops at this stage
 };
 
 struct TxMaps {
@@ -76,6 +77,15 @@ int launch_tc_q8_down(const uint16_t* h16, const float* h_scale, int rows_max, i
 
 // y[rows] = h16 W_down^T for the listed chunks (act_bits 16); bf16 y, or fp32
 // with y_f32.
+// Tests only: launch_tc_down's linear (fp32 y) or, with h_scale set, the
+// exact kernel's linear, with the producer of every CTA stopping before its
+// stage stall_at and every wait limited to wait_ns (the kernels' exit paths).
+int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows_max, int E, int N,
+                             int K, const int32_t* w_packed, const uint16_t* w_scale, float* y,
+                             const int32_t* chunk_e, const int32_t* chunk_row0,
+                             const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                             long long wait_ns, int stall_at, cudaStream_t s);
+
 int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,

@@ -90,7 +90,9 @@ __device__ __forceinline__ uint32_t q_hi_f16(uint32_t v) {
   return r;
 }
 
-template <int MODE, bool WP>
+// STALL (tests only): the producer stops before stage p.stall_at, as if its
+// copies never arrived, so that the other roles' waits run out.
+template <int MODE, bool WP, bool STALL = false>
 __global__ void __launch_bounds__(kQThreads, 1)
     ffn_tc_q8_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         for (int ks = 0; ks < ksteps; ++ks, ++it) {
           const int s = it % kQStages;
           const uint32_t ph = (it / kQStages) & 1u;
-          if (!mbar_wait(&sfree[s], ph ^ 1u, wt)) {
+          if ((STALL && static_cast<int>(it) == p.stall_at) || !mbar_wait(&sfree[s], ph ^ 1u, wt)) {
             ok = false;
             break;
           }
@@ -399,9 +401,9 @@ static bool q8_packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K,
                            CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int MODE, bool WP>
+template <int MODE, bool WP, bool STALL = false>
 static int launch_q8(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
-  auto kern = ffn_tc_q8_kernel<MODE, WP>;
+  auto kern = ffn_tc_q8_kernel<MODE, WP, STALL>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem));
   kern<<<num_sms(), kQThreads, kQSmem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
@@ -461,6 +463,32 @@ int launch_tc_q8_down(const uint16_t* h16, const float* h_scale, int rows_max, i
   p.N = D;
   if (partials) return launch_q8<kQLinear, true>(maps, p, s);
   return y_f32 ? launch_q8<kQLinear, false>(maps, p, s) : launch_q8<kQDown, false>(maps, p, s);
+}
+
+int launch_tc_q8_linear_stalled(const uint16_t* x16, const float* x_scale, int rows_max, int E,
+                                int N, int K, const int32_t* w_packed, const uint16_t* w_scale,
+                                float* y, const int32_t* chunk_e, const int32_t* chunk_row0,
+                                const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                                long long wait_ns, int stall_at, cudaStream_t s) {
+  TxMaps maps;
+  if (!q8_act_map(&maps.a, x16, rows_max, K) || !q8_packed_map(&maps.q0, w_packed, E, N, K, kQM))
+    return MOE_ERR_CUDA;
+  maps.q1 = maps.q0;
+  TxParams p{};
+  p.scale0 = w_scale;
+  p.scale1 = w_scale;
+  p.x_scale = x_scale;
+  p.out = y;
+  p.chunk_e = chunk_e;
+  p.chunk_row0 = chunk_row0;
+  p.chunk_rows = chunk_rows;
+  p.n_chunks = n_chunks;
+  p.status = status;
+  p.wait_ns = wait_ns;
+  p.stall_at = stall_at;
+  p.K = K;
+  p.N = N;
+  return launch_q8<kQLinear, false, true>(maps, p, s);
 }
 
 }  // namespace moe

@@ -707,6 +707,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     assert moe.check_error() == 0
 
 
+@pytest.mark.parametrize("act_bits", [16, 8])
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_pipelined_kernel_exit_paths(moe, kernel, act_bits):
+    """A producer that stops before its fourth copy stage (a test build of the
+    stream and tensor-core kernels): the other roles' bounded waits (20 ms)
+    run out, the kernel records MOE_ERR_TIMEOUT, drains its copies and MMAs,
+    frees its tensor memory and returns; the next call is correct and clean."""
+    rng = np.random.default_rng(77 + kernel + act_bits)
+    K, N, counts = 2048, 512, [20, 40]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed, scale = _random_int4(rng, E, N, K, 0.002, 0.02)
+    x = _bf16(rng.normal(size=(R, K)))
+    if act_bits == 16:
+        xin, xs = x.to(DEV), None
+    else:
+        q, sx = O.quantize_rows_int8(x.float().numpy())
+        xin, xs = _t(q), _t(sx)
+    args = (xin, xs, _t(off), _t(packed), _t(scale, torch.bfloat16))
+    moe.int4_linear_stall_selftest(*args, act_bits, kernel, 3, 20_000_000)
+    assert moe.check_error() == moe.capi.MOE_ERR_TIMEOUT
+    assert moe.check_error() == 0
+    got = moe.int4_linear(*args, act_bits).cpu().numpy()
+    assert moe.check_error() == 0
+    xf = oi.x_f64(x)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        assert rel_l2(got[a:b], O.int4_linear(xf[a:b], packed[e], scale[e], act_bits)) <= 1e-5
+
+
 def test_limits_are_enforced(moe):
     """One past each limit (2048 experts, top-32) is rejected before any launch."""
     x = torch.zeros(4, 256, dtype=torch.bfloat16, device=DEV)
