@@ -35,6 +35,11 @@ int launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t*
 int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
                                 float* y, cudaStream_t s);
 
+// y = x (W_0 + ... + W_{terms-1})^T with fp32 out, split-K partials as
+// launch_linear_tc_f32_splitk; w is [terms][N][K] bf16.
+int launch_linear_tc_f32_terms(const uint16_t* x, const uint16_t* w, int terms, int M, int N, int K,
+                               int kc, float* y, cudaStream_t s);
+
 // y[M, N] = x[M, K] w[N, K]^T in bf16 with fp32 accumulation.
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                        cudaStream_t s);

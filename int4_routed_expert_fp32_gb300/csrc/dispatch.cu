@@ -131,6 +131,61 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
   if (threadIdx.x == 0) offsets[E] = total;
 }
 
+// Many chunks: the column scans run one warp per expert (32 experts per
+// CTA).  Lane l takes 8 consecutive chunks of each 256-chunk segment (its 8
+// loads in flight at once), and a warp scan of the lane sums joins them;
+// segments follow one another with a carry.  counts[e] = the column total.
+// The exclusive scan of the totals into offsets is dispatch_offsets_kernel.
+constexpr int kScanPerLane = 8;
+
+__global__ void __launch_bounds__(1024) dispatch_colscan_kernel(int32_t* __restrict__ hist, int C,
+                                                                int E,
+                                                                int32_t* __restrict__ counts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + warp;
+  if (e >= E) return;
+  int carry = 0;
+  for (int c0 = 0; c0 < C; c0 += 32 * kScanPerLane) {
+    const int cl = c0 + lane * kScanPerLane;
+    int v[kScanPerLane];
+#pragma unroll
+    for (int i = 0; i < kScanPerLane; ++i) v[i] = cl + i < C ? hist[(size_t)(cl + i) * E + e] : 0;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kScanPerLane; ++i) sum += v[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = carry + incl - sum;  // exclusive prefix of this lane's first chunk
+#pragma unroll
+    for (int i = 0; i < kScanPerLane; ++i) {
+      if (cl + i < C) hist[(size_t)(cl + i) * E + e] = run;
+      run += v[i];
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) counts[e] = carry;
+}
+
+// offsets = exclusive scan of counts (E <= 2048), offsets[E] = the total.
+__global__ void __launch_bounds__(1024) dispatch_offsets_kernel(const int32_t* __restrict__ counts,
+                                                                int E,
+                                                                int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[kMaxExperts];
+  __shared__ int32_t total;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = counts[e];
+  __syncthreads();
+  block_exclusive_scan_2048(tot, E, &total);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = tot[e];
+  if (threadIdx.x == 0) offsets[E] = total;
+}
+
+// Chunks from which the column scans run one warp per expert.
+constexpr int kWarpScanMinChunks = 32;
+
 // Quantise the 8 values of one 16-byte bf16 vector with a row scale: IEEE
 // division, round half to even, clamp to [-127, 127]; packs 8 int8 in a uint2.
 // F16: also the fp16 values of the eight codes (exact: |q| <= 127).
@@ -329,8 +384,15 @@ static int run_dispatch(const int32_t* topk_idx, const uint16_t* x, int T, int D
   dispatch_count_kernel<<<(C + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, s>>>(
       topk_idx, T, E, k, hist, local_rank, status);
   MOE_LAUNCH_CHECK();
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, counts, offsets);
-  MOE_LAUNCH_CHECK();
+  if (C < kWarpScanMinChunks) {
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, counts, offsets);
+    MOE_LAUNCH_CHECK();
+  } else {
+    dispatch_colscan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(hist, C, E, counts);
+    MOE_LAUNCH_CHECK();
+    dispatch_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, offsets);
+    MOE_LAUNCH_CHECK();
+  }
   auto place = act_bits == 16 ? (pair ? dispatch_place_kernel<false, true>
                                       : dispatch_place_kernel<false, false>)
                               : (pair ? dispatch_place_kernel<true, true>

@@ -14,22 +14,34 @@
 
 namespace moe {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4;
+constexpr int kTcBM = 128, kTcBK = 64, kTcStages = 4;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KiB
-constexpr int kTcBBytes = kTcBN * kTcBK * 2;  // 32 KiB
-constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
-constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024 + 256;
 constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: epilogue
-constexpr uint32_t kTcCols = 256;
 
-// CTA (x, y, z) computes the 128 x 256 tile (y, x) over the K slice
+template <int BN>
+struct TcTile {
+  static constexpr int kBBytes = BN * kTcBK * 2;             // 32 KiB (BN 256) / 16 KiB (128)
+  static constexpr int kStageBytes = kTcABytes + kBBytes;
+  static constexpr int kSmem = kTcStages * kStageBytes + 1024 + 256;
+  static constexpr uint32_t kCols = BN;                      // TMEM accumulator columns
+};
+
+// CTA (x, y, z) computes the 128 x BN tile (y, x) over the K slice
 // [z * kc, min(K, (z + 1) * kc)) and stores it at columns z * N + n of rows of
 // ldc elements (split-K partials side by side; z = 0, ldc = N: plain C).
-template <bool F32OUT>
+// The B map is three-dimensional [terms][N][K]: every K tile is taken once
+// per term into the same accumulator, so C = A (B_0 + ... + B_{terms-1})^T
+// (terms = 1: a plain GEMM).
+template <bool F32OUT, int BN = 256>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                   void* __restrict__ Cout, int M, int N, int K, int kc, int ldc, int* status,
-                   long long wait_ns) {
+                   void* __restrict__ Cout, int M, int N, int K, int kc, int ldc, int terms,
+                   int* status, long long wait_ns) {
+  constexpr int kTcBN = BN;
+  constexpr int kTcBBytes = TcTile<BN>::kBBytes;
+  constexpr int kTcStageBytes = TcTile<BN>::kStageBytes;
+  constexpr uint32_t kTcCols = TcTile<BN>::kCols;
+  (void)kTcBBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -63,7 +75,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int m0 = blockIdx.y * kTcBM, n0 = blockIdx.x * kTcBN;
   const int kbase = blockIdx.z * kc;
-  const int ktiles = (min(K - kbase, kc) + kTcBK - 1) / kTcBK;
+  const int kt_k = (min(K - kbase, kc) + kTcBK - 1) / kTcBK;  // K tiles
+  const int ktiles = kt_k * terms;                           // K tiles x terms
 
   if (warp == 0) {
     if (lane == 0) {
@@ -75,9 +88,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t ph = (kt / kTcStages) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u, wt)) break;
         uint8_t* st = smem + s * kTcStageBytes;
+        const int kk = kbase + (kt / terms) * kTcBK, term = kt % terms;
         mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-        tma_g2s_2d(st, &ma, &full[s], kbase + kt * kTcBK, m0);
-        tma_g2s_2d(st + kTcABytes, &mb, &full[s], kbase + kt * kTcBK, n0);
+        tma_g2s_2d(st, &ma, &full[s], kk, m0);
+        tma_g2s_3d(st + kTcABytes, &mb, &full[s], kk, n0, term);
       }
       // the issued copies land before the CTA can leave (error path included)
       drain_ring(full, static_cast<uint32_t>(kt), kTcStages, status);
@@ -171,33 +185,52 @@ static bool bf16_map(CUtensorMap* m, const uint16_t* base, int rows, int K, int 
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool F32OUT>
+// [terms][rows][K] bf16, one box of box_rows rows of one term.
+static bool bf16_map3(CUtensorMap* m, const uint16_t* base, int terms, int rows, int K,
+                      int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(terms)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(rows) * K * 2};
+  const uint32_t box[3] = {static_cast<uint32_t>(kTcBK), static_cast<uint32_t>(box_rows), 1};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool F32OUT, int BN = 256>
 static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
-                          int ldc, void* y, cudaStream_t s) {
+                          int ldc, int terms, void* y, cudaStream_t s) {
   if (M == 0) return MOE_OK;
   if (kc <= 0 || kc % kTcBK != 0) return MOE_ERR_INVALID;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   CUtensorMap ma, mb;
-  if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map(&mb, w, N, K, kTcBN)) return MOE_ERR_CUDA;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<F32OUT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem));
-  dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM, (K + kc - 1) / kc);
-  gemm_tc_kernel<F32OUT><<<grid, kTcThreads, kTcSmem, s>>>(ma, mb, y, M, N, K, kc, ldc, status,
-                                                           kDefaultWaitNs);
+  if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map3(&mb, w, terms, N, K, BN)) return MOE_ERR_CUDA;
+  auto kern = gemm_tc_kernel<F32OUT, BN>;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    TcTile<BN>::kSmem));
+  dim3 grid((N + BN - 1) / BN, (M + kTcBM - 1) / kTcBM, (K + kc - 1) / kc);
+  kern<<<grid, kTcThreads, TcTile<BN>::kSmem, s>>>(ma, mb, y, M, N, K, kc, ldc, terms, status,
+                                                     kDefaultWaitNs);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
 int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                      cudaStream_t s) {
-  return launch_tc_gemm<false>(x, w, M, N, K, (K + kTcBK - 1) / kTcBK * kTcBK, N, y, s);
+  return launch_tc_gemm<false>(x, w, M, N, K, (K + kTcBK - 1) / kTcBK * kTcBK, N, 1, y, s);
 }
 
 int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
                                 float* y, cudaStream_t s) {
   const int splits = (K + kc - 1) / kc;
-  return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, y, s);
+  return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, 1, y, s);
+}
+
+int launch_linear_tc_f32_terms(const uint16_t* x, const uint16_t* w, int terms, int M, int N, int K,
+                               int kc, float* y, cudaStream_t s) {
+  const int splits = (K + kc - 1) / kc;
+  // 128-column tiles: a router of 384 experts fills three of them exactly
+  return launch_tc_gemm<true, 128>(x, w, M, N, K, kc, splits * N, terms, y, s);
 }
 
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,

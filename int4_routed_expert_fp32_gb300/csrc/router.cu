@@ -186,9 +186,9 @@ __global__ void __launch_bounds__(256) router_logits_warp_kernel(const uint16_t*
 
 // Tokens from which the router uses the tensor cores.
 constexpr int kRtTcMinTokens = 512;
-// K columns per tensor-core accumulation; the slices' fp32 partials are added
-// in order afterwards (a short accumulation chain per partial, as in the
-// split-K SIMT path).
+// K columns per tensor-core accumulation (the three weight terms of those
+// columns accumulate together); the slices' fp32 partials are added in order
+// afterwards.
 constexpr int kRtTcKSlice = 1024;
 
 static int router_tc_splits(int H) { return (H + kRtTcKSlice - 1) / kRtTcKSlice; }
@@ -288,9 +288,9 @@ using namespace moe;
 
 extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
   if (T <= 0 || H <= 0 || E <= 0) return 256;
-  if (T >= kRtTcMinTokens)  // split weights [3E, H] bf16 + partials [T, splits * 3E] fp32
+  if (T >= kRtTcMinTokens)  // split weights [3, E, H] bf16 + partials [T, splits, E] fp32
     return align_up((size_t)3 * E * H * sizeof(uint16_t), 256) +
-           align_up((size_t)T * router_tc_splits(H) * 3 * E * sizeof(float), 256);
+           align_up((size_t)T * router_tc_splits(H) * E * sizeof(float), 256);
   if (T <= kRwMaxTokens)
     return align_up((size_t)((H + kRwK - 1) / kRwK) * T * E * sizeof(float), 256);
   const RouterSplit sp = router_split(T, H, E);
@@ -311,8 +311,8 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
   int S;
   size_t sp_stride, st_stride;
   if (T >= kRtTcMinTokens) {
-    // tensor cores: partial logits of the three weight terms per K slice,
-    // [T, splits, 3, E] fp32, summed in that order
+    // tensor cores: partial logits per K slice, the three weight terms
+    // accumulated together, [T, splits, E] fp32, summed in slice order
     uint16_t* Ws = static_cast<uint16_t*>(ws);
     part = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                     align_up((size_t)3 * E * H * sizeof(uint16_t), 256));
@@ -321,9 +321,9 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
     router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(w_router, n, Ws);
     MOE_LAUNCH_CHECK();
     const int splits = router_tc_splits(H);
-    const int rc = launch_linear_tc_f32_splitk(x, Ws, T, 3 * E, H, kRtTcKSlice, part, s);
+    const int rc = launch_linear_tc_f32_terms(x, Ws, 3, T, E, H, kRtTcKSlice, part, s);
     if (rc) return rc;
-    S = 3 * splits;
+    S = splits;
     sp_stride = E;
     st_stride = (size_t)S * E;
   } else if (T <= kRwMaxTokens) {
