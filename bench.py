@@ -123,9 +123,9 @@ def roofline(w: wl.Workload, ffn_ms: float, active: int, peaks: dict) -> dict:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     roof.update({"traffic": None,
-                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; ffn_stream_fused_kernel "
-                           "(gate/up + down) for experts of <= 16 rows, ffn_tc_kernel gate/up and "
-                           "down above)",
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedule; ffn_tc_kernel gate/up "
+                           "and down for prefill-shaped batches, ffn_stream_fused_kernel (gate/up + "
+                           "down) for decode-shaped ones)",
                  "kernel_ms": ffn_ms,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                  "active_experts": active, "peak_source": peaks["source"]})

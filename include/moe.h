@@ -234,8 +234,9 @@ size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);
  *   x         bf16 or int8 [rows_max, K]; x_scale fp32 [rows_max] (act_bits 8)
  *   w_packed  int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
  *   out       fp32 [rows_max, N], 16-byte aligned
- * Experts with up to 16 rows run on the stream kernel, larger ones (when
- * rows_max >= 48 and K % 64 == 0) on the tensor-core kernel.  With
+ * When an expert has at least 48 rows and K % 64 == 0, every expert runs on
+ * the tensor-core kernel, otherwise every expert on the stream kernel (the
+ * choice is taken on the device from the offsets).  With
  * act_bits 8 both kernels form the exact integer partial P_g of every
  * 32-column weight group and give the same bits: y = x_scale * acc, acc the
  * fp32 chain fma(scale[n, g], P_g, acc) over the groups in K order. */

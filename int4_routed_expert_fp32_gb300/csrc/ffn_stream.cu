@@ -760,13 +760,29 @@ __global__ void __launch_bounds__(kFsThreads, 1)
   }
 }
 
+// Prefill-shaped batches (an expert holds at least kTcMinBatchRows rows) run
+// every expert on the tensor-core kernels: beyond one stream chunk (16 rows)
+// the stream kernel would stream an expert's weights again, while one
+// tensor-core tile dequantises them once, and the experts of few rows then
+// share the tensor-core launch instead of a stream launch that covers too few
+// experts to fill the GPU (the latent layer's 36 experts of <= 16 rows: 90 us
+// on the stream kernel, 30 us less in the tensor-core launch).  Decode-shaped
+// batches run every expert on the stream kernel.  The host launches the
+// tensor-core kernels only when an expert can hold kTcMinBatchRows rows (so
+// decode pays for no extra launches or fp16 copy); the schedule kernels then
+// take the decision on the actual row counts.
+constexpr int kTcMinRows = 1;
+constexpr int kTcMinBatchRows = 48;
+enum ScheduleRule { kAllShapes = 0, kDecodeShaped = 1, kPrefillShaped = 2 };
+
 // Chunk list of the expert-sorted rows: the rows of every expert whose row
-// count lies in [lo, hi] cut into chunks of at most mc rows.  One CTA of 1024
-// threads.  Offsets that are not non-decreasing or exceed rows_max record
+// count lies in [lo, hi] cut into chunks of at most mc rows, for a batch of
+// the shape `rule` names (no chunk otherwise).  One CTA of 1024 threads.
+// Offsets that are not non-decreasing or exceed rows_max record
 // MOE_ERR_INVALID and give no chunk.
 __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __restrict__ offsets,
                                                             int E, int rows_max, int mc, int lo,
-                                                            int hi, int max_chunks,
+                                                            int hi, int rule, int max_chunks,
                                                             int32_t* __restrict__ chunk_e,
                                                             int32_t* __restrict__ chunk_row0,
                                                             int32_t* __restrict__ chunk_rows,
@@ -776,15 +792,24 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
   __shared__ int32_t nch[kMaxExperts];
   __shared__ int32_t total;
   __shared__ int bad;
-  if (threadIdx.x == 0) bad = 0;
+  __shared__ int max_cnt;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    max_cnt = 0;
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int a = offsets[e], b = offsets[e + 1];
     const int cnt = b - a;
     if (a < 0 || cnt < 0 || b > rows_max) bad = 1;
     nch[e] = (cnt > 0 && cnt >= lo && cnt <= hi) ? (cnt + mc - 1) / mc : 0;
+    atomicMax(&max_cnt, cnt);
   }
   __syncthreads();
+  if (rule != kAllShapes && (rule == kPrefillShaped) != (max_cnt >= kTcMinBatchRows)) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) nch[e] = 0;
+    __syncthreads();
+  }
   if (bad) {
     if (threadIdx.x == 0) {
       record_status(status, MOE_ERR_INVALID);
@@ -844,15 +869,6 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t* __res
   if (threadIdx.x == 0) *n_chunks = total;
 }
 
-// Experts with more than one stream chunk of rows (>= 17) go to the
-// tensor-core path (act_bits 16): from the second chunk on the stream kernel
-// would stream the expert's weights again, while one 128-row tensor-core tile
-// dequantises them once.  The tensor-core kernels are launched only when an
-// expert can hold at least kTcMinBatchRows rows (prefill-shaped batches), so
-// that decode-shaped batches pay for no extra launches or fp16 copy.
-constexpr int kTcMinRows = kFsMc + 1;
-constexpr int kTcMinBatchRows = 48;
-
 static int max_chunks_for(int E, int rows_max, int mc) { return (rows_max + mc - 1) / mc + E; }
 
 struct Schedule {
@@ -888,8 +904,9 @@ static size_t schedule_bytes(int E, int rows_max) {
 }
 
 static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
-                           const Schedule& sc, int* status, cudaStream_t s) {
-  ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, mc, lo, hi, sc.max_chunks,
+                           const Schedule& sc, int* status, cudaStream_t s,
+                           int rule = kAllShapes) {
+  ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, mc, lo, hi, rule, sc.max_chunks,
                                          sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.done,
                                          sc.n_chunks, status);
   MOE_LAUNCH_CHECK();
@@ -1015,14 +1032,17 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
     h16 = reinterpret_cast<uint16_t*>(b);
   }
 
-  // experts with more than one chunk of rows go to the tensor-core kernels
+  // the tensor-core kernels run when an expert can hold kTcMinBatchRows rows;
+  // the schedules then give every expert to one of the two paths, by the
+  // batch's actual shape
   const bool use_tc = tc_path_supported(D) && tc_path_supported(I) &&
                       max_rows_per_expert >= kTcMinBatchRows;
-  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max,
-                           small, status, s);
+  int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
+                           use_tc ? kDecodeShaped : kAllShapes);
   if (rc) return rc;
   if (use_tc) {
-    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s);
+    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s,
+                         kPrefillShaped);
     if (rc) return rc;
   }
 
@@ -1344,8 +1364,8 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   const bool use_tc = tc_path_supported(K) && rows_max >= kTcMinBatchRows;
   int rc = launch_to_pair_rows(x, q8, rows_max, K, offsets + E, xp, status, s);
   if (rc) return rc;
-  rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, use_tc ? kTcMinRows - 1 : rows_max, small,
-                       status, s);
+  rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
+                       use_tc ? kDecodeShaped : kAllShapes);
   if (rc) return rc;
   FsMaps m;
   if (!make_maps(&m, w_packed, w_scale, w_packed, w_scale, E, N, K, kFsRows)) return MOE_ERR_CUDA;
@@ -1365,7 +1385,8 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
   rc = run_stream(kLinear, q8, m, p, s);
   if (rc || !use_tc) return rc;
-  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s);
+  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s,
+                       kPrefillShaped);
   if (rc) return rc;
   const uint16_t* xa = static_cast<const uint16_t*>(xp);
   if (q8) {

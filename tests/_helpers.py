@@ -142,8 +142,9 @@ def targeted_tokens(w: wl.Workload, x, router, n: int = 32, seed: int = 2024) ->
     """n tokens of workload ``w`` chosen to reach the expert kernels' edge
     cases: the last token, the rows of the hottest experts' last (ragged)
     128-row chunk, every 128-row chunk boundary of the hottest experts,
-    experts of exactly 16 and 17 rows (the last stream-kernel size and the
-    first tensor-core size), then random tokens.  Routing is the oracle's."""
+    experts of exactly 16 and 17 rows (one and two 16-row stream chunks; on
+    the tensor cores in prefill-shaped batches), then random tokens.  Routing
+    is the oracle's."""
     if w.T <= n:
         return list(range(w.T))
     W, b = router

@@ -78,7 +78,9 @@ def test_layer_small_all_tokens(moe, case):
 def test_layer_full_size_sampled(moe, name):
     """The full workloads against the oracle on at least 32 tokens each (all
     32 at decode), chosen to reach the hottest experts' last ragged chunks,
-    128-row chunk boundaries and experts of exactly 16 and 17 rows."""
+    128-row chunk boundaries and experts of exactly 16 and 17 rows (the
+    smallest experts, which in these prefill-shaped batches also run on the
+    tensor cores)."""
     w = wl.WORKLOADS[name]
     x = wl.gen_x(w)
     router = wl.gen_router(w)

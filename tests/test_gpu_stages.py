@@ -360,13 +360,14 @@ def _check_columns(got, ref, what):
 
 @pytest.mark.parametrize("act_bits", [16, 8])
 def test_int4_linear_extreme_scales_both_kernels(moe, act_bits):
-    """Weight scales from 1e-30 to 2e4 on both expert kernels (9 rows: stream
-    kernel; 40 rows: tensor cores), each weight row checked on its own:
-    relative L2 <= 3e-5 per column, and the exact mode's fp32 chain bit for
-    bit.  The bound: fp32 accumulation of exact products, plus, on the stream
-    kernel, the start value -(1032 S_lo + 72 S_hi) of each group's fp16
-    chain, which leaves an absolute error of about 2^-24 * 1040 * sum|x| per
-    group (~1e-5 relative on one column; 1e-5 over a whole matrix, as
+    """Weight scales from 1e-30 to 2e4 on both expert kernels (9 + 30 rows: a
+    decode-shaped batch, the stream kernel; 9 + 60 rows: a prefill-shaped
+    batch, every expert on the tensor cores), each weight row checked on its
+    own: relative L2 <= 3e-5 per column, and the exact mode's fp32 chain bit
+    for bit.  The bound: fp32 accumulation of exact products, plus, on the
+    stream kernel, the start value -(1032 S_lo + 72 S_hi) of each group's
+    fp16 chain, which leaves an absolute error of about 2^-24 * 1040 * sum|x|
+    per group (~1e-5 relative on one column; 1e-5 over a whole matrix, as
     test_int4_linear_w4a16 checks).
 
     The stream kernel and the exact mode apply scales in fp32 and take any
@@ -375,51 +376,55 @@ def test_int4_linear_extreme_scales_both_kernels(moe, act_bits):
     MOE_ERR_UNSUPPORTED (checked here), and inside it (scales 1e-5 .. 8000)
     it matches like the stream kernel."""
     rng = np.random.default_rng(17 + act_bits)
-    K, N, counts = 2048, 136, [9, 40]
-    E = len(counts)
-    off = _segments(counts)
-    R = int(off[-1])
+    K, N = 2048, 136
+    E = 2
     packed = rng.integers(0, 2 ** 32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
-    x = _bf16(rng.normal(size=(R, K)))
-    xf = oi.x_f64(x)
-    q, sx = O.quantize_rows_int8(x.float().numpy())
 
-    def run(scale):
+    def run(counts, scale):
+        off = _segments(counts)
+        R = int(off[-1])
+        x = _bf16(rng.normal(size=(R, K)))
+        q, sx = O.quantize_rows_int8(x.float().numpy())
         if act_bits == 16:
-            return moe.int4_linear(x.to(DEV), None, _t(off), _t(packed),
-                                   _t(scale, torch.bfloat16), 16).cpu().numpy()
-        return moe.int4_linear(_t(q), _t(sx), _t(off), _t(packed), _t(scale, torch.bfloat16),
-                               8).cpu().numpy()
+            got = moe.int4_linear(x.to(DEV), None, _t(off), _t(packed),
+                                  _t(scale, torch.bfloat16), 16).cpu().numpy()
+        else:
+            got = moe.int4_linear(_t(q), _t(sx), _t(off), _t(packed), _t(scale, torch.bfloat16),
+                                  8).cpu().numpy()
+        return off, oi.x_f64(x), q, sx, got, moe.check_error()
+
+    def check(off, xf, q, sx, got, scale):
+        for e in range(E):
+            a, b = off[e], off[e + 1]
+            ref = O.int4_linear(xf[a:b], packed[e], scale[e], act_bits)
+            if act_bits == 8:
+                P = O.int4_group_partials(q[a:b], packed[e])
+                assert np.array_equal(got[a:b], fp32_group_chain(P, scale[e], sx[a:b])), e
+            _check_columns(got[a:b], ref, f"expert {e}")
 
     scale = _extreme_scales(rng, E, N, K)
-    got = run(scale)
-    status = moe.check_error()
-    for e in range(E):
-        a, b = off[e], off[e + 1]
-        if act_bits == 16 and e == 1:
-            continue   # out-of-range scales on the fp16 tensor-core path: reported below
-        ref = O.int4_linear(xf[a:b], packed[e], scale[e], act_bits)
-        if act_bits == 8:
-            P = O.int4_group_partials(q[a:b], packed[e])
-            assert np.array_equal(got[a:b], fp32_group_chain(P, scale[e], sx[a:b])), e
-        _check_columns(got[a:b], ref, f"expert {e}")
+    # stream kernel (no expert holds 48 rows): any scale
+    off, xf, q, sx, got, status = run([9, 30], scale)
+    assert status == 0
+    check(off, xf, q, sx, got, scale)
+    # tensor cores (an expert of 60 rows)
+    off, xf, q, sx, got, status = run([9, 60], scale)
     if act_bits == 8:
         assert status == 0
+        check(off, xf, q, sx, got, scale)
         return
     assert status == moe.capi.MOE_ERR_UNSUPPORTED
     # the tensor-core kernel's exact range: 2^-17 (7.6e-6) .. 8160
     scale = _extreme_scales(rng, E, N, K, lo=8e-6, tiny=1e-5, big=64.0, huge=8000.0, small=7.7e-6)
-    got = run(scale)
-    assert moe.check_error() == 0
-    for e in range(E):
-        a, b = off[e], off[e + 1]
-        _check_columns(got[a:b], O.int4_linear(xf[a:b], packed[e], scale[e], 16), f"expert {e}")
+    off, xf, q, sx, got, status = run([9, 60], scale)
+    assert status == 0
+    check(off, xf, q, sx, got, scale)
 
 
 @pytest.mark.parametrize("K,N,counts", [
-    (320, 300, [0, 1, 33, 70, 8]),   # 33 and 70 rows on the tensor cores
+    (320, 300, [0, 1, 33, 70, 8]),   # every expert on the tensor cores (112 rows)
     (7168, 256, [2, 40]),            # all on the stream kernel (fewer than 48 rows)
-    (7168, 256, [2, 40, 17]),        # 40 and 17 rows on the tensor cores, full hidden width
+    (7168, 256, [2, 48, 17]),        # all on the tensor cores, full hidden width
 ])
 def test_int4_linear_exact_integer_accumulators(moe, K, N, counts):
     """Unit scales and an int8 input of scale 1: the output is the integer sum
@@ -448,7 +453,7 @@ def test_int4_linear_exact_integer_accumulators(moe, K, N, counts):
 
 
 @pytest.mark.parametrize("K,N,counts", [
-    (512, 384, [9, 0, 41, 70]),      # 41 and 70 rows on the tensor cores
+    (512, 384, [9, 0, 41, 70]),      # every expert on the tensor cores
     (7168, 300, [5, 17, 0, 40, 130]),  # full width, ragged N tile, one expert of two chunks
 ])
 def test_int4_linear_exact_mode_scaled(moe, K, N, counts):
@@ -515,14 +520,18 @@ def test_int4_linear_exact_group_partials(moe, kernel):
 
 @pytest.mark.parametrize("act_bits", [16, 8])
 @pytest.mark.parametrize("D,I,counts", [
-    (320, 192, [0, 3, 40, 1, 0, 9]),
+    # decode-shaped batches (no expert holds 48 rows): the stream kernel
+    (320, 192, [0, 3, 20, 1, 0, 9]),
     (256, 128, [16, 16]),
-    (1024, 512, [1, 2, 65, 0]),          # one expert on the tensor-core path (>= 17 rows)
-    (320, 192, [130, 5, 64, 0, 16, 17]), # ragged token tiles, ragged N tiles, threshold edges
-    (256, 128, [16, 16, 16, 0, 3]),      # tensor-core kernels launched with no tile to do
-    (256, 192, [400, 3, 0, 193]),        # several 192-row chunks per expert, ragged last chunks
-    # many experts of 17..70 rows on the tensor cores (partial 128-row tiles)
-    (320, 192, [40, 3, 64, 17, 33, 0]),
+    (256, 128, [16, 17, 14]),            # one and two 16-row stream chunks
+    (320, 192, [0, 3, 40, 1, 0, 9]),     # 53 rows: tensor-core kernels launched, no tile
+    (256, 128, [16, 16, 16, 0, 3]),      # the same with experts of <= 16 rows
+    # prefill-shaped batches: every expert on the tensor cores
+    (256, 128, [48, 1, 2, 16, 17]),      # the threshold, and 1- to 17-row experts
+    (1024, 512, [1, 2, 65, 0]),
+    (320, 192, [130, 5, 64, 0, 16, 17]), # ragged token tiles, ragged N tiles
+    (256, 192, [400, 3, 0, 193]),        # several 128-row chunks per expert, ragged last chunks
+    (320, 192, [48, 3, 64, 17, 33, 0]),  # partial 128-row tiles
     (256, 128, [70, 40, 40, 40, 40, 40, 40, 40]),
 ])
 def test_expert_ffn_parity(moe, act_bits, D, I, counts):
@@ -564,7 +573,7 @@ def test_expert_ffn_pairs_equals_expert_ffn(moe, act_bits):
     bits of moe_dispatch + moe_expert_ffn (same kernels after the copy)."""
     rng = np.random.default_rng(31)
     T, k, E, D, I = 40, 4, 6, 320, 192
-    idx = random_topk(T, E, k, rng)       # ~27 rows per expert: most on the tensor cores
+    idx = random_topk(T, E, k, rng)       # ~27 rows per expert: the stream kernel
     x = _bf16(rng.normal(size=(T, D)))
     gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
     up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
@@ -581,12 +590,13 @@ def test_expert_ffn_pairs_equals_expert_ffn(moe, act_bits):
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
-def test_expert_ffn_reports_fp16_overflow_and_recovers(moe):
-    """An intermediate h beyond the fp16 range, on both expert kernels (5 rows:
-    stream kernel; 60 rows: tensor cores), records MOE_ERR_UNSUPPORTED; the call
-    finishes and the next call is clean."""
+@pytest.mark.parametrize("counts", [[5, 30], [5, 60]])
+def test_expert_ffn_reports_fp16_overflow_and_recovers(moe, counts):
+    """An intermediate h beyond the fp16 range, on both expert kernels (5 + 30
+    rows: the stream kernel; 5 + 60 rows: the tensor cores), records
+    MOE_ERR_UNSUPPORTED; the call finishes and the next call is clean."""
     rng = np.random.default_rng(41)
-    D, I, counts = 256, 128, [5, 60]
+    D, I = 256, 128
     E = len(counts)
     off = _segments(counts)
     R = int(off[-1])
@@ -606,8 +616,9 @@ def test_expert_ffn_reports_fp16_overflow_and_recovers(moe):
 
 
 def test_status_word_is_a_report_only(moe):
-    """An error that one call records (an fp16 overflow on both expert
-    kernels, a bounded wait that ran out) leaves later calls unchanged, with
+    """An error that one call records (an fp16 overflow in a prefill-shaped
+    batch, on the tensor cores; a bounded wait that ran out) leaves later
+    calls unchanged, with
     no moe_check_error in between: they give the bits of a clean call, and
     the status word keeps the first error until it is read."""
     rng = np.random.default_rng(43)
