@@ -69,7 +69,7 @@ def expert_bytes(w: wl.Workload) -> int:
 
 def _source_hash() -> str:
     h = hashlib.sha1()
-    for name in ("ffn_stream.cu", "ffn_tc.cu"):
+    for name in ("ffn_stream.cu", "ffn_tc.cu", "ffn_tc_q8.cu", "ffn_tc.cuh"):
         with open(os.path.join(ROOT, "int4_routed_expert_fp32_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]

@@ -54,6 +54,10 @@ ROUTE_CASES = {
     # from 512 tokens the logits come from the tensor cores: ragged in both
     # the 128-token and the 256-logit tiles
     "tc_ragged": wl.workload("tiny", name="tc_ragged", T=601, H=512, E=100, k=6, seed=7),
+    # the one-warp top-k (from 64 tokens) at 8 and 16 scores per lane (E in
+    # (128, 256] and (384, 512]); above 512 experts the one-CTA top-k
+    "E200": wl.workload("tiny", name="E200", T=70, H=256, E=200, k=8, seed=22),
+    "E500_k32": wl.workload("tiny", name="E500", T=64, H=256, E=500, k=32, seed=23),
     # the library's limits: 2048 experts, top-32
     "max_E_k": wl.workload("tiny", name="max_E_k", T=24, H=256, E=2048, k=32, seed=21),
 }
