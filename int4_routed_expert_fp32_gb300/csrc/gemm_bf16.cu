@@ -3,11 +3,14 @@
 // up-projection"; KimiSparseMoeBlock listing: routed_expert_down_proj and
 // routed_expert_up_proj, no bias).
 //
-// gemm_tc_kernel: 128 x 256 output tile per CTA on the 5th-generation tensor
-// cores: a TMA warp streams 128x64 (A) and 256x64 (B) bf16 tiles with the
-// 128-byte swizzle into a 4-stage ring, one warp issues tcgen05.mma
-// (M=128, N=256, K=16) into a 256-column TMEM accumulator, and four epilogue
-// warps read it back with tcgen05.ld and store bf16.
+// gemm_tc_kernel: persistent CTAs (one per SM) walk 128 x 256 output tiles on
+// the 5th-generation tensor cores: a TMA warp streams 128x64 (A) and 256x64
+// (B) bf16 tiles with the 128-byte swizzle into a 4-stage ring, one warp
+// issues tcgen05.mma (M=128, N=256, K=16) into one of two 256-column TMEM
+// accumulators, and four epilogue warps read the other back with tcgen05.ld
+// and store bf16 (or fp32) while the next tile's MMAs run.
+#include <algorithm>
+
 #include "combine.cuh"
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -23,32 +26,33 @@ struct TcTile {
   static constexpr int kBBytes = BN * kTcBK * 2;             // 32 KiB (BN 256) / 16 KiB (128)
   static constexpr int kStageBytes = kTcABytes + kBBytes;
   static constexpr int kSmem = kTcStages * kStageBytes + 1024 + 256;
-  static constexpr uint32_t kCols = BN;                      // TMEM accumulator columns
+  static constexpr uint32_t kCols = 2 * BN;                  // two TMEM accumulators
 };
 
-// CTA (x, y, z) computes the 128 x BN tile (y, x) over the K slice
-// [z * kc, min(K, (z + 1) * kc)) and stores it at columns z * N + n of rows of
-// ldc elements (split-K partials side by side; z = 0, ldc = N: plain C).
-// The B map is three-dimensional [terms][N][K]: every K tile is taken once
-// per term into the same accumulator, so C = A (B_0 + ... + B_{terms-1})^T
-// (terms = 1: a plain GEMM).
+// Persistent: CTA c takes the tiles t = c, c + gridDim.x, ...; tile t is
+// (x, y, z) = (t % tn, (t / tn) % tm, t / (tn tm)): the 128 x BN tile (y, x)
+// over the K slice [z * kc, min(K, (z + 1) * kc)), stored at columns z * N + n
+// of rows of ldc elements (split-K partials side by side; one slice, ldc = N:
+// plain C).  Two TMEM accumulators: the epilogue of a tile overlaps the
+// MMAs of the next.  The B map is three-dimensional [terms][N][K]: every K
+// tile is taken once per term into the same accumulator, so C = A (B_0 + ...
+// + B_{terms-1})^T (terms = 1: a plain GEMM).
 template <bool F32OUT, int BN = 256>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
                    void* __restrict__ Cout, int M, int N, int K, int kc, int ldc, int terms,
                    int* status, long long wait_ns) {
   constexpr int kTcBN = BN;
-  constexpr int kTcBBytes = TcTile<BN>::kBBytes;
   constexpr int kTcStageBytes = TcTile<BN>::kStageBytes;
   constexpr uint32_t kTcCols = TcTile<BN>::kCols;
-  (void)kTcBBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
-  uint64_t* accf = empty + kTcStages;
-  uint64_t* mma_done = accf + 1;  // the MMA warp's last commit (exit path)
+  uint64_t* accfull = empty + kTcStages;  // [2]
+  uint64_t* accempty = accfull + 2;       // [2]
+  uint64_t* mma_done = accempty + 2;      // the MMA warp's last commit (exit path)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   __shared__ int cta_abort;
   const Waiter wt{&cta_abort, status, wait_ns};
@@ -59,7 +63,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], 4);
+    }
     mbar_init(mma_done, 1);
     cta_abort = 0;
     fence_mbarrier_init();
@@ -73,68 +80,93 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  const int m0 = blockIdx.y * kTcBM, n0 = blockIdx.x * kTcBN;
-  const int kbase = blockIdx.z * kc;
-  const int kt_k = (min(K - kbase, kc) + kTcBK - 1) / kTcBK;  // K tiles
-  const int ktiles = kt_k * terms;                           // K tiles x terms
+  const int tn = (N + kTcBN - 1) / kTcBN, tm = (M + kTcBM - 1) / kTcBM;
+  const int tiles = tn * tm * ((K + kc - 1) / kc);
+  // K tiles (x terms) of the slice z
+  auto ktiles_of = [&](int z) { return (min(K - z * kc, kc) + kTcBK - 1) / kTcBK * terms; };
 
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tensor_map(&ma);
       prefetch_tensor_map(&mb);
-      int kt = 0;
-      for (; kt < ktiles; ++kt) {
-        const int s = kt % kTcStages;
-        const uint32_t ph = (kt / kTcStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, wt)) break;
-        uint8_t* st = smem + s * kTcStageBytes;
-        const int kk = kbase + (kt / terms) * kTcBK, term = kt % terms;
-        mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-        tma_g2s_2d(st, &ma, &full[s], kk, m0);
-        tma_g2s_3d(st + kTcABytes, &mb, &full[s], kk, n0, term);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n0 = (t % tn) * kTcBN, m0 = ((t / tn) % tm) * kTcBM, z = t / (tn * tm);
+        const int ktiles = ktiles_of(z);
+        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+          const int s = it % kTcStages;
+          const uint32_t ph = (it / kTcStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wt)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kTcStageBytes;
+          const int kk = z * kc + (kt / terms) * kTcBK, term = kt % terms;
+          mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+          tma_g2s_2d(st, &ma, &full[s], kk, m0);
+          tma_g2s_3d(st + kTcABytes, &mb, &full[s], kk, n0, term);
+        }
       }
       // the issued copies land before the CTA can leave (error path included)
-      drain_ring(full, static_cast<uint32_t>(kt), kTcStages, status);
+      drain_ring(full, it, kTcStages, status);
     }
   } else if (warp == 1) {
     // the whole warp walks the loop; one elected lane issues (see umma_f16_warp)
     constexpr uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
+    uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int kt = 0; kt < ktiles; ++kt) {
-      const int s = kt % kTcStages;
-      const uint32_t ph = (kt / kTcStages) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wt))) {
-        ok = false;
-        break;
-      }
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++uc) {
+      const int b = uc & 1;
+      const int ktiles = ktiles_of(t / (tn * tm));
+      if (!__all_sync(0xffffffffu, mbar_wait(&accempty[b], ((uc >> 1) & 1u) ^ 1u, wt))) break;
       tc_fence_after();
-      const uint8_t* st = smem + s * kTcStageBytes;
-      const uint64_t da = smem_desc_sw128(st);
-      const uint64_t db = smem_desc_sw128(st + kTcABytes);
+      const uint32_t acc = tbase + b * kTcBN;
+      for (int kt = 0; kt < ktiles; ++kt, ++it) {
+        const int s = it % kTcStages;
+        const uint32_t ph = (it / kTcStages) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, wt))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* st = smem + s * kTcStageBytes;
+        const uint64_t da = smem_desc_sw128(st);
+        const uint64_t db = smem_desc_sw128(st + kTcABytes);
 #pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk)
-        umma_f16_warp(tbase, da + 2 * kk, db + 2 * kk, idesc, (kt | kk) != 0);
-      umma_commit_warp(&empty[s]);
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          umma_f16_warp(acc, da + 2 * kk, db + 2 * kk, idesc, (kt | kk) != 0);
+        umma_commit_warp(&empty[s]);
+      }
+      if (ok) umma_commit_warp(&accfull[b]);
     }
-    if (ok) umma_commit_warp(accf);
     // every issued MMA completes before TMEM is freed, on the error path too
     umma_commit_warp(mma_done);
     mbar_drain(mma_done, 0, status);
   } else {
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
-    const int row = m0 + 32 * q + lane;
-    // warp-uniform outcome: tcgen05.ld needs the whole warp
-    if (__all_sync(0xffffffffu, mbar_wait(accf, 0, wt))) {
+    uint32_t uc = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++uc) {
+      const int b = uc & 1;
+      const int n0 = (t % tn) * kTcBN, m0 = ((t / tn) % tm) * kTcBM, z = t / (tn * tm);
+      const int row = m0 + 32 * q + lane;
+      // warp-uniform outcome: tcgen05.ld needs the whole warp
+      if (!__all_sync(0xffffffffu, mbar_wait(&accfull[b], (uc >> 1) & 1u, wt))) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < kTcBN; c0 += 32) {
         uint32_t r[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(32 * q) << 16) + c0, r);
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * q) << 16) + b * kTcBN + c0, r);
         tmem_ld_wait();
+        if (c0 + 32 == kTcBN) {  // the accumulator goes back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[b]);
+        }
         const int col = n0 + c0;
         if (F32OUT && row < M && col < N) {
-          float* dst = static_cast<float*>(Cout) + (size_t)row * ldc + (size_t)blockIdx.z * N + col;
+          float* dst = static_cast<float*>(Cout) + (size_t)row * ldc + (size_t)z * N + col;
           if (col + 32 <= N && (N & 3) == 0 && (ldc & 3) == 0) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -146,8 +178,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (col + i < N) dst[i] = __uint_as_float(r[i]);
           }
-        } else if (row < M && col < N) {
-          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * ldc + (size_t)blockIdx.z * N + col;
+        } else if (!F32OUT && row < M && col < N) {
+          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * ldc + (size_t)z * N + col;
           if (col + 32 <= N && (N & 7) == 0 && (ldc & 7) == 0) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -208,7 +240,9 @@ static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, in
   auto kern = gemm_tc_kernel<F32OUT, BN>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     TcTile<BN>::kSmem));
-  dim3 grid((N + BN - 1) / BN, (M + kTcBM - 1) / kTcBM, (K + kc - 1) / kc);
+  const long tiles =
+      (long)((N + BN - 1) / BN) * ((M + kTcBM - 1) / kTcBM) * ((K + kc - 1) / kc);
+  const int grid = static_cast<int>(std::min<long>(tiles, num_sms()));
   kern<<<grid, kTcThreads, TcTile<BN>::kSmem, s>>>(ma, mb, y, M, N, K, kc, ldc, terms, status,
                                                      kDefaultWaitNs);
   MOE_LAUNCH_CHECK();
