@@ -31,9 +31,11 @@ int launch_expert_ffn(const void* x_sorted, const float* x_scale, const int32_t*
 // Split-K partials of x[M, K] w[N, K]^T (bf16 operands, tcgen05, fp32
 // accumulation over each slice of kc columns, kc a multiple of 64):
 // y[m, z * N + n] = sum over k in [z * kc, (z + 1) * kc) of x[m, k] w[n, k],
-// z = 0 .. ceil(K / kc) - 1.
+// z = 0 .. ceil(K / kc) - 1.  With w2 (same shape) also y2 from x w2^T, in
+// the same launch.
 int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
-                                float* y, cudaStream_t s);
+                                float* y, cudaStream_t s, const uint16_t* w2 = nullptr,
+                                float* y2 = nullptr);
 
 // y = x (W_0 + ... + W_{terms-1})^T with fp32 out, split-K partials as
 // launch_linear_tc_f32_splitk; w is [terms][N][K] bf16.

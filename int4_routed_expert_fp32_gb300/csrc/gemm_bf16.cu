@@ -36,12 +36,15 @@ struct TcTile {
 // plain C).  Two TMEM accumulators: the epilogue of a tile overlaps the
 // MMAs of the next.  The B map is three-dimensional [terms][N][K]: every K
 // tile is taken once per term into the same accumulator, so C = A (B_0 + ...
-// + B_{terms-1})^T (terms = 1: a plain GEMM).
+// + B_{terms-1})^T (terms = 1: a plain GEMM).  A second GEMM of the same
+// shape and A (mb2, Cout2; tiles after the first GEMM's) can share the
+// launch: the shared expert's gate and up projections.
 template <bool F32OUT, int BN = 256>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                   void* __restrict__ Cout, int M, int N, int K, int kc, int ldc, int terms,
-                   int* status, long long wait_ns) {
+                   const __grid_constant__ CUtensorMap mb2, void* __restrict__ Cout,
+                   void* __restrict__ Cout2, int ngemm, int M, int N, int K, int kc, int ldc,
+                   int terms, int* status, long long wait_ns) {
   constexpr int kTcBN = BN;
   constexpr int kTcStageBytes = TcTile<BN>::kStageBytes;
   constexpr uint32_t kTcCols = TcTile<BN>::kCols;
@@ -81,7 +84,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const int tn = (N + kTcBN - 1) / kTcBN, tm = (M + kTcBM - 1) / kTcBM;
-  const int tiles = tn * tm * ((K + kc - 1) / kc);
+  const int tiles1 = tn * tm * ((K + kc - 1) / kc);  // tiles of one GEMM
+  const int tiles = tiles1 * ngemm;
   // K tiles (x terms) of the slice z
   auto ktiles_of = [&](int z) { return (min(K - z * kc, kc) + kTcBK - 1) / kTcBK * terms; };
 
@@ -89,9 +93,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       prefetch_tensor_map(&ma);
       prefetch_tensor_map(&mb);
+      if (ngemm > 1) prefetch_tensor_map(&mb2);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t2 = blockIdx.x; t2 < tiles && ok; t2 += gridDim.x) {
+        const bool second = t2 >= tiles1;
+        const int t = second ? t2 - tiles1 : t2;
+        const CUtensorMap* bmap = second ? &mb2 : &mb;
         const int n0 = (t % tn) * kTcBN, m0 = ((t / tn) % tm) * kTcBM, z = t / (tn * tm);
         const int ktiles = ktiles_of(z);
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int kk = z * kc + (kt / terms) * kTcBK, term = kt % terms;
           mbar_arrive_expect_tx(&full[s], kTcStageBytes);
           tma_g2s_2d(st, &ma, &full[s], kk, m0);
-          tma_g2s_3d(st + kTcABytes, &mb, &full[s], kk, n0, term);
+          tma_g2s_3d(st + kTcABytes, bmap, &full[s], kk, n0, term);
         }
       }
       // the issued copies land before the CTA can leave (error path included)
@@ -116,8 +124,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++uc) {
+    for (int t2 = blockIdx.x; t2 < tiles && ok; t2 += gridDim.x, ++uc) {
       const int b = uc & 1;
+      const int t = t2 >= tiles1 ? t2 - tiles1 : t2;
       const int ktiles = ktiles_of(t / (tn * tm));
       if (!__all_sync(0xffffffffu, mbar_wait(&accempty[b], ((uc >> 1) & 1u) ^ 1u, wt))) break;
       tc_fence_after();
@@ -147,8 +156,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
     uint32_t uc = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++uc) {
+    for (int t2 = blockIdx.x; t2 < tiles; t2 += gridDim.x, ++uc) {
       const int b = uc & 1;
+      const bool second = t2 >= tiles1;
+      const int t = second ? t2 - tiles1 : t2;
+      void* const Cout_t = second ? Cout2 : Cout;
       const int n0 = (t % tn) * kTcBN, m0 = ((t / tn) % tm) * kTcBM, z = t / (tn * tm);
       const int row = m0 + 32 * q + lane;
       // warp-uniform outcome: tcgen05.ld needs the whole warp
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const int col = n0 + c0;
         if (F32OUT && row < M && col < N) {
-          float* dst = static_cast<float*>(Cout) + (size_t)row * ldc + (size_t)z * N + col;
+          float* dst = static_cast<float*>(Cout_t) + (size_t)row * ldc + (size_t)z * N + col;
           if (col + 32 <= N && (N & 3) == 0 && (ldc & 3) == 0) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -179,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (col + i < N) dst[i] = __uint_as_float(r[i]);
           }
         } else if (!F32OUT && row < M && col < N) {
-          uint16_t* dst = static_cast<uint16_t*>(Cout) + (size_t)row * ldc + (size_t)z * N + col;
+          uint16_t* dst = static_cast<uint16_t*>(Cout_t) + (size_t)row * ldc + (size_t)z * N + col;
           if (col + 32 <= N && (N & 7) == 0 && (ldc & 7) == 0) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -228,23 +240,31 @@ static bool bf16_map3(CUtensorMap* m, const uint16_t* base, int terms, int rows,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// y = x w^T, and with w2 set also y2 = x w2^T in the same launch.
 template <bool F32OUT, int BN = 256>
 static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
-                          int ldc, int terms, void* y, cudaStream_t s) {
+                          int ldc, int terms, void* y, cudaStream_t s,
+                          const uint16_t* w2 = nullptr, void* y2 = nullptr) {
   if (M == 0) return MOE_OK;
   if (kc <= 0 || kc % kTcBK != 0) return MOE_ERR_INVALID;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mb2;
   if (!bf16_map(&ma, x, M, K, kTcBM) || !bf16_map3(&mb, w, terms, N, K, BN)) return MOE_ERR_CUDA;
+  const int ngemm = w2 ? 2 : 1;
+  if (w2) {
+    if (!bf16_map3(&mb2, w2, terms, N, K, BN)) return MOE_ERR_CUDA;
+  } else {
+    mb2 = mb;
+  }
   auto kern = gemm_tc_kernel<F32OUT, BN>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     TcTile<BN>::kSmem));
   const long tiles =
-      (long)((N + BN - 1) / BN) * ((M + kTcBM - 1) / kTcBM) * ((K + kc - 1) / kc);
+      (long)((N + BN - 1) / BN) * ((M + kTcBM - 1) / kTcBM) * ((K + kc - 1) / kc) * ngemm;
   const int grid = static_cast<int>(std::min<long>(tiles, num_sms()));
-  kern<<<grid, kTcThreads, TcTile<BN>::kSmem, s>>>(ma, mb, y, M, N, K, kc, ldc, terms, status,
-                                                     kDefaultWaitNs);
+  kern<<<grid, kTcThreads, TcTile<BN>::kSmem, s>>>(ma, mb, mb2, y, w2 ? y2 : y, ngemm, M, N, K,
+                                                     kc, ldc, terms, status, kDefaultWaitNs);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -255,9 +275,9 @@ int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, 
 }
 
 int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
-                                float* y, cudaStream_t s) {
+                                float* y, cudaStream_t s, const uint16_t* w2, float* y2) {
   const int splits = (K + kc - 1) / kc;
-  return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, 1, y, s);
+  return launch_tc_gemm<true>(x, w, M, N, K, kc, splits * N, 1, y, s, w2, y2);
 }
 
 int launch_linear_tc_f32_terms(const uint16_t* x, const uint16_t* w, int terms, int M, int N, int K,

@@ -6,8 +6,9 @@
 // always-active shared expert"; the exact-generator page keeps shared experts
 // as ordinary bf16 linear modules).
 //
-// Three tcgen05 GEMMs with fp32 split-K partials (the split fills the SMs
-// when T is small), one kernel that sums the gate/up partials and stores
+// Two tcgen05 GEMM launches (gate and up together, then down) with fp32
+// split-K partials (the split fills the SMs when T is small), one kernel
+// that sums the gate/up partials and stores
 // h = bf16(SiLU(g) * u) (the module's dtype), and one that adds the summed
 // down partials to the bf16 output with a single rounding.
 #include <math.h>
@@ -43,7 +44,7 @@ struct SharedWs {
 
 SharedWs shared_carve(int T, int H, int I, void* base) {
   SharedWs w{};
-  w.kc_gu = split_kc(T, I, H);
+  w.kc_gu = split_kc(T, 2 * I, H);  // gate and up share one launch
   w.sg = n_splits(H, w.kc_gu);
   w.kc_d = split_kc(T, H, I);
   w.sd = n_splits(I, w.kc_d);
@@ -131,9 +132,8 @@ int launch_shared_expert(const uint16_t* x, int T, int H, int I, const uint16_t*
                          uint16_t* out, void* ws, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const SharedWs w = shared_carve(T, H, I, ws);
-  int rc = launch_linear_tc_f32_splitk(x, gate_w, T, I, H, w.kc_gu, w.g, s);
-  if (rc) return rc;
-  rc = launch_linear_tc_f32_splitk(x, up_w, T, I, H, w.kc_gu, w.u, s);
+  // gate and up in one launch
+  int rc = launch_linear_tc_f32_splitk(x, gate_w, T, I, H, w.kc_gu, w.g, s, up_w, w.u);
   if (rc) return rc;
   const long long n1 = (long long)T * (I / 4);
   shared_silu_mul_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(w.g, w.u, w.sg, T,
