@@ -29,6 +29,8 @@ Readings where the pages are silent:
   - argsort is stable (rows of one expert ascend by token id);
   - nibble j (bits 4j..4j+3) of packed word i is column 8i+j, two's complement;
   - act_bits=16: bf16 activations times exactly dequantised weights;
+  - the weight quantisers (four and eight bits, group 32): scale =
+    bf16(max|w| / 7 or / 127), codes = clamp(rint(w / scale)) in IEEE float32;
   - act_bits=8: per-row symmetric int8, scale = max|v|/127 and
     q = clamp(rint(v/scale), -127, 127), all in IEEE float32; weight-group
     integer partials are exact; the input of every int4 linear is its bf16
@@ -234,6 +236,36 @@ def quantize_weight_int4(w):
     q = np.where(s[..., None] > 0, q, np.float32(0))
     q = np.clip(q, -8, Q4_MAX).astype(np.int64).reshape(N, K)
     return pack_int4(q), s_bits
+
+
+Q8W_MAX = 127       # symmetric int8 weight range used by the 8-bit quantiser
+
+
+def quantize_weight_int8(w):
+    """bf16 weight [N, K] -> (int8 codes [N, K], bf16 scale bits [N, K/32]).
+
+    The eight-bit choice of the conversion the "Kimi exact-generator
+    adaptation" page names (section "The proposed substitution":
+    ExactLinear.from_weight with "four-bit or eight-bit choices and a group
+    size of 32"; no rounding rule is given).  The reading of the four-bit
+    quantiser with 127 in place of 7, per row and 32-column group, every step
+    in IEEE float32: a = max|w| (exact); s = bf16(a / 127) (the division
+    rounded to nearest, then to bf16, ties to even); q = clamp(rint(w / s),
+    -127, 127) with the stored s and rint rounding half to even; s = 0 gives
+    q = 0.  Codes are stored one per byte in column order."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 32")
+    g = w.reshape(N, K // GROUP, GROUP)
+    amax = np.max(np.abs(g), axis=-1)
+    s_bits = f32_to_bf16_bits((amax / np.float32(Q8W_MAX)).astype(np.float32))
+    s = (s_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(g / s[..., None])
+    q = np.where(s[..., None] > 0, q, np.float32(0))
+    q = np.clip(q, -Q8W_MAX, Q8W_MAX).astype(np.int8).reshape(N, K)
+    return q, s_bits
 
 
 def int4_group_partials(qx, packed) -> np.ndarray:

@@ -112,11 +112,26 @@ MUTANTS = [
     ("q4_divisor_8", "weight scale max/8",
      "(amax / np.float32(Q4_MAX))", "(amax / np.float32(8))"),
     ("q4_unrounded_scale", "weight codes from the scale before its bf16 rounding",
-     "q = np.rint(g / s[..., None])", "q = np.rint(g / (amax / np.float32(Q4_MAX))[..., None])"),
+     "q = np.rint(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -8, Q4_MAX)",
+     "q = np.rint(g / (amax / np.float32(Q4_MAX))[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -8, Q4_MAX)"),
     ("q4_truncate", "weight codes truncated instead of rounded",
-     "q = np.rint(g / s[..., None])", "q = np.trunc(g / s[..., None])"),
+     "q = np.rint(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -8, Q4_MAX)",
+     "q = np.trunc(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -8, Q4_MAX)"),
     ("q4_zero_group_unguarded", "a zero group divided by its zero scale",
-     "q = np.where(s[..., None] > 0, q, np.float32(0))", "pass"),
+     "q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -8, Q4_MAX)",
+     "pass\n    q = np.clip(q, -8, Q4_MAX)"),
+    ("q8w_divisor_128", "8-bit weight scale max/128",
+     "f32_to_bf16_bits((amax / np.float32(Q8W_MAX)).astype(np.float32))",
+     "f32_to_bf16_bits((amax / np.float32(128)).astype(np.float32))"),
+    ("q8w_unrounded_scale", "8-bit weight codes from the scale before its bf16 rounding",
+     "    s = (s_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)\n    with np.errstate(divide=\"ignore\", invalid=\"ignore\"):\n        q = np.rint(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -Q8W_MAX",
+     "    s = (amax / np.float32(Q8W_MAX)).astype(np.float32)\n    with np.errstate(divide=\"ignore\", invalid=\"ignore\"):\n        q = np.rint(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -Q8W_MAX"),
+    ("q8w_truncate", "8-bit weight codes truncated instead of rounded",
+     "        q = np.rint(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -Q8W_MAX",
+     "        q = np.trunc(g / s[..., None])\n    q = np.where(s[..., None] > 0, q, np.float32(0))\n    q = np.clip(q, -Q8W_MAX"),
+    ("q8w_group_of_16", "8-bit weight groups of 16 columns",
+     "    g = w.reshape(N, K // GROUP, GROUP)\n    amax = np.max(np.abs(g), axis=-1)\n    s_bits = f32_to_bf16_bits((amax / np.float32(Q8W_MAX))",
+     "    g = w.reshape(N, K // 16, 16)\n    amax = np.max(np.abs(g), axis=-1)\n    s_bits = f32_to_bf16_bits((amax / np.float32(Q8W_MAX))"),
     ("pack_range_unchecked", "out-of-range codes packed silently",
      "if q.size and (q.min() < -8 or q.max() > 7):", "if False:"),
     # expert

@@ -598,6 +598,68 @@ def test_weight_quantiser_zero_group_and_half_ties():
 
 
 # ----------------------------------------------------------------------------
+# int8 weight quantiser (ExactLinear.from_weight with eight bits, group 32)
+# ----------------------------------------------------------------------------
+
+def test_weight_quantiser_int8_recovers_exact_codes():
+    # a group whose largest |code| is 127 and whose scale has at most one
+    # significant bit: 127 * 2^e / 127 is the scale itself, and code * 2^e is
+    # an exact bf16 for |code| <= 127 (7 significant bits), so (q, s) come back
+    N, K = 6, 128
+    q = RNG.integers(-127, 128, size=(N, K))
+    q[:, ::32] = np.where(RNG.random((N, K // 32)) < 0.5, 127, -127)
+    s = np.ldexp(1.0, RNG.integers(-20, 4, size=(N, K // 32)))
+    w = _bf16_exact(q * np.repeat(s, 32, axis=1))
+    q8, s_bits = O.quantize_weight_int8(w)
+    assert q8.dtype == np.int8
+    assert np.array_equal(q8.astype(np.int64), q)
+    assert np.array_equal(O.bf16_bits_to_f64(s_bits), s)
+
+
+def test_weight_quantiser_int8_error_bound_and_range():
+    w = O.round_bf16(RNG.normal(size=(16, 256)) * RNG.uniform(1e-3, 10, size=(16, 1))).astype(np.float32)
+    q, s_bits = O.quantize_weight_int8(w)
+    q = q.astype(np.int64)
+    s = np.repeat(O.bf16_bits_to_f64(s_bits), 32, axis=1)
+    assert q.min() >= -127 and q.max() <= 127
+    # every code is within half a step of w / s (fp32 division, ulp(128) = 2^-16)
+    assert np.all(np.abs(w / s - q) <= 0.5 + 2.0 ** -16)
+    # the scale is a/127 rounded to bf16: within 2^-8 relative of the group's max/127
+    amax = np.abs(w).reshape(16, 8, 32).max(axis=-1)
+    rel = np.abs(O.bf16_bits_to_f64(s_bits) * 127 / amax - 1)
+    assert rel.max() <= 2.0 ** -8
+    # the largest magnitude of each group maps to +-127 (|w| / s <= 127 (1 + 2^-9))
+    assert np.all(np.abs(q).reshape(16, 8, 32).max(axis=-1) == 127)
+
+
+def test_weight_quantiser_int8_zero_group_and_half_ties():
+    w = np.zeros((2, 64), dtype=np.float32)
+    # group 1 of row 0: max 127 (s = 1), values on half steps round to even codes
+    w[0, 32:41] = [127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, -126.5, 125.5]
+    q, s_bits = O.quantize_weight_int8(w)
+    assert s_bits.tolist() == [[0, 0x3F80], [0, 0]]
+    assert q[0, 32:41].tolist() == [127, 0, 2, 2, 0, -2, -2, -126, 126]
+    assert not q[1].any() and not q[0, :32].any()
+
+
+def test_weight_quantisers_agree_on_a_shared_grid():
+    # a group of codes in [-7, 7] with max 7 and scale s: the int4 quantiser
+    # recovers the codes with scale s, the int8 one the same values with
+    # scale 7 s / 127 rounded to bf16 (brute force: each code from one float32
+    # division, rounded half to even)
+    q = np.array([[7, -7, 3, 0, -1, 5, 2, -4] * 4], dtype=np.int64)
+    s = 0.0625
+    w = _bf16_exact(q * s)
+    q4, _ = O.quantize_weight_int4(w)
+    assert np.array_equal(O.unpack_int4(q4), q)
+    q8, s8 = O.quantize_weight_int8(w)
+    s8f = np.float32(O.bf16_bits_to_f64(s8)[0, 0])
+    assert s8f == np.float32(O.round_bf16(np.float32(7 * s) / np.float32(127)))
+    want = [int(np.rint(np.float32(v) / s8f)) for v in w[0]]
+    assert q8[0].tolist() == want
+
+
+# ----------------------------------------------------------------------------
 # shared expert
 # ----------------------------------------------------------------------------
 
