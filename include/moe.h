@@ -292,6 +292,21 @@ int moe_quantize_rows(const uint16_t* v, int R, int C, int8_t* q, float* scale, 
 int moe_quantize_int4(const uint16_t* w, int N, int K, int32_t* packed, uint16_t* scale,
                       void* stream);
 
+/* 8-bit weight quantiser: the eight-bit choice of the same conversion
+ * (ExactLinear.from_weight with "four-bit or eight-bit choices and a group
+ * size of 32", "Kimi exact-generator adaptation" page, section "The proposed
+ * substitution"; no rounding rule is given).  Reading, per row and 32-column
+ * group, in IEEE float32: a = max|w|; s = bf16(a / 127) (division rounded to
+ * nearest, then to bf16, ties to even); q = clamp(rint(w / s), -127, 127)
+ * with the stored s, ties to even; s = 0 gives q = 0.
+ *   w      bf16 [N, K] row-major, device, 16-byte aligned;
+ *   q      int8 [N, K] out, device, 16-byte aligned, column order;
+ *   scale  bf16 [N, K/32] out, device.
+ * K % 32 == 0 (else MOE_ERR_UNSUPPORTED).  A non-finite weight records
+ * MOE_ERR_UNSUPPORTED in the device status word; its group gets s = 0.
+ * Caller-owned buffers; stream-ordered, no host sync. */
+int moe_quantize_int8(const uint16_t* w, int N, int K, int8_t* q, uint16_t* scale, void* stream);
+
 /* --------------------------------------------------------------- combine -- */
 
 /* Un-permute and weighted sum (moe_infer listing; donor-reference "Sum the

@@ -11,7 +11,7 @@ _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "c
             "dispatch", "dispatch_noalloc", "expert_ffn", "int4_linear", "int4_linear_partials",
             "int4_linear_stall_selftest",
             "last_cuda_error", "launch_count",
-            "lib", "linear_bf16", "quantize_int4",
+            "lib", "linear_bf16", "quantize_int4", "quantize_int8",
             "quantize_rows", "shared_expert",
             "rmsnorm", "route", "status_string", "wait_selftest", "capi")
 

@@ -82,6 +82,7 @@ SIGNATURES = {
                                                c_int64, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_quantize_int4": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_quantize_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_shared_expert_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_shared_expert": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -373,6 +374,20 @@ def quantize_int4(w: torch.Tensor):
     _check("moe_quantize_int4", lib.moe_quantize_int4(_p(w), rows, K, _p(packed), _p(scale),
                                                       _stream()))
     return packed, scale
+
+
+def quantize_int8(w: torch.Tensor):
+    """bf16 weight [..., N, K] -> (int8 codes [..., N, K], bf16 scale [..., N, K/32])."""
+    if _arg("w", w, None, torch.bfloat16).dim() < 1:
+        raise ValueError("w: expected at least one dimension")
+    dev = _placed(w=w)
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    q = torch.empty(*w.shape, dtype=torch.int8, device=dev)
+    scale = torch.empty(*w.shape[:-1], K // 32, dtype=torch.bfloat16, device=dev)
+    _check("moe_quantize_int8", lib.moe_quantize_int8(_p(w), rows, K, _p(q), _p(scale),
+                                                      _stream()))
+    return q, scale
 
 
 def shared_expert(x: torch.Tensor, gate_w: torch.Tensor, up_w: torch.Tensor,

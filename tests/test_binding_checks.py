@@ -114,6 +114,7 @@ def test_combine_linear_rmsnorm_quantisers(capi):
     raises("gain: expected shape", capi.rmsnorm, bf16(5, 64), bf16(32), 1e-6)
     raises("v: expected shape", capi.quantize_rows, bf16(64))
     raises(CUDA_ONLY, capi.quantize_int4, bf16(3, 8, 64))
+    raises(CUDA_ONLY, capi.quantize_int8, bf16(3, 8, 64))
 
 
 def test_shared_expert(capi):

@@ -308,6 +308,42 @@ def test_quantize_int4_reports_nonfinite_weights(moe):
     assert moe.check_error() == 0
 
 
+# ------------------------------------------------------------ int8 weight quantiser
+
+@pytest.mark.parametrize("shape", [(3, 40, 96), (1, 7, 32), (2, 513, 7168)])
+def test_quantize_int8_bit_exact(moe, shape):
+    """Codes and bf16 scales equal the oracle's bit for bit (float32 steps on
+    both sides), over magnitudes from 1e-4 to 1e3, zero groups and ties."""
+    rng = np.random.default_rng(sum(shape) + 8)
+    E, N, K = shape
+    w = rng.normal(size=shape) * rng.uniform(1e-4, 1e3, size=(E, N, 1))
+    w[:, :, :32] *= rng.random((E, N, 1)) < 0.8        # some all-zero groups
+    if K >= 64:  # s = 1: max 127 and half steps
+        w[0, 0, 32:64] = np.concatenate([[127.0], np.arange(31) * 0.5 - 7.5])
+    wb = _bf16(w)
+    q, scale = moe.quantize_int8(wb.to(DEV))
+    assert moe.check_error() == 0
+    ref_q, ref_s = O.quantize_weight_int8(wb.float().numpy().reshape(E * N, K))
+    assert np.array_equal(q.cpu().numpy().reshape(E * N, K), ref_q)
+    assert np.array_equal(bf16_bits(scale.cpu()).reshape(E * N, K // 32), ref_s)
+
+
+def test_quantize_int8_reports_nonfinite_weights(moe):
+    w = torch.zeros(4, 64, dtype=torch.bfloat16)
+    w[2, 40] = float("inf")
+    w[3, 3] = float("nan")
+    w[1, 5] = 2.0
+    q, scale = moe.quantize_int8(w.to(DEV))
+    assert moe.check_error() == moe.capi.MOE_ERR_UNSUPPORTED
+    s = bf16_bits(scale.cpu())
+    assert s[2, 1] == 0 and s[3, 0] == 0
+    qc = q.cpu().numpy()
+    assert not qc[2, 32:].any() and not qc[3, :32].any() and qc[1, 5] == 127
+    # the next call is clean
+    moe.quantize_int8(torch.ones(2, 32, dtype=torch.bfloat16, device=DEV))
+    assert moe.check_error() == 0
+
+
 @pytest.mark.parametrize("K,N,counts", [
     (320, 300, [0, 1, 33, 70, 8]),        # ragged K tail, ragged N tile, multi-chunk experts
     (2048, 512, [5, 0, 0, 64, 2]),
