@@ -575,7 +575,7 @@ int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
                      const int32_t* chunk_e,
                      const int32_t* chunk_row0, const int32_t* chunk_rows, const int32_t* n_chunks,
                      int* status, cudaStream_t s) {
-  TxMaps maps;
+  TxMaps maps{};
   if (!act_map(&maps.a, x16, rows_max, D) ||
       !packed_map(&maps.q0, gate_packed, E, I, D, kTxWM) ||
       !packed_map(&maps.q1, up_packed, E, I, D, kTxWM))
@@ -599,7 +599,7 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s) {
-  TxMaps maps;
+  TxMaps maps{};
   if (!act_map(&maps.a, h16, rows_max, I) || !packed_map(&maps.q0, down_packed, E, D, I, 2 * kTxWM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;
@@ -633,7 +633,7 @@ int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows
     return launch_tc_q8_linear_stalled(x16, x_scale, rows_max, E, N, K, w_packed, w_scale, y,
                                        chunk_e, chunk_row0, chunk_rows, n_chunks, status, wait_ns,
                                        stall_at, s);
-  TxMaps maps;
+  TxMaps maps{};
   if (!act_map(&maps.a, x16, rows_max, K) || !packed_map(&maps.q0, w_packed, E, N, K, 2 * kTxWM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;

@@ -416,7 +416,7 @@ int launch_tc_q8_gateup(const uint16_t* x16, const float* x_scale, int rows_max,
                         const int32_t* chunk_e, const int32_t* chunk_row0,
                         const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
                         cudaStream_t s) {
-  TxMaps maps;
+  TxMaps maps{};
   if (!q8_act_map(&maps.a, x16, rows_max, D) ||
       !q8_packed_map(&maps.q0, gate_packed, E, I, D, kQM / 2) ||
       !q8_packed_map(&maps.q1, up_packed, E, I, D, kQM / 2))
@@ -442,7 +442,7 @@ int launch_tc_q8_down(const uint16_t* h16, const float* h_scale, int rows_max, i
                       const int32_t* chunk_e, const int32_t* chunk_row0,
                       const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
                       cudaStream_t s, int32_t* partials) {
-  TxMaps maps;
+  TxMaps maps{};
   if (!q8_act_map(&maps.a, h16, rows_max, I) ||
       !q8_packed_map(&maps.q0, down_packed, E, D, I, kQM))
     return MOE_ERR_CUDA;
@@ -470,7 +470,7 @@ int launch_tc_q8_linear_stalled(const uint16_t* x16, const float* x_scale, int r
                                 float* y, const int32_t* chunk_e, const int32_t* chunk_row0,
                                 const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
                                 long long wait_ns, int stall_at, cudaStream_t s) {
-  TxMaps maps;
+  TxMaps maps{};
   if (!q8_act_map(&maps.a, x16, rows_max, K) || !q8_packed_map(&maps.q0, w_packed, E, N, K, kQM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;
