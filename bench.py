@@ -399,8 +399,12 @@ def _measure(args, w, device, dist, world, local):
     x_dev = x.to(device)
     out = torch.empty_like(x_dev)
 
+    # the layer call, launched as one captured CUDA graph (moe_layer_graph_*)
+    # or kernel by kernel on the stream (--launch stream)
+    graph = layer.graph(x_dev, out) if args.launch == "graph" else None
+    run = graph.launch if graph else (lambda: layer.forward(x_dev, out))
     for _ in range(args.warmup):
-        layer.forward(x_dev, out)
+        run()
     torch.cuda.synchronize()
     rc = moe.check_error()
     if rc != 0:
@@ -416,7 +420,7 @@ def _measure(args, w, device, dist, world, local):
     n0 = moe.launch_count()
     e0.record()
     for _ in range(args.steps):
-        layer.forward(x_dev, out)
+        run()
     e1.record()
     launches = moe.launch_count() - n0
     torch.cuda.synchronize()
@@ -436,10 +440,15 @@ def _measure(args, w, device, dist, world, local):
     # end to end through the C ABI with host buffers (pinned), copies inside
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e_pass(layer, x, w, world, dist, device, min(args.steps, 100))
+        e2e = _e2e_pass(layer, x, w, world, dist, device, min(args.steps, 100), args.launch)
+    cfg = _config(w, world, roof)
+    cfg["launch"] = ("one CUDA graph of moe_layer_forward per step (moe_layer_graph_launch)"
+                     if graph else "moe_layer_forward, kernels launched on the stream")
     res = {"value": job_tokens_per_s(world, w.T, ms), "ms_per_step": ms, "roofline": roof,
-           "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "config": _config(w, world, roof)}
-    del layer, weights, x_dev, out
+           "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "config": cfg}
+    if graph:
+        graph.close()
+    del layer, weights, x_dev, out, graph, run
     gc.collect()
     torch.cuda.empty_cache()
     return res
@@ -467,6 +476,8 @@ def _parser() -> argparse.ArgumentParser:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="layer calls as one captured CUDA graph each, or kernel by kernel")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling case: replace the workload's expert count (routing uncalibrated)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -520,21 +531,27 @@ def main(argv=None):
     return 0
 
 
-def _e2e_pass(layer, x, w, world, dist, device, e_steps):
+def _e2e_pass(layer, x, w, world, dist, device, e_steps, launch="stream"):
+    """moe_layer_forward_host (as a captured graph with --launch graph): the
+    pinned host input copied in, the layer, the output copied out."""
     xh = x.pin_memory()
     oh = torch.empty_like(x).pin_memory()
+    graph = layer.graph(xh, oh, host=True) if launch == "graph" else None
+    run = graph.launch if graph else (lambda: layer.forward_host(xh, oh))
     for _ in range(3):
-        layer.forward_host(xh, oh)
+        run()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record()
     for _ in range(e_steps):
-        layer.forward_host(xh, oh)
+        run()
     e1.record()
     torch.cuda.synchronize()
     wall = (time.perf_counter() - t0) / e_steps
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, device)
+    if graph:
+        graph.close()
     return {"value": job_tokens_per_s(world, w.T, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
             "host_wall_ms_per_step": wall * 1000.0}

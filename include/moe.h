@@ -372,6 +372,30 @@ int moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_
 int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w, const uint16_t* x_host,
                            uint16_t* out_host, void* ws, size_t ws_bytes, void* stream);
 
+/* A captured layer call: one moe_layer_forward (host == 0) or
+ * moe_layer_forward_host (host != 0) call with exactly these arguments,
+ * recorded once as a CUDA graph, for callers that run the layer again and
+ * again on the same buffers (a serving loop).  No page has this call: it
+ * replaces the per-call launches of the library's kernels (about 8 to 16 per
+ * layer) with one graph launch.  All pointers are baked in: the weights, x,
+ * out (pinned host memory when host != 0) and ws must stay valid and are
+ * re-read on every launch.  The capture runs on `stream`, which must not be
+ * capturing already, in thread-local mode; nothing executes during it.
+ * Argument errors are those of the captured call, returned before any
+ * capture; *graph is NULL on every error. */
+typedef struct moe_layer_graph moe_layer_graph;
+int moe_layer_graph_create(const moe_config* cfg, const moe_weights* w, const void* x, void* out,
+                           int host, void* ws, size_t ws_bytes, void* stream,
+                           moe_layer_graph** graph);
+
+/* Runs the captured call on `stream` (stream-ordered, no host sync): the
+ * same kernels, results and device status behaviour as the call it captured.
+ * moe_launch_count() advances by the captured kernel count. */
+int moe_layer_graph_launch(const moe_layer_graph* graph, void* stream);
+
+/* Frees a captured call (NULL is ignored); launches already issued finish. */
+void moe_layer_graph_destroy(moe_layer_graph* graph);
+
 /* ------------------------------------------------------------ status etc -- */
 
 /* Synchronises `stream`, then returns and clears the current device's

@@ -92,6 +92,11 @@ SIGNATURES = {
     "moe_workspace_size": (c_size_t, [POINTER(MoeConfig)]),
     "moe_layer_forward": (c_int, [POINTER(MoeConfig), POINTER(MoeWeights), c_void_p, c_void_p,
                                   c_void_p, c_size_t, c_void_p]),
+    "moe_layer_graph_create": (c_int, [POINTER(MoeConfig), POINTER(MoeWeights), c_void_p, c_void_p,
+                                       c_int, c_void_p, c_size_t, c_void_p,
+                                       POINTER(c_void_p)]),
+    "moe_layer_graph_launch": (c_int, [c_void_p, c_void_p]),
+    "moe_layer_graph_destroy": (None, [c_void_p]),
     "moe_layer_forward_host": (c_int, [POINTER(MoeConfig), POINTER(MoeWeights), c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]),
     "moe_check_error": (c_int, [c_void_p]),
@@ -492,6 +497,56 @@ class MoeLayer:
         _check("moe_layer_forward_host", lib.moe_layer_forward_host(
             ctypes.byref(self.cfg), ctypes.byref(self.wstruct), _p(x_host), _p(out_host),
             _p(self.ws), self.ws.numel(), _stream()))
+
+    def graph(self, x: torch.Tensor, out: torch.Tensor, host: bool = False) -> "LayerGraph":
+        """The forward call (forward_host with host=True: pinned CPU buffers)
+        on exactly these buffers, captured once as a CUDA graph (on a side
+        stream: the legacy default stream cannot capture); LayerGraph.launch()
+        replays it on the current stream."""
+        shape = (self.cfg.T, self.cfg.H)
+        _arg("x", x, shape, torch.bfloat16)
+        _arg("out", out, shape, torch.bfloat16)
+        if host:
+            for name, t in (("x", x), ("out", out)):
+                if t.is_cuda or not t.is_pinned():
+                    raise ValueError(f"{name} must be a pinned host tensor")
+        elif _placed(x=x, out=out) != self.device:
+            raise ValueError("x and out must be on the layer's device")
+        handle = c_void_p()
+        cur = torch.cuda.current_stream(self.device)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            rc = lib.moe_layer_graph_create(
+                ctypes.byref(self.cfg), ctypes.byref(self.wstruct), _p(x), _p(out), int(host),
+                _p(self.ws), self.ws.numel(), _stream(), ctypes.byref(handle))
+        cur.wait_stream(side)
+        _check("moe_layer_graph_create", rc)
+        return LayerGraph(handle, (self, x, out))
+
+
+class LayerGraph:
+    """A captured layer call (moe_layer_graph_*); keeps its layer and buffers alive."""
+
+    def __init__(self, handle: c_void_p, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self) -> None:
+        if not self._h:
+            raise ValueError("the graph was closed")
+        _check("moe_layer_graph_launch", lib.moe_layer_graph_launch(self._h, _stream()))
+
+    def close(self) -> None:
+        if self._h:
+            lib.moe_layer_graph_destroy(self._h)
+            self._h = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def _check_layer_weights(w: Dict[str, torch.Tensor], H: int, E: int, I: int, L: int,

@@ -198,3 +198,66 @@ extern "C" int moe_layer_forward_host(const moe_config* cfg, const moe_weights* 
   MOE_TRY_CUDA(cudaMemcpyAsync(out_host, lw.out_dev, bytes, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }
+
+// ---- captured layer calls (CUDA graphs) -----------------------------------
+
+struct moe_layer_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  uint64_t launches;  // library kernels in the captured call
+};
+
+extern "C" int moe_layer_graph_create(const moe_config* cfg, const moe_weights* w, const void* x,
+                                      void* out, int host, void* ws, size_t ws_bytes,
+                                      void* stream, moe_layer_graph** graph) {
+  moe::Range range_("moe_layer_graph_create");
+  if (!graph) return MOE_ERR_INVALID;
+  *graph = nullptr;
+  // the argument checks of the captured call, before any capture begins
+  int rc = validate(cfg, w);
+  if (rc) return rc;
+  if (!x || !out || !ws || !aligned(ws, 256)) return MOE_ERR_INVALID;
+  if (!host && (!aligned(x, 16) || !aligned(out, 16))) return MOE_ERR_INVALID;
+  if (ws_bytes < carve(*cfg, nullptr).total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  MOE_TRY_CUDA(cudaStreamIsCapturing(s, &cs));
+  if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_INVALID;
+  const uint64_t n0 = moe_launch_count();
+  MOE_TRY_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  rc = host ? moe_layer_forward_host(cfg, w, static_cast<const uint16_t*>(x),
+                                     static_cast<uint16_t*>(out), ws, ws_bytes, stream)
+            : moe_layer_forward(cfg, w, static_cast<const uint16_t*>(x),
+                                static_cast<uint16_t*>(out), ws, ws_bytes, stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(s, &g);  // ends the capture on every path
+  if (rc || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    if (rc) return rc;
+    note_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, g, 0);
+  if (ei != cudaSuccess) {
+    cudaGraphDestroy(g);
+    note_cuda_error(ei);
+    return MOE_ERR_CUDA;
+  }
+  *graph = new moe_layer_graph{g, exec, moe_launch_count() - n0};
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_graph_launch(const moe_layer_graph* graph, void* stream) {
+  if (!graph) return MOE_ERR_INVALID;
+  MOE_TRY_CUDA(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+  for (uint64_t i = 0; i < graph->launches; ++i) count_launch();
+  return MOE_OK;
+}
+
+extern "C" void moe_layer_graph_destroy(moe_layer_graph* graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
+}

@@ -197,6 +197,61 @@ def test_layer_forward_replays_from_a_cuda_graph(moe, case):
     assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("case", ["tiny", "small_latent", "small_adversarial", "tiny_exact"])
+def test_layer_graph_launches_replay_the_call(moe, case):
+    """moe_layer_graph_create / _launch: every launch of the captured call
+    gives the bits of moe_layer_forward (and of forward_host through pinned
+    buffers), and moe_launch_count advances by the captured kernel count."""
+    w = SMALL[case]
+    x = wl.gen_x(w, attempts=conditioned_attempts(w))
+    router = wl.gen_router(w)
+    lat = wl.gen_latent(w)
+    layer = _layer(moe, w, device_weights(w, DEV, router, lat))
+    xd = x.to(DEV)
+    ref = layer.forward(xd)
+    torch.cuda.synchronize()
+    n0 = moe.launch_count()
+    layer.forward(xd, torch.empty_like(ref))
+    per_call = moe.launch_count() - n0
+    out = torch.zeros_like(ref)
+    g = layer.graph(xd, out)
+    assert not out.any()                      # capturing runs nothing
+    n1 = moe.launch_count()
+    for _ in range(2):
+        out.zero_()
+        g.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert moe.launch_count() - n1 == 2 * per_call
+    g.close()
+    xh = x.pin_memory()
+    oh = torch.zeros_like(x).pin_memory()
+    gh = layer.graph(xh, oh, host=True)
+    gh.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+    gh.close()
+    assert moe.check_error() == 0
+
+
+def test_layer_graph_rejects_bad_arguments_before_capture(moe):
+    w = SMALL["tiny"]
+    layer = _layer(moe, w, device_weights(w, DEV))
+    x = torch.zeros(w.T, w.H, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError):
+        layer.graph(x[:-1], torch.empty_like(x))
+    with pytest.raises(ValueError):
+        layer.graph(x.cpu(), torch.empty_like(x).cpu(), host=True)   # not pinned
+    bad = moe.capi.MoeConfig(w.T, w.H, w.E, w.k + w.E, w.I, 0, 16, 1, 1e-6, 0)  # k > E
+    h = moe.capi.c_void_p(123)
+    rc = moe.lib.moe_layer_graph_create(moe.capi.ctypes.byref(bad), moe.capi.ctypes.byref(layer.wstruct),
+                                        x.data_ptr(), x.data_ptr(), 0, layer.ws.data_ptr(),
+                                        layer.ws.numel(), None, moe.capi.ctypes.byref(h))
+    assert rc == moe.capi.MOE_ERR_UNSUPPORTED and not h.value
+    moe.lib.moe_layer_graph_destroy(None)
+    assert moe.check_error() == 0
+
+
 def test_layer_rejects_mis_sized_buffers_before_any_launch(moe):
     w = SMALL["tiny"]
     layer = _layer(moe, w, device_weights(w, DEV))
