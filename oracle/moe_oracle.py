@@ -29,6 +29,8 @@ Readings where the pages are silent:
   - argsort is stable (rows of one expert ascend by token id);
   - nibble j (bits 4j..4j+3) of packed word i is column 8i+j, two's complement;
   - act_bits=16: bf16 activations times exactly dequantised weights;
+  - the int16/int64 reading of act_bits=16 (quantize_rows_int16,
+    int4_linear_int16): the int8 steps with 32767, integer group partials;
   - the weight quantisers (four and eight bits, group 32): scale =
     bf16(max|w| / 7 or / 127), codes = clamp(rint(w / scale)) in IEEE float32;
   - act_bits=8: per-row symmetric int8, scale = max|v|/127 and
@@ -310,6 +312,65 @@ def int4_linear(u, packed, scale_bits, act_bits: int = 16, row_chunk: int = 64) 
     for r0 in range(0, u.shape[0], row_chunk):
         qx, sx = quantize_rows_int8(u[r0:r0 + row_chunk].astype(np.float32))
         P = int4_group_partials(qx, packed)
+        out[r0:r0 + row_chunk] = sx.astype(np.float64)[:, None] * np.einsum("rng,ng->rn", P, s)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# the int16 / int64 reading of act_bits = 16
+# ----------------------------------------------------------------------------
+
+Q16_MAX = 32767      # symmetric int16 activation range
+
+
+def quantize_rows_int16(v):
+    """Per-row symmetric int16 quantisation, every step in IEEE float32.
+
+    The alternative reading of act_bits=16 (the exact-generator page's
+    "int64 exact int4 MAC" with 16-bit activations): the int8 quantiser's
+    steps with 32767 in place of 127.  a = max|v| (exact); scale = a / 32767
+    (RN); q = clamp(rint(v / scale), -32767, 32767) with rint rounding half to
+    even.  A zero row gives scale 0 and q = 0."""
+    v = np.asarray(v, dtype=np.float32)
+    amax = np.max(np.abs(v), axis=-1)
+    scale = (amax / np.float32(Q16_MAX)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q16 = np.rint(v / scale[..., None])
+    q16 = np.where(scale[..., None] > 0, q16, np.float32(0))
+    q16 = np.clip(q16, -Q16_MAX, Q16_MAX).astype(np.int16)
+    return q16, scale
+
+
+def int16_group_partials(q16, packed) -> np.ndarray:
+    """Exact integer partial sums P[r, n, g] = sum_{c in group g} q16[r, c] * qw[n, c].
+
+    |P| <= 32 * 8 * 32767 < 2**23 per group, so the float64 matrix product of
+    the integer operands is exact; returned as int64.  The whole-K bound
+    K * 8 * 32767 < 2**31 (an int32 accumulator over all of K) is asserted."""
+    q16 = np.asarray(q16, dtype=np.int64)
+    qw = unpack_int4(packed).astype(np.int64)
+    R, K = q16.shape
+    N = qw.shape[0]
+    if K * 8 * Q16_MAX >= 2 ** 31:
+        raise ValueError("K*8*32767 must stay below 2**31")
+    G = K // GROUP
+    a = q16.reshape(R, G, GROUP).astype(np.float64).transpose(1, 0, 2)   # [G, R, 32]
+    b = qw.reshape(N, G, GROUP).astype(np.float64).transpose(1, 2, 0)    # [G, 32, N]
+    P = np.rint(np.matmul(a, b).transpose(1, 2, 0)).astype(np.int64)     # [R, N, G]
+    assert np.all(np.abs(P) <= GROUP * 8 * Q16_MAX)
+    return P
+
+
+def int4_linear_int16(u, packed, scale_bits, row_chunk: int = 64) -> np.ndarray:
+    """y = u W^T under the int16/int64 reading of act_bits=16, float64 [R, N]:
+    u quantised per row to int16 (scale sx), integer partials P per weight
+    group, y[r, n] = sx[r] * sum_g scale[n, g] * P[r, n, g]."""
+    u = np.asarray(u, dtype=np.float64)
+    s = bf16_bits_to_f64(scale_bits)  # [N, G]
+    out = np.empty((u.shape[0], s.shape[0]), dtype=np.float64)
+    for r0 in range(0, u.shape[0], row_chunk):
+        q16, sx = quantize_rows_int16(u[r0:r0 + row_chunk].astype(np.float32))
+        P = int16_group_partials(q16, packed)
         out[r0:r0 + row_chunk] = sx.astype(np.float64)[:, None] * np.einsum("rng,ng->rn", P, s)
     return out
 

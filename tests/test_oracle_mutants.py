@@ -98,13 +98,24 @@ MUTANTS = [
     ("q8_truncate", "activation codes truncated instead of rounded",
      "q = np.rint(v / scale[..., None])", "q = np.trunc(v / scale[..., None])"),
     ("q8_in_float64", "activation quantiser evaluated in float64",
-     "v = np.asarray(v, dtype=np.float32)", "v = np.asarray(v, dtype=np.float64)"),
+     "    v = np.asarray(v, dtype=np.float32)\n    amax = np.max(np.abs(v), axis=-1)\n    scale = (amax / np.float32(Q8_MAX))",
+     "    v = np.asarray(v, dtype=np.float64)\n    amax = np.max(np.abs(v), axis=-1)\n    scale = (amax / np.float32(Q8_MAX))"),
     ("q8_clip_126", "activation codes clamped to +-126",
      "q = np.clip(q, -Q8_MAX, Q8_MAX)", "q = np.clip(q, -Q8_MAX + 1, Q8_MAX - 1)"),
+    ("q16_divisor_32768", "int16 activation scale max/32768",
+     "(amax / np.float32(Q16_MAX))", "(amax / np.float32(32768))"),
+    ("q16_truncate", "int16 activation codes truncated instead of rounded",
+     "q16 = np.rint(v / scale[..., None])", "q16 = np.trunc(v / scale[..., None])"),
+    ("q16_in_float64", "int16 activation quantiser evaluated in float64",
+     "    v = np.asarray(v, dtype=np.float32)\n    amax = np.max(np.abs(v), axis=-1)\n    scale = (amax / np.float32(Q16_MAX))",
+     "    v = np.asarray(v, dtype=np.float64)\n    amax = np.max(np.abs(v), axis=-1)\n    scale = (amax / np.float32(Q16_MAX))"),
+    ("q16_partials_group_16", "int16 partials over groups of 16 columns",
+     "a = q16.reshape(R, G, GROUP)", "a = q16.reshape(R, G, GROUP)[:, :, ::-1]"),
     ("int32_bound_loosened", "accumulator bound checked against 2^32",
      "if K * 8 * Q8_MAX >= 2 ** 31:", "if K * 8 * Q8_MAX > 2 ** 32:"),
     ("q8_row_scale_dropped", "activation row scale left out of the output",
-     "sx.astype(np.float64)[:, None] * np.einsum", "np.einsum"),
+     "P = int4_group_partials(qx, packed)\n        out[r0:r0 + row_chunk] = sx.astype(np.float64)[:, None] * np.einsum",
+     "P = int4_group_partials(qx, packed)\n        out[r0:r0 + row_chunk] = np.einsum"),
     ("partials_group_strided", "weight groups taken as strided columns",
      "qw3 = qw.reshape(N, G, GROUP).astype(np.float64).transpose(1, 2, 0)",
      "qw3 = qw.reshape(N, GROUP, G).astype(np.float64).transpose(2, 1, 0)"),

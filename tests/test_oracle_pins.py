@@ -294,6 +294,83 @@ def test_group_partials_int32_bound_rejected():
 
 
 # ----------------------------------------------------------------------------
+# the int16 / int64 reading of act_bits = 16
+# ----------------------------------------------------------------------------
+
+def test_quantizer_int16_identity_on_int16_rows():
+    x = RNG.integers(-32767, 32768, size=(12, 96)).astype(np.float32)
+    x[:, 7] = -32767.0
+    q, s = O.quantize_rows_int16(x)
+    assert q.dtype == np.int16
+    assert np.all(s == 1.0) and np.array_equal(q, x.astype(np.int16))
+
+
+def test_quantizer_int16_bounds_and_rounding():
+    v = (RNG.normal(size=(20, 200)) * RNG.uniform(0.01, 100, size=(20, 1))).astype(np.float32)
+    v[3] = 0.0
+    q, s = O.quantize_rows_int16(v)
+    assert np.abs(q.astype(int)).max() <= 32767
+    assert s[3] == 0 and not q[3].any()
+    for r in range(20):
+        if r == 3:
+            continue
+        sc = Fraction(float(s[r]))
+        assert sc == Fraction(float(np.float32(np.abs(v[r]).max()) / np.float32(32767)))
+        assert np.abs(q[r].astype(int)).max() == 32767
+        for c in range(0, 200, 9):
+            # float32 division: the quotient (up to 32767) carries 2^-9 of rounding
+            assert abs(Fraction(float(v[r, c])) / sc - int(q[r, c])) <= Fraction(1, 2) + Fraction(1, 2 ** 8)
+    # half steps round to even codes (scale 1)
+    q, s = O.quantize_rows_int16(np.array([[32767.0, 0.5, 1.5, 2.5, -2.5, -100.5]], np.float32))
+    assert s[0] == 1.0 and q[0].tolist() == [32767, 0, 2, 2, -2, -100]
+
+
+def test_quantizer_int16_float32_tie_case_by_exact_arithmetic():
+    # the row [a, a/2, -a/2] separates float32 from float64 quantisation: the
+    # exact quotient (a/2)/s lies below the tie 16383.5 by less than half a
+    # float32 ulp there, so the float32 quotient is the tie itself and rint
+    # gives the even code 16384 (float64 would give 16383)
+    a = np.float32(1.925695538520813)
+    q, s = O.quantize_rows_int16(np.array([[a, a / np.float32(2), -a / np.float32(2)]], np.float32))
+    assert q[0].tolist() == [32767, 16384, -16384]
+    sc, v = Fraction(float(s[0])), Fraction(float(a / np.float32(2)))
+    assert abs(sc - Fraction(float(a)) / 32767) <= _f32_half_ulp(s[0])
+    tie = Fraction(32767, 2)
+    assert v / sc < tie and tie - v / sc < _f32_half_ulp(tie)
+
+
+def test_int16_group_partials_brute_force_and_extremes():
+    q16 = RNG.integers(-32767, 32768, size=(3, 96)).astype(np.int16)
+    qw = RNG.integers(-8, 8, size=(4, 96))
+    assert np.array_equal(O.int16_group_partials(q16, O.pack_int4(qw)), _brute_partials(q16, qw))
+    q16 = np.full((1, 64), -32767, dtype=np.int16)
+    qw = np.full((1, 64), -8)
+    assert O.int16_group_partials(q16, O.pack_int4(qw)).tolist() == [[[32 * 8 * 32767] * 2]]
+    K = 2 ** 31 // (8 * 32767) // 32 * 32 + 32   # first multiple of 32 past the int32 bound
+    assert K * 8 * 32767 >= 2 ** 31 and (K - 32) * 8 * 32767 < 2 ** 31
+    with pytest.raises(ValueError):
+        O.int16_group_partials(np.zeros((1, K), np.int16), np.zeros((1, K // 8), np.int32))
+
+
+def test_int4_linear_int16_reduces_to_an_integer_matmul():
+    # integer rows holding +-32767 (scale 1) and unit weight scales: y is the
+    # integer product x qw^T, computed here with Python integers
+    x = RNG.integers(-32767, 32768, size=(4, 64))
+    x[:, 0] = 32767
+    qw = RNG.integers(-8, 8, size=(3, 64))
+    ones = np.full((3, 2), ONE, dtype=np.uint16)
+    y = O.int4_linear_int16(x.astype(np.float64), O.pack_int4(qw), ones)
+    want = [[sum(int(x[r, c]) * int(qw[n, c]) for c in range(64)) for n in range(3)] for r in range(4)]
+    assert y.tolist() == want
+    # a group scale multiplies its group's partial only
+    sc = ones.copy()
+    sc[1, 1] = 0x4000  # 2.0 for group 1 of output 1
+    y2 = O.int4_linear_int16(x.astype(np.float64), O.pack_int4(qw), sc)
+    g1 = [sum(int(x[r, c]) * int(qw[1, c]) for c in range(32, 64)) for r in range(4)]
+    assert np.array_equal(y2[:, 1] - y[:, 1], np.array(g1, dtype=np.float64))
+
+
+# ----------------------------------------------------------------------------
 # PackedInt4Linear and the expert
 # ----------------------------------------------------------------------------
 
