@@ -226,6 +226,35 @@ int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale, const int32_
                          const uint16_t* down_scale, int act_bits, uint16_t* y_sorted, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* The int16 / int64 reading of act_bits 16 for one grouped PackedInt4Linear
+ * (exact-generator adaptation page, "Sources & provenance": PackedInt4Linear
+ * with act_bits 16 by default and an "int64 exact int4 MAC"; the page does
+ * not say what the 16 bits hold).  moe_int4_linear's act_bits 16 (and the
+ * layer's) reads them as bf16 activations times exactly dequantised
+ * weights; this call reads them as int16 codes with integer accumulation:
+ *   per row, in IEEE fp32: a = max|x|; sx = a / 32767 (rounded to nearest);
+ *   q = clamp(rint(x / sx), -32767, 32767), ties to even (a zero row: 0);
+ *   per 32-column weight group g: P_g = sum q * q_w, an exact integer
+ *   (|P_g| < 2^23; K * 8 * 32767 < 2^31, so K <= 8160);
+ *   out[r][n] = sx * acc, acc = the fp32 chain fma(scale[n, g], P_g, acc)
+ *   over the groups in K order from 0.
+ *   x        bf16 [rows_max, K] (rows of expert e: offsets[e] .. offsets[e+1])
+ *   offsets  int32 [E+1] (checked on the device: MOE_ERR_INVALID)
+ *   w_packed int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
+ *   out      fp32 [rows_max, N] (rows >= offsets[E] untouched)
+ *   partials optional int32 [rows_max, N, K/32]: every P_g (NULL: none)
+ * K % 32 == 0 and K <= 8160, else MOE_ERR_UNSUPPORTED.  SIMT integer
+ * arithmetic (not a hot path of the layer). */
+size_t moe_int4_linear_int16_workspace_size(int E, int K, int rows_max);
+int moe_int4_linear_int16(const uint16_t* x, const int32_t* offsets, int E, int K, int N,
+                          int rows_max, const int32_t* w_packed, const uint16_t* w_scale,
+                          float* out, int32_t* partials, void* ws, size_t ws_bytes, void* stream);
+
+/* The int16 codes of that reading on their own: v bf16 [R, C] -> q int16
+ * [R, C], scale fp32 [R] (the steps above). */
+int moe_quantize_rows_int16(const uint16_t* v, int R, int C, int16_t* q, float* scale,
+                            void* stream);
+
 /* Workspace bytes of moe_int4_linear (host only). */
 size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);
 

@@ -9,7 +9,7 @@ import importlib
 
 _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "combine",
             "dispatch", "dispatch_noalloc", "expert_ffn", "int4_linear", "int4_linear_partials",
-            "int4_linear_stall_selftest",
+            "int4_linear_stall_selftest", "int4_linear_int16", "quantize_rows_int16",
             "last_cuda_error", "launch_count",
             "lib", "linear_bf16", "quantize_int4", "quantize_int8",
             "quantize_rows", "shared_expert",

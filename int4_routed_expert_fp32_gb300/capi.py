@@ -83,6 +83,11 @@ SIGNATURES = {
     "moe_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_quantize_int4": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_quantize_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_quantize_rows_int16": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_int4_linear_int16_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "moe_int4_linear_int16": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                      c_void_p]),
     "moe_shared_expert_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_shared_expert": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -393,6 +398,37 @@ def quantize_int8(w: torch.Tensor):
     _check("moe_quantize_int8", lib.moe_quantize_int8(_p(w), rows, K, _p(q), _p(scale),
                                                       _stream()))
     return q, scale
+
+
+def quantize_rows_int16(v: torch.Tensor):
+    """Per-row symmetric int16 codes of bf16 v [R, C]: (int16 [R, C], fp32 scale [R])."""
+    R, C = _arg("v", v, (None, None), torch.bfloat16).shape
+    dev = _placed(v=v)
+    q = torch.empty(R, C, dtype=torch.int16, device=dev)
+    scale = torch.empty(R, dtype=torch.float32, device=dev)
+    _check("moe_quantize_rows_int16", lib.moe_quantize_rows_int16(_p(v), R, C, _p(q), _p(scale),
+                                                                  _stream()))
+    return q, scale
+
+
+def int4_linear_int16(x: torch.Tensor, offsets: torch.Tensor, w_packed: torch.Tensor,
+                      w_scale: torch.Tensor, partials: bool = False):
+    """fp32 [rows, N] = x W_e^T per expert segment under the int16/int64
+    reading of act_bits 16 (per-row int16 codes, exact group partials); with
+    partials=True also the int32 partials [rows, N, K/32]."""
+    E, N = _arg("w_packed", w_packed, (None, None, None), torch.int32).shape[:2]
+    rows, K = _arg("x", x, (None, None), torch.bfloat16).shape
+    _arg("offsets", offsets, (E + 1,), torch.int32)
+    _arg("w_packed", w_packed, (E, N, K // 8), torch.int32)
+    _arg("w_scale", w_scale, (E, N, K // 32), torch.bfloat16)
+    dev = _placed(x=x, offsets=offsets, w_packed=w_packed, w_scale=w_scale)
+    out = torch.empty(rows, N, dtype=torch.float32, device=dev)
+    part = torch.empty(rows, N, K // 32, dtype=torch.int32, device=dev) if partials else None
+    ws = _ws(lib.moe_int4_linear_int16_workspace_size(E, K, rows), dev)
+    _check("moe_int4_linear_int16", lib.moe_int4_linear_int16(
+        _p(x), _p(offsets), E, K, N, rows, _p(w_packed), _p(w_scale), _p(out), _p(part),
+        _p(ws), ws.numel(), _stream()))
+    return (out, part) if partials else out
 
 
 def shared_expert(x: torch.Tensor, gate_w: torch.Tensor, up_w: torch.Tensor,

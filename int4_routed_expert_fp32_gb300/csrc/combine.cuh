@@ -15,6 +15,19 @@ int launch_combine(const void* y, bool y_f32, const int32_t* inv_row, const floa
 // Gated expert MLP over expert-sorted rows (validated arguments); y is bf16
 // [rows_max, D] or, with y_f32, fp32.  No expert has more than
 // max_rows_per_expert rows (the token count when called from the layer).
+// Every expert's rows (offsets) cut into chunks of at most mc rows, on the
+// device (no host sync): the lists are carved from ws (row_chunk_bytes).
+struct RowChunks {
+  int32_t* chunk_e;
+  int32_t* chunk_row0;
+  int32_t* chunk_rows;
+  int32_t* n_chunks;
+  int max_chunks;
+};
+size_t row_chunk_bytes(int E, int rows_max, int mc);
+int launch_row_chunks(const int32_t* offsets, int E, int rows_max, int mc, void* ws,
+                      RowChunks* chunks, int* status, cudaStream_t s);
+
 // Workspace bytes of launch_expert_ffn.
 size_t expert_ffn_ws_bytes(int E, int D, int I, int rows_max, int act_bits);
 

@@ -898,6 +898,24 @@ static Schedule carve_one(char*& b, int E, int rows_max, int mc) {
   return s;
 }
 
+size_t row_chunk_bytes(int E, int rows_max, int mc) { return schedule_bytes_one(E, rows_max, mc); }
+
+static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
+                           const Schedule& sc, int* status, cudaStream_t s,
+                           int rule = kAllShapes);
+
+int launch_row_chunks(const int32_t* offsets, int E, int rows_max, int mc, void* ws,
+                      RowChunks* rc_out, int* status, cudaStream_t s) {
+  char* b = static_cast<char*>(ws);
+  const Schedule sc = carve_one(b, E, rows_max, mc);
+  rc_out->chunk_e = sc.chunk_e;
+  rc_out->chunk_row0 = sc.chunk_row0;
+  rc_out->chunk_rows = sc.chunk_rows;
+  rc_out->n_chunks = sc.n_chunks;
+  rc_out->max_chunks = sc.max_chunks;
+  return launch_schedule(offsets, E, rows_max, mc, 1, rows_max, sc, status, s, kAllShapes);
+}
+
 // Stream-kernel list plus tensor-core list.
 static size_t schedule_bytes(int E, int rows_max) {
   return schedule_bytes_one(E, rows_max, kFsMc) + schedule_bytes_one(E, rows_max, kTcChunkRows);
@@ -905,7 +923,7 @@ static size_t schedule_bytes(int E, int rows_max) {
 
 static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
                            const Schedule& sc, int* status, cudaStream_t s,
-                           int rule = kAllShapes) {
+                           int rule) {
   ffn_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, mc, lo, hi, rule, sc.max_chunks,
                                          sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.done,
                                          sc.n_chunks, status);

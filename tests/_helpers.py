@@ -101,6 +101,46 @@ def fp32_group_chain(P, scale_bits, x_scale) -> np.ndarray:
     return (acc * np.asarray(x_scale, dtype=np.float32)[:, None]).astype(np.float32)
 
 
+def _round_f32(x) -> float:
+    """The float32 nearest to the exact rational x (ties to even), as a float."""
+    from fractions import Fraction
+    x = Fraction(x)
+    if x == 0:
+        return 0.0
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                       # subnormal spacing below 2^-126
+    step = Fraction(2) ** (e - 23)
+    m = a / step
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return float(sign * n * step)
+
+
+def fp32_fma_chain(P, scale_bits, x_scale) -> np.ndarray:
+    """acc = fma(scale[n, g], P[r, n, g], acc) over g in K order from 0, then
+    y = x_scale[r] * acc, each fma and the product rounded once to fp32 (IEEE,
+    ties to even), evaluated with exact rationals: for partials whose
+    products with the scale are not exact in fp32 (the int16 reading)."""
+    from fractions import Fraction
+    P = np.asarray(P)
+    s = O.bf16_bits_to_f64(scale_bits)
+    R, N, G = P.shape
+    out = np.empty((R, N), dtype=np.float32)
+    for r in range(R):
+        for n in range(N):
+            acc = 0.0
+            for g in range(G):
+                acc = _round_f32(Fraction(float(s[n, g])) * int(P[r, n, g]) + Fraction(acc))
+            out[r, n] = _round_f32(Fraction(float(np.float32(x_scale[r]))) * Fraction(acc))
+    return out
+
+
 def _expert_rows(job):
     """Worker: one expert's gated MLP on its rows (oracle, fp64)."""
     w, e, u, act_bits = job

@@ -11,8 +11,8 @@ import torch
 import oracle as O
 import workloads as wl
 from oracle import inputs as oi
-from tests._helpers import (assert_close, bf16_bits, conditioned_attempts, fp32_group_chain,
-                            random_topk, rel_l2)
+from tests._helpers import (assert_close, bf16_bits, conditioned_attempts, fp32_fma_chain,
+                            fp32_group_chain, random_topk, rel_l2)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -305,6 +305,79 @@ def test_quantize_int4_reports_nonfinite_weights(moe):
     assert s[2, 1] == 0 and s[3, 0] == 0
     # the next call is clean
     moe.quantize_int4(torch.ones(2, 32, dtype=torch.bfloat16, device=DEV))
+    assert moe.check_error() == 0
+
+
+# ------------------------------------------------ int16 reading of act_bits 16
+
+def test_quantize_rows_int16_bit_exact(moe):
+    """Codes and scales equal the oracle's bit for bit (float32 steps on both
+    sides): random magnitudes, a zero row, half steps at scale 1 and the row
+    that separates float32 from float64 quantisation."""
+    rng = np.random.default_rng(16)
+    v = (rng.normal(size=(40, 320)) * rng.uniform(1e-3, 1e3, size=(40, 1))).astype(np.float32)
+    v[3] = 0.0
+    v[5, :6] = [32767.0, 0.5, 1.5, 2.5, -2.5, -100.5]
+    v[5, 6:] = 0.0
+    a = np.float32(1.925695538520813)
+    v[7] = 0.0
+    v[7, :3] = [a, a / np.float32(2), -a / np.float32(2)]
+    vb = _bf16(v)
+    q, s = moe.quantize_rows_int16(vb.to(DEV))
+    assert moe.check_error() == 0
+    rq, rs = O.quantize_rows_int16(vb.float().numpy())
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("K,N,counts", [
+    (320, 300, [0, 1, 33, 70, 8]),
+    (7168, 136, [5, 17, 40, 130, 0]),
+    (8160, 64, [3, 16]),                # the largest K with an exact int32 whole-K sum
+])
+def test_int4_linear_int16_partials_and_output(moe, K, N, counts):
+    """The int16 reading: every group partial equals the oracle's exact integer
+    (codes from the oracle's own int16 quantiser), the output matches the
+    oracle's fp64 result, and sampled outputs equal the fp32 fma chain the
+    header states, evaluated with exact rationals."""
+    rng = np.random.default_rng(K + N)
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    packed, scale = _random_int4(rng, E, N, K, 0.005, 0.02)
+    x = _bf16(rng.normal(size=(R, K)) * rng.uniform(0.1, 10, size=(R, 1)))
+    out, part = moe.int4_linear_int16(x.to(DEV), _t(off), _t(packed), _t(scale, torch.bfloat16),
+                                      partials=True)
+    assert moe.check_error() == 0
+    out, part = out.cpu().numpy(), part.cpu().numpy()
+    q16, sx = O.quantize_rows_int16(x.float().numpy())
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        P = O.int16_group_partials(q16[a:b], packed[e])
+        assert np.array_equal(part[a:b], P), e
+        ref = O.int4_linear_int16(oi.x_f64(x)[a:b], packed[e], scale[e])
+        assert rel_l2(out[a:b], ref) <= 2e-6, e
+        rows = [a, b - 1]
+        cols = [0, N // 2, N - 1]
+        chain = fp32_fma_chain(P[[r - a for r in rows]][:, cols], scale[e][cols], sx[rows])
+        assert np.array_equal(out[np.ix_(rows, cols)], chain), e
+
+
+def test_int4_linear_int16_rejections(moe):
+    x = torch.zeros(4, 96, dtype=torch.bfloat16, device=DEV)
+    off = _t(np.array([0, 4], np.int32))
+    w = torch.zeros(1, 8, 96 // 8, dtype=torch.int32, device=DEV)
+    sc = torch.zeros(1, 8, 3, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(moe.MoeError):
+        moe.int4_linear_int16(torch.zeros(4, 8192, dtype=torch.bfloat16, device=DEV), off,
+                              torch.zeros(1, 8, 1024, dtype=torch.int32, device=DEV),
+                              torch.zeros(1, 8, 256, dtype=torch.bfloat16, device=DEV))
+    bad = _t(np.array([0, 9], np.int32))      # offsets beyond the rows
+    moe.int4_linear_int16(x, bad, w, sc)
+    assert moe.check_error() == moe.capi.MOE_ERR_INVALID
+    moe.int4_linear_int16(x, off, w, sc)
     assert moe.check_error() == 0
 
 
