@@ -1179,6 +1179,7 @@ extern "C" int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale,
                                     const int32_t* down_packed, const uint16_t* down_scale,
                                     int act_bits, uint16_t* y_sorted, void* ws, size_t ws_bytes,
                                     void* stream) {
+  moe::Range range_("moe_expert_ffn_pairs");
   const int rc = check_ffn_args(x_pairs, x_scale, offsets, E, D, I, rows_max, gate_packed,
                                 gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
                                 y_sorted, ws);
@@ -1203,6 +1204,7 @@ extern "C" int moe_expert_ffn(const void* x_sorted, const float* x_scale, const 
                               const uint16_t* up_scale, const int32_t* down_packed,
                               const uint16_t* down_scale, int act_bits, uint16_t* y_sorted,
                               void* ws, size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_expert_ffn");
   const int rc0 = check_ffn_args(x_sorted, x_scale, offsets, E, D, I, rows_max, gate_packed,
                                  gate_scale, up_packed, up_scale, down_packed, down_scale,
                                  act_bits, y_sorted, ws);
@@ -1232,6 +1234,7 @@ extern "C" int moe_int4_linear_partials(const int8_t* x, const float* x_scale,
                                         const int32_t* w_packed, const uint16_t* w_scale,
                                         int kernel, float* out, int32_t* partials, void* ws,
                                         size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_int4_linear_partials");
   if (E <= 0 || rows_max < 0 || N <= 0) return MOE_ERR_INVALID;
   if (kernel != 0 && kernel != 1) return MOE_ERR_INVALID;
   if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
@@ -1290,6 +1293,7 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
                                               const uint16_t* w_scale, int act_bits, int kernel,
                                               int stall_stage, int64_t limit_ns, float* out,
                                               void* ws, size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_int4_linear_stall_selftest");
   if (E <= 0 || rows_max <= 0 || N <= 0 || stall_stage < 0) return MOE_ERR_INVALID;
   if (kernel != 0 && kernel != 1) return MOE_ERR_INVALID;
   if (limit_ns < 1000 || limit_ns > 5000000000LL) return MOE_ERR_INVALID;
@@ -1359,6 +1363,7 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
                                int K, int N, int rows_max, const int32_t* w_packed,
                                const uint16_t* w_scale, int act_bits, float* out, void* ws,
                                size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_int4_linear");
   if (E <= 0 || rows_max < 0 || N <= 0) return MOE_ERR_INVALID;
   if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
