@@ -69,7 +69,8 @@ def expert_bytes(w: wl.Workload) -> int:
 
 def _source_hash() -> str:
     h = hashlib.sha1()
-    for name in ("ffn_stream.cu", "ffn_tc.cu", "ffn_tc_q8.cu", "ffn_tc.cuh"):
+    for name in ("ffn_stream.cu", "ffn_tc.cu", "ffn_tc2.cu", "ffn_tc_q8.cu", "ffn_tc.cuh",
+                 "int4_f16.cuh"):
         with open(os.path.join(ROOT, "int4_routed_expert_fp32_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]

@@ -264,7 +264,9 @@ size_t moe_int4_linear_workspace_size(int E, int K, int rows_max);
  *   w_packed  int32 [E, N, K/8]; w_scale bf16 [E, N, K/32]
  *   out       fp32 [rows_max, N], 16-byte aligned
  * When an expert has at least 48 rows and K % 64 == 0, every expert runs on
- * the tensor-core kernel, otherwise every expert on the stream kernel (the
+ * the tensor-core kernels (with act_bits 16 the large experts on the
+ * CTA-pair kernel, see moe_set_tc_pair), otherwise every expert on the
+ * stream kernel (the
  * choice is taken on the device from the offsets).  With
  * act_bits 8 both kernels form the exact integer partial P_g of every
  * 32-column weight group and give the same bits: y = x_scale * acc, acc the
@@ -446,7 +448,9 @@ int moe_wait_selftest(int64_t limit_ns, void* stream);
  * moe_int4_linear (same arguments, workspace of
  * moe_int4_linear_workspace_size) on the kernel `kernel` names -- 0: the
  * stream kernel (chunks of <= 16 rows), 1: the tensor-core kernel (the
- * act_bits 16 one, or the exact one for act_bits 8; chunks of <= 128 rows)
+ * act_bits 16 one, or the exact one for act_bits 8; chunks of <= 128 rows),
+ * 2: the CTA-pair tensor-core kernel (act_bits 16 only, chunks of <= 256
+ * rows; MOE_ERR_UNSUPPORTED where no cluster of two fits)
  * -- in a build of it whose producer stops before its copy stage
  * `stall_stage` (counted per CTA from 0), as if those copies never arrived,
  * with every bounded wait limited to `limit_ns` (1e3 .. 5e9).  The other
@@ -459,6 +463,21 @@ int moe_int4_linear_stall_selftest(const void* x, const float* x_scale, const in
                                    const uint16_t* w_scale, int act_bits, int kernel,
                                    int stall_stage, int64_t limit_ns, float* out, void* ws,
                                    size_t ws_bytes, void* stream);
+
+/* Which tensor-core kernels run the act_bits 16 expert GEMMs of
+ * moe_expert_ffn, moe_layer_forward and moe_int4_linear for prefill-shaped
+ * batches.  enable != 0 (the default), where a cluster of two CTAs fits on
+ * the device: the experts with at least 129 rows run on the CTA-pair kernels
+ * -- clusters of two CTAs whose MMAs (tcgen05 cta_group::2) take 256 weight
+ * rows over two SMs, on chunks of up to 256 token rows -- and the others on
+ * the one-CTA kernels (128 weight rows per MMA, chunks of up to 128 rows);
+ * the pair kernels are launched only when the batch's mean expert load
+ * rows_max / E is at least 64 rows.  enable == 0: every expert on the one-CTA
+ * kernels.  Both kernels take the same K steps of 16 columns for every output
+ * and give the same bits (a GPU test checks it).  Process-wide, host only;
+ * returns the previous setting.  For tests and measurements that compare the
+ * two. */
+int moe_set_tc_pair(int enable);
 
 /* Human-readable name of a status code. */
 const char* moe_status_string(int status);

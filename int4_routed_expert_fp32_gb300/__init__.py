@@ -12,7 +12,7 @@ _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "c
             "int4_linear_stall_selftest", "int4_linear_int16", "quantize_rows_int16",
             "last_cuda_error", "launch_count",
             "lib", "linear_bf16", "quantize_int4", "quantize_int8",
-            "quantize_rows", "shared_expert",
+            "quantize_rows", "set_tc_pair", "shared_expert",
             "rmsnorm", "route", "status_string", "wait_selftest", "capi")
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
-SOURCES = ["common.cu", "router.cu", "dispatch.cu", "ffn_stream.cu", "ffn_tc.cu", "ffn_tc_q8.cu", "combine.cu",
+SOURCES = ["common.cu", "router.cu", "dispatch.cu", "ffn_stream.cu", "ffn_tc.cu", "ffn_tc2.cu", "ffn_tc_q8.cu", "combine.cu",
            "gemm_bf16.cu", "layer.cu", "weights.cu", "shared.cu", "linear_i16.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -110,6 +110,7 @@ SIGNATURES = {
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_version": (ctypes.c_char_p, []),
     "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_set_tc_pair": (c_int, [c_int]),
 }
 
 
@@ -140,6 +141,12 @@ def last_cuda_error() -> str:
 def launch_count() -> int:
     """Kernels the library has launched in this process so far."""
     return int(lib.moe_launch_count())
+
+
+def set_tc_pair(enable: bool) -> bool:
+    """Run the act_bits 16 tensor-core GEMMs on CTA pairs (True, the default)
+    or on the one-CTA kernels (False); returns the previous setting."""
+    return bool(lib.moe_set_tc_pair(1 if enable else 0))
 
 
 def _check(name: str, rc: int) -> None:

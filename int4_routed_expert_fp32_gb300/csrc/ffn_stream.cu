@@ -775,6 +775,28 @@ constexpr int kTcMinRows = 1;
 constexpr int kTcMinBatchRows = 48;
 enum ScheduleRule { kAllShapes = 0, kDecodeShaped = 1, kPrefillShaped = 2 };
 
+// Tensor-core kernels of act_bits 16: 1 = the CTA-pair kernels (ffn_tc2.cu)
+// where a cluster of two fits, 0 = the one-CTA kernels (ffn_tc.cu).  Set by
+// moe_set_tc_pair (tests and measurements compare the two).
+static int g_tc_pair = 1;
+
+static bool use_tc_pair(bool q8) { return !q8 && g_tc_pair != 0 && tc_pair_available(); }
+
+// With the CTA-pair kernels, the experts of a prefill-shaped batch with at
+// least this many rows run on them (chunks of up to 256 rows); the others stay
+// on the one-CTA kernels (chunks of up to 128 rows), which lose less to a
+// part-filled token tile.
+constexpr int kTcPairMinRows = 129;
+// The CTA-pair launches (a schedule and two kernels, ~8 us each when they find
+// no expert) are made only for batches whose mean expert load rows_max / E
+// reaches this many rows, where experts of kTcPairMinRows rows are expected.
+constexpr int kTcPairMinMeanRows = 64;
+
+static bool pair_batch(int rows_max, int E, int max_rows_per_expert) {
+  return max_rows_per_expert >= kTcPairMinRows &&
+         static_cast<long long>(rows_max) >= static_cast<long long>(kTcPairMinMeanRows) * E;
+}
+
 // Chunk list of the expert-sorted rows: the rows of every expert whose row
 // count lies in [lo, hi] cut into chunks of at most mc rows, for a batch of
 // the shape `rule` names (no chunk otherwise).  One CTA of 1024 threads.
@@ -916,9 +938,11 @@ int launch_row_chunks(const int32_t* offsets, int E, int rows_max, int mc, void*
   return launch_schedule(offsets, E, rows_max, mc, 1, rows_max, sc, status, s, kAllShapes);
 }
 
-// Stream-kernel list plus tensor-core list.
+// Stream-kernel list plus the two tensor-core lists (one-CTA and CTA-pair
+// kernels).
 static size_t schedule_bytes(int E, int rows_max) {
-  return schedule_bytes_one(E, rows_max, kFsMc) + schedule_bytes_one(E, rows_max, kTcChunkRows);
+  return schedule_bytes_one(E, rows_max, kFsMc) + schedule_bytes_one(E, rows_max, kTcChunkRows) +
+         schedule_bytes_one(E, rows_max, kTcPairChunkRows);
 }
 
 static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
@@ -1034,6 +1058,7 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   char* b = static_cast<char*>(ws);
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
+  Schedule big2 = carve_one(b, E, rows_max, kTcPairChunkRows);
   uint16_t* h = reinterpret_cast<uint16_t*>(b);
   b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   int8_t* hq = nullptr;
@@ -1055,12 +1080,19 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   // batch's actual shape
   const bool use_tc = tc_path_supported(D) && tc_path_supported(I) &&
                       max_rows_per_expert >= kTcMinBatchRows;
+  // experts of kTcPairMinRows rows or more on the CTA pairs (act_bits 16)
+  const bool pair = use_tc && use_tc_pair(q8) && pair_batch(rows_max, E, max_rows_per_expert);
   int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
                            use_tc ? kDecodeShaped : kAllShapes);
   if (rc) return rc;
   if (use_tc) {
-    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s,
-                         kPrefillShaped);
+    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows,
+                         pair ? kTcPairMinRows - 1 : rows_max, big, status, s, kPrefillShaped);
+    if (rc) return rc;
+  }
+  if (pair) {
+    rc = launch_schedule(offsets, E, rows_max, kTcPairChunkRows, kTcPairMinRows, rows_max, big2,
+                         status, s, kPrefillShaped);
     if (rc) return rc;
   }
 
@@ -1119,6 +1151,12 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
                                h, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks,
                                status, s);
     if (rc) return rc;
+    if (pair) {
+      rc = launch_tc_pair_gateup(xa, rows_max, E, D, I, gate_packed, gate_scale, up_packed,
+                                 up_scale, h, big2.chunk_e, big2.chunk_row0, big2.chunk_rows,
+                                 big2.n_chunks, status, s);
+      if (rc) return rc;
+    }
   }
 
   if (q8) {
@@ -1141,6 +1179,12 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
             : launch_tc_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
                              big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
     if (rc) return rc;
+    if (pair) {
+      rc = launch_tc_pair_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
+                               big2.chunk_e, big2.chunk_row0, big2.chunk_rows, big2.n_chunks,
+                               status, s);
+      if (rc) return rc;
+    }
   }
   return MOE_OK;
 }
@@ -1295,7 +1339,8 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
                                               void* ws, size_t ws_bytes, void* stream) {
   moe::Range range_("moe_int4_linear_stall_selftest");
   if (E <= 0 || rows_max <= 0 || N <= 0 || stall_stage < 0) return MOE_ERR_INVALID;
-  if (kernel != 0 && kernel != 1) return MOE_ERR_INVALID;
+  if (kernel < 0 || kernel > 2) return MOE_ERR_INVALID;
+  if (kernel == 2 && (act_bits != 16 || !tc_pair_available())) return MOE_ERR_UNSUPPORTED;
   if (limit_ns < 1000 || limit_ns > 5000000000LL) return MOE_ERR_INVALID;
   if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
@@ -1309,7 +1354,7 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool q8 = act_bits == 8;
-  const int mc = kernel == 0 ? kFsMc : kTcChunkRows;
+  const int mc = kernel == 0 ? kFsMc : kernel == 1 ? kTcChunkRows : kTcPairChunkRows;
   char* b = static_cast<char*>(ws);
   Schedule sc = carve_one(b, E, rows_max, mc);
   b = static_cast<char*>(ws) + schedule_bytes(E, rows_max);
@@ -1342,6 +1387,10 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
               : launch_stream<kLinear, false, false, true>(m, p, s);
   }
   const uint16_t* xa = static_cast<const uint16_t*>(xp);
+  if (kernel == 2)
+    return launch_tc_pair_linear_stalled(xa, rows_max, E, N, K, w_packed, w_scale, out,
+                                         sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks,
+                                         status, limit_ns, stall_stage, s);
   if (q8) {
     rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
     if (rc) return rc;
@@ -1381,10 +1430,12 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   char* b = static_cast<char*>(ws);
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
+  Schedule big2 = carve_one(b, E, rows_max, kTcPairChunkRows);
   void* xp = b;
   b += align_up((size_t)rows_max * K * sizeof(uint16_t), 256);
   uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
   const bool use_tc = tc_path_supported(K) && rows_max >= kTcMinBatchRows;
+  const bool pair = use_tc && use_tc_pair(q8) && pair_batch(rows_max, E, rows_max);
   int rc = launch_to_pair_rows(x, q8, rows_max, K, offsets + E, xp, status, s);
   if (rc) return rc;
   rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
@@ -1408,9 +1459,14 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
   rc = run_stream(kLinear, q8, m, p, s);
   if (rc || !use_tc) return rc;
-  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows, rows_max, big, status, s,
-                       kPrefillShaped);
+  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows,
+                       pair ? kTcPairMinRows - 1 : rows_max, big, status, s, kPrefillShaped);
   if (rc) return rc;
+  if (pair) {
+    rc = launch_schedule(offsets, E, rows_max, kTcPairChunkRows, kTcPairMinRows, rows_max, big2,
+                         status, s, kPrefillShaped);
+    if (rc) return rc;
+  }
   const uint16_t* xa = static_cast<const uint16_t*>(xp);
   if (q8) {
     rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
@@ -1421,6 +1477,15 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
     return launch_tc_q8_down(xa, x_scale, rows_max, E, N, K, w_packed, w_scale, out, true,
                              big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s,
                              nullptr);
-  return launch_tc_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big.chunk_e,
-                        big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+  rc = launch_tc_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big.chunk_e,
+                      big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
+  if (rc || !pair) return rc;
+  return launch_tc_pair_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big2.chunk_e,
+                             big2.chunk_row0, big2.chunk_rows, big2.n_chunks, status, s);
+}
+
+extern "C" int moe_set_tc_pair(int enable) {
+  const int prev = g_tc_pair;
+  g_tc_pair = enable ? 1 : 0;
+  return prev;
 }

@@ -34,6 +34,9 @@ struct TxMaps {
 // Rows per token tile of the tensor-core path (chunks of that many rows).
 constexpr int kTcChunkRows = 128;
 
+// Rows per token tile of the CTA-pair kernels (ffn_tc2.cu).
+constexpr int kTcPairChunkRows = 256;
+
 // K of the tensor-core path must be a multiple of 64.
 bool tc_path_supported(int K);
 
@@ -90,5 +93,28 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
                    const int32_t* n_chunks, int* status, cudaStream_t s);
+
+// The same two GEMMs (act_bits 16) on CTA pairs (ffn_tc2.cu): chunks of at
+// most kTcPairChunkRows rows, MMAs of 256 weight rows over two SMs.
+// Returns MOE_ERR_UNSUPPORTED when no cluster of two fits on the device.
+bool tc_pair_available();
+// Tests only: launch_tc_linear_stalled's act_bits 16 linear on the CTA-pair
+// kernel.
+int launch_tc_pair_linear_stalled(const uint16_t* x16, int rows_max, int E, int N, int K,
+                                  const int32_t* w_packed, const uint16_t* w_scale, float* y,
+                                  const int32_t* chunk_e, const int32_t* chunk_row0,
+                                  const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                                  long long wait_ns, int stall_at, cudaStream_t s);
+int launch_tc_pair_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
+                          const int32_t* gate_packed, const uint16_t* gate_scale,
+                          const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
+                          const int32_t* chunk_e, const int32_t* chunk_row0,
+                          const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                          cudaStream_t s);
+int launch_tc_pair_down(const uint16_t* h16, int rows_max, int E, int D, int I,
+                        const int32_t* down_packed, const uint16_t* down_scale, void* y,
+                        bool y_f32, const int32_t* chunk_e, const int32_t* chunk_row0,
+                        const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
+                        cudaStream_t s);
 
 }  // namespace moe

@@ -248,6 +248,21 @@ def _t(a, dtype=None):
     return t.to(DEV)
 
 
+class _tc_kernels:
+    """Within the block, run the act_bits 16 tensor-core GEMMs on the
+    CTA-pair kernels (pair=True, the default) or the one-CTA kernels."""
+
+    def __init__(self, moe, pair: bool):
+        self.moe, self.pair = moe, pair
+
+    def __enter__(self):
+        self.prev = self.moe.set_tc_pair(self.pair)
+
+    def __exit__(self, *exc):
+        self.moe.set_tc_pair(self.prev)
+
+
+
 # ------------------------------------------------------------ int4 weight quantiser
 
 @pytest.mark.parametrize("shape", [(3, 40, 96), (1, 7, 32), (2, 513, 7168)])
@@ -417,19 +432,24 @@ def test_quantize_int8_reports_nonfinite_weights(moe):
     assert moe.check_error() == 0
 
 
+@pytest.mark.parametrize("pair", [True, False])
 @pytest.mark.parametrize("K,N,counts", [
     (320, 300, [0, 1, 33, 70, 8]),        # ragged K tail, ragged N tile, multi-chunk experts
     (2048, 512, [5, 0, 0, 64, 2]),
     (128, 64, [3, 3]),                    # K below one stage, N below one tile
+    (256, 320, [256, 257, 31, 32, 33, 0, 300]),  # 256-row chunks and their ragged tails
 ])
-def test_int4_linear_w4a16(moe, K, N, counts):
+def test_int4_linear_w4a16(moe, K, N, counts, pair):
+    """Both tensor-core kernels (CTA pairs and one CTA) on prefill-shaped
+    batches (the stream kernel on the others)."""
     rng = np.random.default_rng(K + N)
     E = len(counts)
     off = _segments(counts)
     R = int(off[-1])
     packed, scale = _random_int4(rng, E, N, K)
     x = _bf16(rng.normal(size=(R, K)))
-    got = moe.int4_linear(x.to(DEV), None, _t(off), _t(packed), _t(scale, torch.bfloat16), 16)
+    with _tc_kernels(moe, pair):
+        got = moe.int4_linear(x.to(DEV), None, _t(off), _t(packed), _t(scale, torch.bfloat16), 16)
     assert moe.check_error() == 0
     got = got.cpu().numpy()
     xf = oi.x_f64(x)
@@ -631,7 +651,7 @@ def test_int4_linear_exact_group_partials(moe, kernel):
 
 # ------------------------------------------------------------- expert FFN
 
-@pytest.mark.parametrize("act_bits", [16, 8])
+@pytest.mark.parametrize("act_bits,pair", [(16, True), (16, False), (8, True)])
 @pytest.mark.parametrize("D,I,counts", [
     # decode-shaped batches (no expert holds 48 rows): the stream kernel
     (320, 192, [0, 3, 20, 1, 0, 9]),
@@ -646,8 +666,12 @@ def test_int4_linear_exact_group_partials(moe, kernel):
     (256, 192, [400, 3, 0, 193]),        # several 128-row chunks per expert, ragged last chunks
     (320, 192, [48, 3, 64, 17, 33, 0]),  # partial 128-row tiles
     (256, 128, [70, 40, 40, 40, 40, 40, 40, 40]),
+    (256, 192, [256, 257, 31, 32, 33, 100, 511, 0]),  # 256-row chunks (CTA pairs), ragged tails
+    (320, 192, [300, 48, 200]),          # a down tile of 256 outputs and a ragged one of 64
 ])
-def test_expert_ffn_parity(moe, act_bits, D, I, counts):
+def test_expert_ffn_parity(moe, act_bits, pair, D, I, counts):
+    """act_bits 16 on both tensor-core kernels (CTA pairs, one CTA), act_bits 8
+    on its own; the decode-shaped cases run the stream kernel either way."""
     rng = np.random.default_rng(D + I + act_bits)
     E = len(counts)
     off = _segments(counts)
@@ -664,7 +688,8 @@ def test_expert_ffn_parity(moe, act_bits, D, I, counts):
     else:
         q, s = O.quantize_rows_int8(x.float().numpy())
         xin, xs = _t(q), _t(s)
-    y = moe.expert_ffn(xin, xs, _t(off), ex, act_bits)
+    with _tc_kernels(moe, pair):
+        y = moe.expert_ffn(xin, xs, _t(off), ex, act_bits)
     assert moe.check_error() == 0
     y = y.float().cpu().numpy()
     xf = oi.x_f64(x)
@@ -701,6 +726,31 @@ def test_expert_ffn_pairs_equals_expert_ffn(moe, act_bits):
     y1 = moe.expert_ffn(prs["x_sorted"], prs["x_scale"], prs["offsets"], ex, act_bits, pairs=True)
     assert moe.check_error() == 0
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+def test_tc_pair_and_one_cta_kernels_agree(moe):
+    """The CTA-pair and one-CTA tensor-core kernels take the same K steps of
+    16 columns for every output, so y and h agree bit for bit, whichever
+    tokens share an MMA (a prefill-shaped batch with chunks of 1 to 300 rows)."""
+    rng = np.random.default_rng(53)
+    D, I = 512, 384
+    counts = [300, 1, 17, 64, 129, 0, 256, 48]
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    x = _bf16(rng.normal(size=(R, D))).to(DEV)
+    ys = []
+    for pair in (True, False):
+        with _tc_kernels(moe, pair):
+            ys.append(moe.expert_ffn(x, None, _t(off), ex, 16))
+    assert moe.check_error() == 0
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
 
 
 @pytest.mark.parametrize("counts", [[5, 30], [5, 60]])
@@ -841,13 +891,13 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     assert moe.check_error() == 0
 
 
-@pytest.mark.parametrize("act_bits", [16, 8])
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("act_bits,kernel", [(16, 0), (8, 0), (16, 1), (8, 1), (16, 2)])
 def test_pipelined_kernel_exit_paths(moe, kernel, act_bits):
     """A producer that stops before its fourth copy stage (a test build of the
-    stream and tensor-core kernels): the other roles' bounded waits (20 ms)
-    run out, the kernel records MOE_ERR_TIMEOUT, drains its copies and MMAs,
-    frees its tensor memory and returns; the next call is correct and clean."""
+    stream, tensor-core and CTA-pair kernels): the other roles' bounded waits
+    (20 ms) run out, the kernel records MOE_ERR_TIMEOUT, drains its copies and
+    MMAs, frees its tensor memory and returns (a CTA pair after both CTAs'
+    roles have stopped); the next call is correct and clean."""
     rng = np.random.default_rng(77 + kernel + act_bits)
     K, N, counts = 2048, 512, [20, 40]
     E = len(counts)
