@@ -124,9 +124,10 @@ def roofline(w: wl.Workload, ffn_ms: float, active: int, peaks: dict) -> dict:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     roof.update({"traffic": None,
-                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedule; ffn_tc_kernel gate/up "
-                           "and down for prefill-shaped batches, ffn_stream_fused_kernel (gate/up + "
-                           "down) for decode-shaped ones)",
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; for prefill-shaped "
+                           "batches ffn_tc_pair_kernel (CTA pairs, experts of >= 129 rows) and "
+                           "ffn_tc_kernel (the others), or ffn_tc_q8_kernel (act_bits 8), gate/up "
+                           "and down; for decode-shaped ones ffn_stream_fused_kernel)",
                  "kernel_ms": ffn_ms,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                  "active_experts": active, "peak_source": peaks["source"]})
