@@ -23,10 +23,12 @@ constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: 
 
 template <int BN>
 struct TcTile {
-  static constexpr int kBBytes = BN * kTcBK * 2;             // 32 KiB (BN 256) / 16 KiB (128)
+  static constexpr int kBBytes = BN * kTcBK * 2;             // 32 KiB (BN 256) .. 16 KiB (128)
   static constexpr int kStageBytes = kTcABytes + kBBytes;
   static constexpr int kSmem = kTcStages * kStageBytes + 1024 + 256;
-  static constexpr uint32_t kCols = 2 * BN;                  // two TMEM accumulators
+  // two TMEM accumulators of BN columns, in an allocation of a power of two
+  static constexpr uint32_t kCols = 2 * BN <= 256 ? 256u : 512u;
+  static_assert(BN % 32 == 0 && 2 * BN <= 512, "accumulator columns");
 };
 
 // Persistent: CTA c takes the tiles t = c, c + gridDim.x, ...; tile t is
@@ -283,7 +285,10 @@ int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int
 int launch_linear_tc_f32_terms(const uint16_t* x, const uint16_t* w, int terms, int M, int N, int K,
                                int kc, float* y, cudaStream_t s) {
   const int splits = (K + kc - 1) / kc;
-  // 128-column tiles: a router of 384 experts fills three of them exactly
+  // 192-column tiles when they divide N (a router of 384 experts: two tiles):
+  // an M = 128, N = 192 MMA reads 10 KiB of shared memory per 96 cycles,
+  // where N = 128 reads 8 KiB per 64 cycles, the whole shared-memory bandwidth
+  if (N % 192 == 0) return launch_tc_gemm<true, 192>(x, w, M, N, K, kc, splits * N, terms, y, s);
   return launch_tc_gemm<true, 128>(x, w, M, N, K, kc, splits * N, terms, y, s);
 }
 
