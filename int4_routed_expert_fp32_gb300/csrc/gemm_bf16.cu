@@ -271,9 +271,24 @@ static int launch_tc_gemm(const uint16_t* x, const uint16_t* w, int M, int N, in
   return MOE_OK;
 }
 
+// Tile width of a bf16 GEMM: 256 columns, or 192 when the last wave of
+// 256-column tiles would leave more SMs idle (a 2048 x 3584 output: 224 tiles
+// of 128 x 256 take two waves of 152 SMs, 304 tiles of 128 x 192 fill two
+// exactly); a 192-column tile is taken as 5% slower per column.
+static int gemm_tile_n(int M, int N) {
+  const long sms = num_sms(), tm = (M + kTcBM - 1) / kTcBM;
+  auto cost = [&](int bn) {
+    const long tiles = tm * ((N + bn - 1) / bn);
+    return static_cast<double>((tiles + sms - 1) / sms) * bn * (bn == 192 ? 1.05 : 1.0);
+  };
+  return cost(192) < cost(256) ? 192 : 256;
+}
+
 int launch_linear_tc(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                      cudaStream_t s) {
-  return launch_tc_gemm<false>(x, w, M, N, K, (K + kTcBK - 1) / kTcBK * kTcBK, N, 1, y, s);
+  const int kc = (K + kTcBK - 1) / kTcBK * kTcBK;
+  if (gemm_tile_n(M, N) == 192) return launch_tc_gemm<false, 192>(x, w, M, N, K, kc, N, 1, y, s);
+  return launch_tc_gemm<false>(x, w, M, N, K, kc, N, 1, y, s);
 }
 
 int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int N, int K, int kc,
