@@ -109,6 +109,8 @@ typedef struct moe_weights {
   const uint16_t* shared_gate; /* bf16 [I_shared, H]  (shared expert only) */
   const uint16_t* shared_up;   /* bf16 [I_shared, H] */
   const uint16_t* shared_down; /* bf16 [H, I_shared] */
+  const uint16_t* router_w_terms; /* optional bf16 [3, E, H] from moe_router_prepare (used
+                                     from T = 512 on), or NULL: split router_w on every call */
 } moe_weights;
 
 /* ---------------------------------------------------------------- router -- */
@@ -127,6 +129,16 @@ size_t moe_route_workspace_size(int T, int H, int E);
 int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
               int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
               size_t ws_bytes, void* stream);
+
+/* One-time preparation of the router weight for calls of 512 tokens or more,
+ * whose logits run on the tensor cores: w_terms (bf16 [3, E, H], 16-byte
+ * aligned, caller-owned) receives three bf16 terms with
+ * w_router = w_terms[0] + w_terms[1] + w_terms[2] (each term the bf16
+ * rounding of what the previous ones leave), exactly for every weight w with
+ * 2^-110 <= |w| < 3.38e38 and for zero (smaller weights leave remainders in
+ * fp32's subnormal range); x times each term is exact in fp32.  Give it to moe_layer_forward in moe_weights.router_w_terms
+ * (the same split is otherwise redone on every call).  Stream-ordered. */
+int moe_router_prepare(const float* w_router, int E, int H, uint16_t* w_terms, void* stream);
 
 /* -------------------------------------------------------------- dispatch -- */
 

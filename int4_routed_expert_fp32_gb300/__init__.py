@@ -13,7 +13,7 @@ _BINDING = ("MoeConfig", "MoeError", "MoeLayer", "MoeWeights", "check_error", "c
             "last_cuda_error", "launch_count",
             "lib", "linear_bf16", "quantize_int4", "quantize_int8",
             "quantize_rows", "set_tc_pair", "shared_expert",
-            "rmsnorm", "route", "status_string", "wait_selftest", "capi")
+            "rmsnorm", "route", "router_prepare", "status_string", "wait_selftest", "capi")
 
 
 def __getattr__(name):

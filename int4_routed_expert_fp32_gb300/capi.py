@@ -44,7 +44,7 @@ class MoeWeights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in (
         "router_w", "router_bias", "gate_packed", "gate_scale", "up_packed", "up_scale",
         "down_packed", "down_scale", "lat_down", "lat_norm", "lat_up", "shared_gate", "shared_up",
-        "shared_down")]
+        "shared_down", "router_w_terms")]
 
 
 # name -> (restype, argtypes); mirrors include/moe.h
@@ -111,6 +111,7 @@ SIGNATURES = {
     "moe_version": (ctypes.c_char_p, []),
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_set_tc_pair": (c_int, [c_int]),
+    "moe_router_prepare": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
 }
 
 
@@ -501,6 +502,16 @@ def wait_selftest(limit_ns: int) -> None:
     _check("moe_wait_selftest", lib.moe_wait_selftest(int(limit_ns), _stream()))
 
 
+def router_prepare(w_router: torch.Tensor) -> torch.Tensor:
+    """The three bf16 terms [3, E, H] of the fp32 router weight (their sum is
+    w_router exactly), for MoeLayer's tensor-core router."""
+    E, H = _arg("w_router", w_router, (None, None), torch.float32).shape
+    dev = _placed(w_router=w_router)
+    terms = torch.empty(3, E, H, dtype=torch.bfloat16, device=dev)
+    _check("moe_router_prepare", lib.moe_router_prepare(_p(w_router), E, H, _p(terms), _stream()))
+    return terms
+
+
 # ------------------------------------------------------------------ layer
 
 class MoeLayer:
@@ -508,11 +519,16 @@ class MoeLayer:
 
     def __init__(self, T: int, H: int, E: int, k: int, I: int, weights: Dict[str, torch.Tensor],
                  L: int = 0, act_bits: int = 16, renorm: bool = True, eps: float = 1e-6,
-                 I_shared: int = 0):
+                 I_shared: int = 0, prepare_router: bool = True):
+        """prepare_router: from T = 512 on, split the router weight into its
+        bf16 terms once here (moe_router_prepare) rather than on every call."""
         self.cfg = MoeConfig(T, H, E, k, I, L, act_bits, int(renorm), eps, I_shared)
-        self.weights = weights
         _check_layer_weights(weights, H, E, I, L, I_shared)
         self.device = _placed(**{n: t for n, t in weights.items() if t is not None})
+        weights = dict(weights)
+        if prepare_router and T >= 512 and weights.get("router_w_terms") is None:
+            weights["router_w_terms"] = router_prepare(weights["router_w"])
+        self.weights = weights
         self.wstruct = MoeWeights(*[_p(weights.get(n)) for n, _ in MoeWeights._fields_])
         self.ws = _ws(lib.moe_workspace_size(ctypes.byref(self.cfg)), self.device)
 
@@ -612,3 +628,5 @@ def _check_layer_weights(w: Dict[str, torch.Tensor], H: int, E: int, I: int, L: 
         _arg("shared_gate", w.get("shared_gate"), (I_shared, H), bf16)
         _arg("shared_up", w.get("shared_up"), (I_shared, H), bf16)
         _arg("shared_down", w.get("shared_down"), (H, I_shared), bf16)
+    if w.get("router_w_terms") is not None:
+        _arg("router_w_terms", w["router_w_terms"], (3, E, H), bf16)

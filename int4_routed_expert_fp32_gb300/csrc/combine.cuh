@@ -55,6 +55,13 @@ int launch_linear_tc_f32_splitk(const uint16_t* x, const uint16_t* w, int M, int
 int launch_linear_tc_f32_terms(const uint16_t* x, const uint16_t* w, int terms, int M, int N, int K,
                                int kc, float* y, cudaStream_t s);
 
+// moe_route with, from 512 tokens, the three bf16 terms of the router weight
+// (bf16 [3, E, H] from moe_router_prepare) read from w_terms instead of
+// split into the workspace on every call (w_terms NULL: split them now).
+int route_with_terms(const uint16_t* x, const float* w_router, const uint16_t* w_terms,
+                     const float* bias, int T, int H, int E, int k, int renorm, int32_t* topk_idx,
+                     float* topk_w, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // y[M, N] = x[M, K] w[N, K]^T in bf16 with fp32 accumulation.
 int launch_linear_bf16(const uint16_t* x, const uint16_t* w, int M, int N, int K, uint16_t* y,
                        cudaStream_t s);

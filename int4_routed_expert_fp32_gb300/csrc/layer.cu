@@ -109,8 +109,8 @@ static int routed(const moe_config& c, const moe_weights& w, const uint16_t* x, 
                   const LayerWs& ws, cudaStream_t s) {
   const int D = c.L > 0 ? c.L : c.H;
   const int R = c.T * c.k;
-  int rc = moe_route(x, w.router_w, w.router_bias, c.T, c.H, c.E, c.k, c.renorm, ws.topk_idx,
-                     ws.topk_w, ws.scratch, ws.scratch_bytes, s);
+  int rc = route_with_terms(x, w.router_w, w.router_w_terms, w.router_bias, c.T, c.H, c.E, c.k,
+                            c.renorm, ws.topk_idx, ws.topk_w, ws.scratch, ws.scratch_bytes, s);
   if (rc) return rc;
   const uint16_t* u = x;
   if (c.L > 0) {

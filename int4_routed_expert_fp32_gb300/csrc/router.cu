@@ -194,8 +194,10 @@ constexpr int kRtTcKSlice = 1024;
 static int router_tc_splits(int H) { return (H + kRtTcKSlice - 1) / kRtTcKSlice; }
 
 // W fp32 [E, H] -> three bf16 terms [3E, H] with W = W1 + W2 + W3 to the last
-// bit of the fp32 significand (each term is the rounded remainder of the
-// previous ones); x (bf16) times each term is exact in fp32.
+// bit of the fp32 significand for 2^-110 <= |W| < 3.38e38 and W = 0 (each
+// term is the rounded remainder of the previous ones; below 2^-110 the last
+// remainder reaches fp32's subnormal range); x (bf16) times each term is
+// exact in fp32.
 __global__ void router_split_kernel(const float* __restrict__ W, size_t n, uint16_t* __restrict__ Ws) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -381,29 +383,33 @@ extern "C" size_t moe_route_workspace_size(int T, int H, int E) {
   return align_up((size_t)sp.splits * T * E * sizeof(float), 256);
 }
 
-extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
-                         int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
-                         size_t ws_bytes, void* stream) {
-  moe::Range range_("moe_route");
+int moe::route_with_terms(const uint16_t* x, const float* w_router, const uint16_t* w_terms,
+                          const float* bias, int T, int H, int E, int k, int renorm,
+                          int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                          cudaStream_t s) {
   if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID;
   if (H % 64 != 0 || E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !w_router || !bias || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID;
   if (ws_bytes < moe_route_workspace_size(T, H, E)) return MOE_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (w_terms && !aligned(w_terms, 16)) return MOE_ERR_INVALID;
   float* part;
   int S;
   size_t sp_stride, st_stride;
   if (T >= kRtTcMinTokens) {
     // tensor cores: partial logits per K slice, the three weight terms
     // accumulated together, [T, splits, E] fp32, summed in slice order
-    uint16_t* Ws = static_cast<uint16_t*>(ws);
+    const uint16_t* Ws = w_terms;
     part = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                     align_up((size_t)3 * E * H * sizeof(uint16_t), 256));
     if (!aligned(x, 16)) return MOE_ERR_INVALID;
-    const size_t n = (size_t)E * H;
-    router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(w_router, n, Ws);
-    MOE_LAUNCH_CHECK();
+    if (!Ws) {  // split the weight now (moe_router_prepare does it once ahead)
+      uint16_t* Wt = static_cast<uint16_t*>(ws);
+      const size_t n = (size_t)E * H;
+      router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(w_router, n, Wt);
+      MOE_LAUNCH_CHECK();
+      Ws = Wt;
+    }
     const int splits = router_tc_splits(H);
     const int rc = launch_linear_tc_f32_terms(x, Ws, 3, T, E, H, kRtTcKSlice, part, s);
     if (rc) return rc;
@@ -450,6 +456,27 @@ extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* 
     router_topk_kernel<<<T, kTopkThreads, smem, s>>>(part, S, sp_stride, st_stride, bias, T, E, k,
                                                      renorm, topk_idx, topk_w);
   }
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+extern "C" int moe_route(const uint16_t* x, const float* w_router, const float* bias, int T, int H,
+                         int E, int k, int renorm, int32_t* topk_idx, float* topk_w, void* ws,
+                         size_t ws_bytes, void* stream) {
+  moe::Range range_("moe_route");
+  return route_with_terms(x, w_router, nullptr, bias, T, H, E, k, renorm, topk_idx, topk_w, ws,
+                          ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_router_prepare(const float* w_router, int E, int H, uint16_t* w_terms,
+                                  void* stream) {
+  moe::Range range_("moe_router_prepare");
+  if (E <= 0 || H <= 0) return MOE_ERR_INVALID;
+  if (!w_router || !w_terms || !aligned(w_router, 4) || !aligned(w_terms, 16))
+    return MOE_ERR_INVALID;
+  const size_t n = (size_t)E * H;
+  router_split_kernel<<<std::min<size_t>((n + 255) / 256, 4096), 256, 0,
+                        static_cast<cudaStream_t>(stream)>>>(w_router, n, w_terms);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -111,6 +111,20 @@ def test_layer_deterministic_and_host_variant(moe):
     assert moe.check_error() == 0
 
 
+def test_layer_router_prepared_terms_give_the_same_bits(moe):
+    """From 512 tokens the router's logits run on the tensor cores with the
+    fp32 weight split into three bf16 terms; a layer given the terms once
+    (moe_router_prepare, MoeLayer's default) and one that splits the weight on
+    every call give the same bits."""
+    w = wl.workload("tiny", name="prep", T=600, H=512, E=48, k=4, I=128, seed=31)
+    x = wl.gen_x(w).to(DEV)
+    weights = device_weights(w, DEV)
+    a = moe.MoeLayer(w.T, w.H, w.E, w.k, w.I, weights).forward(x)
+    b = moe.MoeLayer(w.T, w.H, w.E, w.k, w.I, weights, prepare_router=False).forward(x)
+    assert moe.check_error() == 0
+    assert torch.equal(a, b)
+
+
 def test_layer_zero_tokens(moe):
     w = wl.workload("tiny", T=0)
     weights = device_weights(wl.WORKLOADS["tiny"], DEV)

@@ -84,6 +84,26 @@ def test_route_parity(moe, case):
         assert np.all(np.diff(r) <= 1e-6)
 
 
+def test_router_prepare_terms_sum_exactly(moe):
+    """moe_router_prepare's three bf16 terms add up to the fp32 router weight
+    exactly (the sum is formed in fp64 here), for weights from 2^-100 to 2^100
+    (the split is exact from 2^-110 on) and the fp32 values that need all
+    three terms."""
+    rng = np.random.default_rng(61)
+    E, H = 40, 192
+    mant = rng.uniform(1.0, 2.0, size=(E, H))
+    expo = rng.integers(-100, 100, size=(E, H))
+    sign = rng.choice([-1.0, 1.0], size=(E, H))
+    W = (sign * mant * np.exp2(expo)).astype(np.float32)
+    W[0, :8] = [0.0, -0.0, 1.0, np.float32(1 + 2 ** -23), np.float32(3.0000002),
+                np.float32(-1e-30), np.float32(1e30), np.float32(2 ** -126)]
+    terms = moe.router_prepare(torch.from_numpy(W).to(DEV))
+    assert moe.check_error() == 0
+    t = terms.view(torch.int16).cpu().numpy().astype(np.uint16).astype(np.uint32) << 16
+    t = t.view(np.float32).astype(np.float64)
+    assert np.array_equal(t[0] + t[1] + t[2], W.astype(np.float64))
+
+
 @pytest.mark.parametrize("T,kernels", [(40, 2), (512, 3)])
 def test_route_launch_count(moe, T, kernels):
     # the library counts its launches: SIMT logits + top-k below 512 tokens,
