@@ -534,29 +534,39 @@ def main(argv=None):
 
 
 def _e2e_pass(layer, x, w, world, dist, device, e_steps, launch="stream"):
-    """moe_layer_forward_host (as a captured graph with --launch graph): the
-    pinned host input copied in, the layer, the output copied out."""
+    """Every step copies its pinned host input in, runs the layer and copies
+    its output out.  --launch graph: through a layer pipe (moe_layer_pipe_*,
+    the layer captured as a graph per device slot; a step's copies overlap
+    the neighbouring steps' compute); --launch stream: moe_layer_forward_host,
+    copies and layer in order on one stream."""
     xh = x.pin_memory()
     oh = torch.empty_like(x).pin_memory()
-    graph = layer.graph(xh, oh, host=True) if launch == "graph" else None
-    run = graph.launch if graph else (lambda: layer.forward_host(xh, oh))
+    pipe = layer.pipe() if launch == "graph" else None
+    run = (lambda: pipe.submit(xh, oh)) if pipe else (lambda: layer.forward_host(xh, oh))
     for _ in range(3):
         run()
+    if pipe:
+        pipe.join()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record()
     for _ in range(e_steps):
         run()
+    if pipe:
+        pipe.join()  # the last step's output copy is inside the timed region
     e1.record()
     torch.cuda.synchronize()
     wall = (time.perf_counter() - t0) / e_steps
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, device)
-    if graph:
-        graph.close()
+    if pipe:
+        pipe.close()
     return {"value": job_tokens_per_s(world, w.T, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(x.numel() * 2),
-            "host_wall_ms_per_step": wall * 1000.0}
+            "host_wall_ms_per_step": wall * 1000.0,
+            "api": ("moe_layer_pipe_submit per step (its copies overlap the neighbouring steps' "
+                    "compute), moe_layer_pipe_join after the last" if launch == "graph"
+                    else "moe_layer_forward_host per step")}
 
 
 def _report(args, world, head, others, cpu):

@@ -439,6 +439,36 @@ int moe_layer_graph_launch(const moe_layer_graph* graph, void* stream);
 /* Frees a captured call (NULL is ignored); launches already issued finish. */
 void moe_layer_graph_destroy(moe_layer_graph* graph);
 
+/* Pipelined layer calls on host buffers, for a serving loop that feeds one
+ * call after another from pinned host memory (no page has this call).  Call n
+ * of a pipe copies its x_host in on a stream of the pipe, runs the layer as a
+ * captured graph (moe_layer_graph) on `stream` in device slot n % 2, and
+ * copies out back on a second stream of the pipe, so that the copies of one
+ * call overlap the compute of the calls before and after it.  The results
+ * are those of moe_layer_forward_host.
+ *   moe_layer_pipe_workspace_size: ws bytes (the layer's workspace plus two
+ *     device slots for x and out; 0 for an invalid cfg).
+ *   moe_layer_pipe_create: checks the arguments (those of moe_layer_forward,
+ *     T > 0), creates the pipe's two streams and events and captures the two
+ *     slots' graphs on `stream`, which must not be capturing.  The arrays w
+ *     points to and ws must stay valid until destroy.  *pipe is NULL on
+ *     every error.
+ *   moe_layer_pipe_submit: enqueues one call (no host sync); x_host and
+ *     out_host (T x H bf16, pinned) must stay valid until the call's output
+ *     copy has finished; every submit to a pipe uses the same `stream`.
+ *   moe_layer_pipe_join: makes `stream` wait for the output copies of every
+ *     call submitted so far (synchronise the stream before reading them).
+ *   moe_layer_pipe_destroy: waits for the pipe's copies, then frees it
+ *     (NULL is ignored). */
+typedef struct moe_layer_pipe moe_layer_pipe;
+size_t moe_layer_pipe_workspace_size(const moe_config* cfg);
+int moe_layer_pipe_create(const moe_config* cfg, const moe_weights* w, void* ws, size_t ws_bytes,
+                          void* stream, moe_layer_pipe** pipe);
+int moe_layer_pipe_submit(moe_layer_pipe* pipe, const uint16_t* x_host, uint16_t* out_host,
+                          void* stream);
+int moe_layer_pipe_join(moe_layer_pipe* pipe, void* stream);
+void moe_layer_pipe_destroy(moe_layer_pipe* pipe);
+
 /* ------------------------------------------------------------ status etc -- */
 
 /* Synchronises `stream`, then returns and clears the current device's

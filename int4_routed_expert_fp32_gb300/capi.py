@@ -102,6 +102,12 @@ SIGNATURES = {
                                        POINTER(c_void_p)]),
     "moe_layer_graph_launch": (c_int, [c_void_p, c_void_p]),
     "moe_layer_graph_destroy": (None, [c_void_p]),
+    "moe_layer_pipe_workspace_size": (c_size_t, [POINTER(MoeConfig)]),
+    "moe_layer_pipe_create": (c_int, [POINTER(MoeConfig), POINTER(MoeWeights), c_void_p, c_size_t,
+                                      c_void_p, POINTER(c_void_p)]),
+    "moe_layer_pipe_submit": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_layer_pipe_join": (c_int, [c_void_p, c_void_p]),
+    "moe_layer_pipe_destroy": (None, [c_void_p]),
     "moe_layer_forward_host": (c_int, [POINTER(MoeConfig), POINTER(MoeWeights), c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]),
     "moe_check_error": (c_int, [c_void_p]),
@@ -582,6 +588,65 @@ class MoeLayer:
         cur.wait_stream(side)
         _check("moe_layer_graph_create", rc)
         return LayerGraph(handle, (self, x, out))
+
+    def pipe(self) -> "LayerPipe":
+        """Pipelined calls on pinned host buffers (see LayerPipe); the pipe has
+        its own workspace, so it can run beside this layer's other calls."""
+        ws = _ws(lib.moe_layer_pipe_workspace_size(ctypes.byref(self.cfg)), self.device)
+        handle = c_void_p()
+        cur = torch.cuda.current_stream(self.device)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            rc = lib.moe_layer_pipe_create(ctypes.byref(self.cfg), ctypes.byref(self.wstruct),
+                                           _p(ws), ws.numel(), _stream(), ctypes.byref(handle))
+        cur.wait_stream(side)
+        _check("moe_layer_pipe_create", rc)
+        return LayerPipe(handle, (self, ws), (self.cfg.T, self.cfg.H))
+
+
+class LayerPipe:
+    """Pipelined layer calls on pinned host buffers (moe_layer_pipe_*): the
+    copies of one call overlap the compute of its neighbours.  Submit every
+    call from the same current stream; join() makes it wait for the output
+    copies of the calls submitted so far."""
+
+    def __init__(self, handle: c_void_p, keep, shape):
+        self._h = handle
+        self._keep = keep
+        self._shape = shape
+        self._pending = []  # host buffers of calls not yet joined
+
+    def submit(self, x_host: torch.Tensor, out_host: torch.Tensor) -> None:
+        if not self._h:
+            raise ValueError("the pipe was closed")
+        for name, t in (("x_host", x_host), ("out_host", out_host)):
+            _arg(name, t, self._shape, torch.bfloat16)
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError(f"{name} must be a pinned host tensor")
+        _check("moe_layer_pipe_submit",
+               lib.moe_layer_pipe_submit(self._h, _p(x_host), _p(out_host), _stream()))
+        self._pending.append((x_host, out_host))
+
+    def join(self) -> None:
+        if not self._h:
+            raise ValueError("the pipe was closed")
+        _check("moe_layer_pipe_join", lib.moe_layer_pipe_join(self._h, _stream()))
+        # the buffers stay referenced until the stream has passed the join
+        self._joined = self._pending
+        self._pending = []
+
+    def close(self) -> None:
+        if self._h:
+            lib.moe_layer_pipe_destroy(self._h)
+            self._h = c_void_p()
+            self._pending = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class LayerGraph:

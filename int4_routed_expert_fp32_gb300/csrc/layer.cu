@@ -261,3 +261,126 @@ extern "C" void moe_layer_graph_destroy(moe_layer_graph* graph) {
   cudaGraphDestroy(graph->graph);
   delete graph;
 }
+
+// ---- pipelined calls on host buffers ---------------------------------------
+//
+// Two device slots for x and out; call n uses slot n % 2.  Its input copy
+// (own stream) waits until call n - 2's compute has read the slot, its
+// compute (the caller's stream, a captured graph per slot) waits for the
+// input copy and for call n - 2's output copy, and its output copy (own
+// stream) waits for the compute.  So the copies of one call overlap the
+// compute of its neighbours.
+
+struct moe_layer_pipe {
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t in_done[2] = {}, comp_done[2] = {}, out_done[2] = {}, join = nullptr;
+  moe_layer_graph* g[2] = {};
+  uint16_t* x_dev[2] = {};
+  uint16_t* out_dev[2] = {};
+  size_t bytes = 0;  // T * H * 2
+  uint64_t n = 0;    // calls submitted
+};
+
+static size_t pipe_slot_bytes(const moe_config& c) {
+  return align_up((size_t)c.T * c.H * sizeof(uint16_t), 256);
+}
+
+extern "C" size_t moe_layer_pipe_workspace_size(const moe_config* cfg) {
+  const size_t layer = moe_workspace_size(cfg);
+  if (!layer) return 0;
+  return layer + 4 * pipe_slot_bytes(*cfg);
+}
+
+static void pipe_free(moe_layer_pipe* p) {
+  if (!p) return;
+  // the last calls' compute (on the caller's stream) and copies finish first
+  for (int j = 0; j < 2; ++j)
+    if (p->comp_done[j]) cudaEventSynchronize(p->comp_done[j]);
+  if (p->s_in) cudaStreamSynchronize(p->s_in);
+  if (p->s_out) cudaStreamSynchronize(p->s_out);
+  for (int j = 0; j < 2; ++j) {
+    moe_layer_graph_destroy(p->g[j]);
+    if (p->in_done[j]) cudaEventDestroy(p->in_done[j]);
+    if (p->comp_done[j]) cudaEventDestroy(p->comp_done[j]);
+    if (p->out_done[j]) cudaEventDestroy(p->out_done[j]);
+  }
+  if (p->join) cudaEventDestroy(p->join);
+  if (p->s_in) cudaStreamDestroy(p->s_in);
+  if (p->s_out) cudaStreamDestroy(p->s_out);
+  delete p;
+}
+
+extern "C" int moe_layer_pipe_create(const moe_config* cfg, const moe_weights* w, void* ws,
+                                     size_t ws_bytes, void* stream, moe_layer_pipe** pipe) {
+  moe::Range range_("moe_layer_pipe_create");
+  if (!pipe) return MOE_ERR_INVALID;
+  *pipe = nullptr;
+  int rc = validate(cfg, w);
+  if (rc) return rc;
+  if (cfg->T == 0) return MOE_ERR_INVALID;
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID;
+  const size_t layer = carve(*cfg, nullptr).total;
+  if (ws_bytes < moe_layer_pipe_workspace_size(cfg)) return MOE_ERR_WORKSPACE;
+  moe_layer_pipe* p = new moe_layer_pipe;
+  p->bytes = (size_t)cfg->T * cfg->H * sizeof(uint16_t);
+  char* slots = static_cast<char*>(ws) + layer;
+  for (int j = 0; j < 2; ++j) {
+    p->x_dev[j] = reinterpret_cast<uint16_t*>(slots + (2 * j) * pipe_slot_bytes(*cfg));
+    p->out_dev[j] = reinterpret_cast<uint16_t*>(slots + (2 * j + 1) * pipe_slot_bytes(*cfg));
+  }
+  cudaError_t e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking);
+  for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
+    e = cudaEventCreateWithFlags(&p->in_done[j], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->comp_done[j], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->out_done[j], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    pipe_free(p);
+    return MOE_ERR_CUDA;
+  }
+  for (int j = 0; j < 2; ++j) {
+    rc = moe_layer_graph_create(cfg, w, p->x_dev[j], p->out_dev[j], 0, ws, layer, stream, &p->g[j]);
+    if (rc) {
+      pipe_free(p);
+      return rc;
+    }
+  }
+  *pipe = p;
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_pipe_submit(moe_layer_pipe* p, const uint16_t* x_host, uint16_t* out_host,
+                                     void* stream) {
+  if (!p || !x_host || !out_host) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int j = static_cast<int>(p->n & 1);
+  // input: slot j's x is free once call n - 2's compute has read it
+  MOE_TRY_CUDA(cudaStreamWaitEvent(p->s_in, p->comp_done[j], 0));
+  MOE_TRY_CUDA(cudaMemcpyAsync(p->x_dev[j], x_host, p->bytes, cudaMemcpyHostToDevice, p->s_in));
+  MOE_TRY_CUDA(cudaEventRecord(p->in_done[j], p->s_in));
+  // compute: the input has landed and call n - 2's output has been copied out
+  MOE_TRY_CUDA(cudaStreamWaitEvent(s, p->in_done[j], 0));
+  MOE_TRY_CUDA(cudaStreamWaitEvent(s, p->out_done[j], 0));
+  const int rc = moe_layer_graph_launch(p->g[j], stream);
+  if (rc) return rc;
+  MOE_TRY_CUDA(cudaEventRecord(p->comp_done[j], s));
+  // output
+  MOE_TRY_CUDA(cudaStreamWaitEvent(p->s_out, p->comp_done[j], 0));
+  MOE_TRY_CUDA(cudaMemcpyAsync(out_host, p->out_dev[j], p->bytes, cudaMemcpyDeviceToHost,
+                               p->s_out));
+  MOE_TRY_CUDA(cudaEventRecord(p->out_done[j], p->s_out));
+  ++p->n;
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_pipe_join(moe_layer_pipe* p, void* stream) {
+  if (!p) return MOE_ERR_INVALID;
+  MOE_TRY_CUDA(cudaEventRecord(p->join, p->s_out));
+  MOE_TRY_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->join, 0));
+  return MOE_OK;
+}
+
+extern "C" void moe_layer_pipe_destroy(moe_layer_pipe* p) { pipe_free(p); }

@@ -248,6 +248,37 @@ def test_layer_graph_launches_replay_the_call(moe, case):
     assert moe.check_error() == 0
 
 
+@pytest.mark.parametrize("case", ["tiny", "small_latent", "tiny_exact"])
+def test_layer_pipe_gives_each_call_its_bits(moe, case):
+    """Five calls with different inputs through a pipe (input and output
+    copies on the pipe's own streams, overlapping the neighbouring calls'
+    compute, two device slots used in turn) give, in each call's own host
+    buffer, the bits of forward on that input."""
+    w = SMALL[case]
+    layer = _layer(moe, w, device_weights(w, DEV))
+    x0 = wl.gen_x(w)
+    xs = [torch.roll(x0, i, dims=0).contiguous() for i in range(5)]
+    want = [layer.forward(x.to(DEV)).cpu() for x in xs]
+    pipe = layer.pipe()
+    xh = [x.pin_memory() for x in xs]
+    oh = [torch.empty_like(x).pin_memory() for x in xs]
+    for a, b in zip(xh, oh):
+        pipe.submit(a, b)
+    pipe.join()
+    torch.cuda.current_stream().synchronize()
+    assert moe.check_error() == 0
+    for i in range(5):
+        assert torch.equal(oh[i], want[i]), i
+    # a second round through the same pipe
+    for a, b in zip(xh[::-1], oh):
+        pipe.submit(a, b)
+    pipe.join()
+    torch.cuda.current_stream().synchronize()
+    for i in range(5):
+        assert torch.equal(oh[i], want[4 - i]), i
+    pipe.close()
+
+
 def test_layer_graph_rejects_bad_arguments_before_capture(moe):
     w = SMALL["tiny"]
     layer = _layer(moe, w, device_weights(w, DEV))
