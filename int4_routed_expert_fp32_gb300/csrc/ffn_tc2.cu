@@ -60,15 +60,19 @@ constexpr int kPXBytes = 2 * kPXBoxBytes;       // 32 KiB: the CTA's half of the
 constexpr int kPQBytes = kPM * kPBK / 2;        // 8 KiB packed int4 (128 rows x 64 bytes)
 constexpr int kPStageBytes = kPXBytes + kPQBytes;
 constexpr int kPDqWarps = 16;                   // (lane quarter, 32-column group of the stage)
-constexpr int kPEpWarps = 8;                    // two per lane quarter
 constexpr int kPEpWarp0 = 2 + kPDqWarps;
-constexpr int kPThreads = (2 + kPDqWarps + kPEpWarps) * 32;
+// Epilogue warps: two per lane quarter for gate/up (whose h packing needs the
+// registers), three for down, whose accumulator then drains in two thirds of
+// the time (2 + 16 + 12 warps: 960 threads).
+constexpr int pair_ep_warps(int mode) { return mode == 0 ? 8 : 12; }
+constexpr int pair_threads(int mode) { return (2 + kPDqWarps + pair_ep_warps(mode)) * 32; }
 constexpr uint32_t kPCols = 512;
 constexpr uint32_t kPACol = kPTN;               // A ring after the 256-column accumulator
 constexpr uint32_t kPASlot = kPBK / 2;          // 64 columns: 128 fp16 per row
 constexpr int kPSmem = kPStages * kPStageBytes + 1024 + 256;
 static_assert(kPStageBytes % 1024 == 0, "stage alignment");
 static_assert(kPDqWarps * 32 == kPM * (kPBK / kGroup), "one thread per row and group");
+static_assert((2 + kPDqWarps + 12) * 32 <= 1024, "threads per CTA");
 static_assert(kPACol + kPAStages * kPASlot <= kPCols, "TMEM budget");
 
 enum PMode { kPGateUp = 0, kPDown = 1, kPLinear = 2 };
@@ -86,7 +90,7 @@ __device__ __forceinline__ int pair_n(int rows) { return rows <= 32 ? 32 : (rows
 // STALL (tests only): each CTA's producer stops before its stage p.stall_at,
 // as if its copies never arrived, so that the other roles' waits run out.
 template <int MODE, bool STALL = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(MODE), 1)
     ffn_tc_pair_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -114,7 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&afree[a], 1);
     }
     mbar_init(accfull, 1);
-    mbar_init(accempty, 2 * kPEpWarps);
+    mbar_init(accempty, 2 * pair_ep_warps(MODE));
     mbar_init(mma_done, 1);
     cta_abort = 0;
     fence_mbarrier_init();
@@ -287,8 +291,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // two warps per TMEM lane quarter: half eh takes the 16-token slices
-    // 16 eh, 16 eh + 32, ...
+    // nq warps per TMEM lane quarter: warp eh of a quarter takes the 16-token
+    // slices 16 eh, 16 eh + 16 nq, ...
+    constexpr int nq = pair_ep_warps(MODE) / 4;
     const int qd = warp & 3;
     const int eh = (warp - kPEpWarp0) >> 2;
     const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
@@ -351,11 +356,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       } else {
         const int n = n0 + kPM * static_cast<int>(rank) + 32 * qd + lane;
 #pragma unroll 1
-        for (int c0 = 16 * eh; c0 < rows; c0 += 32) {
+        for (int c0 = 16 * eh; c0 < rows; c0 += 16 * nq) {
           uint32_t v[16];
           tmem_ld16(tbase + t_lane + c0, v);
           tmem_ld_wait();
-          if (c0 + 32 >= rows) {
+          if (c0 + 16 * nq >= rows) {
             // the last slice is in registers: release the accumulator
             tc_fence_before();
             __syncwarp();
@@ -424,7 +429,7 @@ static int pair_grid_clusters() {
     return 0;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * ((num_sms() + 1) / 2));
-  cfg.blockDim = dim3(kPThreads);
+  cfg.blockDim = dim3(pair_threads(MODE));
   cfg.dynamicSmemBytes = kPSmem;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
@@ -444,7 +449,7 @@ static int launch_pair(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
   if (n <= 0) return MOE_ERR_UNSUPPORTED;
   auto kern = ffn_tc_pair_kernel<MODE, STALL>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem));
-  kern<<<2 * n, kPThreads, kPSmem, s>>>(maps, p);
+  kern<<<2 * n, pair_threads(MODE), kPSmem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
