@@ -25,7 +25,7 @@
 //     MMAs into one 256-column fp32 accumulator, and commits that arrive on
 //     the barriers of both CTAs (shared-memory slot free, TMEM slot free,
 //     accumulator full);
-//   * warps 18-25: the epilogue of the CTA's 128 rows (lane = weight row,
+//   * warps 18-25 (18-29 for down): the epilogue of the CTA's 128 rows (lane = weight row,
 //     column = token).  Gate/up lane quarters hold 16 gate rows (lanes 0-15)
 //     and the up rows of the same outputs (lanes 16-31): one shuffle per
 //     token pairs them, the gate lane finishing the first 8 tokens of a
