@@ -100,6 +100,20 @@ def test_argument_errors_return_before_any_launch(capi):
     bad = capi.MoeConfig(4, 64, 8, 2, 64, 0, 4, 1, 1e-6)
     assert L.moe_layer_forward(ctypes.byref(bad), ctypes.byref(w), n, n, n, 0, n) == \
         capi.MOE_ERR_UNSUPPORTED
+    # router preparation and the layer pipe
+    assert L.moe_router_prepare(n, 8, 64, n, n) == capi.MOE_ERR_INVALID
+    assert L.moe_router_prepare(n, 0, 64, n, n) == capi.MOE_ERR_INVALID
+    pipe = ctypes.c_void_p(1)
+    assert L.moe_layer_pipe_create(ctypes.byref(cfg), ctypes.byref(w), n, 0, n,
+                                   ctypes.byref(pipe)) == capi.MOE_ERR_INVALID
+    assert pipe.value is None  # NULL on every error
+    assert L.moe_layer_pipe_create(ctypes.byref(bad), ctypes.byref(w), n, 0, n,
+                                   ctypes.byref(pipe)) == capi.MOE_ERR_UNSUPPORTED
+    assert L.moe_layer_pipe_submit(n, n, n, n) == capi.MOE_ERR_INVALID
+    assert L.moe_layer_pipe_join(n, n) == capi.MOE_ERR_INVALID
+    L.moe_layer_pipe_destroy(n)  # NULL is ignored
+    assert L.moe_layer_pipe_workspace_size(ctypes.byref(cfg)) == \
+        L.moe_workspace_size(ctypes.byref(cfg)) + 4 * 512  # two slots of x and out, 4 x 64 bf16
     assert capi.launch_count() == launches
 
 

@@ -276,7 +276,15 @@ def test_layer_pipe_gives_each_call_its_bits(moe, case):
     torch.cuda.current_stream().synchronize()
     for i in range(5):
         assert torch.equal(oh[i], want[4 - i]), i
+    # host buffers that are not pinned, or on the device, are refused
+    with pytest.raises(ValueError):
+        pipe.submit(xs[0], oh[0])
+    with pytest.raises(ValueError):
+        pipe.submit(xh[0], want[0].to(DEV))
     pipe.close()
+    with pytest.raises(ValueError):
+        pipe.submit(xh[0], oh[0])
+    assert moe.check_error() == 0
 
 
 def test_layer_graph_rejects_bad_arguments_before_capture(moe):
