@@ -102,18 +102,19 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 }
 
 // Decode-sized batches (T <= 32): one lane per token.  A CTA of eight warps
-// takes 32 experts x 512 columns: the fp32 weight tile and the tokens' bf16
+// takes 32 experts x 256 columns (336 CTAs at H = 7168, E = 384: four fit on
+// an SM, so the whole weight is in flight at once): the fp32 weight tile and the tokens' bf16
 // x slice are copied to shared memory up front (16-byte cp.async, all in
 // flight at once; x rows padded by 16 bytes so that the lanes' 16-byte reads
 // of 32 different rows hit distinct banks), then each lane accumulates its
 // token against the four experts of its warp, the weights read as
 // shared-memory broadcasts (one 16-byte read per four FMAs).
-// part[z, t, e] = the z-th 512-column slice's dot product, in column order.
+// part[z, t, e] = the z-th 256-column slice's dot product, in column order.
 constexpr int kRwExperts = 32;               // experts per CTA (4 per warp)
-constexpr int kRwK = 512;                    // K columns per CTA
+constexpr int kRwK = 256;                    // K columns per CTA
 constexpr int kRwMaxTokens = 32;             // one lane per token
 constexpr int kRwXStride = kRwK * 2 + 16;    // bytes per x row in shared memory
-constexpr int kRwSmem = kRwExperts * kRwK * 4 + kRwMaxTokens * kRwXStride;  // 97 KiB
+constexpr int kRwSmem = kRwExperts * kRwK * 4 + kRwMaxTokens * kRwXStride;  // 48.5 KiB
 
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
