@@ -492,7 +492,8 @@ int moe_wait_selftest(int64_t limit_ns, void* stream);
  * stream kernel (chunks of <= 16 rows), 1: the tensor-core kernel (the
  * act_bits 16 one, or the exact one for act_bits 8; chunks of <= 128 rows),
  * 2: the CTA-pair tensor-core kernel (act_bits 16 only, chunks of <= 256
- * rows; MOE_ERR_UNSUPPORTED where no cluster of two fits)
+ * rows; MOE_ERR_UNSUPPORTED where no cluster of two fits), 3: the small-tile
+ * layout of the act_bits 16 tensor-core kernel (chunks of <= 64 rows)
  * -- in a build of it whose producer stops before its copy stage
  * `stall_stage` (counted per CTA from 0), as if those copies never arrived,
  * with every bounded wait limited to `limit_ns` (1e3 .. 5e9).  The other
@@ -512,7 +513,8 @@ int moe_int4_linear_stall_selftest(const void* x, const float* x_scale, const in
  * the device: the experts with at least 129 rows run on the CTA-pair kernels
  * -- clusters of two CTAs whose MMAs (tcgen05 cta_group::2) take 256 weight
  * rows over two SMs, on chunks of up to 256 token rows -- and the others on
- * the one-CTA kernels (128 weight rows per MMA, chunks of up to 128 rows);
+ * the one-CTA kernels (128 weight rows per MMA, chunks of up to 128 rows; for
+ * experts of at most 64 rows a layout with 64-row tiles and deeper rings);
  * the pair kernels are launched only when the batch's mean expert load
  * rows_max / E is at least 64 rows.  enable == 0: every expert on the one-CTA
  * kernels.  Both kernels take the same K steps of 16 columns for every output

@@ -797,6 +797,31 @@ static bool pair_batch(int rows_max, int E, int max_rows_per_expert) {
          static_cast<long long>(rows_max) >= static_cast<long long>(kTcPairMinMeanRows) * E;
 }
 
+// The tensor-core kernels of a batch that can be prefill-shaped.  act_bits 16:
+// the experts of at most kTcSmallChunkRows rows on the small-tile layout of
+// the one-CTA kernels, those of kTcPairMinRows rows or more on the CTA pairs
+// (pair_batch), the others on the one-CTA kernels; act_bits 8: every expert
+// on the exact kernels.
+struct TcPlan {
+  bool small_one;      // experts of 1 .. kTcSmallChunkRows rows, small-tile layout
+  bool pair;           // experts of kTcPairMinRows rows or more, CTA pairs
+  int one_lo, one_hi;  // row counts of the experts on the one-CTA (128-row) kernels
+};
+
+static TcPlan tc_plan(bool q8, int rows_max, int E, int max_rows_per_expert) {
+  TcPlan t{};
+  t.small_one = !q8;
+  t.pair = use_tc_pair(q8) && pair_batch(rows_max, E, max_rows_per_expert);
+  t.one_lo = t.small_one ? kTcSmallChunkRows + 1 : kTcMinRows;
+  t.one_hi = t.pair ? kTcPairMinRows - 1 : rows_max;
+  return t;
+}
+
+struct Schedule;
+static int launch_tc_schedules(const int32_t* offsets, int E, int rows_max, const TcPlan& t,
+                               const Schedule& one, const Schedule& small_one,
+                               const Schedule& pair, int* status, cudaStream_t s);
+
 // Chunk list of the expert-sorted rows: the rows of every expert whose row
 // count lies in [lo, hi] cut into chunks of at most mc rows, for a batch of
 // the shape `rule` names (no chunk otherwise).  One CTA of 1024 threads.
@@ -938,11 +963,12 @@ int launch_row_chunks(const int32_t* offsets, int E, int rows_max, int mc, void*
   return launch_schedule(offsets, E, rows_max, mc, 1, rows_max, sc, status, s, kAllShapes);
 }
 
-// Stream-kernel list plus the two tensor-core lists (one-CTA and CTA-pair
-// kernels).
+// Stream-kernel list plus the three tensor-core lists (one-CTA kernels,
+// their small-tile layout, and the CTA-pair kernels).
 static size_t schedule_bytes(int E, int rows_max) {
   return schedule_bytes_one(E, rows_max, kFsMc) + schedule_bytes_one(E, rows_max, kTcChunkRows) +
-         schedule_bytes_one(E, rows_max, kTcPairChunkRows);
+         schedule_bytes_one(E, rows_max, kTcPairChunkRows) +
+         schedule_bytes_one(E, rows_max, kTcSmallChunkRows);
 }
 
 static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, int lo, int hi,
@@ -953,6 +979,20 @@ static int launch_schedule(const int32_t* offsets, int E, int rows_max, int mc, 
                                          sc.n_chunks, status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+static int launch_tc_schedules(const int32_t* offsets, int E, int rows_max, const TcPlan& t,
+                               const Schedule& one, const Schedule& small_one,
+                               const Schedule& pair, int* status, cudaStream_t s) {
+  int rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, t.one_lo, t.one_hi, one, status, s,
+                           kPrefillShaped);
+  if (!rc && t.small_one)
+    rc = launch_schedule(offsets, E, rows_max, kTcSmallChunkRows, kTcMinRows, kTcSmallChunkRows,
+                         small_one, status, s, kPrefillShaped);
+  if (!rc && t.pair)
+    rc = launch_schedule(offsets, E, rows_max, kTcPairChunkRows, kTcPairMinRows, rows_max, pair,
+                         status, s, kPrefillShaped);
+  return rc;
 }
 
 // Tensor map of a packed weight [E, N, K/8] int32 with a box of `rows` rows x
@@ -1059,6 +1099,7 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
   Schedule big2 = carve_one(b, E, rows_max, kTcPairChunkRows);
+  Schedule sm1 = carve_one(b, E, rows_max, kTcSmallChunkRows);
   uint16_t* h = reinterpret_cast<uint16_t*>(b);
   b += align_up((size_t)rows_max * I * sizeof(uint16_t), 256);
   int8_t* hq = nullptr;
@@ -1080,19 +1121,12 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
   // batch's actual shape
   const bool use_tc = tc_path_supported(D) && tc_path_supported(I) &&
                       max_rows_per_expert >= kTcMinBatchRows;
-  // experts of kTcPairMinRows rows or more on the CTA pairs (act_bits 16)
-  const bool pair = use_tc && use_tc_pair(q8) && pair_batch(rows_max, E, max_rows_per_expert);
+  const TcPlan plan = tc_plan(q8, rows_max, E, max_rows_per_expert);
   int rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
                            use_tc ? kDecodeShaped : kAllShapes);
   if (rc) return rc;
   if (use_tc) {
-    rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows,
-                         pair ? kTcPairMinRows - 1 : rows_max, big, status, s, kPrefillShaped);
-    if (rc) return rc;
-  }
-  if (pair) {
-    rc = launch_schedule(offsets, E, rows_max, kTcPairChunkRows, kTcPairMinRows, rows_max, big2,
-                         status, s, kPrefillShaped);
+    rc = launch_tc_schedules(offsets, E, rows_max, plan, big, sm1, big2, status, s);
     if (rc) return rc;
   }
 
@@ -1151,7 +1185,13 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
                                h, big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks,
                                status, s);
     if (rc) return rc;
-    if (pair) {
+    if (plan.small_one) {
+      rc = launch_tc_gateup(xa, rows_max, E, D, I, gate_packed, gate_scale, up_packed, up_scale,
+                            h, sm1.chunk_e, sm1.chunk_row0, sm1.chunk_rows, sm1.n_chunks, status,
+                            s, true);
+      if (rc) return rc;
+    }
+    if (plan.pair) {
       rc = launch_tc_pair_gateup(xa, rows_max, E, D, I, gate_packed, gate_scale, up_packed,
                                  up_scale, h, big2.chunk_e, big2.chunk_row0, big2.chunk_rows,
                                  big2.n_chunks, status, s);
@@ -1179,7 +1219,12 @@ int moe::launch_expert_ffn(const void* x_sorted, const float* x_scale, const int
             : launch_tc_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
                              big.chunk_e, big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
     if (rc) return rc;
-    if (pair) {
+    if (plan.small_one) {
+      rc = launch_tc_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32, sm1.chunk_e,
+                          sm1.chunk_row0, sm1.chunk_rows, sm1.n_chunks, status, s, true);
+      if (rc) return rc;
+    }
+    if (plan.pair) {
       rc = launch_tc_pair_down(ha, rows_max, E, D, I, down_packed, down_scale, y, y_f32,
                                big2.chunk_e, big2.chunk_row0, big2.chunk_rows, big2.n_chunks,
                                status, s);
@@ -1339,8 +1384,9 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
                                               void* ws, size_t ws_bytes, void* stream) {
   moe::Range range_("moe_int4_linear_stall_selftest");
   if (E <= 0 || rows_max <= 0 || N <= 0 || stall_stage < 0) return MOE_ERR_INVALID;
-  if (kernel < 0 || kernel > 2) return MOE_ERR_INVALID;
+  if (kernel < 0 || kernel > 3) return MOE_ERR_INVALID;
   if (kernel == 2 && (act_bits != 16 || !tc_pair_available())) return MOE_ERR_UNSUPPORTED;
+  if (kernel == 3 && act_bits != 16) return MOE_ERR_UNSUPPORTED;
   if (limit_ns < 1000 || limit_ns > 5000000000LL) return MOE_ERR_INVALID;
   if (check_width(K) || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (act_bits != 16 && act_bits != 8) return MOE_ERR_UNSUPPORTED;
@@ -1354,7 +1400,10 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool q8 = act_bits == 8;
-  const int mc = kernel == 0 ? kFsMc : kernel == 1 ? kTcChunkRows : kTcPairChunkRows;
+  const int mc = kernel == 0   ? kFsMc
+                 : kernel == 1 ? kTcChunkRows
+                 : kernel == 2 ? kTcPairChunkRows
+                               : kTcSmallChunkRows;
   char* b = static_cast<char*>(ws);
   Schedule sc = carve_one(b, E, rows_max, mc);
   b = static_cast<char*>(ws) + schedule_bytes(E, rows_max);
@@ -1398,7 +1447,7 @@ extern "C" int moe_int4_linear_stall_selftest(const void* x, const float* x_scal
   }
   return launch_tc_linear_stalled(xa, q8 ? x_scale : nullptr, rows_max, E, N, K, w_packed, w_scale,
                                   out, sc.chunk_e, sc.chunk_row0, sc.chunk_rows, sc.n_chunks,
-                                  status, limit_ns, stall_stage, s);
+                                  status, limit_ns, stall_stage, s, kernel == 3);
 }
 
 extern "C" size_t moe_int4_linear_workspace_size(int E, int K, int rows_max) {
@@ -1431,11 +1480,12 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   Schedule small = carve_one(b, E, rows_max, kFsMc);
   Schedule big = carve_one(b, E, rows_max, kTcChunkRows);
   Schedule big2 = carve_one(b, E, rows_max, kTcPairChunkRows);
+  Schedule sm1 = carve_one(b, E, rows_max, kTcSmallChunkRows);
   void* xp = b;
   b += align_up((size_t)rows_max * K * sizeof(uint16_t), 256);
   uint16_t* x16 = reinterpret_cast<uint16_t*>(b);
   const bool use_tc = tc_path_supported(K) && rows_max >= kTcMinBatchRows;
-  const bool pair = use_tc && use_tc_pair(q8) && pair_batch(rows_max, E, rows_max);
+  const TcPlan plan = tc_plan(q8, rows_max, E, rows_max);
   int rc = launch_to_pair_rows(x, q8, rows_max, K, offsets + E, xp, status, s);
   if (rc) return rc;
   rc = launch_schedule(offsets, E, rows_max, kFsMc, 0, rows_max, small, status, s,
@@ -1459,14 +1509,8 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
   p.tma_scales = tma_scales_ok(K, w_scale, w_scale) ? 1 : 0;
   rc = run_stream(kLinear, q8, m, p, s);
   if (rc || !use_tc) return rc;
-  rc = launch_schedule(offsets, E, rows_max, kTcChunkRows, kTcMinRows,
-                       pair ? kTcPairMinRows - 1 : rows_max, big, status, s, kPrefillShaped);
+  rc = launch_tc_schedules(offsets, E, rows_max, plan, big, sm1, big2, status, s);
   if (rc) return rc;
-  if (pair) {
-    rc = launch_schedule(offsets, E, rows_max, kTcPairChunkRows, kTcPairMinRows, rows_max, big2,
-                         status, s, kPrefillShaped);
-    if (rc) return rc;
-  }
   const uint16_t* xa = static_cast<const uint16_t*>(xp);
   if (q8) {
     rc = launch_to_f16_rows(xp, true, rows_max, K, offsets + E, x16, s);
@@ -1479,9 +1523,13 @@ extern "C" int moe_int4_linear(const void* x, const float* x_scale, const int32_
                              nullptr);
   rc = launch_tc_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big.chunk_e,
                       big.chunk_row0, big.chunk_rows, big.n_chunks, status, s);
-  if (rc || !pair) return rc;
-  return launch_tc_pair_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big2.chunk_e,
+  if (!rc && plan.small_one)
+    rc = launch_tc_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, sm1.chunk_e,
+                        sm1.chunk_row0, sm1.chunk_rows, sm1.n_chunks, status, s, true);
+  if (!rc && plan.pair)
+    rc = launch_tc_pair_down(xa, rows_max, E, N, K, w_packed, w_scale, out, true, big2.chunk_e,
                              big2.chunk_row0, big2.chunk_rows, big2.n_chunks, status, s);
+  return rc;
 }
 
 extern "C" int moe_set_tc_pair(int enable) {

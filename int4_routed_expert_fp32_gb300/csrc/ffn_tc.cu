@@ -45,34 +45,53 @@
 namespace moe {
 
 constexpr int kTxWM = 128;                     // weight rows per MMA block (M, TMEM lanes)
-constexpr int kTxTN = 128;                     // token rows per unit (largest MMA N)
 constexpr int kTxBK = 128;                     // K per stage
 constexpr int kTxXK = 64;                      // K per activation box (one 128-byte swizzle atom)
-constexpr int kTxStages = 4;                   // shared-memory ring
-constexpr int kTxAStages = 2;                  // TMEM ring of dequantised weights
-constexpr int kTxXBoxBytes = kTxTN * kTxXK * 2;  // 16 KiB: 128 tokens x 64 columns
-constexpr int kTxXBytes = 2 * kTxXBoxBytes;    // 32 KiB token tile
 constexpr int kTxQBytes = 2 * kTxWM * kTxBK / 2;  // 16 KiB packed int4 (256 rows x 64 bytes)
-constexpr int kTxStageBytes = kTxXBytes + kTxQBytes;
 constexpr int kTxDqWarps = 16;                 // (lane quarter, block, half of the stage)
 constexpr int kTxEpWarps = 8;                  // two per TMEM lane quarter
 constexpr int kTxThreads = (2 + kTxDqWarps + kTxEpWarps) * 32;
-constexpr uint32_t kTxCols = 512;              // 2 x 128 accumulator + 2 x 128 A columns
-constexpr uint32_t kTxAcc1 = kTxTN;            // column of the second accumulator
-constexpr uint32_t kTxACol = 2 * kTxTN;        // first A column
+constexpr uint32_t kTxCols = 512;
 constexpr uint32_t kTxASlot = 2 * (kTxBK / 2);  // A columns per stage: 2 blocks x 64
-constexpr int kTxSmem = kTxStages * kTxStageBytes + 1024 + 256;
-static_assert(kTxStageBytes % 1024 == 0, "stage alignment");
 static_assert(kTxDqWarps * 32 == 2 * 2 * kTxWM, "one dequantisation thread per row and half stage");
-static_assert(kTxACol + kTxAStages * kTxASlot <= kTxCols, "TMEM budget");
+
+// Layout for token tiles of at most TN rows.  TN = 128: 4 stages of 48 KiB,
+// two 128-column accumulators and two A slots.  TN = 64 (experts of at most
+// 64 rows): 6 stages of 32 KiB, two 64-column accumulators and three A slots,
+// and the conversion warps in two teams of eight that take alternate stages
+// (a warp converts a whole 128-column row of its stages).  Measured on
+// GB300 (int4_linear, 128 experts x 64 rows, K = 7168): 0.332 ms with the
+// TN = 128 layout, 0.304 ms with this one; each of its three changes alone
+// gained 1-3%.
+template <int TN>
+struct TxCfg {
+  static constexpr int kXBoxBytes = TN * kTxXK * 2;         // 16 KiB (TN 128) / 8 KiB (TN 64)
+  static constexpr int kXBytes = 2 * kXBoxBytes;
+  static constexpr int kStageBytes = kXBytes + kTxQBytes;
+  static constexpr int kStages = TN == 128 ? 4 : 6;         // shared-memory ring
+  static constexpr int kAStages = TN == 128 ? 2 : 3;        // TMEM ring of dequantised weights
+  static constexpr uint32_t kAcc1 = TN;                     // column of the second accumulator
+  static constexpr uint32_t kACol = 2 * TN;                 // first A column
+  static constexpr bool kTeams = TN != 128;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kACol + kAStages * kTxASlot <= kTxCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert((2 * kStages + 2 * kAStages + 3) * 8 + 4 <= 256, "barrier area");
+};
 
 enum TxMode { kTxGateUp = 0, kTxDown = 1, kTxLinear = 2 };
 
 // STALL (tests only): the producer stops before stage p.stall_at, as if its
 // copies never arrived, so that the other roles' waits run out.
-template <int MODE, bool STALL = false>
+template <int MODE, int TN = 128, bool STALL = false>
 __global__ void __launch_bounds__(kTxThreads, 1)
     ffn_tc_kernel(const __grid_constant__ TxMaps maps, const TxParams p) {
+  using C = TxCfg<TN>;
+  constexpr int kTxStages = C::kStages, kTxAStages = C::kAStages;
+  constexpr int kTxStageBytes = C::kStageBytes, kTxXBytes = C::kXBytes;
+  constexpr int kTxXBoxBytes = C::kXBoxBytes;
+  constexpr uint32_t kTxAcc1 = C::kAcc1, kTxACol = C::kACol;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -94,7 +113,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       mbar_init(&sfree[s], 1);
     }
     for (int a = 0; a < kTxAStages; ++a) {
-      mbar_init(&aready[a], kTxDqWarps);
+      mbar_init(&aready[a], C::kTeams ? kTxDqWarps / 2 : kTxDqWarps);
       mbar_init(&afree[a], 1);
     }
     mbar_init(accfull, 1);
@@ -198,87 +217,173 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     mbar_drain(mma_done, 0, p.status);
   } else if (warp < 2 + kTxDqWarps) {
     // ----------------------------------------------------- dequantisation
-    // TMEM lane quarter of this warp: warp % 4.  Warps 2-5: block 0, first
-    // half of each stage (K columns 0-63, scale groups 0 and 1); 6-9: block 0,
-    // second half (64-127, groups 2 and 3); 10-13 and 14-17: the same for
-    // block 1.
-    const int qd = warp & 3;
-    const int blk = (warp - 2) >> 3;
-    const int gh = ((warp - 2) >> 2) & 1;  // half of the stage
-    const int m = 32 * qd + lane;        // TMEM lane = row within the block
-    const int r = blk * kTxWM + m;       // row within the 256-row tile
-    const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
-    // int4 rows of 64 bytes, stored with the 64-byte swizzle: 16-byte chunk c
-    // of row r sits at chunk c ^ ((r >> 1) & 3); this thread reads chunks
-    // 2 gh and 2 gh + 1
-    const int qsw = (r >> 1) & 3;
-    const uint32_t qoff0 = static_cast<uint32_t>(r * 64 + (((2 * gh) ^ qsw) << 4));
-    const uint32_t qoff1 = static_cast<uint32_t>(r * 64 + (((2 * gh + 1) ^ qsw) << 4));
-    uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const int q = u / n_tiles, jt = u - q * n_tiles;
-      const int e = p.chunk_e[q];
-      const int n0 = jt * tile_n;
-      int n;
-      const uint16_t* sb;
-      if (MODE == kTxGateUp) {
-        n = n0 + m;
-        sb = blk == 0 ? p.scale0 : p.scale1;
-      } else {
-        n = n0 + r;
-        sb = p.scale0;
-      }
-      const bool valid = n < N;
-      // bf16 scales of this thread's two groups of stage ks (4 ks + 2 gh and
-      // + 1: one 4-byte word), fetched three stages ahead; groups beyond K
-      // (a last half stage) are 0
-      const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all + 2 * gh;
-      auto scale_word = [&](int ks2) -> uint32_t {
-        return (valid && ks2 < ksteps && 4 * ks2 + 2 * gh < G_all)
-                   ? *reinterpret_cast<const uint32_t*>(srow + 4 * ks2)
-                   : 0u;
-      };
-      uint32_t s_a = scale_word(0), s_b = scale_word(1), s_c = scale_word(2);
-      bool exact = true;  // every scale of this unit's row converts exactly
-      for (int ks = 0; ks < ksteps; ++ks, ++it) {
-        const uint32_t sw = s_a;
-        s_a = s_b;
-        s_b = s_c;
-        s_c = scale_word(ks + 3);
-        const int s = it % kTxStages, a = it % kTxAStages;
-        // warp-uniform outcome: the tcgen05.st below needs the whole warp
-        const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, wt) &&
-                         mbar_wait(&afree[a], ((it / kTxAStages) & 1u) ^ 1u, wt);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
+    if constexpr (C::kTeams) {
+      // Two teams of eight warps take alternate stages (team = parity of the
+      // stage counter); a thread converts its row's whole stage (4 groups).
+      // Warps 2-5 / 10-13: team 0, blocks 0 / 1; warps 6-9 / 14-17: team 1.
+      const int qd = warp & 3;
+      const int blk = (warp - 2) >> 3;
+      const int team = ((warp - 2) >> 2) & 1;
+      const int m = 32 * qd + lane;
+      const int r = blk * kTxWM + m;
+      const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
+      const int qsw = (r >> 1) & 3;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int q = u / n_tiles, jt = u - q * n_tiles;
+        const int e = p.chunk_e[q];
+        const int n0 = jt * tile_n;
+        int n;
+        const uint16_t* sb;
+        if (MODE == kTxGateUp) {
+          n = n0 + m;
+          sb = blk == 0 ? p.scale0 : p.scale1;
+        } else {
+          n = n0 + r;
+          sb = p.scale0;
         }
-        const uint8_t* qt = smem + s * kTxStageBytes + kTxXBytes;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(qt + qoff0);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(qt + qoff1);
-        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        exact &= scales_exact_f16(sw);
-        const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 4 ks + 2 gh
-        const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 4 ks + 2 gh + 1
-        uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
+        const bool valid = n < N;
+        // bf16 scales of groups 4 ks + 2 h and + 1 (h = 0, 1; one 4-byte word
+        // each), fetched one of this team's stages ahead; groups beyond K are 0
+        const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all;
+        auto scale_word = [&](int ks2, int h) -> uint32_t {
+          return (valid && ks2 < ksteps && 4 * ks2 + 2 * h < G_all)
+                     ? *reinterpret_cast<const uint32_t*>(srow + 4 * ks2 + 2 * h)
+                     : 0u;
+        };
+        const int ks0 = (team - static_cast<int>(it)) & 1;  // first stage of this team
+        uint32_t pa0 = scale_word(ks0, 0), pa1 = scale_word(ks0, 1);
+        bool exact = true;
+        for (int ks = ks0; ks < ksteps; ks += 2) {
+          const uint32_t sw0 = pa0, sw1 = pa1;
+          pa0 = scale_word(ks + 2, 0);
+          pa1 = scale_word(ks + 2, 1);
+          const uint32_t itk = it + ks;
+          const int s = itk % kTxStages, a = itk % kTxAStages;
+          // warp-uniform outcome: the tcgen05.st below needs the whole warp
+          const bool got = mbar_wait(&full[s], (itk / kTxStages) & 1u, wt) &&
+                           mbar_wait(&afree[a], ((itk / kTxAStages) & 1u) ^ 1u, wt);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* qt = smem + s * kTxStageBytes + kTxXBytes;
+          exact &= scales_exact_f16(sw0) && scales_exact_f16(sw1);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t w = wv[c];
-          const uint32_t sc = c < 4 ? s_lo : s_hi;
-          const uint32_t w8 = w >> 8;
-          av[4 * c + 0] = nib_lo_f16(w, sc);   // (n0, n4)
-          av[4 * c + 1] = nib_hi_f16(w, sc);   // (n1, n5)
-          av[4 * c + 2] = nib_lo_f16(w8, sc);  // (n2, n6)
-          av[4 * c + 3] = nib_hi_f16(w8, sc);  // (n3, n7)
+          for (int h = 0; h < 2; ++h) {
+            // chunks 2h and 2h + 1 of the row (64-byte swizzle: chunk c at c ^ qsw)
+            const uint4 w0 = *reinterpret_cast<const uint4*>(qt + r * 64 + (((2 * h) ^ qsw) << 4));
+            const uint4 w1 =
+                *reinterpret_cast<const uint4*>(qt + r * 64 + (((2 * h + 1) ^ qsw) << 4));
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const uint32_t sw = h ? sw1 : sw0;
+            const uint32_t s_lo = scale_f16x2(sw & 0xffffu);
+            const uint32_t s_hi = scale_f16x2(sw >> 16);
+            uint32_t av[32];  // pair order, as below
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t w = wv[c];
+              const uint32_t sc = c < 4 ? s_lo : s_hi;
+              const uint32_t w8 = w >> 8;
+              av[4 * c + 0] = nib_lo_f16(w, sc);
+              av[4 * c + 1] = nib_hi_f16(w, sc);
+              av[4 * c + 2] = nib_lo_f16(w8, sc);
+              av[4 * c + 3] = nib_hi_f16(w8, sc);
+            }
+            tmem_st32(tbase + t_lane + kTxACol + a * kTxASlot + blk * (kTxBK / 2) + h * 32, av);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&aready[a]);
         }
-        tmem_st32(tbase + t_lane + kTxACol + a * kTxASlot + blk * (kTxBK / 2) + gh * 32, av);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aready[a]);
+        it += ksteps;
+        if (!exact) record_status(p.status, MOE_ERR_UNSUPPORTED);
       }
-      if (!exact) record_status(p.status, MOE_ERR_UNSUPPORTED);
+    } else {
+      // TMEM lane quarter of this warp: warp % 4.  Warps 2-5: block 0, first
+      // half of each stage (K columns 0-63, scale groups 0 and 1); 6-9: block 0,
+      // second half (64-127, groups 2 and 3); 10-13 and 14-17: the same for
+      // block 1.
+      const int qd = warp & 3;
+      const int blk = (warp - 2) >> 3;
+      const int gh = ((warp - 2) >> 2) & 1;  // half of the stage
+      const int m = 32 * qd + lane;        // TMEM lane = row within the block
+      const int r = blk * kTxWM + m;       // row within the 256-row tile
+      const uint32_t t_lane = static_cast<uint32_t>(32 * qd) << 16;
+      // int4 rows of 64 bytes, stored with the 64-byte swizzle: 16-byte chunk c
+      // of row r sits at chunk c ^ ((r >> 1) & 3); this thread reads chunks
+      // 2 gh and 2 gh + 1
+      const int qsw = (r >> 1) & 3;
+      const uint32_t qoff0 = static_cast<uint32_t>(r * 64 + (((2 * gh) ^ qsw) << 4));
+      const uint32_t qoff1 = static_cast<uint32_t>(r * 64 + (((2 * gh + 1) ^ qsw) << 4));
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int q = u / n_tiles, jt = u - q * n_tiles;
+        const int e = p.chunk_e[q];
+        const int n0 = jt * tile_n;
+        int n;
+        const uint16_t* sb;
+        if (MODE == kTxGateUp) {
+          n = n0 + m;
+          sb = blk == 0 ? p.scale0 : p.scale1;
+        } else {
+          n = n0 + r;
+          sb = p.scale0;
+        }
+        const bool valid = n < N;
+        // bf16 scales of this thread's two groups of stage ks (4 ks + 2 gh and
+        // + 1: one 4-byte word), fetched three stages ahead; groups beyond K
+        // (a last half stage) are 0
+        const uint16_t* srow = sb + ((size_t)e * N + (valid ? n : 0)) * G_all + 2 * gh;
+        auto scale_word = [&](int ks2) -> uint32_t {
+          return (valid && ks2 < ksteps && 4 * ks2 + 2 * gh < G_all)
+                     ? *reinterpret_cast<const uint32_t*>(srow + 4 * ks2)
+                     : 0u;
+        };
+        uint32_t s_a = scale_word(0), s_b = scale_word(1), s_c = scale_word(2);
+        bool exact = true;  // every scale of this unit's row converts exactly
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const uint32_t sw = s_a;
+          s_a = s_b;
+          s_b = s_c;
+          s_c = scale_word(ks + 3);
+          const int s = it % kTxStages, a = it % kTxAStages;
+          // warp-uniform outcome: the tcgen05.st below needs the whole warp
+          const bool got = mbar_wait(&full[s], (it / kTxStages) & 1u, wt) &&
+                           mbar_wait(&afree[a], ((it / kTxAStages) & 1u) ^ 1u, wt);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* qt = smem + s * kTxStageBytes + kTxXBytes;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(qt + qoff0);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(qt + qoff1);
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          exact &= scales_exact_f16(sw);
+          const uint32_t s_lo = scale_f16x2(sw & 0xffffu);  // group 4 ks + 2 gh
+          const uint32_t s_hi = scale_f16x2(sw >> 16);      // group 4 ks + 2 gh + 1
+          uint32_t av[32];  // pair order: column 4c + j holds weight columns 8c + j, 8c + j + 4
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w = wv[c];
+            const uint32_t sc = c < 4 ? s_lo : s_hi;
+            const uint32_t w8 = w >> 8;
+            av[4 * c + 0] = nib_lo_f16(w, sc);   // (n0, n4)
+            av[4 * c + 1] = nib_hi_f16(w, sc);   // (n1, n5)
+            av[4 * c + 2] = nib_lo_f16(w8, sc);  // (n2, n6)
+            av[4 * c + 3] = nib_hi_f16(w8, sc);  // (n3, n7)
+          }
+          tmem_st32(tbase + t_lane + kTxACol + a * kTxASlot + blk * (kTxBK / 2) + gh * 32, av);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&aready[a]);
+        }
+        if (!exact) record_status(p.status, MOE_ERR_UNSUPPORTED);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -384,10 +489,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   }
 }
 
-static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K) {
+static bool act_map(CUtensorMap* m, const uint16_t* x16, int rows, int K, int box_rows = 128) {
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
   const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
-  const uint32_t box[2] = {static_cast<uint32_t>(kTxXK), static_cast<uint32_t>(kTxTN)};
+  const uint32_t box[2] = {static_cast<uint32_t>(kTxXK), static_cast<uint32_t>(box_rows)};
   return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -506,11 +611,12 @@ static bool packed_map(CUtensorMap* m, const int32_t* w, int E, int N, int K, in
                            CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int MODE, bool STALL = false>
+template <int MODE, int TN = 128, bool STALL = false>
 static int launch_tc(const TxMaps& maps, const TxParams& p, cudaStream_t s) {
-  auto kern = ffn_tc_kernel<MODE, STALL>;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTxSmem));
-  kern<<<num_sms(), kTxThreads, kTxSmem, s>>>(maps, p);
+  auto kern = ffn_tc_kernel<MODE, TN, STALL>;
+  constexpr int smem = TxCfg<TN>::kSmem;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  kern<<<num_sms(), kTxThreads, smem, s>>>(maps, p);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -524,9 +630,9 @@ int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
                      const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e,
                      const int32_t* chunk_row0, const int32_t* chunk_rows, const int32_t* n_chunks,
-                     int* status, cudaStream_t s) {
+                     int* status, cudaStream_t s, bool small) {
   TxMaps maps{};
-  if (!act_map(&maps.a, x16, rows_max, D) ||
+  if (!act_map(&maps.a, x16, rows_max, D, small ? 64 : 128) ||
       !packed_map(&maps.q0, gate_packed, E, I, D, kTxWM) ||
       !packed_map(&maps.q1, up_packed, E, I, D, kTxWM))
     return MOE_ERR_CUDA;
@@ -542,15 +648,16 @@ int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
   p.wait_ns = kDefaultWaitNs;
   p.K = D;
   p.N = I;
-  return launch_tc<kTxGateUp>(maps, p, s);
+  return small ? launch_tc<kTxGateUp, 64>(maps, p, s) : launch_tc<kTxGateUp>(maps, p, s);
 }
 
 int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
-                   const int32_t* n_chunks, int* status, cudaStream_t s) {
+                   const int32_t* n_chunks, int* status, cudaStream_t s, bool small) {
   TxMaps maps{};
-  if (!act_map(&maps.a, h16, rows_max, I) || !packed_map(&maps.q0, down_packed, E, D, I, 2 * kTxWM))
+  if (!act_map(&maps.a, h16, rows_max, I, small ? 64 : 128) ||
+      !packed_map(&maps.q0, down_packed, E, D, I, 2 * kTxWM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;
   TxParams p{};
@@ -565,6 +672,8 @@ int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
   p.wait_ns = kDefaultWaitNs;
   p.K = I;
   p.N = D;
+  if (small)
+    return y_f32 ? launch_tc<kTxLinear, 64>(maps, p, s) : launch_tc<kTxDown, 64>(maps, p, s);
   return y_f32 ? launch_tc<kTxLinear>(maps, p, s) : launch_tc<kTxDown>(maps, p, s);
 }
 
@@ -578,13 +687,14 @@ int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows
                              int K, const int32_t* w_packed, const uint16_t* w_scale, float* y,
                              const int32_t* chunk_e, const int32_t* chunk_row0,
                              const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
-                             long long wait_ns, int stall_at, cudaStream_t s) {
+                             long long wait_ns, int stall_at, cudaStream_t s, bool small) {
   if (x_scale)
     return launch_tc_q8_linear_stalled(x16, x_scale, rows_max, E, N, K, w_packed, w_scale, y,
                                        chunk_e, chunk_row0, chunk_rows, n_chunks, status, wait_ns,
                                        stall_at, s);
   TxMaps maps{};
-  if (!act_map(&maps.a, x16, rows_max, K) || !packed_map(&maps.q0, w_packed, E, N, K, 2 * kTxWM))
+  if (!act_map(&maps.a, x16, rows_max, K, small ? 64 : 128) ||
+      !packed_map(&maps.q0, w_packed, E, N, K, 2 * kTxWM))
     return MOE_ERR_CUDA;
   maps.q1 = maps.q0;
   TxParams p{};
@@ -600,7 +710,7 @@ int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows
   p.stall_at = stall_at;
   p.K = K;
   p.N = N;
-  return launch_tc<kTxLinear, true>(maps, p, s);
+  return small ? launch_tc<kTxLinear, 64, true>(maps, p, s) : launch_tc<kTxLinear, 128, true>(maps, p, s);
 }
 
 }  // namespace moe

@@ -31,8 +31,10 @@ struct TxMaps {
   CUtensorMap q1;
 };
 
-// Rows per token tile of the tensor-core path (chunks of that many rows).
+// Rows per token tile of the tensor-core path (chunks of that many rows), and
+// of its small-tile layout for experts of at most kTcSmallChunkRows rows.
 constexpr int kTcChunkRows = 128;
+constexpr int kTcSmallChunkRows = 64;
 
 // Rows per token tile of the CTA-pair kernels (ffn_tc2.cu).
 constexpr int kTcPairChunkRows = 256;
@@ -54,12 +56,14 @@ int launch_to_f16_rows(const void* src, bool src_i8, int R, int C, const int32_t
 // h[rows] = SiLU(x W_gate^T) * (x W_up^T) for the listed 128-row chunks
 // (act_bits 16); x16 is the fp16 copy of the activations (pair order), h is
 // written in fp16, pair order.
+// small: chunks of at most kTcSmallChunkRows rows (64-row token tiles, a
+// deeper ring; ffn_tc.cu).
 int launch_tc_gateup(const uint16_t* x16, int rows_max, int E, int D, int I,
                      const int32_t* gate_packed, const uint16_t* gate_scale,
                      const int32_t* up_packed, const uint16_t* up_scale, uint16_t* h,
                      const int32_t* chunk_e, const int32_t* chunk_row0,
                      const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
-                     cudaStream_t s);
+                     cudaStream_t s, bool small = false);
 
 // act_bits 8 on the tensor cores (ffn_tc_q8.cu): exact int4 x int8 group
 // partials, y = sc_x * (fp32 chain of fma(s_w[g], P[g], .) in group order).
@@ -87,12 +91,12 @@ int launch_tc_linear_stalled(const uint16_t* x16, const float* x_scale, int rows
                              int K, const int32_t* w_packed, const uint16_t* w_scale, float* y,
                              const int32_t* chunk_e, const int32_t* chunk_row0,
                              const int32_t* chunk_rows, const int32_t* n_chunks, int* status,
-                             long long wait_ns, int stall_at, cudaStream_t s);
+                             long long wait_ns, int stall_at, cudaStream_t s, bool small = false);
 
 int launch_tc_down(const uint16_t* h16, int rows_max, int E, int D, int I,
                    const int32_t* down_packed, const uint16_t* down_scale, void* y, bool y_f32,
                    const int32_t* chunk_e, const int32_t* chunk_row0, const int32_t* chunk_rows,
-                   const int32_t* n_chunks, int* status, cudaStream_t s);
+                   const int32_t* n_chunks, int* status, cudaStream_t s, bool small = false);
 
 // The same two GEMMs (act_bits 16) on CTA pairs (ffn_tc2.cu): chunks of at
 // most kTcPairChunkRows rows, MMAs of 256 weight rows over two SMs.

@@ -911,10 +911,10 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     assert moe.check_error() == 0
 
 
-@pytest.mark.parametrize("act_bits,kernel", [(16, 0), (8, 0), (16, 1), (8, 1), (16, 2)])
+@pytest.mark.parametrize("act_bits,kernel", [(16, 0), (8, 0), (16, 1), (8, 1), (16, 2), (16, 3)])
 def test_pipelined_kernel_exit_paths(moe, kernel, act_bits):
     """A producer that stops before its fourth copy stage (a test build of the
-    stream, tensor-core and CTA-pair kernels): the other roles' bounded waits
+    stream, tensor-core (both tile layouts) and CTA-pair kernels): the other roles' bounded waits
     (20 ms) run out, the kernel records MOE_ERR_TIMEOUT, drains its copies and
     MMAs, frees its tensor memory and returns (a CTA pair after both CTAs'
     roles have stopped); the next call is correct and clean."""
