@@ -124,10 +124,12 @@ def roofline(w: wl.Workload, ffn_ms: float, active: int, peaks: dict) -> dict:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     roof.update({"traffic": None,
-                 "kernel": "expert FFN call (moe_expert_ffn_pairs: schedules; for prefill-shaped "
-                           "batches ffn_tc_pair_kernel (CTA pairs, experts of >= 129 rows) and "
-                           "ffn_tc_kernel (the others), or ffn_tc_q8_kernel (act_bits 8), gate/up "
-                           "and down; for decode-shaped ones ffn_stream_fused_kernel)",
+                 "kernel": "expert FFN call (moe_expert_ffn_pairs_bounded, T rows per expert "
+                           "at most: schedules; for prefill-shaped batches ffn_tc_pair_kernel "
+                           "(CTA pairs, experts of >= 129 rows) and ffn_tc_kernel (the others; "
+                           "64-row tiles for experts of <= 64 rows), or ffn_tc_q8_kernel "
+                           "(act_bits 8), gate/up and down; for decode-shaped ones "
+                           "ffn_stream_fused_kernel)",
                  "kernel_ms": ffn_ms,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                  "active_experts": active, "peak_source": peaks["source"]})
@@ -197,8 +199,9 @@ def _setup(w: wl.Workload, device):
 
 
 def _ffn_pass(moe, w, layer, weights, x_dev, steps):
-    """Average duration of the expert-FFN call (moe_expert_ffn_pairs: schedules,
-    stream and tensor-core kernels) inside a layer step, timed with CUDA events
+    """Average duration of the expert-FFN call (moe_expert_ffn_pairs_bounded with
+    the layer's bound of T rows per expert: schedules, stream and tensor-core
+    kernels) inside a layer step, timed with CUDA events
     on its stream; the step is the work of moe_layer_forward, issued stage by
     stage through the C ABI (on the latent path the layer keeps y in fp32; this
     replay writes bf16 y)."""
@@ -234,11 +237,12 @@ def _ffn_pass(moe, w, layer, weights, x_dev, steps):
                                       s) == 0
         if i is not None:
             ev[i][0].record()
-        assert lib.moe_expert_ffn_pairs(p(xs), p(xsc), p(offsets), E, D, I, R,
-                                        p(weights["gate_packed"]), p(weights["gate_scale"]),
-                                        p(weights["up_packed"]), p(weights["up_scale"]),
-                                        p(weights["down_packed"]), p(weights["down_scale"]),
-                                        w.act_bits, p(y), p(ws), ws.numel(), s) == 0
+        # at most T rows per expert, as the layer call knows
+        assert lib.moe_expert_ffn_pairs_bounded(p(xs), p(xsc), p(offsets), E, D, I, R, T,
+                                                p(weights["gate_packed"]), p(weights["gate_scale"]),
+                                                p(weights["up_packed"]), p(weights["up_scale"]),
+                                                p(weights["down_packed"]), p(weights["down_scale"]),
+                                                w.act_bits, p(y), p(ws), ws.numel(), s) == 0
         if i is not None:
             ev[i][1].record()
         assert lib.moe_combine(p(y), p(inv), p(tw), T, D, k, p(out), s) == 0

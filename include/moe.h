@@ -238,6 +238,24 @@ int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale, const int32_
                          const uint16_t* down_scale, int act_bits, uint16_t* y_sorted, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* moe_expert_ffn_pairs for a caller that knows a bound on the rows of any one
+ * expert: max_rows_per_expert >= the largest offsets[e+1] - offsets[e] (the
+ * token count T of a layer call, as a token picks an expert at most once).
+ * With a bound below 48 no tensor-core kernel is launched (the batch cannot
+ * be prefill-shaped), and the CTA-pair kernels only when it reaches 129: the
+ * launches that would find no work are skipped.  With a true bound the
+ * results are the bits of moe_expert_ffn_pairs; a bound below the true
+ * count can only move experts to the stream kernel (same values within
+ * rounding, other bits), never leave one uncomputed.
+ * max_rows_per_expert < 0: MOE_ERR_INVALID. */
+int moe_expert_ffn_pairs_bounded(const void* x_pairs, const float* x_scale,
+                                 const int32_t* offsets, int E, int D, int I, int rows_max,
+                                 int max_rows_per_expert, const int32_t* gate_packed,
+                                 const uint16_t* gate_scale, const int32_t* up_packed,
+                                 const uint16_t* up_scale, const int32_t* down_packed,
+                                 const uint16_t* down_scale, int act_bits, uint16_t* y_sorted,
+                                 void* ws, size_t ws_bytes, void* stream);
+
 /* The int16 / int64 reading of act_bits 16 for one grouped PackedInt4Linear
  * (exact-generator adaptation page, "Sources & provenance": PackedInt4Linear
  * with act_bits 16 by default and an "int64 exact int4 MAC"; the page does

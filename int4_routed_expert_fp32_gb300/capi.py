@@ -118,6 +118,10 @@ SIGNATURES = {
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_set_tc_pair": (c_int, [c_int]),
     "moe_router_prepare": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
+    "moe_expert_ffn_pairs_bounded": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                             c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                             c_size_t, c_void_p]),
 }
 
 
@@ -299,9 +303,10 @@ def _rows_args(x: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.
 
 def expert_ffn(x_sorted: torch.Tensor, x_scale: Optional[torch.Tensor], offsets: torch.Tensor,
                experts: Dict[str, torch.Tensor], act_bits: int = 16,
-               pairs: bool = False) -> torch.Tensor:
+               pairs: bool = False, max_rows_per_expert: Optional[int] = None) -> torch.Tensor:
     """y_sorted bf16 [rows, D] = down(SiLU(gate(x)) * up(x)) per expert segment
-    (pairs=True: moe_expert_ffn_pairs on rows from dispatch(..., pairs=True))."""
+    (pairs=True: moe_expert_ffn_pairs on rows from dispatch(..., pairs=True);
+    with max_rows_per_expert, moe_expert_ffn_pairs_bounded)."""
     E, I = _arg("gate_packed", experts.get("gate_packed"), (None, None, None), torch.int32).shape[:2]
     x_scale = _rows_args(x_sorted, x_scale, offsets, act_bits,
                          torch.float16 if pairs else torch.bfloat16, E)
@@ -312,11 +317,17 @@ def expert_ffn(x_sorted: torch.Tensor, x_scale: Optional[torch.Tensor], offsets:
     y = torch.empty(rows, D, dtype=torch.bfloat16, device=dev)
     name = "moe_expert_ffn_pairs" if pairs else "moe_expert_ffn"
     ws = _ws(getattr(lib, name + "_workspace_size")(E, D, I, rows, act_bits), dev)
-    _check(name, getattr(lib, name)(
-        _p(x_sorted), _p(x_scale), _p(offsets), E, D, I, rows,
-        _p(experts["gate_packed"]), _p(experts["gate_scale"]), _p(experts["up_packed"]),
-        _p(experts["up_scale"]), _p(experts["down_packed"]), _p(experts["down_scale"]), act_bits,
-        _p(y), _p(ws), ws.numel(), _stream()))
+    wargs = (_p(experts["gate_packed"]), _p(experts["gate_scale"]), _p(experts["up_packed"]),
+             _p(experts["up_scale"]), _p(experts["down_packed"]), _p(experts["down_scale"]),
+             act_bits, _p(y), _p(ws), ws.numel(), _stream())
+    if max_rows_per_expert is not None:
+        if not pairs:
+            raise ValueError("max_rows_per_expert needs pairs=True")
+        _check("moe_expert_ffn_pairs_bounded", lib.moe_expert_ffn_pairs_bounded(
+            _p(x_sorted), _p(x_scale), _p(offsets), E, D, I, rows, int(max_rows_per_expert),
+            *wargs))
+        return y
+    _check(name, getattr(lib, name)(_p(x_sorted), _p(x_scale), _p(offsets), E, D, I, rows, *wargs))
     return y
 
 

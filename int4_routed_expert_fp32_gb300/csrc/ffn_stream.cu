@@ -1280,6 +1280,33 @@ extern "C" int moe_expert_ffn_pairs(const void* x_pairs, const float* x_scale,
                            y_sorted, false, ws, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int moe_expert_ffn_pairs_bounded(const void* x_pairs, const float* x_scale,
+                                            const int32_t* offsets, int E, int D, int I,
+                                            int rows_max, int max_rows_per_expert,
+                                            const int32_t* gate_packed, const uint16_t* gate_scale,
+                                            const int32_t* up_packed, const uint16_t* up_scale,
+                                            const int32_t* down_packed,
+                                            const uint16_t* down_scale, int act_bits,
+                                            uint16_t* y_sorted, void* ws, size_t ws_bytes,
+                                            void* stream) {
+  moe::Range range_("moe_expert_ffn_pairs_bounded");
+  if (max_rows_per_expert < 0) return MOE_ERR_INVALID;
+  const int rc = check_ffn_args(x_pairs, x_scale, offsets, E, D, I, rows_max, gate_packed,
+                                gate_scale, up_packed, up_scale, down_packed, down_scale, act_bits,
+                                y_sorted, ws);
+  if (rc || rows_max == 0) return rc;
+  if (ws_bytes < moe_expert_ffn_pairs_workspace_size(E, D, I, rows_max, act_bits))
+    return MOE_ERR_WORKSPACE;
+  // the bound only selects which kernels are launched: every expert still
+  // gets a kernel whatever its row count (a bound below 48 puts all of them
+  // on the stream kernel)
+  return launch_expert_ffn(x_pairs, x_scale, offsets, E, D, I, rows_max,
+                           max_rows_per_expert < rows_max ? max_rows_per_expert : rows_max,
+                           gate_packed, gate_scale,
+                           up_packed, up_scale, down_packed, down_scale, act_bits, y_sorted, false,
+                           ws, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t moe_expert_ffn_workspace_size(int E, int D, int I, int rows_max, int act_bits) {
   if (E <= 0 || D <= 0 || I <= 0 || rows_max < 0) return 256;
   // + the pair-ordered copy of x_sorted

@@ -112,6 +112,8 @@ def test_argument_errors_return_before_any_launch(capi):
     assert L.moe_layer_pipe_submit(n, n, n, n) == capi.MOE_ERR_INVALID
     assert L.moe_layer_pipe_join(n, n) == capi.MOE_ERR_INVALID
     L.moe_layer_pipe_destroy(n)  # NULL is ignored
+    assert L.moe_expert_ffn_pairs_bounded(n, n, n, 8, 128, 128, 8, -1, n, n, n, n, n, n, 16, n, n,
+                                          0, n) == capi.MOE_ERR_INVALID
     assert L.moe_layer_pipe_workspace_size(ctypes.byref(cfg)) == \
         L.moe_workspace_size(ctypes.byref(cfg)) + 4 * 512  # two slots of x and out, 4 x 64 bf16
     assert capi.launch_count() == launches

@@ -773,6 +773,41 @@ def test_tc_pair_and_one_cta_kernels_agree(moe):
     assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
 
 
+@pytest.mark.parametrize("act_bits", [16, 8])
+@pytest.mark.parametrize("counts,bound", [([5, 30, 0, 12], 30), ([5, 60, 200, 17], 200),
+                                          ([5, 60, 200, 17], 10)])
+def test_expert_ffn_pairs_bounded_gives_the_same_bits(moe, act_bits, counts, bound):
+    """moe_expert_ffn_pairs_bounded with a true bound on the rows per expert
+    gives the bits of moe_expert_ffn_pairs; a bound below the true count (10
+    rows for a batch with 200) moves every expert to the stream kernel: the
+    same values within the kernels' rounding."""
+    rng = np.random.default_rng(71 + act_bits + bound)
+    D, I = 256, 192
+    E = len(counts)
+    off = _segments(counts)
+    R = int(off[-1])
+    gp, gs = _random_int4(rng, E, I, D, 0.005, 0.02)
+    up, us = _random_int4(rng, E, I, D, 0.005, 0.02)
+    dp, ds = _random_int4(rng, E, D, I, 0.005, 0.02)
+    ex = {"gate_packed": _t(gp), "gate_scale": _t(gs, torch.bfloat16),
+          "up_packed": _t(up), "up_scale": _t(us, torch.bfloat16),
+          "down_packed": _t(dp), "down_scale": _t(ds, torch.bfloat16)}
+    T = R  # one token per row
+    idx = np.zeros((T, 1), dtype=np.int32)
+    for e in range(E):
+        idx[off[e]:off[e + 1], 0] = e
+    x = _bf16(rng.normal(size=(T, D)))
+    d = moe.dispatch(torch.from_numpy(idx).to(DEV), x.to(DEV), E, act_bits, pairs=True)
+    y0 = moe.expert_ffn(d["x_sorted"], d["x_scale"], d["offsets"], ex, act_bits, pairs=True)
+    y1 = moe.expert_ffn(d["x_sorted"], d["x_scale"], d["offsets"], ex, act_bits, pairs=True,
+                        max_rows_per_expert=bound)
+    assert moe.check_error() == 0
+    if bound >= max(counts):
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    else:
+        assert rel_l2(y1.float().cpu().numpy(), y0.float().cpu().numpy()) <= 5e-3
+
+
 @pytest.mark.parametrize("counts", [[5, 30], [5, 60]])
 def test_expert_ffn_reports_fp16_overflow_and_recovers(moe, counts):
     """An intermediate h beyond the fp16 range, on both expert kernels (5 + 30
