@@ -437,8 +437,8 @@ int moe_layer_forward_host(const moe_config* cfg, const moe_weights* w, const ui
  * moe_layer_forward_host (host != 0) call with exactly these arguments,
  * recorded once as a CUDA graph, for callers that run the layer again and
  * again on the same buffers (a serving loop).  No page has this call: it
- * replaces the per-call launches of the library's kernels (about 8 to 16 per
- * layer) with one graph launch.  All pointers are baked in: the weights, x,
+ * replaces the per-call launches of the library's kernels (8 to 18 per layer
+ * in the measured workloads) with one graph launch.  All pointers are baked in: the weights, x,
  * out (pinned host memory when host != 0) and ws must stay valid and are
  * re-read on every launch.  The capture runs on `stream`, which must not be
  * capturing already, in thread-local mode; nothing executes during it.
